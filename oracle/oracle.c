@@ -1,0 +1,341 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU oracle of the TokenSwift attention-side
+ * hot path.  TEST INFRASTRUCTURE ONLY: the test-suite, the smoke check and
+ * the benchmark's CPU-baseline leg call it; the product library never does.
+ * It shares no code, header or table with the CUDA path.
+ *
+ * Sources (TokenSwift pages):
+ *   - model card "TokenSwift-Qwen2.5-7B", "Example using TokenSwift command
+ *     line": retrieval budget 4096, gamma 4, min_p 0.1, temperature 1.0,
+ *     ngram_topk 20, penalty 1.2, penalty_length 1024;
+ *   - tool listing, "How it works": drafts from a partial KV cache, a
+ *     tree-based attention over candidates, verification with the full KV
+ *     cache, exact match of draft and target tokens, one longest valid draft
+ *     kept;
+ *   - ICML 2025 summary, "Approach": partial KV cache ranked by query-key
+ *     importance, windowed contextual penalty; ablation table: tree
+ *     [1,3,3,3], theta 1.2, W 1024.
+ * Where the pages are silent the plainest reading is used; every reading is
+ * listed in the design notes (scale 1/sqrt(d); head h uses KV head h/G;
+ * chunk score = max over the group of q . sum(K_chunk); ties to the lower
+ * index; penalty divides positive logits and multiplies the others once per
+ * distinct id in the window; penalty, then temperature, then min-p; greedy
+ * target; lowest row among the longest accepted paths).
+ *
+ * Everything is computed straight from the definitions, in fp64 unless the
+ * decision itself is taken in the kernel's precision (selection on fp32
+ * scores, penalty/min-p on fp32 logits).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 is the upper half of an IEEE binary32 word. */
+static double bf16_value(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ---------------------------------------------------------------------- */
+/* Visibility inside the speculative batch.  Row i sees row j (j in the     */
+/* batch) iff j == i or j is an ancestor of i in the parent forest.  The    */
+/* tree-based attention of "How it works"; chains are parent = previous.    */
+/* vis is T*T bytes, row-major.  Returns 0, or 1 for an invalid parent.     */
+/* ---------------------------------------------------------------------- */
+int oracle_visible(const int32_t *parent, int T, uint8_t *vis)
+{
+    for (int i = 0; i < T; ++i)
+        if (parent[i] < -1 || parent[i] >= i) return 1;
+    memset(vis, 0, (size_t)T * (size_t)T);
+    for (int i = 0; i < T; ++i)
+        for (int j = i; j >= 0; j = parent[j]) vis[(size_t)i * T + j] = 1;
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Tree-masked attention for a list of output rows.                        */
+/*   q: bf16 [T][Hq][d];  k, v: bf16 [Hkv][ld_kv][d]; prefix rows [0,N),   */
+/*   the batch's own rows at [N, N+T).  Row id r = t*Hq + h.               */
+/*   For row (t,h), KV head g = h / (Hq/Hkv).  Visible keys: every prefix  */
+/*   token, and batch token N+u when u is t itself or an ancestor of t.    */
+/*   s_j = scale * (q . k_j)   (fp64 from the bf16 values)                  */
+/*   o   = sum_j softmax(s)_j v_j,   lse = log sum_j exp(s_j)               */
+/*   out: double [n_rows][d];  lse_out: double [n_rows] (nullable).         */
+/* Returns 0, 1 on a bad parent array, 2 on bad sizes.                     */
+/* ---------------------------------------------------------------------- */
+int oracle_tree_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int64_t ld_kv, int64_t N, int T, int Hq, int Hkv, int d,
+                          double scale, const int32_t *parent,
+                          const int32_t *row_ids, int n_rows,
+                          double *out, double *lse_out)
+{
+    if (T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || N < 0 || ld_kv < N + T)
+        return 2;
+    uint8_t *vis = (uint8_t *)malloc((size_t)(T > 0 ? T : 1) * (size_t)(T > 0 ? T : 1));
+    if (!vis) return 2;
+    if (T > 0 && oracle_visible(parent, T, vis)) { free(vis); return 1; }
+    for (int r = 0; r < n_rows; ++r)
+        if (row_ids[r] < 0 || row_ids[r] >= T * Hq) { free(vis); return 2; }
+    const int G = Hq / Hkv;
+    const int64_t L = N + T;
+    int err = 0;
+
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        uint8_t *seen = (uint8_t *)malloc((size_t)(L > 0 ? L : 1));
+        double *acc = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!s || !seen || !acc) {
+#pragma omp atomic write
+            err = 2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n_rows; ++r) {
+            if (!s || !seen || !acc) continue;
+            const int t = row_ids[r] / Hq;
+            const int h = row_ids[r] % Hq;
+            const int g = h / G;
+            const uint16_t *qr = q + ((size_t)t * Hq + h) * d;
+            const uint16_t *kh = k + (size_t)g * ld_kv * d;
+            const uint16_t *vh = v + (size_t)g * ld_kv * d;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < L; ++j) {
+                seen[j] = (j < N) ? 1 : vis[(size_t)t * T + (j - N)];
+                if (!seen[j]) continue;
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c)
+                    dot += bf16_value(qr[c]) * bf16_value(kh[j * d + c]);
+                s[j] = scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int c = 0; c < d; ++c) acc[c] = 0.0;
+            for (int64_t j = 0; j < L; ++j) {
+                if (!seen[j]) continue;
+                double p = exp(s[j] - m);
+                l += p;
+                for (int c = 0; c < d; ++c) acc[c] += p * bf16_value(vh[j * d + c]);
+            }
+            for (int c = 0; c < d; ++c) out[(size_t)r * d + c] = acc[c] / l;
+            if (lse_out) lse_out[r] = m + log(l);
+        }
+        free(s);
+        free(seen);
+        free(acc);
+    }
+    free(vis);
+    return err;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Chunk importance ("partial KV cache ranked by query-key importance").   */
+/*   score[g][c] = max_{h in group g} q_h . sum_{t in chunk c} k_t          */
+/* over prefix tokens only; the last chunk may be partial.  Unscaled.      */
+/*   q_row: bf16 [Hq][d];  scores: double [Hkv][ceil(N/chunk)].             */
+/* ---------------------------------------------------------------------- */
+int oracle_score_chunks(const uint16_t *q_row, const uint16_t *k, int64_t ld_kv, int64_t N,
+                        int Hq, int Hkv, int d, int chunk, double *scores)
+{
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || d > 512 || chunk <= 0 || N < 0 || ld_kv < N)
+        return 2;
+    const int G = Hq / Hkv;
+    const int64_t nc = (N + chunk - 1) / chunk;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int g = 0; g < Hkv; ++g) {
+        for (int64_t c = 0; c < nc; ++c) {
+            double ksum[512];
+            for (int e = 0; e < d; ++e) ksum[e] = 0.0;
+            int64_t t_end = (c + 1) * chunk < N ? (c + 1) * chunk : N;
+            for (int64_t t = c * chunk; t < t_end; ++t)
+                for (int e = 0; e < d; ++e)
+                    ksum[e] += bf16_value(k[((size_t)g * ld_kv + t) * d + e]);
+            double best = -INFINITY;
+            for (int j = 0; j < G; ++j) {
+                const uint16_t *qh = q_row + (size_t)(g * G + j) * d;
+                double dot = 0.0;
+                for (int e = 0; e < d; ++e) dot += bf16_value(qh[e]) * ksum[e];
+                if (dot > best) best = dot;
+            }
+            scores[(size_t)g * nc + c] = best;
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Top-k chunk selection up to the retrieval budget.                       */
+/* Per KV head: the k chunks with the largest fp32 score; equal scores go  */
+/* to the lower chunk index; the chosen indices are returned ascending.    */
+/* Scores compare as values (so -0 equals +0).                             */
+/*   scores: float [Hkv][nc];  sel: int32 [Hkv][k] with k = min(k, nc).     */
+/* ---------------------------------------------------------------------- */
+static const float *g_sort_keys;
+static int by_score_then_index(const void *a, const void *b)
+{
+    int ia = *(const int *)a, ib = *(const int *)b;
+    float sa = g_sort_keys[ia], sb = g_sort_keys[ib];
+    if (sa > sb) return -1;
+    if (sa < sb) return 1;
+    return (ia > ib) - (ia < ib);
+}
+static int ascending(const void *a, const void *b)
+{
+    int ia = *(const int *)a, ib = *(const int *)b;
+    return (ia > ib) - (ia < ib);
+}
+
+int oracle_select(const float *scores, int Hkv, int nc, int k, int32_t *sel)
+{
+    if (Hkv <= 0 || nc < 0 || k < 0) return 2;
+    if (k > nc) k = nc;
+    int *idx = (int *)malloc(sizeof(int) * (size_t)(nc > 0 ? nc : 1));
+    if (!idx) return 2;
+    for (int g = 0; g < Hkv; ++g) {
+        for (int c = 0; c < nc; ++c) {
+            if (scores[(size_t)g * nc + c] != scores[(size_t)g * nc + c]) { free(idx); return 3; }
+            idx[c] = c;
+        }
+        g_sort_keys = scores + (size_t)g * nc;
+        qsort(idx, (size_t)nc, sizeof(int), by_score_then_index);
+        qsort(idx, (size_t)k, sizeof(int), ascending);
+        for (int i = 0; i < k; ++i) sel[(size_t)g * k + i] = idx[i];
+    }
+    free(idx);
+    return 0;
+}
+
+/* Gather the selected chunks into a compact cache (byte copy).            */
+/*   dst[g][i*chunk + t] = src[g][sel[g][i]*chunk + t] for i<k, t<chunk,    */
+/* rows of d bf16 elements; tokens at or past N are not copied (a partial  */
+/* last chunk leaves its trailing rows of dst untouched).                  */
+int oracle_gather(const int32_t *sel, int Hkv, int k, int chunk, int64_t N,
+                  const uint16_t *src, int64_t ld_src, int d, uint16_t *dst, int64_t ld_dst)
+{
+    if ((int64_t)k * chunk > ld_dst) return 2;
+    for (int g = 0; g < Hkv; ++g)
+        for (int i = 0; i < k; ++i) {
+            int64_t c = sel[(size_t)g * k + i];
+            for (int t = 0; t < chunk; ++t) {
+                int64_t s = c * chunk + t;
+                if (s >= N) break;
+                memcpy(dst + ((size_t)g * ld_dst + (size_t)i * chunk + t) * d,
+                       src + ((size_t)g * ld_src + s) * d, sizeof(uint16_t) * (size_t)d);
+            }
+        }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Windowed contextual penalty, temperature, min-p and greedy target.      */
+/*   S = distinct ids among the last W generated tokens (history[0..W)).   */
+/*   For v in S: l > 0 ? l / theta : l * theta   (fp32 result, IEEE RN: the */
+/*   fp64 quotient/product rounded once to fp32 equals the fp32 operation). */
+/*   Then l / temperature (same rounding argument).                        */
+/*   m = max, target = lowest id attaining m.                              */
+/*   kept = #{v : (double)l_v >= fl64(m + log_min_p)}  -- min-p in logit    */
+/*   space, p_v >= min_p * p_max; log_min_p is computed once by the caller. */
+/*   pen_out (nullable): the final fp32 logits.                             */
+/* Returns 0, or 4 for a history id outside [0, V).                        */
+/* ---------------------------------------------------------------------- */
+int oracle_penalty_minp(const float *logits, int T, int V, const int32_t *history, int W,
+                        float theta, float temperature, double log_min_p,
+                        int32_t *target, int32_t *kept, float *pen_out)
+{
+    uint8_t *inwin = (uint8_t *)calloc((size_t)(V > 0 ? V : 1), 1);
+    if (!inwin) return 2;
+    for (int w = 0; w < W; ++w) {
+        if (history[w] < 0 || history[w] >= V) { free(inwin); return 4; }
+        inwin[history[w]] = 1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < T; ++i) {
+        float *row = (float *)malloc(sizeof(float) * (size_t)(V > 0 ? V : 1));
+        float m = -INFINITY;
+        int arg = -1;
+        for (int vv = 0; vv < V; ++vv) {
+            float l = logits[(size_t)i * V + vv];
+            if (inwin[vv]) {
+                if (l > 0.0f) l = (float)((double)l / (double)theta);
+                else          l = (float)((double)l * (double)theta);
+            }
+            l = (float)((double)l / (double)temperature);
+            row[vv] = l;
+            if (arg < 0 || l > m) { m = l; arg = vv; }
+        }
+        double thr = (double)m + log_min_p;
+        int cnt = 0;
+        for (int vv = 0; vv < V; ++vv)
+            if ((double)row[vv] >= thr) ++cnt;
+        target[i] = arg;
+        kept[i] = cnt;
+        if (pen_out) memcpy(pen_out + (size_t)i * V, row, sizeof(float) * (size_t)V);
+        free(row);
+    }
+    free(inwin);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Exact-match acceptance along every tree / n-gram path ("How it works":  */
+/* drafts must exactly match the target tokens; one of the longest valid   */
+/* drafts is kept -- here the lowest row among them).                      */
+/*   expected(i) = parent[i] >= 0 ? target[parent[i]] : anchor              */
+/*   acc(i) = draft[i] == expected(i) && (parent[i] < 0 || acc(parent[i]))  */
+/*   depth(root) = 1, depth(i) = depth(parent[i]) + 1                       */
+/*   L = max depth over accepted rows (0 if none); best = lowest such row;  */
+/*   bonus = L > 0 ? target[best] : anchor; path = root..best.              */
+/*   result = {L, best, bonus, status}; path int32[T], unused entries -1.   */
+/* ---------------------------------------------------------------------- */
+int oracle_accept(const int32_t *draft, const int32_t *parent, const int32_t *target, int T,
+                  int32_t anchor, int32_t *result, int32_t *path)
+{
+    for (int i = 0; i < T; ++i) path[i] = -1;
+    for (int i = 0; i < T; ++i)
+        if (parent[i] < -1 || parent[i] >= i) {
+            result[0] = 0; result[1] = -1; result[2] = anchor; result[3] = 5;
+            return 1;
+        }
+    int *acc = (int *)calloc((size_t)(T > 0 ? T : 1), sizeof(int));
+    int *depth = (int *)calloc((size_t)(T > 0 ? T : 1), sizeof(int));
+    int L = 0, best = -1;
+    for (int i = 0; i < T; ++i) {
+        int p = parent[i];
+        int32_t expected = p >= 0 ? target[p] : anchor;
+        acc[i] = (draft[i] == expected) && (p < 0 || acc[p]);
+        depth[i] = p >= 0 ? depth[p] + 1 : 1;
+        if (acc[i] && depth[i] > L) { L = depth[i]; best = i; }
+    }
+    result[0] = L;
+    result[1] = best;
+    result[2] = L > 0 ? target[best] : anchor;
+    result[3] = 0;
+    for (int j = best, pos = L - 1; j >= 0; j = parent[j], --pos) path[pos] = j;
+    free(acc);
+    free(depth);
+    return 0;
+}

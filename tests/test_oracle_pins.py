@@ -1,0 +1,397 @@
+"""Pins of the fp64 oracle to things other than itself (CPU only).
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong index, a transposed operand, a wrong mask bit, a wrong tie rule) fails:
+  * attention: torch's scaled_dot_product_attention in fp64 with a mask built
+    by boolean transitive closure (a different algorithm from the oracle's
+    parent walk); closed forms (zero query -> mean of visible values, constant
+    values, a lone visible key); the chain-is-causal and all-roots-is-decode
+    special cases; invariance under permuting prefix tokens and under a
+    topological relabelling of the batch;
+  * chunk scores: exact int64 brute force by a different association
+    (sum over tokens of q.k instead of q . sum k), and a closed form;
+  * selection: numpy lexsort, plus hand-made tie and signed-zero cases;
+  * gather: identity when the budget covers the cache;
+  * penalty/min-p and acceptance: hand-worked examples in tests/golden, plus
+    min-p checked against a scipy softmax, and acceptance against path
+    enumeration with networkx.
+"""
+import math
+import os
+
+import networkx as nx
+import numpy as np
+import pytest
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+import oracle
+from long_context_attention_tree_b300 import workloads as W
+
+
+# ---------------------------------------------------------------- helpers
+def closure_mask(parent):
+    """Ancestor-or-self relation by repeated boolean matrix products."""
+    T = len(parent)
+    A = np.zeros((T, T), dtype=bool)
+    for i, p in enumerate(parent):
+        if p >= 0:
+            A[i, p] = True
+    R = np.eye(T, dtype=bool) | A
+    while True:
+        R2 = R | ((R.astype(np.int64) @ R.astype(np.int64)) > 0)
+        if (R2 == R).all():
+            return R
+        R = R2
+
+
+def sdpa_reference(q, k, v, N, vis, scale):
+    """torch SDPA in fp64 with an explicit boolean mask (GQA by repeat)."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[0]
+    G = Hq // Hkv
+    L = N + T
+    kk = k[:, :L].double().repeat_interleave(G, dim=0)  # [Hq][L][d]
+    vv = v[:, :L].double().repeat_interleave(G, dim=0)
+    qq = q.double().permute(1, 0, 2)  # [Hq][T][d]
+    mask = torch.zeros((T, L), dtype=torch.bool)
+    mask[:, :N] = True
+    mask[:, N:] = torch.from_numpy(vis)
+    out = F.scaled_dot_product_attention(qq.unsqueeze(0), kk.unsqueeze(0), vv.unsqueeze(0),
+                                         attn_mask=mask, scale=scale)[0]
+    scores = torch.einsum("htd,hld->htl", qq, kk) * scale
+    scores = scores.masked_fill(~mask, -math.inf)
+    lse = torch.from_numpy(scipy.special.logsumexp(scores.numpy(), axis=-1))
+    return out.permute(1, 0, 2).numpy(), lse.permute(1, 0).numpy()
+
+
+def run_oracle(q, k, v, N, parent, scale):
+    return oracle.tree_attn(q, k, v, N, parent, scale)
+
+
+SHAPES = [
+    # (T, Hq, Hkv, d, N, value_kind)
+    (40, 4, 1, 64, 200, "int"),
+    (13, 8, 2, 64, 77, "normal"),
+    (7, 6, 3, 128, 0, "normal"),
+    (20, 5, 5, 32, 65, "int"),
+]
+
+
+# ---------------------------------------------------------------- visibility
+@pytest.mark.parametrize("parent", [
+    W.tree_parents([1, 3, 3, 3]),
+    W.verify_parents(),
+    W.tree_parents([3, 3, 3]),
+    W.chain_parents(5, 4),
+    [-1] * 9,
+])
+def test_visible_matches_networkx_ancestors(parent):
+    vis = oracle.visible(parent)
+    g = nx.DiGraph()
+    g.add_nodes_from(range(len(parent)))
+    g.add_edges_from((p, i) for i, p in enumerate(parent) if p >= 0)
+    for i in range(len(parent)):
+        want = nx.ancestors(g, i) | {i}
+        assert set(np.nonzero(vis[i])[0].tolist()) == want
+
+
+def test_visible_rejects_bad_parents():
+    with pytest.raises(ValueError):
+        oracle.visible([-1, 1])      # parent[i] >= i
+    with pytest.raises(ValueError):
+        oracle.visible([-1, -2])     # below -1
+
+
+def test_tree_shapes_from_ablation_table():
+    assert len(W.tree_parents([1, 3, 3, 3])) == 40
+    assert len(W.tree_parents([3, 3, 3, 3])) == 120
+    assert len(W.tree_parents([1, 9, 9, 9])) == 1 + 9 + 81 + 729
+    assert W.tree_parents([1, 3, 3, 3])[:13] == [-1, 0, 0, 0, 1, 1, 1, 2, 2, 2, 3, 3, 3]
+    assert len(W.verify_parents()) == 120
+
+
+# ---------------------------------------------------------------- attention
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("tree", ["verify", "chain", "roots"])
+def test_attention_matches_torch_sdpa(shape, tree):
+    T, Hq, Hkv, d, N, kind = shape
+    if tree == "verify":
+        parent = (W.tree_parents([1, 3, 3, 3]) + W.chain_parents(20, 4, offset=40))[:T]
+        parent = [p if p < T else -1 for p in parent]
+    elif tree == "chain":
+        parent = [-1] + list(range(T - 1))
+    else:
+        parent = [-1] * T
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=7 + T + N, value_kind=kind, ld_extra=3)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_oracle(q, k, v, N, parent, scale)
+    ro, rlse = sdpa_reference(q, k, v, N, closure_mask(parent), scale)
+    np.testing.assert_allclose(o, ro, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(lse, rlse, rtol=0, atol=1e-10)
+
+
+def test_chain_equals_causal_attention():
+    """A chain batch is plain causal attention over prefix + batch."""
+    T, Hq, Hkv, d, N = 9, 4, 2, 64, 50
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=3, value_kind="normal")
+    o, _ = run_oracle(q, k, v, N, [-1] + list(range(T - 1)), 0.125)
+    G = Hq // Hkv
+    kk = k.double().repeat_interleave(G, 0)
+    vv = v.double().repeat_interleave(G, 0)
+    # causal over the full N+T sequence, keep the last T query positions
+    qfull = torch.zeros((Hq, N + T, d), dtype=torch.float64)
+    qfull[:, N:] = q.double().permute(1, 0, 2)
+    ref = F.scaled_dot_product_attention(qfull[None], kk[None], vv[None], is_causal=True, scale=0.125)[0, :, N:]
+    np.testing.assert_allclose(o, ref.permute(1, 0, 2).numpy(), atol=1e-10, rtol=0)
+
+
+def test_zero_query_gives_mean_of_visible_values():
+    T, Hq, Hkv, d, N = 40, 4, 1, 64, 33
+    parent = W.tree_parents([1, 3, 3, 3])
+    _, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=11, value_kind="normal")
+    q = torch.zeros((T, Hq, d), dtype=torch.bfloat16)
+    o, lse = run_oracle(q, k, v, N, parent, 0.125)
+    vis = closure_mask(parent)
+    vd = v.double().numpy()
+    for t in range(T):
+        idx = list(range(N)) + [N + u for u in range(T) if vis[t, u]]
+        want = vd[0, idx].mean(axis=0)
+        for h in range(Hq):
+            np.testing.assert_allclose(o[t, h], want, atol=1e-12)
+            assert abs(lse[t, h] - math.log(len(idx))) < 1e-12
+
+
+def test_constant_values_and_lone_key():
+    T, Hq, Hkv, d = 6, 2, 1, 64
+    q, k, _ = W.make_qkv(T, Hq, Hkv, d, 0, seed=5, value_kind="normal")
+    v = torch.full((Hkv, T, d), 1.5, dtype=torch.bfloat16)
+    o, _ = run_oracle(q, k, v, 0, [-1, 0, 1, 2, 3, 4], 0.125)
+    np.testing.assert_allclose(o, 1.5, atol=1e-12)
+    # N = 0 and every row a root: each row sees only its own key
+    v2 = torch.randn((Hkv, T, d)).to(torch.bfloat16)
+    o2, lse2 = run_oracle(q, k, v2, 0, [-1] * T, 0.125)
+    for t in range(T):
+        for h in range(Hq):
+            np.testing.assert_array_equal(o2[t, h], v2[0, t].double().numpy())
+            s = 0.125 * float((q[t, h].double() * k[0, t].double()).sum())
+            assert abs(lse2[t, h] - s) < 1e-12
+
+
+def test_prefix_permutation_invariance():
+    T, Hq, Hkv, d, N = 40, 4, 2, 64, 130
+    parent = W.tree_parents([1, 3, 3, 3])
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=21, value_kind="normal")
+    o, lse = run_oracle(q, k, v, N, parent, 0.125)
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(1))
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :N] = k[:, perm]
+    v2[:, :N] = v[:, perm]
+    o2, lse2 = run_oracle(q, k2, v2, N, parent, 0.125)
+    np.testing.assert_allclose(o2, o, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, atol=1e-12)
+
+
+def test_topological_relabel_permutes_outputs():
+    """Listing the batch in DFS order instead of BFS permutes the output rows."""
+    parent = W.tree_parents([1, 3, 3])
+    T = len(parent)
+    kids = {}
+    for i, p in enumerate(parent):
+        kids.setdefault(p, []).append(i)
+    order = []
+
+    def dfs(n):
+        order.append(n)
+        for c in kids.get(n, []):
+            dfs(c)
+    dfs(0)
+    new_of = {old: new for new, old in enumerate(order)}
+    parent2 = [-1 if parent[old] < 0 else new_of[parent[old]] for old in order]
+    Hq, Hkv, d, N = 4, 2, 64, 40
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=9, value_kind="normal")
+    o, _ = run_oracle(q, k, v, N, parent, 0.125)
+    idx = torch.tensor(order)
+    q2 = q[idx]
+    k2 = torch.cat([k[:, :N], k[:, N:N + T][:, idx]], dim=1)
+    v2 = torch.cat([v[:, :N], v[:, N:N + T][:, idx]], dim=1)
+    o2, _ = run_oracle(q2, k2, v2, N, parent2, 0.125)
+    np.testing.assert_allclose(o2, o[order], atol=1e-12)
+
+
+def test_sampled_rows_equal_full():
+    T, Hq, Hkv, d, N = 40, 4, 2, 64, 100
+    parent = W.tree_parents([1, 3, 3, 3])
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=2)
+    o, lse = oracle.tree_attn(q, k, v, N, parent, 0.125)
+    rows = np.array([0, 5, 77, 159])
+    os_, ls_ = oracle.tree_attn(q, k, v, N, parent, 0.125, rows=rows)
+    np.testing.assert_array_equal(os_, o.reshape(-1, d)[rows])
+    np.testing.assert_array_equal(ls_, lse.reshape(-1)[rows])
+
+
+# ---------------------------------------------------------------- chunk scores
+@pytest.mark.parametrize("N", [1, 63, 64, 65, 300])
+def test_chunk_scores_int64_brute_force(N):
+    Hq, Hkv, d = 8, 2, 64
+    q, k, _ = W.make_qkv(1, Hq, Hkv, d, N, seed=N)
+    s = oracle.score_chunks(q[0], k, N, 64)
+    qi = q[0].to(torch.int64).numpy()
+    ki = k[:, :N].to(torch.int64).numpy()
+    G = Hq // Hkv
+    nc = (N + 63) // 64
+    for g in range(Hkv):
+        per_tok = qi[g * G:(g + 1) * G] @ ki[g].T       # [G][N] exact q.k per token
+        for c in range(nc):
+            want = per_tok[:, c * 64:(c + 1) * 64].sum(axis=1).max()
+            assert s[g, c] == float(want)
+
+
+def test_chunk_scores_closed_form_ones():
+    Hq, Hkv, d, N = 4, 1, 64, 100
+    q, _, _ = W.make_qkv(1, Hq, Hkv, d, 0, seed=4)
+    k = torch.ones((Hkv, N, d), dtype=torch.bfloat16)
+    s = oracle.score_chunks(q[0], k, N, 64)
+    qsum = q[0].double().sum(dim=1).max().item()
+    assert s[0, 0] == 64 * qsum and s[0, 1] == 36 * qsum
+
+
+# ---------------------------------------------------------------- selection
+def test_select_matches_lexsort():
+    rng = np.random.default_rng(0)
+    s = rng.integers(-5, 6, size=(3, 300)).astype(np.float32)  # many ties
+    sel = oracle.select(s, 64)
+    for g in range(3):
+        order = np.lexsort((np.arange(300), -s[g]))[:64]
+        np.testing.assert_array_equal(sel[g], np.sort(order))
+
+
+def test_select_hand_cases():
+    s = np.array([[5, 5, 3, 5, 1]], dtype=np.float32)
+    np.testing.assert_array_equal(oracle.select(s, 2)[0], [0, 1])
+    np.testing.assert_array_equal(oracle.select(s, 3)[0], [0, 1, 3])
+    np.testing.assert_array_equal(oracle.select(s, 4)[0], [0, 1, 2, 3])
+    np.testing.assert_array_equal(oracle.select(s, 9)[0], [0, 1, 2, 3, 4])
+    z = np.array([[-0.0, 0.0, -1.0]], dtype=np.float32)   # -0 equals +0: lower index wins
+    np.testing.assert_array_equal(oracle.select(z, 1)[0], [0])
+    z2 = np.array([[0.0, -0.0, 2.0]], dtype=np.float32)
+    np.testing.assert_array_equal(oracle.select(z2, 2)[0], [0, 2])
+
+
+# ---------------------------------------------------------------- gather
+def test_gather_identity_when_budget_covers_cache():
+    Hkv, d, N = 2, 64, 192
+    _, k, _ = W.make_qkv(1, 2, Hkv, d, N, seed=8)
+    sel = np.tile(np.arange(3, dtype=np.int32), (Hkv, 1))
+    kp = oracle.gather(sel, k, N, 64, ld_dst=N + 4)
+    assert torch.equal(kp[:, :N], k[:, :N])
+
+
+def test_gather_moves_the_named_chunk():
+    Hkv, d, N = 1, 64, 256
+    _, k, _ = W.make_qkv(1, 1, Hkv, d, N, seed=12)
+    kp = oracle.gather(np.array([[3, 1]], dtype=np.int32), k, N, 64, ld_dst=128)
+    assert torch.equal(kp[0, :64], k[0, 192:256]) and torch.equal(kp[0, 64:128], k[0, 64:128])
+
+
+# ---------------------------------------------------------------- penalty / min-p
+def _parse(path):
+    rows = []
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        rows.append([f.strip() for f in line.split("|")])
+    return rows
+
+
+def _nums(s, typ):
+    return [] if s.strip() == "-" else [typ(x) for x in s.split()]
+
+
+def test_penalty_minp_hand_examples(golden_dir):
+    rows = _parse(os.path.join(golden_dir, "penalty_minp_hand.txt"))
+    assert len(rows) >= 8
+    for name, lg, hist, theta, mp, temp, final, tgt, kept in rows:
+        logits = np.array([_nums(lg, float)], dtype=np.float32)
+        t, kp, pen = oracle.penalty_minp(logits, np.array(_nums(hist, int), dtype=np.int32),
+                                         float(theta), float(mp), float(temp), return_logits=True)
+        np.testing.assert_array_equal(pen[0], np.array(_nums(final, float), dtype=np.float32), err_msg=name)
+        assert t[0] == int(tgt), name
+        assert kp[0] == int(kept), name
+
+
+def test_minp_count_matches_softmax_definition():
+    rng = np.random.default_rng(3)
+    logits = (rng.standard_normal((6, 5000)) * 3).astype(np.float32)
+    hist = rng.integers(0, 5000, size=300).astype(np.int32)
+    t, kp, pen = oracle.penalty_minp(logits, hist, 1.2, 0.1, 1.0, return_logits=True)
+    p = scipy.special.softmax(pen.astype(np.float64), axis=1)
+    for i in range(6):
+        ratio = p[i] / p[i].max()
+        assert not np.any(np.abs(ratio - np.float32(0.1)) < 1e-9)   # no boundary case
+        assert kp[i] == int((ratio >= np.float64(np.float32(0.1))).sum())
+        assert t[i] == int(np.argmax(pen[i]))
+
+
+def test_penalty_empty_window_is_plain_argmax():
+    rng = np.random.default_rng(4)
+    logits = (rng.standard_normal((3, 777)) * 3).astype(np.float32)
+    t, _ = oracle.penalty_minp(logits, np.zeros(0, dtype=np.int32), 1.2, 0.1, 1.0)
+    np.testing.assert_array_equal(t, logits.argmax(axis=1))
+
+
+def test_penalty_rejects_out_of_range_history():
+    with pytest.raises(ValueError):
+        oracle.penalty_minp(np.zeros((1, 4), np.float32), np.array([4], np.int32), 1.2, 0.1, 1.0)
+
+
+# ---------------------------------------------------------------- acceptance
+def test_accept_hand_examples(golden_dir):
+    rows = _parse(os.path.join(golden_dir, "accept_hand.txt"))
+    assert len(rows) >= 5
+    for name, par, dr, tg, anc, res, path in rows:
+        r, p = oracle.accept(_nums(dr, int), _nums(par, int), _nums(tg, int), int(anc))
+        L, best, bonus = _nums(res, int)
+        assert (r[0], r[1], r[2], r[3]) == (L, best, bonus, 0), name
+        want = _nums(path, int)
+        assert p[:len(want)].tolist() == want and all(x == -1 for x in p[len(want):]), name
+
+
+def _accept_by_enumeration(draft, parent, target, anchor):
+    g = nx.DiGraph()
+    g.add_node("r")
+    for i, p in enumerate(parent):
+        g.add_edge("r" if p < 0 else p, i)
+    best_len, best_row = 0, -1
+    for i in range(len(parent)):
+        path = nx.shortest_path(g, "r", i)[1:]
+        ok = all(draft[n] == (anchor if parent[n] < 0 else target[parent[n]]) for n in path)
+        if ok and len(path) > best_len:
+            best_len, best_row = len(path), i
+    return best_len, best_row
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_accept_matches_path_enumeration(seed):
+    parent = W.verify_parents()
+    vi = W.make_vocab_inputs(parent, V=500, W=50, seed=seed)
+    target = vi.designed_target.numpy()
+    r, path = oracle.accept(vi.draft.numpy(), parent, target, vi.anchor)
+    L, best = _accept_by_enumeration(vi.draft.tolist(), parent, target.tolist(), vi.anchor)
+    assert (r[0], r[1]) == (L, best)
+    assert r[2] == (target[best] if L > 0 else vi.anchor)
+    if L:
+        assert path[L - 1] == best
+
+
+def test_planted_targets_are_the_oracle_targets():
+    """The input generator's designed tokens are what the greedy step picks."""
+    parent = W.verify_parents()
+    vi = W.make_vocab_inputs(parent, V=4000, W=256, seed=1, flip_rows=0.5)
+    t, _ = oracle.penalty_minp(vi.logits.numpy(), vi.history.numpy(), 1.2, 0.1, 1.0)
+    np.testing.assert_array_equal(t, vi.designed_target.numpy())
+    # without the penalty the flipped rows pick the history token instead
+    t0, _ = oracle.penalty_minp(vi.logits.numpy(), vi.history.numpy(), 1.0, 0.1, 1.0)
+    assert (t0 != t).sum() > 10
