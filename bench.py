@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the TokenSwift attention-side hot path on B300.
+
+Default workload: one full speculative step of a Qwen2.5-14B-shaped model at
+102400 tokens of context (48 layers, 40 query heads, 8 KV heads, head dim 128,
+bf16 KV cache of 20.1 GB), every layer running the 120-row tree + n-gram
+verify attention over the full cache (chunk importance fused), top-64 chunk
+selection + gather into a 4096-token partial cache and 4-row draft attention
+over it; then the vocabulary stage on 120 x 152064 fp32 logits (penalty 1.2
+over a 1024-token window, min-p 0.1, greedy target, acceptance).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                    [--workload qwen14b-100k|llama8b-<N>|llama2-7b-100k] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  Metric: verify-attention KV throughput
+(prefix K+V bytes read by the verify pass, per second of the whole step).
+Multi-GPU: N independent replicas (the step has no cross-GPU exchange);
+value = total KV bytes of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify attn KV GB/s (% of HBM peak) at 100K ctx; µs/layer/spec step"
+UNIT = "GB/s"
+
+
+def workload_config(name: str):
+    from long_context_attention_tree_b300 import workloads as W
+    if name == "qwen14b-100k":
+        return W.CONFIGS[5]
+    if name == "llama2-7b-100k":
+        return W.CONFIGS[4]
+    if name.startswith("llama8b-"):
+        N = int(name.split("-")[1].lower().replace("k", "")) * 1024 if name.lower().endswith("k") else int(name.split("-")[1])
+        return W.CONFIGS[3].with_N(N)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    sm_max=d.get("sm_max_mhz", 2032.0), source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, sm_max=2032.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [line.strip().split(", ") for line in self.f if line.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        return rows
+
+    @staticmethod
+    def summarize(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            if len(r) < 9:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        pw = [float(r[3]) for r in rows if len(r) >= 9 and r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------- distributed helpers
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, seconds_per_rank: float, ws: int):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    t = max_over_ranks(seconds_per_rank, ws)
+    return units_per_rank * ws / t, t
+
+
+# ---------------------------------------------------------------------------- CPU oracle baseline
+def cpu_oracle_sample(cfg, layer_fraction_rows: float = 1.0, seed_layer: int = 0):
+    """Time the fp64 oracle on one layer of the workload (host cores).
+
+    Returns (seconds, kv_bytes_equivalent, description, threads)."""
+    import oracle
+    from long_context_attention_tree_b300 import workloads as W
+    oracle.build()
+    x = W.make_layer_inputs(cfg, seed_layer, device="cpu")
+    T, Hq = cfg.T, cfg.Hq
+    n_rows = T * Hq
+    rows = np.arange(n_rows, dtype=np.int32)
+    if layer_fraction_rows < 1.0:
+        step = max(1, int(round(1 / layer_fraction_rows)))
+        rows = rows[::step]
+    t0 = time.perf_counter()
+    oracle.tree_attn(x.q, x.k, x.v, cfg.N, cfg.parents, cfg.scale, rows=rows)
+    sc = oracle.score_chunks(x.q[0], x.k, cfg.N).astype(np.float32)
+    sel = oracle.select(sc, cfg.k_sel)
+    B = cfg.k_sel * cfg.chunk
+    kp = oracle.gather(sel, x.k, cfg.N, cfg.chunk, B + cfg.draft_rows)
+    vp = oracle.gather(sel, x.v, cfg.N, cfg.chunk, B + cfg.draft_rows)
+    kp[:, B:] = x.k_draft_tail
+    vp[:, B:] = x.v_draft_tail
+    oracle.tree_attn(x.q_draft, kp, vp, B, [-1] + list(range(cfg.draft_rows - 1)), cfg.scale)
+    t_layer = time.perf_counter() - t0
+    frac = rows.size / n_rows
+    t_vocab = 0.0
+    if cfg.vocab:
+        vi = W.make_vocab_inputs(cfg.parents, cfg.vocab, cfg.window, seed=1000 * cfg.cid + 999, device="cpu")
+        t1 = time.perf_counter()
+        tgt, _ = oracle.penalty_minp(vi.logits.numpy(), vi.history.numpy(), cfg.theta, cfg.min_p, cfg.temperature)
+        oracle.accept(vi.draft.numpy(), cfg.parents, tgt, vi.anchor)
+        t_vocab = time.perf_counter() - t1
+    # per-layer share of the vocab stage; verify rows scale the KV bytes
+    seconds = t_layer + t_vocab / max(cfg.layers, 1)
+    kv = cfg.kv_bytes_per_layer() * frac
+    desc = (f"layer {seed_layer} of {cfg.layers}: verify attention on {rows.size}/{n_rows} rows, chunk scores, "
+            f"top-{cfg.k_sel} selection, gather, {cfg.draft_rows}-row draft attention"
+            + (f"; vocab stage ({T}x{cfg.vocab}) counted as 1/{cfg.layers} of a step" if cfg.vocab else "")
+            + "; KV bytes scaled by the verify row fraction")
+    return seconds, kv, desc, oracle.num_threads()
+
+
+# ---------------------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    cfg = workload_config(args.workload)
+    import oracle
+    oracle.build()
+    frac = args.ref_row_fraction
+    vals = []
+    desc = threads = None
+    for i in range(args.warmup + args.steps):
+        s, kv, desc, threads = cpu_oracle_sample(cfg, frac, seed_layer=i % cfg.layers)
+        if i >= args.warmup:
+            vals.append((s, kv))
+    secs = sum(s for s, _ in vals)
+    kv = sum(k for _, k in vals)
+    value = kv / secs / 1e9
+    ms_per_step = secs / len(vals) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload + " (one layer per step, oracle)", "layers": cfg.layers, "N": cfg.N,
+                   "Hq": cfg.Hq, "Hkv": cfg.Hkv, "d": cfg.d, "T": cfg.T},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- native arm
+def run_native(args, ws, rank, local):
+    import long_context_attention_tree_b300 as ts
+    from long_context_attention_tree_b300.step import SpecStep
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    ts.lib()
+    cfg = workload_config(args.workload)
+    peaks = read_peaks()
+    step = SpecStep(cfg)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    # warm-up
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            step.run(s)
+    s.synchronize()
+
+    # ---- timed region: eager launches on one stream, events around every verify call
+    nL = step.n_layers
+    ev_v = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
+            for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    launches0 = ts.ts_launch_count()
+    with torch.cuda.stream(s):
+        ev0.record(s)
+        for k in range(args.steps):
+            for i in range(nL):
+                ev_v[k][i][0].record(s)
+                step.run_verify(i, s)
+                ev_v[k][i][1].record(s)
+                step.run_refresh(i, s)
+                step.run_draft(i, s)
+            if step.vocab:
+                step.run_vocab(s)
+        ev1.record(s)
+    s.synchronize()
+    launches = ts.ts_launch_count() - launches0
+    torch.cuda.synchronize()
+    barrier(ws)
+    time.sleep(0.2)
+    clk = ClockSampler.summarize(clocks.stop())
+    t_total = ev0.elapsed_time(ev1) / 1e3
+    kv_step = step.kv_bytes_per_step()
+    value_bps, t_max = aggregate(kv_step * args.steps, t_total, ws)
+    ms_per_step = t_max / args.steps * 1e3
+    verify_ms = [ev_v[k][i][0].elapsed_time(ev_v[k][i][1]) for k in range(args.steps) for i in range(nL)]
+    verify_avg_s = statistics.mean(verify_ms) / 1e3
+
+    # ---- dominant kernel roofline: the verify attention call
+    T, Hq, d, N = cfg.T, cfg.Hq, cfg.d, cfg.N
+    flops = 4.0 * T * Hq * N * d
+    kv_layer = cfg.kv_bytes_per_layer()
+    tensor_path = T >= 64 and d == 128 and os.environ.get("TS_FORCE_SIMT", "0") != "1" and \
+        getattr(ts, "TENSOR_PATH", False)
+    if tensor_path:
+        roof = {"bound": "tensor", "achieved": flops / verify_avg_s / 1e12, "peak": peaks["bf16_sus"],
+                "unit": "TFLOP/s", "peak_source": f"bf16 sustained, {peaks['source']}"}
+    else:
+        # CUDA-core fp32 FMA path: 148 SMs x 128 lanes x 2 flop x max SM clock
+        alu_peak = 148 * 128 * 2 * peaks["sm_max"] * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": flops / verify_avg_s / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
+                "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 flop x 2032 MHz"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "ts_tree_attn (verify, T=%d)" % T
+    roof["algorithmic_per_launch"] = {"kv_bytes": kv_layer, "flops": flops}
+    roof["verify_us_per_layer"] = verify_avg_s * 1e6
+    roof["verify_kv_gbs"] = kv_layer / verify_avg_s / 1e9
+    roof["verify_kv_frac_of_hbm"] = kv_layer / verify_avg_s / 1e9 / peaks["hbm"]
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(step, s, args, ws)
+
+    # ---- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if ws == 1 and rank == 0 and not args.no_cpu_baseline:
+        secs, kv, desc, threads = cpu_oracle_sample(cfg, args.cpu_row_fraction)
+        cpu = {"value": kv / secs / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": secs}
+
+    if rank == 0:
+        value = value_bps / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "model_shape": cfg.name, "layers": cfg.layers, "N": N,
+                       "Hq": Hq, "Hkv": cfg.Hkv, "d": d, "T_verify": T, "tree": list(cfg.branching),
+                       "ngram_chains": cfg.n_chains, "budget": cfg.budget, "draft_rows": cfg.draft_rows,
+                       "vocab": cfg.vocab, "parallelism": f"replicas{ws}",
+                       "l2": f"inputs larger than L2 ({kv_step / 1e9:.1f} GB of KV per step)"},
+            "us_per_layer_step": ms_per_step * 1e3 / cfg.layers,
+            "kv_frac_of_hbm_peak": value / ws / peaks["hbm"],
+            "kv_frac_of_hbm_nominal_8tbs": value / ws / 8000.0,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "peaks": peaks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(step, s, args, ws):
+    """Same metric through the public API with host buffers: every step copies
+    that step's inputs (per-layer Q, the batch's own K/V rows, draft Q; logits,
+    history, drafts, parents) from pinned host memory and reads the result back."""
+    cfg = step.cfg
+    N, T = cfg.N, cfg.T
+    host = []
+    h2d = 0
+    for L in step.layers:
+        hq = L.q.cpu().pin_memory()
+        hkt = L.k[:, N:N + T].contiguous().cpu().pin_memory()
+        hvt = L.v[:, N:N + T].contiguous().cpu().pin_memory()
+        hqd = L.q_draft.cpu().pin_memory()
+        host.append((hq, hkt, hvt, hqd))
+        h2d += sum(t.numel() * t.element_size() for t in (hq, hkt, hvt, hqd))
+    hv = None
+    if step.vocab:
+        vi = step.vocab_inputs
+        hv = (vi.logits.cpu().pin_memory(), vi.history.cpu().pin_memory(), vi.draft.cpu().pin_memory(),
+              vi.parent.cpu().pin_memory())
+        h2d += sum(t.numel() * t.element_size() for t in hv)
+        out_h = torch.empty(4 + T, dtype=torch.int32).pin_memory()
+    else:
+        out_h = torch.empty(step.layers[-1].out.numel(), dtype=torch.bfloat16).pin_memory()
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one_step():
+        for i, L in enumerate(step.layers):
+            hq, hkt, hvt, hqd = host[i]
+            L.q.copy_(hq, non_blocking=True)
+            L.k[:, N:N + T].copy_(hkt, non_blocking=True)
+            L.v[:, N:N + T].copy_(hvt, non_blocking=True)
+            L.q_draft.copy_(hqd, non_blocking=True)
+            step.run_layer(i, s)
+        if step.vocab:
+            vi = step.vocab_inputs
+            vi.logits.copy_(hv[0], non_blocking=True)
+            vi.history.copy_(hv[1], non_blocking=True)
+            vi.draft.copy_(hv[2], non_blocking=True)
+            vi.parent.copy_(hv[3], non_blocking=True)
+            step.run_vocab(s)
+            out_h[:4].copy_(step.result, non_blocking=True)
+            out_h[4:].copy_(step.path, non_blocking=True)
+        else:
+            out_h.copy_(step.layers[-1].out.reshape(-1), non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(max(1, min(args.warmup, 2))):
+            one_step()
+    s.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(args.steps):
+            one_step()
+        e1.record(s)
+    s.synchronize()
+    t = e0.elapsed_time(e1) / 1e3
+    val, _ = aggregate(step.kv_bytes_per_step() * args.steps, t, ws)
+    return {"value": val / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": t / args.steps * 1e3}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="qwen14b-100k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-row-fraction", type=float, default=0.25,
+                    help="fraction of verify rows the CPU oracle baseline computes")
+    ap.add_argument("--ref-row-fraction", type=float, default=1.0 / 32,
+                    help="fraction of verify rows per reference-arm step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank)
+        else:
+            run_native(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

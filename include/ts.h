@@ -1,0 +1,191 @@
+/*
+ * ts.h -- C ABI of the TokenSwift attention-side hot path on NVIDIA B300 (sm_103a).
+ *
+ * TokenSwift ("From Hours to Minutes: Lossless Acceleration of Ultra Long
+ * Sequence Generation up to 100K Tokens", ICML 2025) drafts with the target
+ * model over a partial KV cache, verifies a draft tree plus n-gram candidates
+ * against the full KV cache, and keeps the longest draft that exactly matches
+ * the target tokens.  This library implements the per-step work of that loop
+ * that touches the KV cache and the vocabulary:
+ *
+ *   ts_tree_attn             tree-masked GQA attention over a bf16 KV cache
+ *                            (verify pass over the full cache; draft pass over
+ *                            the partial cache), split over the KV length with
+ *                            a log-sum-exp merge, optional fused chunk scores;
+ *   ts_score_chunks          query-key importance of every 64-token KV chunk;
+ *   ts_select_gather         top-k chunks up to the retrieval budget, gathered
+ *                            into a compact partial cache;
+ *   ts_penalty_minp_verify   windowed contextual penalty, temperature, min-p,
+ *                            greedy target and exact-match acceptance.
+ *
+ * Conventions shared by every call:
+ *   - Pointers without a _host suffix are device memory owned by the caller.
+ *     The library never allocates, frees or synchronizes: it validates its
+ *     arguments on the host, enqueues kernels on `stream` and returns.
+ *     Results are valid once the stream has reached that point.
+ *   - bf16 tensors are raw IEEE bfloat16 (uint16 bit patterns).  Every device
+ *     pointer must be 16-byte aligned.
+ *   - Q/O layout [T][Hq][d]; K/V layout [Hkv][ld_kv][d] (row stride d, head
+ *     stride ld_kv*d).  A cache holds N prefix tokens in rows [0, N) and the
+ *     speculative batch's own T rows in [N, N+T), so ld_kv >= N + T.
+ *   - Query head h reads KV head h / (Hq/Hkv)  (grouped-query attention).
+ *   - Validation errors return before anything is enqueued.  Errors that can
+ *     only be seen on the device (a history id outside the vocabulary, a bad
+ *     parent index) are written to a status word, never trapped.
+ *   - Not thread-safe per stream: concurrent calls on different streams are
+ *     fine; ts_last_error() is per host thread.
+ */
+#ifndef TS_H_
+#define TS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ts_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    TS_OK = 0,
+    TS_ERR_INVALID_ARG = 1,  /* bad pointer, size, stride or alignment */
+    TS_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement */
+    TS_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    TS_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up */
+    TS_ERR_DATA = 5          /* bad data found on the device (status word) */
+} ts_status;
+
+/* Message describing the last non-OK status returned on this host thread. */
+const char *ts_last_error(void);
+
+/* Library version string. */
+const char *ts_version(void);
+
+/* Number of kernels this library has launched in this process so far
+ * (all devices, all streams).  Diagnostic; monotonically increasing. */
+uint64_t ts_launch_count(void);
+
+/*
+ * Ancestor-or-self mask of a speculative batch ("How it works": tree-based
+ * attention over the candidate tokens; the n-gram candidates are chains).
+ *   parent_host: int32[T], parent_host[i] = parent row of i, or -1 for a root;
+ *                requires -1 <= parent_host[i] < i (topological order).
+ *   mask_host:   uint64[T][2]; bit u of row i (word u/64, bit u%64) is set
+ *                iff u == i or u is an ancestor of i.
+ *   T in [0, 128].  Host memory only; no CUDA call.
+ * Errors: TS_ERR_INVALID_ARG for a null pointer, T out of range or a parent
+ * index out of order.
+ */
+ts_status ts_tree_mask_from_parents(const int32_t *parent_host, int T, uint64_t *mask_host);
+
+/*
+ * Device workspace (bytes) ts_tree_attn needs for these sizes on the current
+ * device (the split count depends on the SM count).  0 means none.
+ */
+size_t ts_tree_attn_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t N);
+
+/*
+ * Tree-masked grouped-query attention over a bf16 KV cache: the verify pass
+ * ("fed into the LLM with a full KV cache", "How it works") when k/v are the
+ * full cache, and the self-drafting pass when they are the partial cache.
+ *
+ * For batch row t and query head h, with g = h / (Hq/Hkv):
+ *   s_j  = scale * q[t][h] . k[g][j]   over j in [0, N) and j = N+u for every
+ *          u with bit u of mask[t] set;
+ *   out[t][h] = sum_j softmax(s)_j v[g][j]            (bf16, fp32 accumulate)
+ *   lse[t][h] = log sum_j exp(s_j)                     (natural log, fp32)
+ *
+ *   q        bf16 [T][Hq][d]
+ *   k, v     bf16 [Hkv][ld_kv][d], ld_kv >= N + T
+ *   mask     device uint64 [T][2] from ts_tree_mask_from_parents; every row
+ *            must see itself
+ *   out      bf16 [T][Hq][d]
+ *   lse      fp32 [T][Hq] or NULL
+ *   chunk_scores  fp32 [Hkv][ceil(N/64)] or NULL: when given, the chunk
+ *            importance of ts_score_chunks for query row `score_row` is
+ *            produced by the same pass (for bf16 inputs whose products and
+ *            chunk sums are exact in fp32 -- e.g. small integers -- the
+ *            values are identical to ts_score_chunks; otherwise they agree
+ *            up to fp32 summation order).
+ *   workspace at least ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N) bytes,
+ *            or NULL when that is 0.
+ * Supported: d in {64, 128}; Hq % Hkv == 0; Hq/Hkv <= 32; 0 <= T <= 128;
+ * N >= 0; N + T >= 1 when T >= 1.  T >= 64 with d == 128 runs on the tensor
+ * cores (tcgen05, TMEM accumulators); other shapes run on the CUDA cores.
+ * T == 0 is a no-op.
+ */
+ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_kv,
+                       int64_t N, int T, int Hq, int Hkv, int d, float scale,
+                       const uint64_t *mask, void *out, float *lse,
+                       float *chunk_scores, int score_row,
+                       void *workspace, size_t ws_bytes, ts_stream_t stream);
+
+/*
+ * Query-key importance of every KV chunk ("a dynamically updated partial KV
+ * cache ranked by query-key importance", ICML 2025 summary, "Approach"):
+ *   scores[g][c] = max over the query heads h of group g of
+ *                  q_row[h] . sum_{t in chunk c, t < N} k[g][t]     (unscaled fp32)
+ *   q_row   bf16 [Hq][d]   (the scoring query: one row of the verify batch)
+ *   k       bf16 [Hkv][ld_kv][d], ld_kv >= N
+ *   scores  fp32 [Hkv][ceil(N/chunk)]
+ * Supported: chunk == 64, d in {64, 128}, Hq/Hkv <= 32, N >= 0.
+ */
+ts_status ts_score_chunks(const void *q_row, const void *k, int64_t ld_kv, int64_t N,
+                          int Hq, int Hkv, int d, int chunk, float *scores, ts_stream_t stream);
+
+/*
+ * Top-k chunk selection and gather into the compact partial cache
+ * (retrieval budget of the model card's command line, 4096 tokens; the
+ * partial cache the drafting pass reads, "How it works").
+ *   Per KV head g: the k = min(budget_tokens/chunk, ceil(N/chunk)) chunks
+ *   with the largest scores[g][.]; equal scores (-0 equals +0) go to the
+ *   lower chunk index; sel[g][0..k) lists them in ascending order.  Then
+ *     k_part[g][i*chunk + t] = k[g][sel[g][i]*chunk + t]  (same for v)
+ *   for i < k, t < chunk.
+ *   scores  fp32 [Hkv][ceil(N/chunk)], finite
+ *   k, v    bf16 [Hkv][ld_kv][d], ld_kv >= N
+ *   sel     int32 [Hkv][k]
+ *   k_part, v_part  bf16 [Hkv][ld_part][d], ld_part >= k*chunk
+ * Supported: chunk == 64, d in {64, 128}, budget_tokens % chunk == 0,
+ * N % chunk == 0, ceil(N/chunk) <= 16384.
+ */
+ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
+                           const void *k, const void *v, int64_t ld_kv, int d,
+                           int32_t *sel, void *k_part, void *v_part, int64_t ld_part,
+                           ts_stream_t stream);
+
+/*
+ * Vocabulary side of one verification step (model card flags --penalty,
+ * --penalty_length, --min_p, --temperature; "How it works": exact-match
+ * verification, one longest valid draft kept).
+ *   For every batch row i of logits (fp32 [T][V]):
+ *     a token id in history[0..W) (counted once) has l > 0 ? l/theta : l*theta;
+ *     then l / temperature;  m = max;  target[i] = lowest id attaining m;
+ *     kept[i] = #{v : l_v >= m + ln(min_p)}   (min-p: p_v >= min_p * p_max;
+ *     the comparison is exact: ln(min_p) is taken in double on the host and
+ *     m + ln(min_p) rounded up to fp32).
+ *   Then acceptance along the parent forest: row i is accepted iff
+ *     draft[i] == (parent[i] >= 0 ? target[parent[i]] : anchor) and its parent
+ *     is accepted; L = the largest depth (roots have depth 1) of an accepted
+ *     row, best = the lowest such row, bonus = L > 0 ? target[best] : anchor.
+ *   result int32[4] = {L, best (-1 if L == 0), bonus, status}; status is
+ *     TS_OK, or TS_ERR_DATA if a history id is outside [0, V) or a parent
+ *     index is out of order.
+ *   path   int32[T]: rows root..best in path[0..L), -1 after.
+ *   draft, parent: int32 [T] device.  history: int32 [W] device (W >= 0).
+ *   workspace: unused, pass NULL / 0.
+ * Supported: 1 <= T <= 1024, 1 <= V <= 163840, theta > 0, temperature > 0,
+ * 0 <= min_p <= 1.
+ */
+ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_t *history, int W,
+                                 float theta, float min_p, float temperature,
+                                 const int32_t *draft, const int32_t *parent, int32_t anchor,
+                                 int32_t *target, int32_t *kept, int32_t *result, int32_t *path,
+                                 void *workspace, size_t ws_bytes, ts_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TS_H_ */

@@ -1,0 +1,142 @@
+"""B300-native (sm_103a) attention-side hot path of TokenSwift speculative decoding.
+
+The compute lives in the C-ABI library ``libts.so`` (hand-written CUDA, see
+``include/ts.h``); this package is a thin ctypes binding with the same names.
+It marshals torch tensors into raw pointers and the current CUDA stream, and
+raises :class:`TSError` on any non-OK status.  There is no fallback: if the
+library is missing, every call raises.
+
+``workloads`` (seeded synthetic inputs) imports nothing from here.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libts.so")
+
+TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT, TS_ERR_DATA = range(6)
+_STATUS = {0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_UNSUPPORTED", 3: "TS_ERR_CUDA",
+           4: "TS_ERR_TIMEOUT", 5: "TS_ERR_DATA"}
+
+__all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree_attn_workspace_bytes",
+           "ts_launch_count", "ts_tree_attn", "ts_score_chunks", "ts_select_gather", "ts_penalty_minp_verify"]
+
+
+class TSError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libts.so (built in-tree by ``python -m long_context_attention_tree_b300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m long_context_attention_tree_b300.build` (no fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        L.ts_last_error.restype = ctypes.c_char_p
+        L.ts_version.restype = ctypes.c_char_p
+        L.ts_launch_count.restype = ctypes.c_uint64
+        L.ts_tree_mask_from_parents.argtypes = [P, i32, P]
+        L.ts_tree_attn_workspace_bytes.argtypes = [i32, i32, i32, i32, i64]
+        L.ts_tree_attn_workspace_bytes.restype = sz
+        L.ts_tree_attn.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P, sz, P]
+        L.ts_score_chunks.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P, P]
+        L.ts_select_gather.argtypes = [P, i32, i64, i32, i32, P, P, i64, i32, P, P, P, i64, P]
+        L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
+                                             P, P, P, P, P, sz, P]
+        for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_score_chunks", "ts_select_gather",
+                     "ts_penalty_minp_verify"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != TS_OK:
+        raise TSError(status, lib().ts_last_error().decode())
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def ts_version() -> str:
+    return lib().ts_version().decode()
+
+
+def ts_launch_count() -> int:
+    """Kernels the library has launched so far in this process."""
+    return int(lib().ts_launch_count())
+
+
+def ts_tree_mask_from_parents(parent) -> np.ndarray:
+    """uint64 [T][2] ancestor-or-self mask (host)."""
+    p = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+    T = p.size
+    mask = np.zeros((max(T, 1), 2), dtype=np.uint64)
+    _check(lib().ts_tree_mask_from_parents(p.ctypes.data_as(ctypes.c_void_p), T,
+                                           mask.ctypes.data_as(ctypes.c_void_p)))
+    return mask[:T]
+
+
+def ts_tree_attn_workspace_bytes(T: int, Hq: int, Hkv: int, d: int, N: int) -> int:
+    return int(lib().ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N))
+
+
+def ts_tree_attn(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_row: int = 0,
+                 workspace=None, scale: Optional[float] = None, stream=None) -> None:
+    """Tree-masked GQA attention.  q [T][Hq][d], k/v [Hkv][ld][d] (bf16, CUDA),
+    mask uint64 [T][2] (CUDA), out bf16 [T][Hq][d]; lse fp32 [T][Hq] optional;
+    chunk_scores fp32 [Hkv][ceil(N/64)] optional; workspace uint8 CUDA tensor."""
+    T, Hq, d = q.shape
+    Hkv, ld, _ = k.shape
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ts_tree_attn(_ptr(q), _ptr(k), _ptr(v), ld, N, T, Hq, Hkv, d, scale, _ptr(mask), _ptr(out),
+                              _ptr(lse), _ptr(chunk_scores), score_row, _ptr(workspace), ws_bytes,
+                              _stream(stream)))
+
+
+def ts_score_chunks(q_row, k, N: int, scores, chunk: int = 64, stream=None) -> None:
+    Hq, d = q_row.shape
+    Hkv, ld, _ = k.shape
+    _check(lib().ts_score_chunks(_ptr(q_row), _ptr(k), ld, N, Hq, Hkv, d, chunk, _ptr(scores), _stream(stream)))
+
+
+def ts_select_gather(scores, N: int, budget_tokens: int, k, v, sel, k_part, v_part, chunk: int = 64,
+                     stream=None) -> None:
+    Hkv, ld, d = k.shape
+    ld_part = k_part.shape[1]
+    _check(lib().ts_select_gather(_ptr(scores), Hkv, N, budget_tokens, chunk, _ptr(k), _ptr(v), ld, d,
+                                  _ptr(sel), _ptr(k_part), _ptr(v_part), ld_part, _stream(stream)))
+
+
+def ts_penalty_minp_verify(logits, history, theta: float, min_p: float, temperature: float, draft, parent,
+                           anchor: int, target, kept, result, path, stream=None) -> None:
+    T, V = logits.shape
+    W = 0 if history is None else history.numel()
+    _check(lib().ts_penalty_minp_verify(_ptr(logits), T, V, _ptr(history) if W else None, W, theta, min_p,
+                                        temperature, _ptr(draft), _ptr(parent), int(anchor), _ptr(target),
+                                        _ptr(kept), _ptr(result), _ptr(path), None, 0, _stream(stream)))

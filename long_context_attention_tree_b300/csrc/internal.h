@@ -1,0 +1,73 @@
+// Internal launch interface between the C ABI (ts_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ts {
+
+// Counts every kernel launch the library enqueues (diagnostic).
+void note_launches(int n);
+
+struct AttnArgs {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k;
+    const __nv_bfloat16 *v;
+    int64_t ld_kv;
+    int64_t N;
+    int T, Hq, Hkv, G, d;
+    float scale_log2;  // softmax scale * log2(e)
+    const uint64_t *mask;
+    __nv_bfloat16 *out;
+    float *lse;
+    float *chunk_scores;  // nullable
+    int score_row;
+    int n_chunks;         // ceil(N / 64)
+    float *ws_o;          // [splits][T][Hq][d] unnormalised partial outputs
+    float *ws_ml;         // [splits][T][Hq] (m, l) pairs, log2 domain
+    // plan
+    int splits, tiles_per_split, n_tiles, tpb;
+};
+
+struct MergeArgs {
+    const float *ws_o;
+    const float *ws_ml;
+    __nv_bfloat16 *out;
+    float *lse;
+    int T, Hq, splits;
+};
+
+struct SimtPlan {
+    int rb, tpb, n_rb, n_tiles, splits, tiles_per_split;
+};
+
+SimtPlan simt_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms);
+cudaError_t launch_tree_attn_simt(const AttnArgs &a, const SimtPlan &p, cudaStream_t st);
+cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st);
+
+// chunk scoring / selection / gather
+cudaError_t launch_score_chunks(const __nv_bfloat16 *q_row, const __nv_bfloat16 *k, int64_t ld_kv, int64_t N,
+                                int Hq, int Hkv, int d, float *scores, cudaStream_t st);
+cudaError_t launch_select_gather(const float *scores, int Hkv, int n_chunks, int k_sel,
+                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
+                                 int32_t *sel, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part, int64_t ld_part,
+                                 int num_sms, cudaStream_t st);
+
+// vocab stage
+struct VocabArgs {
+    const float *logits;
+    int T, V;
+    const int32_t *history;
+    int W;
+    float theta, temperature;
+    double log_min_p;
+    const int32_t *draft;
+    const int32_t *parent;
+    int32_t anchor;
+    int32_t *target, *kept, *result, *path;
+};
+cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st);
+
+}  // namespace ts

@@ -1,0 +1,285 @@
+// Dynamic partial-KV-cache maintenance: chunk importance, top-k selection up
+// to the retrieval budget, and the gather into the compact partial cache
+// (TokenSwift ICML 2025 summary, "Approach": "a dynamically updated partial KV
+// cache ranked by query-key importance"; model card: retrieval budget 4096).
+#include "internal.h"
+#include "ts_common.cuh"
+
+namespace ts {
+
+constexpr int CHUNK = 64;
+
+// ---------------------------------------------------------------------------
+// Standalone chunk scoring: score[g][c] = max_{h in g} q_h . sum_{t in c} K[g][t].
+// CTA = (CPB consecutive chunks, KV head).  128 threads: 16 lanes x 16 bytes
+// cover one 128-dim bf16 row, 8 rows in flight; column sums reduce in smem.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128)
+score_chunks_kernel(const __nv_bfloat16 *__restrict__ q_row, const __nv_bfloat16 *__restrict__ k,
+                    int64_t ld_kv, int64_t N, int Hq, int G, int n_chunks, int cpb, float *__restrict__ scores) {
+    constexpr int LPR = D / 8;             // 16-byte lanes per row
+    constexpr int RIF = 128 / LPR;         // rows in flight
+    __shared__ float part[RIF][D];
+    __shared__ float ksum[D];
+    __shared__ float hmax[32];
+    const int g = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int lane16 = tid % LPR, rr = tid / LPR;
+    const __nv_bfloat16 *kh = k + (size_t)g * ld_kv * D;
+    for (int cc = 0; cc < cpb; ++cc) {
+        const int c = blockIdx.x * cpb + cc;
+        if (c >= n_chunks) break;
+        const int64_t t0 = (int64_t)c * CHUNK;
+        const int64_t t1 = (t0 + CHUNK < N) ? t0 + CHUNK : N;
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int64_t t = t0 + rr; t < t1; t += RIF) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(kh + (size_t)t * D + lane16 * 8);
+            acc[0] += bf16_lo(w.x); acc[1] += bf16_hi(w.x); acc[2] += bf16_lo(w.y); acc[3] += bf16_hi(w.y);
+            acc[4] += bf16_lo(w.z); acc[5] += bf16_hi(w.z); acc[6] += bf16_lo(w.w); acc[7] += bf16_hi(w.w);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part[rr][lane16 * 8 + e] = acc[e];
+        __syncthreads();
+        for (int e = tid; e < D; e += 128) {
+            float s = 0.f;
+#pragma unroll
+            for (int r = 0; r < RIF; ++r) s += part[r][e];
+            ksum[e] = s;
+        }
+        __syncthreads();
+        // one warp per query head of the group (4 warps stride over G <= 32)
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int j = warp; j < G; j += 4) {
+            const __nv_bfloat16 *qh = q_row + (size_t)(g * G + j) * D;
+            float dot = 0.f;
+            for (int e = lane; e < D; e += 32) dot = fmaf(__bfloat162float(qh[e]), ksum[e], dot);
+            dot = warp_sum(dot);
+            if (lane == 0) hmax[j] = dot;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float best = hmax[0];
+            for (int j = 1; j < G; ++j) best = fmaxf(best, hmax[j]);
+            scores[(size_t)g * n_chunks + c] = best;
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_score_chunks(const __nv_bfloat16 *q_row, const __nv_bfloat16 *k, int64_t ld_kv, int64_t N,
+                                int Hq, int Hkv, int d, float *scores, cudaStream_t st) {
+    const int nc = (int)((N + CHUNK - 1) / CHUNK);
+    if (nc == 0) return cudaSuccess;
+    const int cpb = 4;
+    dim3 grid((nc + cpb - 1) / cpb, Hkv);
+    const int G = Hq / Hkv;
+    if (d == 128)
+        score_chunks_kernel<128><<<grid, 128, 0, st>>>(q_row, k, ld_kv, N, Hq, G, nc, cpb, scores);
+    else
+        score_chunks_kernel<64><<<grid, 128, 0, st>>>(q_row, k, ld_kv, N, Hq, G, nc, cpb, scores);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Top-k selection (radix select on order-preserving keys) + gather.
+// CTA = (part p, KV head g).  Every CTA of a head computes the same selection
+// from the head's scores (a few KB, L2-resident), then copies its share of the
+// selected chunks.  Part 0 also writes sel[g][.].
+// ---------------------------------------------------------------------------
+constexpr int SG_THREADS = 512;
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+    x = x + 0.0f;  // -0 -> +0 (round-to-nearest), so equal values get equal keys
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive block scan of one int per thread; returns the prefix, writes the total.
+__device__ int block_exclusive_scan(int x, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int w = lane < nw ? warp_tot[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        if (lane < nw) warp_tot[lane] = wi - w;  // exclusive warp offsets
+        if (lane == nw - 1) *total = wi;
+    }
+    __syncthreads();
+    const int r = warp_tot[warp] + incl - x;
+    __syncthreads();
+    return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(SG_THREADS)
+select_gather_kernel(const float *__restrict__ scores, int n_chunks, int k_sel,
+                     const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v, int64_t ld_kv,
+                     int32_t *__restrict__ sel, __nv_bfloat16 *__restrict__ k_part,
+                     __nv_bfloat16 *__restrict__ v_part, int64_t ld_part, int chunks_per_part) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw);          // [n_chunks]
+    int32_t *list = reinterpret_cast<int32_t *>(keys + n_chunks);     // [k_sel]
+    __shared__ int hist[256];
+    __shared__ int warp_tot[32];
+    __shared__ int s_total;
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_remaining;
+
+    const int g = blockIdx.y, p = blockIdx.x, tid = threadIdx.x;
+    const float *sc = scores + (size_t)g * n_chunks;
+    for (int c = tid; c < n_chunks; c += SG_THREADS) keys[c] = order_key(sc[c]);
+    for (int i = tid; i < k_sel; i += SG_THREADS) list[i] = 0;
+    if (tid == 0) {
+        s_prefix = 0u;
+        s_remaining = k_sel;
+    }
+    __syncthreads();
+
+    // --- radix select of the k-th largest key, 8 bits at a time from the top
+    uint32_t pmask = 0u;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += SG_THREADS) hist[b] = 0;
+        __syncthreads();
+        const uint32_t prefix = s_prefix;
+        for (int c = tid; c < n_chunks; c += SG_THREADS) {
+            const uint32_t key = keys[c];
+            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // lane L owns digits 255-8L .. 248-8L (descending)
+            int cnt[8];
+            int lsum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cnt[i] = hist[255 - 8 * tid - i];
+                lsum += cnt[i];
+            }
+            int incl = lsum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            const int excl = incl - lsum;
+            const int rem = s_remaining;
+            const bool here = excl < rem && incl >= rem;
+            const unsigned who = __ballot_sync(0xffffffffu, here);
+            if (here) {
+                int cum = excl;
+                int digit = 255 - 8 * tid;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (cum + cnt[i] >= rem) {
+                        digit = 255 - 8 * tid - i;
+                        break;
+                    }
+                    cum += cnt[i];
+                }
+                s_prefix = prefix | ((uint32_t)digit << shift);
+                s_remaining = rem - cum;
+            }
+            (void)who;
+        }
+        __syncthreads();
+        pmask |= 255u << shift;
+    }
+    const uint32_t kth = s_prefix;   // k-th largest key
+    const int need_eq = s_remaining; // how many keys equal to kth are taken (lowest indices)
+
+    // --- flags in index order: key > kth, or key == kth among the first need_eq equals
+    const int per = (n_chunks + SG_THREADS - 1) / SG_THREADS;
+    const int c_begin = min(n_chunks, tid * per), c_end = min(n_chunks, c_begin + per);
+    int eq_local = 0;
+    for (int c = c_begin; c < c_end; ++c) eq_local += keys[c] == kth;
+    int eq_before = block_exclusive_scan(eq_local, warp_tot, &s_total);
+    int sel_local = 0;
+    {
+        int e = eq_before;
+        for (int c = c_begin; c < c_end; ++c) {
+            const uint32_t key = keys[c];
+            if (key > kth) ++sel_local;
+            else if (key == kth) { if (e < need_eq) ++sel_local; ++e; }
+        }
+    }
+    int pos = block_exclusive_scan(sel_local, warp_tot, &s_total);
+    {
+        int e = eq_before;
+        for (int c = c_begin; c < c_end; ++c) {
+            const uint32_t key = keys[c];
+            bool take = false;
+            if (key > kth) take = true;
+            else if (key == kth) { take = e < need_eq; ++e; }
+            if (take) {
+                if (pos < k_sel) {  // exactly k_sel are taken; the guard only bounds the writes
+                    list[pos] = c;
+                    if (p == 0) sel[(size_t)g * k_sel + pos] = c;
+                }
+                ++pos;
+            }
+        }
+    }
+    __syncthreads();
+
+    // --- gather this part's chunks (K then V), 16 bytes per thread per step
+    constexpr int U = D / 8;  // 16-byte units per row
+    const int i0 = p * chunks_per_part, i1 = min(k_sel, i0 + chunks_per_part);
+    const __nv_bfloat16 *kh = k + (size_t)g * ld_kv * D;
+    const __nv_bfloat16 *vh = v + (size_t)g * ld_kv * D;
+    __nv_bfloat16 *kp = k_part + (size_t)g * ld_part * D;
+    __nv_bfloat16 *vp = v_part + (size_t)g * ld_part * D;
+    for (int i = i0; i < i1; ++i) {
+        const int c = min(max(list[i], 0), n_chunks - 1);
+        const size_t src_row = (size_t)c * CHUNK, dst_row = (size_t)i * CHUNK;
+        for (int e = tid; e < CHUNK * U; e += SG_THREADS) {
+            const int r = e / U, u = e % U;
+            const uint4 wk = *reinterpret_cast<const uint4 *>(kh + (src_row + r) * D + u * 8);
+            const uint4 wv = *reinterpret_cast<const uint4 *>(vh + (src_row + r) * D + u * 8);
+            *reinterpret_cast<uint4 *>(kp + (dst_row + r) * D + u * 8) = wk;
+            *reinterpret_cast<uint4 *>(vp + (dst_row + r) * D + u * 8) = wv;
+        }
+    }
+}
+
+cudaError_t launch_select_gather(const float *scores, int Hkv, int n_chunks, int k_sel,
+                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
+                                 int32_t *sel, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part, int64_t ld_part,
+                                 int num_sms, cudaStream_t st) {
+    if (k_sel <= 0 || n_chunks <= 0) return cudaSuccess;
+    int parts = (2 * num_sms + Hkv - 1) / Hkv;
+    if (parts > k_sel) parts = k_sel;
+    if (parts < 1) parts = 1;
+    const int cpp = (k_sel + parts - 1) / parts;
+    parts = (k_sel + cpp - 1) / cpp;
+    const size_t smem = sizeof(uint32_t) * (size_t)n_chunks + sizeof(int32_t) * (size_t)k_sel;
+    dim3 grid(parts, Hkv);
+    cudaError_t e;
+    if (d == 128) {
+        e = cudaFuncSetAttribute(select_gather_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        select_gather_kernel<128><<<grid, SG_THREADS, smem, st>>>(scores, n_chunks, k_sel, k, v, ld_kv, sel,
+                                                                  k_part, v_part, ld_part, cpp);
+    } else {
+        e = cudaFuncSetAttribute(select_gather_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        select_gather_kernel<64><<<grid, SG_THREADS, smem, st>>>(scores, n_chunks, k_sel, k, v, ld_kv, sel,
+                                                                 k_part, v_part, ld_part, cpp);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ts

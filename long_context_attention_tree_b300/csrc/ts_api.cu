@@ -1,0 +1,274 @@
+// C ABI of the ts library: argument validation, planning and kernel launch.
+// Every entry point validates on the host and returns before enqueuing
+// anything when an argument is wrong; nothing here allocates, frees or
+// synchronizes.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "../../include/ts.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+ts_status fail(ts_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+ts_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(TS_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+
+// SM count of the current device (148 on B300); cached per device.
+int num_sms() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 148;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 148;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool force_simt() {
+    const char *e = getenv("TS_FORCE_SIMT");
+    return e != nullptr && e[0] == '1';
+}
+
+ts_status check_attn_shape(int T, int Hq, int Hkv, int d, int64_t N) {
+    if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+        return fail(TS_ERR_INVALID_ARG, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+    if (Hq / Hkv > 32) return fail(TS_ERR_UNSUPPORTED, "group size Hq/Hkv=%d > 32", Hq / Hkv);
+    if (T < 0 || T > 128) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [0, 128]", T);
+    if (N < 0) return fail(TS_ERR_INVALID_ARG, "N=%lld < 0", (long long)N);
+    if (N > (int64_t)1 << 30) return fail(TS_ERR_UNSUPPORTED, "N=%lld too large", (long long)N);
+    return TS_OK;
+}
+
+}  // namespace
+
+namespace ts {
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace ts
+
+extern "C" {
+
+uint64_t ts_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *ts_last_error(void) { return g_last_error.c_str(); }
+
+const char *ts_version(void) { return "ts 0.1 (sm_103a)"; }
+
+ts_status ts_tree_mask_from_parents(const int32_t *parent_host, int T, uint64_t *mask_host) {
+    if (T < 0 || T > 128) return fail(TS_ERR_INVALID_ARG, "T=%d outside [0, 128]", T);
+    if (T > 0 && (parent_host == nullptr || mask_host == nullptr))
+        return fail(TS_ERR_INVALID_ARG, "null parent or mask pointer");
+    for (int i = 0; i < T; ++i)
+        if (parent_host[i] < -1 || parent_host[i] >= i)
+            return fail(TS_ERR_INVALID_ARG, "parent[%d]=%d must satisfy -1 <= parent[i] < i", i, parent_host[i]);
+    for (int i = 0; i < T; ++i) {
+        // a row's ancestors are its parent's ancestors plus the parent itself
+        uint64_t w0 = 0, w1 = 0;
+        const int p = parent_host[i];
+        if (p >= 0) {
+            w0 = mask_host[2 * p];
+            w1 = mask_host[2 * p + 1];
+        }
+        if (i < 64) w0 |= 1ull << i; else w1 |= 1ull << (i - 64);
+        mask_host[2 * i] = w0;
+        mask_host[2 * i + 1] = w1;
+    }
+    return TS_OK;
+}
+
+size_t ts_tree_attn_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t N) {
+    if (check_attn_shape(T, Hq, Hkv, d, N) != TS_OK || T == 0) return 0;
+    const ts::SimtPlan p = ts::simt_plan(T, Hq, Hkv, d, N, num_sms());
+    if (p.splits <= 1) return 0;
+    return (size_t)p.splits * T * Hq * ((size_t)d + 2) * sizeof(float);
+}
+
+ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_kv,
+                       int64_t N, int T, int Hq, int Hkv, int d, float scale,
+                       const uint64_t *mask, void *out, float *lse,
+                       float *chunk_scores, int score_row,
+                       void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    ts_status st = check_attn_shape(T, Hq, Hkv, d, N);
+    if (st != TS_OK) return st;
+    if (T == 0) return TS_OK;
+    if (!q || !k || !v || !mask || !out) return fail(TS_ERR_INVALID_ARG, "null q/k/v/mask/out");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(TS_ERR_INVALID_ARG, "q/k/v/out must be 16-byte aligned");
+    if (!aligned4(mask) || (lse && !aligned4(lse)) || (chunk_scores && !aligned4(chunk_scores)))
+        return fail(TS_ERR_INVALID_ARG, "mask/lse/chunk_scores misaligned");
+    if (ld_kv < N + T) return fail(TS_ERR_INVALID_ARG, "ld_kv=%lld < N+T=%lld", (long long)ld_kv, (long long)(N + T));
+    if (!(scale > 0.f) || !isfinite(scale)) return fail(TS_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (chunk_scores && (score_row < 0 || score_row >= T))
+        return fail(TS_ERR_INVALID_ARG, "score_row=%d outside [0, T=%d)", score_row, T);
+
+    const int sms = num_sms();
+    const ts::SimtPlan p = ts::simt_plan(T, Hq, Hkv, d, N, sms);
+    const size_t need = p.splits > 1 ? (size_t)p.splits * T * Hq * ((size_t)d + 2) * sizeof(float) : 0;
+    if (need > 0 && (workspace == nullptr || ws_bytes < need))
+        return fail(TS_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if (need > 0 && !aligned16(workspace)) return fail(TS_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+
+    ts::AttnArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k = static_cast<const __nv_bfloat16 *>(k);
+    a.v = static_cast<const __nv_bfloat16 *>(v);
+    a.ld_kv = ld_kv;
+    a.N = N;
+    a.T = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.d = d;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.mask = mask;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.lse = lse;
+    a.chunk_scores = chunk_scores;
+    a.score_row = score_row;
+    a.n_chunks = (int)((N + 63) / 64);
+    a.ws_o = static_cast<float *>(workspace);
+    a.ws_ml = need > 0 ? a.ws_o + (size_t)p.splits * T * Hq * d : nullptr;
+    a.splits = p.splits;
+    a.tiles_per_split = p.tiles_per_split;
+    a.n_tiles = p.n_tiles;
+    a.tpb = p.tpb;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = ts::launch_tree_attn_simt(a, p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tree_attn_simt launch");
+    ts::note_launches(1);
+    if (p.splits > 1) {
+        ts::MergeArgs m{a.ws_o, a.ws_ml, a.out, a.lse, T, Hq, p.splits};
+        e = ts::launch_lse_merge(m, d, s);
+        if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
+        ts::note_launches(1);
+    }
+    return TS_OK;
+}
+
+ts_status ts_score_chunks(const void *q_row, const void *k, int64_t ld_kv, int64_t N,
+                          int Hq, int Hkv, int d, int chunk, float *scores, ts_stream_t stream) {
+    if (chunk != 64) return fail(TS_ERR_UNSUPPORTED, "chunk=%d (supported: 64)", chunk);
+    ts_status st = check_attn_shape(1, Hq, Hkv, d, N);
+    if (st != TS_OK) return st;
+    if (N == 0) return TS_OK;
+    if (!q_row || !k || !scores) return fail(TS_ERR_INVALID_ARG, "null q_row/k/scores");
+    if (!aligned16(q_row) || !aligned16(k) || !aligned4(scores))
+        return fail(TS_ERR_INVALID_ARG, "q_row/k must be 16-byte aligned, scores 4-byte aligned");
+    if (ld_kv < N) return fail(TS_ERR_INVALID_ARG, "ld_kv < N");
+    cudaError_t e = ts::launch_score_chunks(static_cast<const __nv_bfloat16 *>(q_row),
+                                            static_cast<const __nv_bfloat16 *>(k), ld_kv, N, Hq, Hkv, d, scores,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "score_chunks launch");
+    ts::note_launches(1);
+    return TS_OK;
+}
+
+ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
+                           const void *k, const void *v, int64_t ld_kv, int d,
+                           int32_t *sel, void *k_part, void *v_part, int64_t ld_part,
+                           ts_stream_t stream) {
+    if (chunk != 64) return fail(TS_ERR_UNSUPPORTED, "chunk=%d (supported: 64)", chunk);
+    if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    if (Hkv <= 0) return fail(TS_ERR_INVALID_ARG, "Hkv=%d", Hkv);
+    if (N < 0 || budget_tokens < 0) return fail(TS_ERR_INVALID_ARG, "negative N or budget");
+    if (budget_tokens % chunk) return fail(TS_ERR_INVALID_ARG, "budget %d not a multiple of chunk", budget_tokens);
+    if (N % chunk) return fail(TS_ERR_UNSUPPORTED, "N=%lld not a multiple of the chunk", (long long)N);
+    const int64_t nc = N / chunk;
+    if (nc > 16384) return fail(TS_ERR_UNSUPPORTED, "%lld chunks > 16384", (long long)nc);
+    const int k_sel = (int)((int64_t)(budget_tokens / chunk) < nc ? budget_tokens / chunk : nc);
+    if (k_sel == 0) return TS_OK;
+    if (!scores || !k || !v || !sel || !k_part || !v_part) return fail(TS_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_part) || !aligned16(v_part) || !aligned4(scores) ||
+        !aligned4(sel))
+        return fail(TS_ERR_INVALID_ARG, "misaligned pointer");
+    if (ld_kv < N) return fail(TS_ERR_INVALID_ARG, "ld_kv < N");
+    if (ld_part < (int64_t)k_sel * chunk)
+        return fail(TS_ERR_INVALID_ARG, "ld_part=%lld < k*chunk=%lld", (long long)ld_part, (long long)k_sel * chunk);
+    cudaError_t e = ts::launch_select_gather(scores, Hkv, (int)nc, k_sel, static_cast<const __nv_bfloat16 *>(k),
+                                             static_cast<const __nv_bfloat16 *>(v), ld_kv, d, sel,
+                                             static_cast<__nv_bfloat16 *>(k_part),
+                                             static_cast<__nv_bfloat16 *>(v_part), ld_part, num_sms(),
+                                             reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "select_gather launch");
+    ts::note_launches(1);
+    return TS_OK;
+}
+
+ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_t *history, int W,
+                                 float theta, float min_p, float temperature,
+                                 const int32_t *draft, const int32_t *parent, int32_t anchor,
+                                 int32_t *target, int32_t *kept, int32_t *result, int32_t *path,
+                                 void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    if (T < 1 || T > 1024) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [1, 1024]", T);
+    if (V < 1 || V > 163840) return fail(TS_ERR_UNSUPPORTED, "V=%d outside [1, 163840]", V);
+    if (W < 0) return fail(TS_ERR_INVALID_ARG, "W=%d < 0", W);
+    if (!(theta > 0.f) || !isfinite(theta)) return fail(TS_ERR_INVALID_ARG, "theta must be finite and > 0");
+    if (!(temperature > 0.f) || !isfinite(temperature))
+        return fail(TS_ERR_INVALID_ARG, "temperature must be finite and > 0");
+    if (!(min_p >= 0.f && min_p <= 1.f)) return fail(TS_ERR_INVALID_ARG, "min_p outside [0, 1]");
+    if (!logits || !draft || !parent || !target || !kept || !result || !path || (W > 0 && !history))
+        return fail(TS_ERR_INVALID_ARG, "null pointer");
+    if (!aligned4(logits) || !aligned4(draft) || !aligned4(parent) || !aligned4(target) || !aligned4(kept) ||
+        !aligned4(result) || !aligned4(path) || (history && !aligned4(history)))
+        return fail(TS_ERR_INVALID_ARG, "misaligned pointer");
+    ts::VocabArgs a{};
+    a.logits = logits;
+    a.T = T;
+    a.V = V;
+    a.history = history;
+    a.W = W;
+    a.theta = theta;
+    a.temperature = temperature;
+    // ln(min_p) in double on the host; the kernel compares against m + ln(min_p)
+    a.log_min_p = min_p > 0.f ? log((double)min_p) : -INFINITY;
+    a.draft = draft;
+    a.parent = parent;
+    a.anchor = anchor;
+    a.target = target;
+    a.kept = kept;
+    a.result = result;
+    a.path = path;
+    cudaError_t e = ts::launch_vocab(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "vocab launch");
+    ts::note_launches(2);
+    return TS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,200 @@
+// Vocabulary side of one TokenSwift verification step: windowed contextual
+// penalty, temperature, min-p, greedy target, and exact-match acceptance
+// along the draft tree / n-gram paths.
+//   model card, "Example using TokenSwift command line": --penalty 1.2
+//     --penalty_length 1024 --min_p 0.1 --temperature 1.0;
+//   tool listing, "How it works": drafts are accepted when they exactly match
+//     the target tokens, and one of the longest valid drafts is kept.
+//
+// Row pass: one thread-block cluster of VOCAB_CLUSTER CTAs per batch row; each
+// CTA owns a contiguous slice of the vocabulary, holds it in registers, and
+// the CTAs exchange (max, argmax) and then the min-p counts through
+// distributed shared memory.  The logits are read from HBM exactly once.
+#include <cooperative_groups.h>
+
+#include "internal.h"
+#include "ts_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace ts {
+
+constexpr int VOCAB_CLUSTER = 8;
+constexpr int VOCAB_THREADS = 512;
+constexpr int VOCAB_CACHE = 40;                     // register-resident logits per thread
+constexpr int VOCAB_MAX_SLICE = VOCAB_THREADS * VOCAB_CACHE;  // 20480
+constexpr int VOCAB_BITMAP_WORDS = VOCAB_MAX_SLICE / 32;
+
+struct ArgMax {
+    float v;
+    int i;
+};
+__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
+    // larger value wins; equal values: lower index wins; index -1 = empty
+    if (a.i < 0) return b;
+    if (b.i < 0) return a;
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+    return a;
+}
+
+__global__ void __cluster_dims__(VOCAB_CLUSTER, 1, 1) __launch_bounds__(VOCAB_THREADS)
+penalty_minp_kernel(const VocabArgs a, int slice) {
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ uint32_t bitmap[VOCAB_BITMAP_WORDS];
+    __shared__ ArgMax warp_best[VOCAB_THREADS / 32];
+    __shared__ ArgMax cta_best;
+    __shared__ int warp_cnt[VOCAB_THREADS / 32];
+    __shared__ int cta_cnt;
+
+    const int row = blockIdx.y;
+    const unsigned rank = cluster.block_rank();
+    const int v0 = (int)rank * slice;
+    const int v1 = min(a.V, v0 + slice);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // window bitmap restricted to this slice (ids outside [0, V) are ignored
+    // here; the acceptance kernel reports them)
+    for (int w = tid; w < VOCAB_BITMAP_WORDS; w += VOCAB_THREADS) bitmap[w] = 0u;
+    __syncthreads();
+    for (int w = tid; w < a.W; w += VOCAB_THREADS) {
+        const int id = a.history[w];
+        if (id >= v0 && id < v1) atomicOr(&bitmap[(id - v0) >> 5], 1u << ((id - v0) & 31));
+    }
+    __syncthreads();
+
+    const float *lrow = a.logits + (size_t)row * a.V;
+    float x[VOCAB_CACHE];
+    ArgMax best{-INFINITY, -1};
+#pragma unroll
+    for (int i = 0; i < VOCAB_CACHE; ++i) {
+        const int vv = v0 + i * VOCAB_THREADS + tid;
+        float l = -INFINITY;
+        if (vv < v1) {
+            l = __ldcs(lrow + vv);
+            const int o = vv - v0;
+            if ((bitmap[o >> 5] >> (o & 31)) & 1u) l = l > 0.f ? __fdiv_rn(l, a.theta) : __fmul_rn(l, a.theta);
+            l = __fdiv_rn(l, a.temperature);
+            best = better(best, ArgMax{l, vv});
+        }
+        x[i] = l;
+    }
+    // block (max, argmax)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ArgMax other{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.i, o)};
+        best = better(best, other);
+    }
+    if (lane == 0) warp_best[warp] = best;
+    __syncthreads();
+    if (tid == 0) {
+        ArgMax b = warp_best[0];
+        for (int w = 1; w < VOCAB_THREADS / 32; ++w) b = better(b, warp_best[w]);
+        cta_best = b;
+    }
+    cluster.sync();
+    // every CTA reduces the cluster's candidates in rank order
+    ArgMax gbest{-INFINITY, -1};
+    for (int r = 0; r < VOCAB_CLUSTER; ++r) {
+        const ArgMax *rb = cluster.map_shared_rank(&cta_best, r);
+        gbest = better(gbest, *rb);
+    }
+    // min-p threshold: smallest fp32 >= m + ln(min_p) (exact comparison)
+    const double thr = (double)gbest.v + a.log_min_p;
+    const float f = __double2float_ru(thr);
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < VOCAB_CACHE; ++i) {
+        const int vv = v0 + i * VOCAB_THREADS + tid;
+        if (vv < v1 && x[i] >= f) ++cnt;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) warp_cnt[warp] = cnt;
+    __syncthreads();
+    if (tid == 0) {
+        int c = 0;
+        for (int w = 0; w < VOCAB_THREADS / 32; ++w) c += warp_cnt[w];
+        cta_cnt = c;
+    }
+    cluster.sync();
+    if (rank == 0 && tid == 0) {
+        int total = 0;
+        for (int r = 0; r < VOCAB_CLUSTER; ++r) total += *cluster.map_shared_rank(&cta_cnt, r);
+        a.target[row] = gbest.i;
+        a.kept[row] = total;
+    }
+    cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
+}
+
+// Acceptance: one CTA, one thread per batch row walking its (short) ancestor
+// chain; the longest accepted depth wins, ties to the lowest row.
+__global__ void __launch_bounds__(1024) accept_kernel(const VocabArgs a) {
+    __shared__ int s_parent[1024];
+    __shared__ int s_target[1024];
+    __shared__ int s_draft[1024];
+    __shared__ int s_bad;
+    __shared__ int s_key;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_bad = 0;
+        s_key = -1;
+    }
+    __syncthreads();
+    for (int i = tid; i < a.T; i += blockDim.x) {
+        const int p = a.parent[i];
+        s_parent[i] = p;
+        s_target[i] = a.target[i];
+        s_draft[i] = a.draft[i];
+        if (p < -1 || p >= i) atomicOr(&s_bad, 1);
+        a.path[i] = -1;
+    }
+    for (int w = tid; w < a.W; w += blockDim.x) {
+        const int id = a.history[w];
+        if (id < 0 || id >= a.V) atomicOr(&s_bad, 2);
+    }
+    __syncthreads();
+    if (s_bad & 1) {  // a bad parent array: report, accept nothing
+        if (tid == 0) {
+            a.result[0] = 0; a.result[1] = -1; a.result[2] = a.anchor; a.result[3] = 5;  // TS_ERR_DATA
+        }
+        return;
+    }
+    for (int i = tid; i < a.T; i += blockDim.x) {
+        bool ok = true;
+        int depth = 0;
+        // parent[n] < n strictly, so the walk ends within i+1 steps
+        for (int n = i; n >= 0; n = s_parent[n]) {
+            const int pn = s_parent[n];
+            const int expected = pn >= 0 ? s_target[pn] : a.anchor;
+            ok = ok && (s_draft[n] == expected);
+            ++depth;
+        }
+        if (ok) atomicMax(&s_key, (depth << 16) | (0xffff - i));
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int key = s_key;
+        const int L = key < 0 ? 0 : (key >> 16);
+        const int best = key < 0 ? -1 : 0xffff - (key & 0xffff);
+        a.result[0] = L;
+        a.result[1] = best;
+        a.result[2] = L > 0 ? s_target[best] : a.anchor;
+        a.result[3] = (s_bad & 2) ? 5 : 0;
+        int pos = L - 1;
+        for (int n = best; n >= 0 && pos >= 0; n = s_parent[n], --pos) a.path[pos] = n;
+    }
+}
+
+cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st) {
+    int slice = (a.V + VOCAB_CLUSTER - 1) / VOCAB_CLUSTER;
+    slice = (slice + 31) & ~31;
+    if (slice > VOCAB_MAX_SLICE) return cudaErrorInvalidValue;
+    dim3 grid(VOCAB_CLUSTER, a.T);
+    penalty_minp_kernel<<<grid, VOCAB_THREADS, 0, st>>>(a, slice);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    accept_kernel<<<1, 1024, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ts

@@ -1,0 +1,138 @@
+"""One TokenSwift speculative step over all layers, on device-resident buffers.
+
+Per layer (the order of "How it works" on the TokenSwift tool listing, with the
+partial cache refreshed every step as the ICML 2025 summary's ablation
+favours, dynamic over one-time):
+  1. verify attention: the T-row batch (draft tree + n-gram chains) against
+     the full KV cache, producing the chunk importance of the scoring row in
+     the same pass;
+  2. top-k chunk selection up to the retrieval budget and gather into the
+     compact partial cache;
+  3. draft attention: the 4-row self-drafting batch over the partial cache.
+Then, once per step, the vocabulary stage (penalty, min-p, greedy target,
+acceptance).
+
+Every step is one C-ABI call into libts.so; this module only owns device
+memory (allocated once, through torch) and orders the calls on one stream.
+The step can be captured into a CUDA graph.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+from . import (ts_penalty_minp_verify, ts_select_gather, ts_tree_attn, ts_tree_attn_workspace_bytes,
+               ts_tree_mask_from_parents)
+from . import workloads as W
+
+
+@dataclasses.dataclass
+class LayerBuffers:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    q_draft: torch.Tensor
+    k_part: torch.Tensor
+    v_part: torch.Tensor
+    out: torch.Tensor
+    lse: torch.Tensor
+    scores: torch.Tensor
+    sel: torch.Tensor
+    out_draft: torch.Tensor
+    lse_draft: torch.Tensor
+
+
+class SpecStep:
+    def __init__(self, cfg: W.Config, device="cuda", layers: Optional[int] = None, vocab: Optional[bool] = None,
+                 value_kind: str = "int", fill_draft_tail: bool = True):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.n_layers = cfg.layers if layers is None else layers
+        self.T = cfg.T
+        self.Td = cfg.draft_rows
+        self.k_sel = cfg.k_sel
+        self.B = self.k_sel * cfg.chunk
+        parents = cfg.parents
+        self.parents = parents
+        self.draft_parents = [-1] + list(range(self.Td - 1))
+        self.mask = torch.from_numpy(ts_tree_mask_from_parents(parents).view(np.int64)).to(self.device)
+        self.mask_draft = torch.from_numpy(ts_tree_mask_from_parents(self.draft_parents).view(np.int64)).to(self.device)
+        ws = max(ts_tree_attn_workspace_bytes(self.T, cfg.Hq, cfg.Hkv, cfg.d, cfg.N),
+                 ts_tree_attn_workspace_bytes(self.Td, cfg.Hq, cfg.Hkv, cfg.d, self.B))
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.device)
+        self.layers: List[LayerBuffers] = []
+        nc = cfg.n_chunks
+        for layer in range(self.n_layers):
+            x = W.make_layer_inputs(cfg, layer, device=self.device, value_kind=value_kind)
+            kp = torch.zeros((cfg.Hkv, self.B + self.Td, cfg.d), dtype=torch.bfloat16, device=self.device)
+            vp = torch.zeros_like(kp)
+            if fill_draft_tail:
+                kp[:, self.B:] = x.k_draft_tail
+                vp[:, self.B:] = x.v_draft_tail
+            self.layers.append(LayerBuffers(
+                q=x.q, k=x.k, v=x.v, q_draft=x.q_draft, k_part=kp, v_part=vp,
+                out=torch.empty((self.T, cfg.Hq, cfg.d), dtype=torch.bfloat16, device=self.device),
+                lse=torch.empty((self.T, cfg.Hq), dtype=torch.float32, device=self.device),
+                scores=torch.empty((cfg.Hkv, nc), dtype=torch.float32, device=self.device),
+                sel=torch.empty((cfg.Hkv, self.k_sel), dtype=torch.int32, device=self.device),
+                out_draft=torch.empty((self.Td, cfg.Hq, cfg.d), dtype=torch.bfloat16, device=self.device),
+                lse_draft=torch.empty((self.Td, cfg.Hq), dtype=torch.float32, device=self.device),
+            ))
+        self.vocab = (cfg.vocab > 0) if vocab is None else vocab
+        if self.vocab:
+            vi = W.make_vocab_inputs(parents, cfg.vocab, cfg.window, seed=1000 * cfg.cid + 999,
+                                     device=self.device, flip_rows=0.25)
+            self.vocab_inputs = vi
+            self.target = torch.empty(self.T, dtype=torch.int32, device=self.device)
+            self.kept = torch.empty(self.T, dtype=torch.int32, device=self.device)
+            self.result = torch.empty(4, dtype=torch.int32, device=self.device)
+            self.path = torch.empty(self.T, dtype=torch.int32, device=self.device)
+
+    # ------------------------------------------------------------------
+    def run_verify(self, i: int, stream=None) -> None:
+        cfg, L = self.cfg, self.layers[i]
+        ts_tree_attn(L.q, L.k, L.v, cfg.N, self.mask, L.out, lse=L.lse, chunk_scores=L.scores, score_row=0,
+                     workspace=self.workspace, scale=cfg.scale, stream=stream)
+
+    def run_refresh(self, i: int, stream=None) -> None:
+        cfg, L = self.cfg, self.layers[i]
+        ts_select_gather(L.scores, cfg.N, cfg.budget, L.k, L.v, L.sel, L.k_part, L.v_part, chunk=cfg.chunk,
+                         stream=stream)
+
+    def run_draft(self, i: int, stream=None) -> None:
+        cfg, L = self.cfg, self.layers[i]
+        ts_tree_attn(L.q_draft, L.k_part, L.v_part, self.B, self.mask_draft, L.out_draft, lse=L.lse_draft,
+                     workspace=self.workspace, scale=cfg.scale, stream=stream)
+
+    def run_layer(self, i: int, stream=None) -> None:
+        self.run_verify(i, stream)
+        self.run_refresh(i, stream)
+        self.run_draft(i, stream)
+
+    def run_vocab(self, stream=None) -> None:
+        cfg, vi = self.cfg, self.vocab_inputs
+        ts_penalty_minp_verify(vi.logits, vi.history, cfg.theta, cfg.min_p, cfg.temperature, vi.draft, vi.parent,
+                               vi.anchor, self.target, self.kept, self.result, self.path, stream=stream)
+
+    def run(self, stream=None) -> None:
+        for i in range(self.n_layers):
+            self.run_layer(i, stream)
+        if self.vocab:
+            self.run_vocab(stream)
+
+    # ------------------------------------------------------------------
+    def capture(self, stream: torch.cuda.Stream) -> torch.cuda.CUDAGraph:
+        """Capture one whole step into a CUDA graph (launch gaps removed)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.run(stream)  # warm-up outside capture (sets kernel attributes)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            self.run(stream)
+        return g
+
+    def kv_bytes_per_step(self) -> int:
+        return self.n_layers * self.cfg.kv_bytes_per_layer()

@@ -1,0 +1,152 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every
+symbol the header declares, computes tree masks on the host, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import long_context_attention_tree_b300 as ts
+import oracle
+from long_context_attention_tree_b300 import build as ts_build
+from long_context_attention_tree_b300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    ts_build.build()
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "ts.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ts_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = header_symbols()
+    assert len(names) >= 8
+    L = ts.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert "sm_103a" in ts.ts_version()
+
+
+@pytest.mark.parametrize("parent", [
+    W.verify_parents(), W.tree_parents([1, 3, 3, 3]), W.tree_parents([3, 3, 3, 3]),
+    W.chain_parents(32, 4), [-1] * 128, [-1] + list(range(127)), [],
+])
+def test_mask_matches_oracle_visibility(parent):
+    mask = ts.ts_tree_mask_from_parents(parent)
+    T = len(parent)
+    if T == 0:
+        return
+    vis = oracle.visible(parent)
+    for i in range(T):
+        bits = [(int(mask[i, u // 64]) >> (u % 64)) & 1 for u in range(T)]
+        assert bits == vis[i].astype(int).tolist()
+        assert all(((int(mask[i, u // 64]) >> (u % 64)) & 1) == 0 for u in range(T, 128))
+
+
+@pytest.mark.parametrize("parent", [[-1, 1], [0], [-1, -2], [-1, 0, 5]])
+def test_mask_rejects_bad_parents(parent):
+    with pytest.raises(ts.TSError) as e:
+        ts.ts_tree_mask_from_parents(parent)
+    assert e.value.status == ts.TS_ERR_INVALID_ARG
+
+
+def test_mask_rejects_too_many_rows():
+    with pytest.raises(ts.TSError):
+        ts.ts_tree_mask_from_parents([-1] * 129)
+
+
+def _attn(**kw):
+    """Call ts_tree_attn with fake (never dereferenced) aligned pointers."""
+    L = ts.lib()
+    P = 0x10000
+    a = dict(q=P, k=P, v=P, ld=5000, N=4096, T=40, Hq=4, Hkv=1, d=64, scale=0.125, mask=P, out=P,
+             lse=None, scores=None, score_row=0, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return L.ts_tree_attn(a["q"], a["k"], a["v"], a["ld"], a["N"], a["T"], a["Hq"], a["Hkv"], a["d"], a["scale"],
+                          a["mask"], a["out"], a["lse"], a["scores"], a["score_row"], a["ws"], a["ws_bytes"],
+                          a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), ts.TS_ERR_UNSUPPORTED),
+    (dict(Hq=6, Hkv=4), ts.TS_ERR_INVALID_ARG),
+    (dict(Hq=66, Hkv=1), ts.TS_ERR_UNSUPPORTED),
+    (dict(T=129), ts.TS_ERR_UNSUPPORTED),
+    (dict(N=-1), ts.TS_ERR_INVALID_ARG),
+    (dict(q=None), ts.TS_ERR_INVALID_ARG),
+    (dict(mask=None), ts.TS_ERR_INVALID_ARG),
+    (dict(k=0x10008), ts.TS_ERR_INVALID_ARG),
+    (dict(ld=4100), ts.TS_ERR_INVALID_ARG),
+    (dict(scale=0.0), ts.TS_ERR_INVALID_ARG),
+    (dict(scores=0x10000, score_row=40), ts.TS_ERR_INVALID_ARG),
+    (dict(ws=None), ts.TS_ERR_INVALID_ARG),
+    (dict(ws_bytes=16), ts.TS_ERR_INVALID_ARG),
+])
+def test_tree_attn_rejects_before_launch(kw, status):
+    assert _attn(**kw) == status
+    assert ts.lib().ts_last_error()
+
+
+def test_tree_attn_empty_batch_is_noop():
+    assert _attn(T=0, q=None, mask=None) == ts.TS_OK
+
+
+def test_workspace_size_is_consistent():
+    for (T, Hq, Hkv, d, N) in [(40, 4, 1, 64, 4096), (120, 32, 8, 128, 20480), (4, 40, 8, 128, 4096)]:
+        need = ts.ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N)
+        assert need % 4 == 0
+        if need:
+            assert _attn(T=T, Hq=Hq, Hkv=Hkv, d=d, N=N, ld=N + T, ws_bytes=need - 4) == ts.TS_ERR_INVALID_ARG
+
+
+def test_select_gather_rejects():
+    L = ts.lib()
+    P = 0x10000
+    # N not a multiple of the chunk
+    assert L.ts_select_gather(P, 8, 4100, 4096, 64, P, P, 5000, 128, P, P, P, 4096, None) == ts.TS_ERR_UNSUPPORTED
+    # budget not a multiple of the chunk
+    assert L.ts_select_gather(P, 8, 4096, 100, 64, P, P, 5000, 128, P, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    # partial cache too short
+    assert L.ts_select_gather(P, 8, 8192, 4096, 64, P, P, 8192, 128, P, P, P, 4000, None) == ts.TS_ERR_INVALID_ARG
+    # chunk other than 64
+    assert L.ts_select_gather(P, 8, 8192, 4096, 32, P, P, 8192, 128, P, P, P, 4096, None) == ts.TS_ERR_UNSUPPORTED
+
+
+def test_vocab_rejects():
+    L = ts.lib()
+    P = 0x10000
+    f = L.ts_penalty_minp_verify
+    ok = dict(logits=P, T=120, V=152064, history=P, W=1024, theta=1.2, min_p=0.1, temp=1.0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["logits"], a["T"], a["V"], a["history"], a["W"], a["theta"], a["min_p"], a["temp"],
+                 P, P, 0, P, P, P, P, None, 0, None)
+    assert call(T=0) == ts.TS_ERR_UNSUPPORTED
+    assert call(V=200000) == ts.TS_ERR_UNSUPPORTED
+    assert call(theta=0.0) == ts.TS_ERR_INVALID_ARG
+    assert call(temp=-1.0) == ts.TS_ERR_INVALID_ARG
+    assert call(min_p=1.5) == ts.TS_ERR_INVALID_ARG
+    assert call(history=None) == ts.TS_ERR_INVALID_ARG
+    assert call(logits=0x10002) == ts.TS_ERR_INVALID_ARG
+
+
+def test_product_does_not_import_oracle():
+    """The product package and its sources never reference the oracle."""
+    pkg = os.path.join(ROOT, "long_context_attention_tree_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "liboracle" not in text, fn

@@ -1,0 +1,325 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bars: bit-exact for chunk scores on integer data, selected indices, gathered
+caches, targets, min-p counts and acceptance; bf16 attention outputs within
+max-abs 2e-2 and relative L2 1e-2 of the fp64 result; LSE within 1e-3."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_attention_tree_b300 as ts
+import oracle
+from long_context_attention_tree_b300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-2
+REL_L2 = 1e-2
+LSE_ABS = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    from long_context_attention_tree_b300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+    torch.cuda.init()
+
+
+def dev_mask(parent):
+    return torch.from_numpy(ts.ts_tree_mask_from_parents(parent).view(np.int64)).cuda()
+
+
+def run_attn(q, k, v, N, parent, scale, scores=False, score_row=0, stream=None):
+    T, Hq, d = q.shape
+    Hkv = k.shape[0]
+    out = torch.empty((T, Hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+    nc = (N + 63) // 64
+    sc = torch.full((Hkv, max(nc, 1)), float("nan"), dtype=torch.float32, device="cuda") if scores else None
+    ws_n = ts.ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    ts.ts_tree_attn(q, k, v, N, dev_mask(parent), out, lse=lse, chunk_scores=sc, score_row=score_row,
+                    workspace=ws, scale=scale, stream=stream)
+    torch.cuda.synchronize()
+    return out, lse, sc
+
+
+def check_attn(out, lse, ref_o, ref_lse, what=""):
+    o = out.float().cpu().double().numpy().reshape(ref_o.shape)
+    err = np.abs(o - ref_o)
+    rel = np.linalg.norm(o - ref_o) / max(np.linalg.norm(ref_o), 1e-30)
+    assert err.max() <= MAX_ABS, f"{what}: max abs {err.max():.3e}"
+    assert rel <= REL_L2, f"{what}: rel L2 {rel:.3e}"
+    l = lse.cpu().double().numpy().reshape(ref_lse.shape)
+    assert np.abs(l - ref_lse).max() <= LSE_ABS, f"{what}: lse err {np.abs(l - ref_lse).max():.3e}"
+
+
+def verify_parent(T):
+    p = W.verify_parents()[:T] if T <= 120 else W.verify_parents() + W.chain_parents((T - 120) // 4 + 1, 4, 120)
+    return p[:T]
+
+
+CASES = [
+    # T, Hq, Hkv, d, N, kind
+    (1, 4, 1, 64, 0, "int"),
+    (1, 8, 8, 128, 1, "normal"),
+    (4, 32, 8, 128, 63, "int"),
+    (4, 40, 8, 128, 4096, "int"),
+    (40, 4, 1, 64, 4096, "int"),
+    (40, 5, 1, 64, 65, "normal"),
+    (64, 8, 2, 128, 64, "int"),
+    (64, 16, 4, 128, 1000, "normal"),
+    (120, 32, 8, 128, 2111, "int"),
+    (120, 40, 8, 128, 640, "normal"),
+    (128, 8, 8, 128, 777, "int"),
+    (128, 4, 1, 64, 300, "normal"),
+    (13, 20, 4, 128, 5000, "normal"),
+    (120, 32, 1, 128, 129, "int"),   # group 32
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "T{}_Hq{}_Hkv{}_d{}_N{}_{}".format(*c))
+def test_tree_attn_matches_oracle(case):
+    T, Hq, Hkv, d, N, kind = case
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=100 + T + N, device="cuda", value_kind=kind, ld_extra=5)
+    parent = verify_parent(T)
+    scale = 1.0 / math.sqrt(d)
+    out, lse, _ = run_attn(q, k, v, N, parent, scale)
+    ro, rl = oracle.tree_attn(q.cpu(), k.cpu(), v.cpu(), N, parent, scale)
+    check_attn(out, lse, ro, rl, str(case))
+
+
+def test_tree_attn_forced_cuda_core_path_matches(monkeypatch):
+    """Force the CUDA-core kernel at T=120 (cross-check of the tensor-core path)."""
+    monkeypatch.setenv("TS_FORCE_SIMT", "1")
+    T, Hq, Hkv, d, N = 120, 32, 8, 128, 3000
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=5, device="cuda")
+    parent = W.verify_parents()
+    out, lse, _ = run_attn(q, k, v, N, parent, 1 / math.sqrt(d))
+    ro, rl = oracle.tree_attn(q.cpu(), k.cpu(), v.cpu(), N, parent, 1 / math.sqrt(d))
+    check_attn(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("cid", [1, 2])
+def test_config_full_parity(cid):
+    """The tiny config and the LLaMA3.1-8B 20K layer, every output row."""
+    cfg = W.CONFIGS[cid]
+    x = W.make_layer_inputs(cfg, 0, device="cuda")
+    out, lse, sc = run_attn(x.q, x.k, x.v, cfg.N, cfg.parents, cfg.scale, scores=True)
+    ro, rl = oracle.tree_attn(x.q.cpu(), x.k.cpu(), x.v.cpu(), cfg.N, cfg.parents, cfg.scale)
+    check_attn(out, lse, ro, rl, cfg.name)
+    rs = oracle.score_chunks(x.q[0].cpu(), x.k.cpu(), cfg.N)
+    np.testing.assert_array_equal(sc.cpu().numpy(), rs.astype(np.float32))
+
+
+@pytest.mark.parametrize("N", [1, 63, 64, 65, 4096, 20480])
+def test_score_chunks_bit_exact(N):
+    Hq, Hkv, d = 32, 8, 128
+    q, k, _ = W.make_qkv(120, Hq, Hkv, d, N, seed=N, device="cuda")
+    nc = (N + 63) // 64
+    sc = torch.full((Hkv, nc), float("nan"), dtype=torch.float32, device="cuda")
+    ts.ts_score_chunks(q[0], k, N, sc)
+    torch.cuda.synchronize()
+    rs = oracle.score_chunks(q[0].cpu(), k.cpu(), N)
+    np.testing.assert_array_equal(sc.cpu().numpy(), rs.astype(np.float32))
+    # the fused scores of the attention pass agree bit for bit
+    _, _, fs = run_attn(q, k, _dummy_v(k), N, W.verify_parents(), 1 / math.sqrt(d), scores=True, score_row=0)
+    np.testing.assert_array_equal(fs.cpu().numpy(), sc.cpu().numpy())
+
+
+def _dummy_v(k):
+    return torch.zeros_like(k)
+
+
+@pytest.mark.parametrize("score_row", [0, 7, 119])
+def test_fused_scores_any_row(score_row):
+    Hq, Hkv, d, N = 40, 8, 128, 1280
+    q, k, v = W.make_qkv(120, Hq, Hkv, d, N, seed=score_row, device="cuda")
+    _, _, fs = run_attn(q, k, v, N, W.verify_parents(), 1 / math.sqrt(d), scores=True, score_row=score_row)
+    rs = oracle.score_chunks(q[score_row].cpu(), k.cpu(), N)
+    np.testing.assert_array_equal(fs.cpu().numpy(), rs.astype(np.float32))
+
+
+@pytest.mark.parametrize("N,budget,d", [(4096, 1024, 64), (20480, 4096, 128), (64 * 70, 4096, 128),
+                                        (102400, 4096, 128), (640, 4096, 128)])
+def test_select_gather_bit_exact(N, budget, d):
+    Hq, Hkv = 32, 8
+    q, k, v = W.make_qkv(1, Hq, Hkv, d, N, seed=N + budget, device="cuda")
+    nc = N // 64
+    sc = torch.empty((Hkv, nc), dtype=torch.float32, device="cuda")
+    ts.ts_score_chunks(q[0], k, N, sc)
+    kk = min(budget // 64, nc)
+    sel = torch.empty((Hkv, kk), dtype=torch.int32, device="cuda")
+    ld_part = kk * 64 + 4
+    kp = torch.zeros((Hkv, ld_part, d), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    ts.ts_select_gather(sc, N, budget, k, v, sel, kp, vp)
+    torch.cuda.synchronize()
+    scores = sc.cpu().numpy()
+    np.testing.assert_array_equal(scores, oracle.score_chunks(q[0].cpu(), k.cpu(), N).astype(np.float32))
+    rsel = oracle.select(scores, budget // 64)
+    np.testing.assert_array_equal(sel.cpu().numpy(), rsel)
+    assert torch.equal(kp.cpu(), oracle.gather(rsel, k.cpu(), N, 64, ld_part))
+    assert torch.equal(vp.cpu(), oracle.gather(rsel, v.cpu(), N, 64, ld_part))
+
+
+def test_select_ties_and_signed_zero():
+    Hkv, nc = 3, 300
+    rng = np.random.default_rng(1)
+    s = rng.integers(-3, 4, size=(Hkv, nc)).astype(np.float32)
+    s[1, ::2] = -0.0
+    s[1, 1::2] = 0.0
+    s[2, :] = 5.0
+    d = 64
+    k = torch.randn((Hkv, nc * 64, d), device="cuda").to(torch.bfloat16)
+    v = torch.randn((Hkv, nc * 64, d), device="cuda").to(torch.bfloat16)
+    for budget in (64, 64 * 17, 64 * 150, 64 * 300, 64 * 400):
+        kk = min(budget // 64, nc)
+        sel = torch.empty((Hkv, kk), dtype=torch.int32, device="cuda")
+        kp = torch.zeros((Hkv, kk * 64, d), dtype=torch.bfloat16, device="cuda")
+        ts.ts_select_gather(torch.from_numpy(s).cuda(), nc * 64, budget, k, v, sel, kp, torch.zeros_like(kp))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(sel.cpu().numpy(), oracle.select(s, budget // 64))
+
+
+def test_draft_attention_over_partial_cache():
+    cfg = W.CONFIGS[2]
+    x = W.make_layer_inputs(cfg, 0, device="cuda")
+    N = cfg.N
+    sc = torch.empty((cfg.Hkv, cfg.n_chunks), dtype=torch.float32, device="cuda")
+    ts.ts_score_chunks(x.q[0], x.k, N, sc)
+    B = cfg.k_sel * 64
+    sel = torch.empty((cfg.Hkv, cfg.k_sel), dtype=torch.int32, device="cuda")
+    kp = torch.zeros((cfg.Hkv, B + 4, cfg.d), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    kp[:, B:] = x.k_draft_tail
+    vp[:, B:] = x.v_draft_tail
+    ts.ts_select_gather(sc, N, cfg.budget, x.k, x.v, sel, kp, vp)
+    parent = [-1, 0, 1, 2]
+    out, lse, _ = run_attn(x.q_draft, kp, vp, B, parent, cfg.scale)
+    rsel = oracle.select(sc.cpu().numpy(), cfg.k_sel)
+    rkp = oracle.gather(rsel, x.k.cpu(), N, 64, B + 4, fill=kp.cpu())
+    rvp = oracle.gather(rsel, x.v.cpu(), N, 64, B + 4, fill=vp.cpu())
+    ro, rl = oracle.tree_attn(x.q_draft.cpu(), rkp, rvp, B, parent, cfg.scale)
+    check_attn(out, lse, ro, rl, "draft")
+
+
+def test_budget_covering_cache_gives_full_attention_bitwise():
+    """Budget >= N: the partial cache is the full cache and draft attention
+    over it equals attention over the full cache bit for bit."""
+    Hq, Hkv, d, N, T = 32, 8, 128, 4096, 4
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=77, device="cuda")
+    sc = torch.empty((Hkv, N // 64), dtype=torch.float32, device="cuda")
+    ts.ts_score_chunks(q[0], k, N, sc)
+    sel = torch.empty((Hkv, N // 64), dtype=torch.int32, device="cuda")
+    kp = torch.zeros((Hkv, N + T, d), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    kp[:, N:] = k[:, N:N + T]
+    vp[:, N:] = v[:, N:N + T]
+    ts.ts_select_gather(sc, N, 8192, k, v, sel, kp, vp)
+    parent = [-1, 0, 1, 2]
+    o1, l1, _ = run_attn(q, k, v, N, parent, 1 / math.sqrt(d))
+    o2, l2, _ = run_attn(q, kp, vp, N, parent, 1 / math.sqrt(d))
+    assert torch.equal(sel.cpu(), torch.arange(N // 64, dtype=torch.int32).repeat(Hkv, 1))
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_non_default_stream():
+    T, Hq, Hkv, d, N = 40, 4, 1, 64, 999
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=3, device="cuda")
+    s = torch.cuda.Stream()
+    parent = W.tree_parents([1, 3, 3, 3])
+    with torch.cuda.stream(s):
+        out, lse, _ = run_attn(q, k, v, N, parent, 0.125, stream=s)
+    ro, rl = oracle.tree_attn(q.cpu(), k.cpu(), v.cpu(), N, parent, 0.125)
+    check_attn(out, lse, ro, rl)
+
+
+# ----------------------------------------------------------------------------- vocab stage
+def run_vocab(logits, history, parent, draft, anchor, theta=1.2, min_p=0.1, temp=1.0):
+    T = logits.shape[0]
+    target = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    kept = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    result = torch.full((4,), -7, dtype=torch.int32, device="cuda")
+    path = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    ts.ts_penalty_minp_verify(logits, history, theta, min_p, temp, draft, parent, anchor, target, kept, result,
+                              path)
+    torch.cuda.synchronize()
+    return target.cpu().numpy(), kept.cpu().numpy(), result.cpu().numpy(), path.cpu().numpy()
+
+
+@pytest.mark.parametrize("V,W_,flip,seed", [(152064, 1024, 0.25, 0), (152064, 1024, 0.0, 1), (1000, 50, 0.5, 2),
+                                            (33, 5, 0.0, 3), (152064, 0, 0.0, 4), (163840, 2048, 0.3, 5)])
+def test_vocab_stage_bit_exact(V, W_, flip, seed):
+    parent = W.verify_parents()
+    vi = W.make_vocab_inputs(parent, V, W_, seed=seed, device="cuda", flip_rows=flip)
+    t, kp, r, p = run_vocab(vi.logits, vi.history, vi.parent, vi.draft, vi.anchor)
+    rt, rk = oracle.penalty_minp(vi.logits.cpu().numpy(), vi.history.cpu().numpy(), 1.2, 0.1, 1.0)
+    np.testing.assert_array_equal(t, rt)
+    np.testing.assert_array_equal(kp, rk)
+    rr, rp = oracle.accept(vi.draft.cpu().numpy(), parent, rt, vi.anchor)
+    np.testing.assert_array_equal(r, rr)
+    np.testing.assert_array_equal(p, rp)
+
+
+@pytest.mark.parametrize("theta,min_p,temp", [(1.0, 0.1, 1.0), (1.2, 0.0, 1.0), (1.2, 1.0, 1.0), (1.5, 0.05, 0.7),
+                                              (1.2, 0.1, 2.0)])
+def test_vocab_parameters(theta, min_p, temp):
+    parent = W.verify_parents()
+    vi = W.make_vocab_inputs(parent, 5000, 300, seed=9, device="cuda", flip_rows=0.3)
+    t, kp, r, p = run_vocab(vi.logits, vi.history, vi.parent, vi.draft, vi.anchor, theta, min_p, temp)
+    rt, rk = oracle.penalty_minp(vi.logits.cpu().numpy(), vi.history.cpu().numpy(), theta, min_p, temp)
+    np.testing.assert_array_equal(t, rt)
+    np.testing.assert_array_equal(kp, rk)
+    rr, rp = oracle.accept(vi.draft.cpu().numpy(), parent, rt, vi.anchor)
+    np.testing.assert_array_equal(r, rr)
+
+
+def test_vocab_hand_examples(golden_dir):
+    import os
+    from tests.test_oracle_pins import _nums, _parse
+    for name, lg, hist, theta, mp, temp, final, tgt, kept in _parse(os.path.join(golden_dir, "penalty_minp_hand.txt")):
+        logits = torch.tensor([_nums(lg, float)], dtype=torch.float32, device="cuda")
+        h = torch.tensor(_nums(hist, int), dtype=torch.int32, device="cuda")
+        one = torch.tensor([-1], dtype=torch.int32, device="cuda")
+        t, k, _, _ = run_vocab(logits, h if h.numel() else None, one, torch.tensor([0], dtype=torch.int32, device="cuda"),
+                               0, float(theta), float(mp), float(temp))
+        assert t[0] == int(tgt) and k[0] == int(kept), name
+
+
+def test_accept_hand_examples(golden_dir):
+    import os
+    from tests.test_oracle_pins import _nums, _parse
+    for name, par, dr, tg, anc, res, path in _parse(os.path.join(golden_dir, "accept_hand.txt")):
+        T = len(_nums(par, int))
+        # logits whose greedy tokens are the example's targets
+        V = 16
+        logits = torch.zeros((T, V), dtype=torch.float32)
+        for i, x in enumerate(_nums(tg, int)):
+            logits[i, x] = 5.0
+        _, _, r, p = run_vocab(logits.cuda(), None, torch.tensor(_nums(par, int), dtype=torch.int32, device="cuda"),
+                               torch.tensor(_nums(dr, int), dtype=torch.int32, device="cuda"), int(anc))
+        L, best, bonus = _nums(res, int)
+        assert (r[0], r[1], r[2], r[3]) == (L, best, bonus, 0), name
+        want = _nums(path, int)
+        assert p[:len(want)].tolist() == want and all(x == -1 for x in p[len(want):]), name
+
+
+def test_vocab_data_errors_reported_not_trapped():
+    parent = W.verify_parents()
+    vi = W.make_vocab_inputs(parent, 1000, 20, seed=4, device="cuda")
+    bad_hist = vi.history.clone()
+    bad_hist[3] = 1000
+    _, _, r, _ = run_vocab(vi.logits, bad_hist, vi.parent, vi.draft, vi.anchor)
+    assert r[3] == ts.TS_ERR_DATA
+    bad_parent = vi.parent.clone()
+    bad_parent[5] = 7
+    _, _, r, p = run_vocab(vi.logits, vi.history, bad_parent, vi.draft, vi.anchor)
+    assert r[3] == ts.TS_ERR_DATA and r[0] == 0 and (p == -1).all()
+    # the context is still usable
+    t, _, r, _ = run_vocab(vi.logits, vi.history, vi.parent, vi.draft, vi.anchor)
+    assert r[3] == 0
