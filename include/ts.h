@@ -122,6 +122,30 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
                        void *workspace, size_t ws_bytes, ts_stream_t stream);
 
 /*
+ * Allocation-free ts_tree_attn.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory -- code running
+ * inside another runtime's execution callback (an inference-server plugin, a
+ * host function queued in someone else's stream) or a C caller without an
+ * allocator, where cudaMalloc is forbidden or would synchronize the device.
+ * Same arguments, semantics and results as ts_tree_attn, without the
+ * workspace: the split partials go to a file-scope device array of
+ * TS_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds until
+ * the process exits.  It never calls cudaMalloc/cudaFree.
+ *   - Sizes whose ts_tree_attn_workspace_bytes exceeds the array return
+ *     TS_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the array: calls whose kernels overlap on the GPU race
+ *     on it; calls ordered on one stream are safe.  Its contents carry over
+ *     between calls and nothing in it needs clearing.
+ */
+#define TS_NOALLOC_SCRATCH_BYTES (64u << 20)
+ts_status ts_tree_attn_noalloc(const void *q, const void *k, const void *v, int64_t ld_kv,
+                               int64_t N, int T, int Hq, int Hkv, int d, float scale,
+                               const uint64_t *mask, void *out, float *lse,
+                               float *chunk_scores, int score_row, ts_stream_t stream);
+
+/*
  * Query-key importance of every KV chunk ("a dynamically updated partial KV
  * cache ranked by query-key importance", ICML 2025 summary, "Approach"):
  *   scores[g][c] = max over the query heads h of group g of

@@ -19,12 +19,13 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libts.so")
 
+TS_NOALLOC_SCRATCH_BYTES = 64 << 20
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT, TS_ERR_DATA = range(6)
 _STATUS = {0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_UNSUPPORTED", 3: "TS_ERR_CUDA",
            4: "TS_ERR_TIMEOUT", 5: "TS_ERR_DATA"}
 
 __all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree_attn_workspace_bytes",
-           "ts_launch_count", "ts_tree_attn", "ts_score_chunks", "ts_select_gather", "ts_penalty_minp_verify"]
+           "ts_launch_count", "ts_tree_attn", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_select_gather", "ts_penalty_minp_verify"]
 
 
 class TSError(RuntimeError):
@@ -52,12 +53,13 @@ def lib() -> ctypes.CDLL:
         L.ts_tree_attn_workspace_bytes.argtypes = [i32, i32, i32, i32, i64]
         L.ts_tree_attn_workspace_bytes.restype = sz
         L.ts_tree_attn.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P, sz, P]
+        L.ts_tree_attn_noalloc.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P]
         L.ts_score_chunks.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P, P]
         L.ts_select_gather.argtypes = [P, i32, i64, i32, i32, P, P, i64, i32, P, P, P, i64, P]
         L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
                                              P, P, P, P, P, sz, P]
-        for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_score_chunks", "ts_select_gather",
-                     "ts_penalty_minp_verify"):
+        for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_noalloc", "ts_score_chunks",
+                     "ts_select_gather", "ts_penalty_minp_verify"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -117,6 +119,20 @@ def ts_tree_attn(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_
     _check(lib().ts_tree_attn(_ptr(q), _ptr(k), _ptr(v), ld, N, T, Hq, Hkv, d, scale, _ptr(mask), _ptr(out),
                               _ptr(lse), _ptr(chunk_scores), score_row, _ptr(workspace), ws_bytes,
                               _stream(stream)))
+
+
+def ts_tree_attn_noalloc(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_row: int = 0,
+                         scale: Optional[float] = None, stream=None) -> None:
+    """ts_tree_attn without a caller workspace, for callers that cannot
+    allocate device memory: the split partials go to the library's own
+    file-scope device array (TS_NOALLOC_SCRATCH_BYTES, held by every GPU
+    that loads the library).  Calls that overlap on the GPU race on it."""
+    T, Hq, d = q.shape
+    Hkv, ld, _ = k.shape
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    _check(lib().ts_tree_attn_noalloc(_ptr(q), _ptr(k), _ptr(v), ld, N, T, Hq, Hkv, d, scale, _ptr(mask),
+                                      _ptr(out), _ptr(lse), _ptr(chunk_scores), score_row, _stream(stream)))
 
 
 def ts_score_chunks(q_row, k, N: int, scores, chunk: int = 64, stream=None) -> None:

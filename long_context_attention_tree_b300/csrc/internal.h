@@ -6,10 +6,15 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/ts.h"
+
 namespace ts {
 
 // Counts every kernel launch the library enqueues (diagnostic).
 void note_launches(int n);
+
+// Records `msg` as this host thread's last error message and returns `st`.
+ts_status report_error(ts_status st, const char *msg);
 
 struct AttnArgs {
     const __nv_bfloat16 *q;

@@ -78,6 +78,7 @@ ts_status check_attn_shape(int T, int Hq, int Hkv, int d, int64_t N) {
 
 namespace ts {
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+ts_status report_error(ts_status st, const char *msg) { return fail(st, "%s", msg ? msg : "error"); }
 }  // namespace ts
 
 extern "C" {
