@@ -230,7 +230,7 @@ def run_native(args, ws, rank, local):
     ts.lib()
     cfg = workload_config(args.workload)
     peaks = read_peaks()
-    step = SpecStep(cfg)
+    step = SpecStep(cfg, layers=args.layers)
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -264,6 +264,7 @@ def run_native(args, ws, rank, local):
         ev1.record(s)
     s.synchronize()
     launches = ts.ts_launch_count() - launches0
+    dev_status = ts.ts_device_error(True)
     torch.cuda.synchronize()
     barrier(ws)
     time.sleep(0.2)
@@ -279,8 +280,7 @@ def run_native(args, ws, rank, local):
     T, Hq, d, N = cfg.T, cfg.Hq, cfg.d, cfg.N
     flops = 4.0 * T * Hq * N * d
     kv_layer = cfg.kv_bytes_per_layer()
-    tensor_path = T >= 64 and d == 128 and os.environ.get("TS_FORCE_SIMT", "0") != "1" and \
-        getattr(ts, "TENSOR_PATH", False)
+    tensor_path = ts.ts_tree_attn_uses_tensor_cores(T, Hq, cfg.Hkv, d, N)
     if tensor_path:
         roof = {"bound": "tensor", "achieved": flops / verify_avg_s / 1e12, "peak": peaks["bf16_sus"],
                 "unit": "TFLOP/s", "peak_source": f"bf16 sustained, {peaks['source']}"}
@@ -313,18 +313,19 @@ def run_native(args, ws, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "model_shape": cfg.name, "layers": cfg.layers, "N": N,
+            "config": {"workload": args.workload, "model_shape": cfg.name, "layers": step.n_layers, "N": N,
                        "Hq": Hq, "Hkv": cfg.Hkv, "d": d, "T_verify": T, "tree": list(cfg.branching),
                        "ngram_chains": cfg.n_chains, "budget": cfg.budget, "draft_rows": cfg.draft_rows,
                        "vocab": cfg.vocab, "parallelism": f"replicas{ws}",
                        "l2": f"inputs larger than L2 ({kv_step / 1e9:.1f} GB of KV per step)"},
-            "us_per_layer_step": ms_per_step * 1e3 / cfg.layers,
+            "us_per_layer_step": ms_per_step * 1e3 / step.n_layers,
             "kv_frac_of_hbm_peak": value / ws / peaks["hbm"],
             "kv_frac_of_hbm_nominal_8tbs": value / ws / 8000.0,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
+            "device_status": dev_status,
             "clocks": clk,
             "peaks": peaks,
         }
@@ -403,6 +404,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="qwen14b-100k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None, help="run only this many layers (profiling)")
     ap.add_argument("--cpu-row-fraction", type=float, default=0.25,
                     help="fraction of verify rows the CPU oracle baseline computes")
     ap.add_argument("--ref-row-fraction", type=float, default=1.0 / 32,

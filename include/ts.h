@@ -122,6 +122,23 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
                        void *workspace, size_t ws_bytes, ts_stream_t stream);
 
 /*
+ * 1 when ts_tree_attn runs these sizes on the tensor cores (tcgen05), 0 when
+ * on the CUDA cores (or the sizes are unsupported).  Setting the environment
+ * variable TS_FORCE_SIMT=1 before the call forces the CUDA-core kernel.
+ */
+int ts_tree_attn_uses_tensor_cores(int T, int Hq, int Hkv, int d, int64_t N);
+
+/*
+ * Sticky device-side status.  A kernel whose bounded wait gave up (a
+ * pipeline stall of seconds, which correct inputs never cause) finishes
+ * early, leaves its outputs undefined and records TS_ERR_TIMEOUT here.
+ * Returns TS_OK or that status; `clear` != 0 resets it.  This call copies
+ * from the device and therefore waits for the device: a diagnostic, not a
+ * hot-path call.
+ */
+ts_status ts_device_error(int clear);
+
+/*
  * Allocation-free ts_tree_attn.  The pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory -- code running
  * inside another runtime's execution callback (an inference-server plugin, a

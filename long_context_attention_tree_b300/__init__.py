@@ -25,7 +25,7 @@ _STATUS = {0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_UNSUPPORTED", 3: "TS_
            4: "TS_ERR_TIMEOUT", 5: "TS_ERR_DATA"}
 
 __all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree_attn_workspace_bytes",
-           "ts_launch_count", "ts_tree_attn", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_select_gather", "ts_penalty_minp_verify"]
+           "ts_launch_count", "ts_tree_attn_uses_tensor_cores", "ts_device_error", "ts_tree_attn", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_select_gather", "ts_penalty_minp_verify"]
 
 
 class TSError(RuntimeError):
@@ -52,6 +52,10 @@ def lib() -> ctypes.CDLL:
         L.ts_tree_mask_from_parents.argtypes = [P, i32, P]
         L.ts_tree_attn_workspace_bytes.argtypes = [i32, i32, i32, i32, i64]
         L.ts_tree_attn_workspace_bytes.restype = sz
+        L.ts_tree_attn_uses_tensor_cores.argtypes = [i32, i32, i32, i32, i64]
+        L.ts_tree_attn_uses_tensor_cores.restype = i32
+        L.ts_device_error.argtypes = [i32]
+        L.ts_device_error.restype = i32
         L.ts_tree_attn.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P, sz, P]
         L.ts_tree_attn_noalloc.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P]
         L.ts_score_chunks.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P, P]
@@ -104,6 +108,18 @@ def ts_tree_mask_from_parents(parent) -> np.ndarray:
 
 def ts_tree_attn_workspace_bytes(T: int, Hq: int, Hkv: int, d: int, N: int) -> int:
     return int(lib().ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N))
+
+
+def ts_tree_attn_uses_tensor_cores(T: int, Hq: int, Hkv: int, d: int, N: int) -> bool:
+    """True when these sizes run on the tcgen05 tensor-core kernel."""
+    return bool(lib().ts_tree_attn_uses_tensor_cores(T, Hq, Hkv, d, N))
+
+
+def ts_device_error(clear: bool = True) -> int:
+    """Sticky device status (0 = OK, TS_ERR_TIMEOUT if a bounded wait gave up).
+    Waits for the device."""
+    st = lib().ts_device_error(1 if clear else 0)
+    return int(st)
 
 
 def ts_tree_attn(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_row: int = 0,

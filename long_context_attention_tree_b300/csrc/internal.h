@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (ts_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -51,6 +52,18 @@ struct SimtPlan {
 SimtPlan simt_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms);
 cudaError_t launch_tree_attn_simt(const AttnArgs &a, const SimtPlan &p, cudaStream_t st);
 cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st);
+
+// tensor-core (tcgen05) path, head_dim 128, 64 <= T <= 128
+struct TcPlan {
+    bool ok;
+    int tpb, n_mtiles, n_mpairs, n_tiles, splits, tiles_per_split;
+};
+TcPlan tc_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms);
+size_t tc_smem_bytes();
+cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                                const CUtensorMap &tv, cudaStream_t st);
+// sticky device-side error word (TS_ERR_TIMEOUT when a bounded wait gave up)
+cudaError_t read_device_error(int *value, bool clear);
 
 // chunk scoring / selection / gather
 cudaError_t launch_score_chunks(const __nv_bfloat16 *q_row, const __nv_bfloat16 *k, int64_t ld_kv, int64_t N,

@@ -12,6 +12,8 @@
 #include <mutex>
 #include <string>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/ts.h"
 #include "internal.h"
 
@@ -61,6 +63,63 @@ int num_sms() {
 bool force_simt() {
     const char *e = getenv("TS_FORCE_SIMT");
     return e != nullptr && e[0] == '1';
+}
+
+// Which kernel runs and how the KV length is split; used both to size the
+// workspace and to launch, so the two always agree.
+struct AttnPlan {
+    bool tc;
+    ts::TcPlan tcp;
+    ts::SimtPlan sp;
+    int splits;
+};
+
+AttnPlan plan_attention(int T, int Hq, int Hkv, int d, int64_t N) {
+    AttnPlan p{};
+    const int sms = num_sms();
+    p.tcp = ts::tc_plan(T, Hq, Hkv, d, N, sms);
+    p.tc = p.tcp.ok && !force_simt();
+    if (p.tc) {
+        p.splits = p.tcp.splits;
+    } else {
+        p.sp = ts::simt_plan(T, Hq, Hkv, d, N, sms);
+        p.splits = p.sp.splits;
+    }
+    return p;
+}
+
+size_t workspace_for(const AttnPlan &p, int T, int Hq, int d) {
+    return p.splits > 1 ? (size_t)p.splits * T * Hq * ((size_t)d + 2) * sizeof(float) : 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map with 128-byte swizzle: dims/strides innermost first.
+bool encode_map(CUtensorMap *m, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 ts_status check_attn_shape(int T, int Hq, int Hkv, int d, int64_t N) {
@@ -113,9 +172,20 @@ ts_status ts_tree_mask_from_parents(const int32_t *parent_host, int T, uint64_t 
 
 size_t ts_tree_attn_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t N) {
     if (check_attn_shape(T, Hq, Hkv, d, N) != TS_OK || T == 0) return 0;
-    const ts::SimtPlan p = ts::simt_plan(T, Hq, Hkv, d, N, num_sms());
-    if (p.splits <= 1) return 0;
-    return (size_t)p.splits * T * Hq * ((size_t)d + 2) * sizeof(float);
+    return workspace_for(plan_attention(T, Hq, Hkv, d, N), T, Hq, d);
+}
+
+ts_status ts_device_error(int clear) {
+    int v = 0;
+    cudaError_t e = ts::read_device_error(&v, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e, "ts_device_error");
+    if (v != 0) return fail((ts_status)v, "a kernel reported device status %d (bounded wait gave up)", v);
+    return TS_OK;
+}
+
+int ts_tree_attn_uses_tensor_cores(int T, int Hq, int Hkv, int d, int64_t N) {
+    if (check_attn_shape(T, Hq, Hkv, d, N) != TS_OK || T == 0) return 0;
+    return plan_attention(T, Hq, Hkv, d, N).tc ? 1 : 0;
 }
 
 ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_kv,
@@ -136,9 +206,8 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
     if (chunk_scores && (score_row < 0 || score_row >= T))
         return fail(TS_ERR_INVALID_ARG, "score_row=%d outside [0, T=%d)", score_row, T);
 
-    const int sms = num_sms();
-    const ts::SimtPlan p = ts::simt_plan(T, Hq, Hkv, d, N, sms);
-    const size_t need = p.splits > 1 ? (size_t)p.splits * T * Hq * ((size_t)d + 2) * sizeof(float) : 0;
+    const AttnPlan plan = plan_attention(T, Hq, Hkv, d, N);
+    const size_t need = workspace_for(plan, T, Hq, d);
     if (need > 0 && (workspace == nullptr || ws_bytes < need))
         return fail(TS_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
     if (need > 0 && !aligned16(workspace)) return fail(TS_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
@@ -162,18 +231,35 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
     a.score_row = score_row;
     a.n_chunks = (int)((N + 63) / 64);
     a.ws_o = static_cast<float *>(workspace);
-    a.ws_ml = need > 0 ? a.ws_o + (size_t)p.splits * T * Hq * d : nullptr;
-    a.splits = p.splits;
-    a.tiles_per_split = p.tiles_per_split;
-    a.n_tiles = p.n_tiles;
-    a.tpb = p.tpb;
+    a.ws_ml = need > 0 ? a.ws_o + (size_t)plan.splits * T * Hq * d : nullptr;
+    a.splits = plan.splits;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = ts::launch_tree_attn_simt(a, p, s);
-    if (e != cudaSuccess) return cuda_fail(e, "tree_attn_simt launch");
+    cudaError_t e;
+    if (plan.tc) {
+        const ts::TcPlan &p = plan.tcp;
+        a.tiles_per_split = p.tiles_per_split;
+        a.n_tiles = p.n_tiles;
+        a.tpb = p.tpb;
+        CUtensorMap tq, tk, tv;
+        const uint64_t row_bytes = (uint64_t)d * 2;
+        if (!encode_map(&tq, q, d, Hq, T, row_bytes, row_bytes * Hq, 64, a.G, p.tpb) ||
+            !encode_map(&tk, k, d, N + T, Hkv, row_bytes, row_bytes * ld_kv, 64, 128, 1) ||
+            !encode_map(&tv, v, d, N + T, Hkv, row_bytes, row_bytes * ld_kv, 64, 128, 1))
+            return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled failed (or the driver entry point is missing)");
+        e = ts::launch_tree_attn_tc(a, p, tq, tk, tv, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tree_attn_tc launch");
+    } else {
+        const ts::SimtPlan &p = plan.sp;
+        a.tiles_per_split = p.tiles_per_split;
+        a.n_tiles = p.n_tiles;
+        a.tpb = p.tpb;
+        e = ts::launch_tree_attn_simt(a, p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tree_attn_simt launch");
+    }
     ts::note_launches(1);
-    if (p.splits > 1) {
-        ts::MergeArgs m{a.ws_o, a.ws_ml, a.out, a.lse, T, Hq, p.splits};
+    if (plan.splits > 1) {
+        ts::MergeArgs m{a.ws_o, a.ws_ml, a.out, a.lse, T, Hq, plan.splits};
         e = ts::launch_lse_merge(m, d, s);
         if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
         ts::note_launches(1);

@@ -93,6 +93,30 @@ def test_tree_attn_matches_oracle(case):
     check_attn(out, lse, ro, rl, str(case))
 
 
+def test_tensor_core_path_is_selected_and_status_clean():
+    assert ts.ts_tree_attn_uses_tensor_cores(120, 32, 8, 128, 20480)
+    assert ts.ts_tree_attn_uses_tensor_cores(64, 40, 8, 128, 1)
+    assert not ts.ts_tree_attn_uses_tensor_cores(63, 32, 8, 128, 20480)
+    assert not ts.ts_tree_attn_uses_tensor_cores(120, 4, 1, 64, 4096)
+    assert ts.ts_device_error(True) == ts.TS_OK
+
+
+@pytest.mark.parametrize("T", [64, 65, 100, 120, 128])
+@pytest.mark.parametrize("G", [1, 3, 4, 5, 8, 32])
+def test_tensor_core_group_sizes(T, G):
+    Hkv = 2 if G < 32 else 1
+    Hq, d, N = G * Hkv, 128, 1000 + 7 * T
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=T * 100 + G, device="cuda", value_kind="normal", ld_extra=3)
+    parent = verify_parent(T)
+    assert ts.ts_tree_attn_uses_tensor_cores(T, Hq, Hkv, d, N)
+    out, lse, sc = run_attn(q, k, v, N, parent, 1 / math.sqrt(d), scores=True, score_row=T - 1)
+    ro, rl = oracle.tree_attn(q.cpu(), k.cpu(), v.cpu(), N, parent, 1 / math.sqrt(d))
+    check_attn(out, lse, ro, rl, f"T{T} G{G}")
+    rs = oracle.score_chunks(q[T - 1].cpu(), k.cpu(), N)
+    np.testing.assert_allclose(sc.cpu().numpy(), rs, rtol=1e-4, atol=1e-2)
+    assert ts.ts_device_error(True) == ts.TS_OK
+
+
 def test_tree_attn_forced_cuda_core_path_matches(monkeypatch):
     """Force the CUDA-core kernel at T=120 (cross-check of the tensor-core path)."""
     monkeypatch.setenv("TS_FORCE_SIMT", "1")
