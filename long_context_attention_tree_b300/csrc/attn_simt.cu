@@ -279,13 +279,14 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeArgs a) {
     if (warp >= rows) return;
     const size_t stride = (size_t)rows;
     const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml);
+    const int n_split = (warp / a.Hq) < a.t_split ? a.splits : a.splits_hi;
     float m = -INFINITY;
-    for (int s = 0; s < a.splits; ++s) m = fmaxf(m, ml[s * stride + warp].x);
+    for (int s = 0; s < n_split; ++s) m = fmaxf(m, ml[s * stride + warp].x);
     float l = 0.f;
     float acc[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) acc[c] = 0.f;
-    for (int s = 0; s < a.splits; ++s) {
+    for (int s = 0; s < n_split; ++s) {
         const float2 p = ml[s * stride + warp];
         if (p.x == -INFINITY) continue;  // split saw no visible key for this row
         const float w = exp2f(p.x - m);

@@ -1,27 +1,41 @@
 // Split-KV tree-masked GQA attention on the 5th-generation tensor cores
 // (tcgen05, TMEM accumulators, TMA), for the TokenSwift verify pass: a batch
 // of T >= 64 speculative rows (draft tree + n-gram chains) against the full
-// bf16 KV cache ("fed into the LLM with a full KV cache", "How it works").
+// bf16 KV cache ("fed into the LLM with a full KV cache", "How it works" on
+// the TokenSwift tool listing).
 //
 // Rows of one KV head g are the T x G pairs (t, j), t-major; an M-tile is
 // tpb = floor(128/G) whole batch rows times the G query heads of the group,
 // so every K/V byte staged in shared memory serves all G heads.  A CTA owns
-// two M-tiles (256 rows) of one KV head and a contiguous range of 128-token
-// KV tiles; the grid is (splits, M-tile pairs, Hkv) and the split partials
-// are merged by the log-sum-exp merge kernel.
+// one or two M-tiles of one KV head (a "pair" or "single" stream; two tiles
+// share every K/V load) and a contiguous range of 64-token KV tiles.  The
+// split counts are chosen on the host so that every CTA carries about the
+// same tensor-core work; the partials are combined by the log-sum-exp merge.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: Q once, then K/V tiles into a 2-stage ring;
-//   warp 1      owns TMEM (512 columns) and issues every tcgen05.mma from one
-//               thread: S_m = Q_m K^T (SS, K-major), O_m += P_m V (TS, P from
-//               TMEM, V MN-major);
-//   warps 2-5   softmax warpgroup of M-tile 0 (thread = row);
-//   warps 6-9   softmax warpgroup of M-tile 1.
-// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,384) O_1 [384,512); P_m
-// (bf16, two per column) overwrites the first 64 columns of S_m.
-// The running max is updated lazily: O and l are rescaled only when a row's
-// max grows by more than 2^8, which keeps every P below 256 and makes the
-// (TMEM round-trip) rescale rare.  Every wait is bounded (see tc_ptx.cuh).
+// Per KV tile i and M-tile m (TMEM columns: S_m 64, P_m 2 x 32, O_m 128):
+//   S_m(i) = Q_m K_i^T            8 MMAs, M=128 N=64 K=16, operands K-major
+//   softmax_m(i)                  S_m -> registers; P = 2^(s*c - m) -> P_m
+//   O_m   += P_m(i) V_i           4 MMAs, M=128 N=128 K=16, P from TMEM,
+//                                 V MN-major in shared memory
+// P has columns of its own, so S_m(i+1) is issued as soon as softmax_m(i)
+// has read S_m(i): the tensor pipe computes the next scores while the
+// softmax works.  P is double-buffered (buffer i&1), so softmax_m(i) only
+// waits for O_m += P(i-2) V, issued a whole tile earlier: the MMA latency
+// stays off the softmax's critical path and the tensor pipe sets the pace.
+//
+// Warp roles (384 threads, three warpgroups):
+//   warp 0      TMA producer: Q once, then K and V tiles into rings;
+//   warp 1      owns TMEM (512 columns); one thread issues every tcgen05.mma;
+//   warps 2-3   idle (they complete the control warpgroup, whose registers
+//               are handed to the softmax warpgroups with setmaxnreg);
+//   warps 4-7   softmax warpgroup 0 (thread = row of M-tile 0);
+//   warps 8-11  softmax warpgroup 1 (M-tile 1 of a pair stream).
+// The running max is lazy: O and l are rescaled only when a row's max grows
+// by more than 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so
+// the TMEM round trip of a rescale is rare.  The chunk importance of the
+// scoring row is summed from the same S values.  Every wait is bounded (see
+// tc_ptx.cuh): a wait that gives up raises the CTA's abort flag and the
+// sticky device status word, and the CTA winds down.
 #include "internal.h"
 #include "tc_ptx.cuh"
 #include "ts_common.cuh"
@@ -32,63 +46,171 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int TC_THREADS = 320;
-constexpr int KV_TILE = 128;
-constexpr int NSTAGE = 2;
-constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two 64-column swizzled halves)
-constexpr int HALF_BYTES = TILE_BYTES / 2;
-constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+constexpr int TC_THREADS = 384;
+// Register split (setmaxnreg): the control warpgroup drops to CTRL_REGS, the
+// two softmax warpgroups rise to SOFTMAX_REGS.  128*CTRL + 256*SOFTMAX must
+// not exceed 384 x the kernel's launch register count (checked on the host).
+constexpr int CTRL_REGS = 96;
+constexpr int SOFTMAX_REGS = 200;
+constexpr int KV_TILE = TC_KV_TILE;             // 64 tokens
+constexpr int Q_TILE_BYTES = 128 * 128 * 2;     // 128 rows x 128 dims (two 64-column swizzled halves)
+constexpr int Q_HALF_BYTES = Q_TILE_BYTES / 2;
+constexpr int KV_TILE_BYTES = KV_TILE * 128 * 2;  // 64 tokens x 128 dims
+constexpr int KV_HALF_BYTES = KV_TILE_BYTES / 2;
+constexpr int SMEM_DATA_BYTES = 224 * 1024;     // pair: 2 Q + 4+4 KV stages; single: 1 Q + 6+6 KV stages
+constexpr float RESCALE_THRESHOLD = 20.0f;      // log2 units
+// TMEM columns
+constexpr uint32_t COL_S = 0;    // S_m at m*64
+constexpr uint32_t COL_P = 128;  // P_m buffer b at 128 + m*64 + b*32 (bf16 pairs)
+constexpr uint32_t COL_O = 256;  // O_m at 256 + m*128
 
 struct __align__(8) TcSmemTail {
     uint64_t q_full;
-    uint64_t k_full[NSTAGE], k_empty[NSTAGE];
-    uint64_t v_full[NSTAGE], v_empty[NSTAGE];
-    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t k_full[6], k_empty[6];
+    uint64_t v_full[6], v_empty[6];
+    uint64_t s_full[2], s_free[2];
+    // [M-tile][P buffer]: a tile's P written / its O += P V complete.  One
+    // barrier per buffer: with P double-buffered the softmax may run a whole
+    // tile ahead of the issuer, which a single barrier's parity cannot tell.
+    uint64_t p_full[2][2], o_done[2][2];
     uint64_t mma_done;
-    uint64_t score_bar[2];       // G score rows arrive once per tile (by tile parity)
+    uint64_t score_bar[2];    // the G score rows arrive once per tile (by tile parity)
     uint32_t tmem_base;
     int abort_flag;
-    float score_part[2][32][2];  // [tile parity][head j][chunk half]
+    float score_part[2][32];  // [tile parity][head j]
 };
 
-constexpr size_t TC_SMEM_BYTES = 1024 /*alignment slack*/ + 2 * TILE_BYTES /*Q*/ + 2 * NSTAGE * TILE_BYTES /*K,V*/ +
-                                 sizeof(TcSmemTail);
+constexpr size_t TC_SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)SMEM_DATA_BYTES + sizeof(TcSmemTail);
+static_assert(TC_SMEM_BYTES <= 232448, "shared memory above the 227 KB per-block limit");
+static_assert(2 * Q_TILE_BYTES + 8 * KV_TILE_BYTES <= SMEM_DATA_BYTES, "pair layout");
+static_assert(1 * Q_TILE_BYTES + 12 * KV_TILE_BYTES <= SMEM_DATA_BYTES, "single layout");
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
+// Per-launch constants derived from the host plan.
+struct TcLaunch {
+    int tpb, n_mtiles, n_pair, s_pair, s_single, tl_pair, tl_single, n_tiles, ctas_per_head;
+    int direct;  // 1: every stream has one split, write the normalised output directly
+};
 
 __device__ __forceinline__ void raise_abort(TcSmemTail *tl) {
     *(volatile int *)&tl->abort_flag = 1;
     atomicExch(&g_device_error, (int)TS_ERR_TIMEOUT);
 }
 
+// S[128 x 64] = Q[128 x 128] K^T: 8 MMAs with K = 16 over the head dim.
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem, uint32_t idesc) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t in_row = (uint32_t)(k & 3) * 32;  // 16 bf16 = 32 bytes inside the 128-byte swizzled row
+        tc::mma_ss(d_tmem, tc::smem_desc_sw128(q_smem + (k >> 2) * Q_HALF_BYTES + in_row, 16, 1024),
+                   tc::smem_desc_sw128(k_smem + (k >> 2) * KV_HALF_BYTES + in_row, 16, 1024), idesc, k > 0);
+    }
+}
+// O[128 x 128] += P[128 x 64 tokens] V[64 tokens x 128]: 4 MMAs with K = 16 tokens.
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t idesc,
+                                         bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        tc::mma_ts(o_tmem, p_tmem + kk * 8, tc::smem_desc_sw128(v_smem + kk * 2048, KV_HALF_BYTES, 1024), idesc,
+                   (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Softmax helpers on one 32-token chunk of a row of S held in registers.
+// Hide tokens this row may not see: tokens past the prefix are visible only
+// when their batch row is an ancestor-or-self (mask bits), tokens past the
+// batch never.
+__device__ __forceinline__ void mask_chunk(uint32_t (&x)[32], int64_t tok0, int64_t N, int T, uint64_t mk0,
+                                           uint64_t mk1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int64_t tok = tok0 + i;
+        bool vis = tok < N;
+        if (!vis && tok < N + T) {
+            const int u = (int)(tok - N);
+            vis = ((u < 64 ? (mk0 >> u) : (mk1 >> (u - 64))) & 1ull) != 0;
+        }
+        if (!vis) x[i] = __float_as_uint(-INFINITY);
+    }
+}
+__device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        m0 = tc::fmax3(m0, __uint_as_float(x[i + 0]), __uint_as_float(x[i + 1]));
+        m1 = tc::fmax3(m1, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]));
+        m2 = tc::fmax3(m2, __uint_as_float(x[i + 4]), __uint_as_float(x[i + 5]));
+        m3 = tc::fmax3(m3, __uint_as_float(x[i + 6]), __uint_as_float(x[i + 7]));
+    }
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+// P = 2^(x*c - m) for 32 tokens -> 16 packed bf16x2 words (even token in the
+// lower half); returns the fp32 sum of the 32 bf16-rounded values, so that the
+// normaliser l sums exactly the weights the P.V product uses (a row dominated
+// by one key then reproduces that key's value without the weight's rounding).
+__device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], float2 c2, float2 nm2, uint32_t (&pk)[16]) {
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), c2, nm2);
+        const float2 y1 =
+            __ffma2_rn(make_float2(__uint_as_float(x[2 * i + 2]), __uint_as_float(x[2 * i + 3])), c2, nm2);
+        pk[i] = tc::pack_bf16x2(tc::ex2(y0.x), tc::ex2(y0.y));
+        pk[i + 1] = tc::pack_bf16x2(tc::ex2(y1.x), tc::ex2(y1.y));
+        acc0 = __fadd2_rn(acc0, make_float2(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u)));
+        acc1 = __fadd2_rn(acc1,
+                          make_float2(__uint_as_float(pk[i + 1] << 16), __uint_as_float(pk[i + 1] & 0xffff0000u)));
+    }
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+__device__ __forceinline__ float sum_chunk(const uint32_t (&x)[32], int lim) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (i < lim) s += __uint_as_float(x[i]);
+    return s;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const int n_mtiles) {
+                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const TcLaunch L) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    unsigned char *sQ = base;                           // [2][TILE_BYTES]
-    unsigned char *sK = sQ + 2 * TILE_BYTES;            // [NSTAGE][TILE_BYTES]
-    unsigned char *sV = sK + NSTAGE * TILE_BYTES;       // [NSTAGE][TILE_BYTES]
-    TcSmemTail *tl = reinterpret_cast<TcSmemTail *>(sV + NSTAGE * TILE_BYTES);
+    TcSmemTail *tl = reinterpret_cast<TcSmemTail *>(base + SMEM_DATA_BYTES);
     volatile int *abort_flag = &tl->abort_flag;
 
+    // ---- which (KV head, stream, KV range) this CTA owns
+    const int g = blockIdx.x / L.ctas_per_head;
+    int rr = blockIdx.x % L.ctas_per_head;
+    bool pair;
+    int mt0, split, tiles_per;
+    if (rr < L.n_pair * L.s_pair) {
+        pair = true;
+        mt0 = 2 * (rr / L.s_pair);
+        split = rr % L.s_pair;
+        tiles_per = L.tl_pair;
+    } else {
+        rr -= L.n_pair * L.s_pair;
+        pair = false;
+        mt0 = 2 * L.n_pair + rr / L.s_single;
+        split = rr % L.s_single;
+        tiles_per = L.tl_single;
+    }
+    const int nm = pair ? 2 : 1;
+    const int nst = pair ? 4 : 6;
+    const int tile_begin = split * tiles_per;
+    const int n_my = max(0, min(L.n_tiles, tile_begin + tiles_per) - tile_begin);
+    unsigned char *sQ = base;                                  // [nm][Q_TILE_BYTES]
+    unsigned char *sK = sQ + (size_t)nm * Q_TILE_BYTES;        // [nst][KV_TILE_BYTES]
+    unsigned char *sV = sK + (size_t)nst * KV_TILE_BYTES;      // [nst][KV_TILE_BYTES]
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, mp = blockIdx.y, g = blockIdx.z;
-    const int G = a.G, tpb = a.tpb;
-    const int mt0 = 2 * mp;
-    const int nm = min(2, n_mtiles - mt0);  // M-tiles owned (1 or 2)
-    const int tile_begin = split * a.tiles_per_split;
-    const int n_my = min(a.n_tiles, tile_begin + a.tiles_per_split) - tile_begin;
+    const int G = a.G, tpb = L.tpb;
+    const int rows_loaded = tpb * G;
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&tl->q_full, 1);
-        for (int s = 0; s < NSTAGE; ++s) {
+        for (int s = 0; s < 6; ++s) {
             tc::mbar_init(&tl->k_full[s], 1);
             tc::mbar_init(&tl->k_empty[s], 1);
             tc::mbar_init(&tl->v_full[s], 1);
@@ -96,14 +218,28 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         for (int m = 0; m < 2; ++m) {
             tc::mbar_init(&tl->s_full[m], 1);
-            tc::mbar_init(&tl->p_full[m], 128);
-            tc::mbar_init(&tl->o_done[m], 1);
+            tc::mbar_init(&tl->s_free[m], 128);
+            for (int b = 0; b < 2; ++b) {
+                tc::mbar_init(&tl->p_full[m][b], 128);
+                tc::mbar_init(&tl->o_done[m][b], 1);
+            }
         }
         tc::mbar_init(&tl->mma_done, 1);
-        tc::mbar_init(&tl->score_bar[0], (uint32_t)a.G);
-        tc::mbar_init(&tl->score_bar[1], (uint32_t)a.G);
+        tc::mbar_init(&tl->score_bar[0], (uint32_t)G);
+        tc::mbar_init(&tl->score_bar[1], (uint32_t)G);
         tl->abort_flag = 0;
         tc::fence_mbar_init();
+    }
+    // Q rows the TMA box does not cover (rows_loaded..127 of each M-tile) are
+    // zeroed so that every S row is finite.
+    if (rows_loaded < 128) {
+        const int per_half = (128 - rows_loaded) * 8;  // 16-byte units
+        for (int e = threadIdx.x; e < nm * 2 * per_half; e += TC_THREADS) {
+            const int mh = e / per_half, u = e % per_half;
+            uint4 *dst = reinterpret_cast<uint4 *>(sQ + (size_t)mh * Q_HALF_BYTES + (size_t)rows_loaded * 128) + u;
+            *dst = make_uint4(0u, 0u, 0u, 0u);
+        }
+        tc::fence_proxy_async();
     }
     if (warp == 1) {
         tc::tmem_alloc(&tl->tmem_base, 512);
@@ -114,95 +250,122 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc::fence_after_sync();
     const uint32_t tbase = tl->tmem_base;
 
-    if (warp == 0) {
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
+      if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n_my > 0) {
             tc::prefetch_tmap(&tm_q);
             tc::prefetch_tmap(&tm_k);
             tc::prefetch_tmap(&tm_v);
-            const uint32_t qbytes = (uint32_t)(2 * 128 * G * tpb);  // two 64-column halves of tpb*G rows
+            const uint32_t qbytes = (uint32_t)(2 * 128 * rows_loaded);  // two 64-column halves
             tc::mbar_arrive_expect_tx(&tl->q_full, qbytes * nm);
             for (int m = 0; m < nm; ++m)
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sQ + m * TILE_BYTES + h * HALF_BYTES, &tm_q, &tl->q_full, h * 64, g * G,
+                    tc::tma_load_3d(sQ + m * Q_TILE_BYTES + h * Q_HALF_BYTES, &tm_q, &tl->q_full, h * 64, g * G,
                                     (mt0 + m) * tpb);
             int nk = 0, nv = 0;  // K and V tiles issued
+            int st = 0;
+            uint32_t ph = 0;
             for (int it = 0; it < n_my; ++it) {
-                const int st = it % NSTAGE;
-                const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
                 const int tok0 = (tile_begin + it) * KV_TILE;
-                if (it >= NSTAGE && !tc::mbar_wait(&tl->k_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
-                tc::mbar_arrive_expect_tx(&tl->k_full[st], TILE_BYTES);
+                if (it >= nst && !tc::mbar_wait(&tl->k_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
+                tc::mbar_arrive_expect_tx(&tl->k_full[st], KV_TILE_BYTES);
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sK + st * TILE_BYTES + h * HALF_BYTES, &tm_k, &tl->k_full[st], h * 64, tok0, g);
+                    tc::tma_load_3d(sK + st * KV_TILE_BYTES + h * KV_HALF_BYTES, &tm_k, &tl->k_full[st], h * 64,
+                                    tok0, g);
                 nk = it + 1;
-                if (it >= NSTAGE && !tc::mbar_wait(&tl->v_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
-                tc::mbar_arrive_expect_tx(&tl->v_full[st], TILE_BYTES);
+                if (it >= nst && !tc::mbar_wait(&tl->v_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
+                tc::mbar_arrive_expect_tx(&tl->v_full[st], KV_TILE_BYTES);
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sV + st * TILE_BYTES + h * HALF_BYTES, &tm_v, &tl->v_full[st], h * 64, tok0, g);
+                    tc::tma_load_3d(sV + st * KV_TILE_BYTES + h * KV_HALF_BYTES, &tm_v, &tl->v_full[st], h * 64,
+                                    tok0, g);
                 nv = it + 1;
+                if (++st == nst) { st = 0; ph ^= 1u; }
             }
             // never leave with a copy in flight into this CTA's shared memory
             tc::mbar_wait(&tl->q_full, 0, nullptr);
-            for (int it = max(0, nk - NSTAGE); it < nk; ++it)
-                tc::mbar_wait(&tl->k_full[it % NSTAGE], (uint32_t)(it / NSTAGE) & 1u, nullptr);
-            for (int it = max(0, nv - NSTAGE); it < nv; ++it)
-                tc::mbar_wait(&tl->v_full[it % NSTAGE], (uint32_t)(it / NSTAGE) & 1u, nullptr);
+            for (int j = max(0, nk - nst); j < nk; ++j)
+                tc::mbar_wait(&tl->k_full[j % nst], (uint32_t)(j / nst) & 1u, nullptr);
+            for (int j = max(0, nv - nst); j < nv; ++j)
+                tc::mbar_wait(&tl->v_full[j % nst], (uint32_t)(j / nst) & 1u, nullptr);
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n_my > 0) {
-            const uint32_t id_s = tc::idesc_bf16_f32(128, 128, false);
+            const uint32_t id_s = tc::idesc_bf16_f32(128, KV_TILE, false);
             const uint32_t id_o = tc::idesc_bf16_f32(128, 128, true);
+            const uint32_t q_addr0 = tc::smem_u32(sQ), q_addr1 = tc::smem_u32(sQ + Q_TILE_BYTES);
+            int kst = 0, vst = 0;
+            uint32_t kph = 0, vph = 0;
             bool ok = tc::mbar_wait(&tl->q_full, 0, abort_flag);
-            for (int it = 0; ok && it < n_my; ++it) {
-                const int st = it % NSTAGE;
-                const uint32_t ph = (uint32_t)(it / NSTAGE) & 1u;
-                if (!(ok = tc::mbar_wait(&tl->k_full[st], ph, abort_flag))) break;
+            if (ok) ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag);
+            if (ok) {
                 tc::fence_after_sync();
-                const uint32_t kbase = tc::smem_u32(sK + st * TILE_BYTES);
-                for (int m = 0; m < nm; ++m) {
-                    const uint32_t qbase = tc::smem_u32(sQ + m * TILE_BYTES);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = (uint32_t)((k >> 2) * HALF_BYTES + (k & 3) * 32);
-                        tc::mma_ss(tbase + m * 128, tc::smem_desc_sw128(qbase + off, 16, 1024),
-                                   tc::smem_desc_sw128(kbase + off, 16, 1024), id_s, k > 0);
-                    }
-                    tc::mma_commit(&tl->s_full[m]);
+                const uint32_t kb = tc::smem_u32(sK + kst * KV_TILE_BYTES);
+                issue_s(tbase + COL_S, q_addr0, kb, id_s);
+                tc::mma_commit(&tl->s_full[0]);
+                if (pair) {
+                    issue_s(tbase + COL_S + 64, q_addr1, kb, id_s);
+                    tc::mma_commit(&tl->s_full[1]);
                 }
-                tc::mma_commit(&tl->k_empty[st]);
-                if (!(ok = tc::mbar_wait(&tl->v_full[st], ph, abort_flag))) break;
-                const uint32_t vbase = tc::smem_u32(sV + st * TILE_BYTES);
-                for (int m = 0; m < nm; ++m) {
-                    if (!(ok = tc::mbar_wait(&tl->p_full[m], (uint32_t)it & 1u, abort_flag))) break;
+                tc::mma_commit(&tl->k_empty[kst]);
+                if (++kst == nst) { kst = 0; kph ^= 1u; }
+            }
+            for (int it = 0; ok && it < n_my; ++it) {
+                const uint32_t par = (uint32_t)it & 1u;
+                // next scores first (as soon as the softmax has read S_m(it)), then O += P V
+                if (it + 1 < n_my) {
+                    if (!(ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag))) break;
+                    const uint32_t kb = tc::smem_u32(sK + kst * KV_TILE_BYTES);
+                    if (!(ok = tc::mbar_wait(&tl->s_free[0], par, abort_flag))) break;
                     tc::fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ts(tbase + 256 + m * 128, tbase + m * 128 + kk * 8,
-                                   tc::smem_desc_sw128(vbase + kk * 2048, HALF_BYTES, 1024), id_o, (it > 0 || kk > 0));
-                    tc::mma_commit(&tl->o_done[m]);
+                    issue_s(tbase + COL_S, q_addr0, kb, id_s);
+                    tc::mma_commit(&tl->s_full[0]);
+                    if (pair) {
+                        if (!(ok = tc::mbar_wait(&tl->s_free[1], par, abort_flag))) break;
+                        tc::fence_after_sync();
+                        issue_s(tbase + COL_S + 64, q_addr1, kb, id_s);
+                        tc::mma_commit(&tl->s_full[1]);
+                    }
+                    tc::mma_commit(&tl->k_empty[kst]);
+                    if (++kst == nst) { kst = 0; kph ^= 1u; }
                 }
-                if (!ok) break;
-                tc::mma_commit(&tl->v_empty[st]);
+                if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
+                const uint32_t vb = tc::smem_u32(sV + vst * KV_TILE_BYTES);
+                const uint32_t pb = 32u * (uint32_t)(it & 1);
+                const uint32_t ppar = (uint32_t)(it >> 1) & 1u;
+                if (!(ok = tc::mbar_wait(&tl->p_full[0][it & 1], ppar, abort_flag))) break;
+                tc::fence_after_sync();
+                issue_pv(tbase + COL_O, tbase + COL_P + pb, vb, id_o, it > 0);
+                tc::mma_commit(&tl->o_done[0][it & 1]);
+                if (pair) {
+                    if (!(ok = tc::mbar_wait(&tl->p_full[1][it & 1], ppar, abort_flag))) break;
+                    tc::fence_after_sync();
+                    issue_pv(tbase + COL_O + 128, tbase + COL_P + 64 + pb, vb, id_o, it > 0);
+                    tc::mma_commit(&tl->o_done[1][it & 1]);
+                }
+                tc::mma_commit(&tl->v_empty[vst]);
+                if (++vst == nst) { vst = 0; vph ^= 1u; }
             }
             if (!ok) raise_abort(tl);
             // drain: every issued MMA completes before TMEM is released
             tc::mma_commit(&tl->mma_done);
             tc::mbar_wait(&tl->mma_done, 0, nullptr);
         }
+      }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
         // ------------------------------------------------------------ softmax warpgroups
-        const int wg = (warp - 2) >> 2;          // 0 or 1: M-tile owned
-        const int quad = warp & 3;               // TMEM lane quadrant this warp may access
-        const int r = quad * 32 + lane;          // row inside the M-tile
+        const int wg = (warp - 4) >> 2;  // 0 or 1
+        const int quad = warp & 3;       // TMEM lane quadrant this warp may access
+        const int r = quad * 32 + lane;  // row inside the M-tile
         const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
-        const uint32_t s_col = (uint32_t)wg * 128, o_col = 256 + (uint32_t)wg * 128;
         if (wg < nm && n_my > 0) {
             const int mt = mt0 + wg;
             const int t = mt * tpb + r / G;
             const int j = r % G;
-            const bool row_valid = r < tpb * G && t < a.T;
+            const bool row_valid = r < rows_loaded && t < a.T;
             uint64_t mk0 = 0, mk1 = 0;
             if (row_valid) {
                 mk0 = a.mask[2 * t];
@@ -211,120 +374,105 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const bool score_wg = a.chunk_scores != nullptr && a.score_row / tpb == mt;
             const bool is_score_row = score_wg && row_valid && t == a.score_row;
             const bool is_score_reducer = score_wg && r == (a.score_row % tpb) * G;
+            const bool score_warp = __any_sync(0xffffffffu, is_score_row || is_score_reducer);
+            const uint32_t s_addr = lane_addr + COL_S + 64u * (uint32_t)wg;
+            const uint32_t p_addr = lane_addr + COL_P + 64u * (uint32_t)wg;
+            const uint32_t o_addr = lane_addr + COL_O + 128u * (uint32_t)wg;
             const float c = a.scale_log2;
+            const float2 c2 = make_float2(c, c);
             float m_run = -INFINITY, l_run = 0.f;
             bool ok = true;
             for (int it = 0; it < n_my; ++it) {
+                const uint32_t par = (uint32_t)it & 1u;
                 const int tile = tile_begin + it;
                 const int64_t tok0 = (int64_t)tile * KV_TILE;
-                ok = tc::mbar_wait(&tl->s_full[wg], (uint32_t)it & 1u, abort_flag);
+                ok = tc::mbar_wait(&tl->s_full[wg], par, abort_flag);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc::fence_after_sync();
-                // Tiles wholly inside the prefix need no mask; others test each token.
-                const bool full_tile = tok0 + KV_TILE <= a.N;
-                auto visible = [&](int64_t tok) -> bool {
-                    if (tok < a.N) return true;
-                    if (tok >= a.N + a.T) return false;
-                    const int u = (int)(tok - a.N);
-                    return ((u < 64 ? (mk0 >> u) : (mk1 >> (u - 64))) & 1ull) != 0;
-                };
-                // ---- pass 1: row max (raw q.k) and the fused chunk sums of the scoring row
-                float mx = -INFINITY, s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lane_addr + s_col + cc * 32, v);
-                    tc::tmem_wait_ld();
-                    if (row_valid) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float xv = __uint_as_float(v[i]);
-                            const int64_t tok = tok0 + cc * 32 + i;
-                            if (is_score_row && tok < a.N) {
-                                if (cc < 2) s0 += xv; else s1 += xv;
+                uint32_t x0[32], x1[32];
+                tc::tmem_ld32(s_addr + 0, x0);
+                tc::tmem_ld32(s_addr + 32, x1);
+                tc::tmem_wait_ld();
+                // S_m is in registers: the next tile's scores may overwrite it
+                tc::fence_before_sync();
+                tc::mbar_arrive(&tl->s_free[wg]);
+
+                // ---- fused chunk importance of the scoring row (raw q.k, tokens < N)
+                if (score_warp) {
+                    if (is_score_row) {
+                        const int64_t lim64 = a.N - tok0;
+                        const int lim = lim64 >= 64 ? 64 : (lim64 < 0 ? 0 : (int)lim64);
+                        tl->score_part[it & 1][j] = sum_chunk(x0, lim) + sum_chunk(x1, lim - 32);
+                        tc::mbar_arrive(&tl->score_bar[it & 1]);
+                    }
+                    if (is_score_reducer) {
+                        if (tc::mbar_wait(&tl->score_bar[it & 1], (uint32_t)(it >> 1) & 1u, abort_flag)) {
+                            if (tok0 < a.N) {
+                                float best = tl->score_part[it & 1][0];
+                                for (int jj = 1; jj < G; ++jj) best = fmaxf(best, tl->score_part[it & 1][jj]);
+                                a.chunk_scores[(size_t)g * a.n_chunks + tile] = best;
                             }
-                            if (full_tile || visible(tok)) mx = fmaxf(mx, xv);
+                        } else {
+                            raise_abort(tl);
                         }
                     }
                 }
-                if (is_score_row) {
-                    tl->score_part[it & 1][j][0] = s0;
-                    tl->score_part[it & 1][j][1] = s1;
-                    tc::mbar_arrive(&tl->score_bar[it & 1]);
+
+                // ---- tiles that reach past the prefix: hide what this row may not see
+                if (tok0 + KV_TILE > a.N) {
+                    mask_chunk(x0, tok0 + 0, a.N, a.T, mk0, mk1);
+                    mask_chunk(x1, tok0 + 32, a.N, a.T, mk0, mk1);
                 }
-                if (is_score_reducer) {
-                    // the G score rows may sit in two warps: gather them through shared memory
-                    if (tc::mbar_wait(&tl->score_bar[it & 1], (uint32_t)(it >> 1) & 1u, abort_flag)) {
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int64_t cidx = (int64_t)tile * 2 + hh;
-                            if (cidx * 64 < a.N) {
-                                float best = tl->score_part[it & 1][0][hh];
-                                for (int jj = 1; jj < G; ++jj) best = fmaxf(best, tl->score_part[it & 1][jj][hh]);
-                                a.chunk_scores[(size_t)g * a.n_chunks + cidx] = best;
-                            }
-                        }
-                    } else {
-                        raise_abort(tl);
-                    }
-                }
+
+                // ---- row max (raw units), lazy running-max update
+                const float mx = fmaxf(max_chunk(x0), max_chunk(x1));
                 const float m_new = fmaxf(m_run, mx * c);
                 const bool resc = m_new > m_run + RESCALE_THRESHOLD;
-                const float alpha = resc ? ex2(m_run - m_new) : 1.f;
+                const float alpha = resc ? tc::ex2(m_run - m_new) : 1.f;
+                if (resc) {
+                    l_run *= alpha;
+                    m_run = m_new;
+                }
+
+                // ---- P = 2^(s*c - m) in bf16 (token k -> P column k/2, even k in the lower half)
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                const float2 nm2 = make_float2(neg_m, neg_m);
+                uint32_t pk0[16], pk1[16];
+                const float lsum = exp_chunk(x0, c2, nm2, pk0) + exp_chunk(x1, c2, nm2, pk1);
+
+                // ---- P buffer it&1 was last read by O += P(it-2) V: wait for it
+                // (each buffer's barrier completes once per two tiles, phase it>>1)
+                const int pbuf = it & 1;
+                if (it >= 2) {
+                    ok = tc::mbar_wait(&tl->o_done[wg][pbuf], (uint32_t)((it >> 1) - 1) & 1u, abort_flag);
+                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                }
+                // ---- rescale O_m by alpha: every earlier O += P V must be complete
                 if (it > 0 && __any_sync(0xffffffffu, resc)) {
-                    // O_m holds the previous tiles: wait for their P.V, then scale this warp's rows
-                    ok = tc::mbar_wait(&tl->o_done[wg], (uint32_t)(it - 1) & 1u, abort_flag);
+                    ok = tc::mbar_wait(&tl->o_done[wg][pbuf ^ 1], (uint32_t)((it - 1) >> 1) & 1u, abort_flag);
                     if (!(ok = __all_sync(0xffffffffu, ok))) break;
                     tc::fence_after_sync();
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         uint32_t ov[32];
-                        tc::tmem_ld32(lane_addr + o_col + cc * 32, ov);
+                        tc::tmem_ld32(o_addr + cc * 32, ov);
                         tc::tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tc::tmem_st32(lane_addr + o_col + cc * 32, ov);
+                        tc::tmem_st32(o_addr + cc * 32, ov);
                     }
-                    tc::tmem_wait_st();
                 }
-                if (resc) {
-                    l_run *= alpha;
-                    m_run = m_new;
-                }
-                // ---- pass 2: P = 2^(s*c - m) in bf16 over the first 64 columns of S_m
-                // (token k -> column k/2, even k in the lower half).  Chunk cc of S
-                // lands in P columns [16cc, 16cc+16), all already read.
-                const bool none_visible = (m_run == -INFINITY) || !row_valid;
-                const float neg_m = none_visible ? 0.f : -m_run;
-                float lsum = 0.f;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lane_addr + s_col + cc * 32, v);
-                    tc::tmem_wait_ld();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int64_t tok = tok0 + cc * 32 + 2 * i;
-                        float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), c, neg_m));
-                        float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), c, neg_m));
-                        if (none_visible) { p0 = 0.f; p1 = 0.f; }
-                        if (!full_tile) {
-                            if (!visible(tok)) p0 = 0.f;
-                            if (!visible(tok + 1)) p1 = 0.f;
-                        }
-                        lsum += p0 + p1;
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-                        pk[i] = *reinterpret_cast<uint32_t *>(&b2);
-                    }
-                    tc::tmem_st16(lane_addr + s_col + cc * 16, pk);
-                }
+                tc::fence_after_sync();
+                tc::tmem_st16(p_addr + 32 * pbuf + 0, pk0);
+                tc::tmem_st16(p_addr + 32 * pbuf + 16, pk1);
                 l_run += lsum;
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
-                tc::mbar_arrive(&tl->p_full[wg]);
+                tc::mbar_arrive(&tl->p_full[wg][pbuf]);
             }
-            // ---- epilogue: final O_m of this split
-            if (ok) ok = tc::mbar_wait(&tl->o_done[wg], (uint32_t)(n_my - 1) & 1u, abort_flag);
+
+            // ---- epilogue: O of this range
+            if (ok) ok = tc::mbar_wait(&tl->o_done[wg][(n_my - 1) & 1], (uint32_t)((n_my - 1) >> 1) & 1u, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 raise_abort(tl);
@@ -336,22 +484,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t ov[32];
-                    tc::tmem_ld32(lane_addr + o_col + cc * 32, ov);
+                    tc::tmem_ld32(o_addr + cc * 32, ov);
                     tc::tmem_wait_ld();
                     if (row_valid) {
-                        if (a.splits == 1) {
+                        if (L.direct) {
                             uint32_t pk[16];
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(ov[2 * i]) * inv,
-                                                                          __uint_as_float(ov[2 * i + 1]) * inv);
-                                pk[i] = *reinterpret_cast<uint32_t *>(&b2);
-                            }
+                            for (int i = 0; i < 16; ++i)
+                                pk[i] = tc::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv,
+                                                        __uint_as_float(ov[2 * i + 1]) * inv);
                             uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * 128 + cc * 32);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                         } else {
-                            float4 *dst = reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * 128 + cc * 32);
+                            float4 *dst = reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * 128 +
+                                                                     cc * 32);
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
                                 dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
@@ -360,10 +508,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     }
                 }
                 if (row_valid) {
-                    if (a.splits == 1) {
+                    if (L.direct) {
                         if (a.lse != nullptr) a.lse[row] = (m_run + log2f(l_run)) * TS_LN2;
                     } else {
-                        reinterpret_cast<float2 *>(a.ws_ml)[(size_t)split * a.T * a.Hq + row] = make_float2(m_run, l_run);
+                        reinterpret_cast<float2 *>(a.ws_ml)[(size_t)split * a.T * a.Hq + row] =
+                            make_float2(m_run, l_run);
                     }
                 }
             }
@@ -383,31 +532,84 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 // ----------------------------------------------------------------------------
 size_t tc_smem_bytes() { return TC_SMEM_BYTES; }
 
+static int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
 TcPlan tc_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms) {
     TcPlan p{};
     const int G = Hq / Hkv;
-    p.ok = d == 128 && T >= 64 && T <= 128 && G <= 32;
+    p.ok = d == 128 && T >= 64 && T <= 128 && G >= 1 && G <= 32;
     if (!p.ok) return p;
     p.tpb = 128 / G;
-    p.n_mtiles = (T + p.tpb - 1) / p.tpb;
-    p.n_mpairs = (p.n_mtiles + 1) / 2;
-    p.n_tiles = (int)((N + T + KV_TILE - 1) / KV_TILE);
-    const int base = Hkv * p.n_mpairs;
-    int splits = num_sms / base;
-    if (splits < 1) splits = 1;
-    if (splits > p.n_tiles) splits = p.n_tiles;
-    p.tiles_per_split = (p.n_tiles + splits - 1) / splits;
-    p.splits = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    p.n_mtiles = ceil_div(T, p.tpb);
+    p.n_pair = p.n_mtiles / 2;
+    p.n_single = p.n_mtiles % 2;
+    p.n_tiles = ceil_div(N + T, KV_TILE);
+    const int budget = num_sms / Hkv > 1 ? num_sms / Hkv : 1;  // CTAs per KV head that fit in one wave
+    int sp = 0, ss = 0;
+    if (p.n_pair == 0) {
+        ss = budget / p.n_single;
+    } else if (p.n_single == 0) {
+        sp = budget / p.n_pair;
+    } else {
+        // A pair stream does twice the MMA work per KV tile of a single stream:
+        // choose the split counts that minimise the largest CTA's work.
+        int best_cost = 0;
+        for (int cand = 1; cand <= p.n_tiles; ++cand) {
+            const int rest = budget - p.n_pair * cand;
+            if (rest < p.n_single) break;
+            const int cs = rest / p.n_single < p.n_tiles ? rest / p.n_single : p.n_tiles;
+            const int cost = 2 * ceil_div(p.n_tiles, cand) > ceil_div(p.n_tiles, cs) ? 2 * ceil_div(p.n_tiles, cand)
+                                                                                     : ceil_div(p.n_tiles, cs);
+            if (best_cost == 0 || cost < best_cost) {
+                best_cost = cost;
+                sp = cand;
+                ss = cs;
+            }
+        }
+    }
+    if (p.n_pair > 0) {
+        sp = sp < 1 ? 1 : (sp > p.n_tiles ? p.n_tiles : sp);
+        p.tl_pair = ceil_div(p.n_tiles, sp);
+        p.s_pair = ceil_div(p.n_tiles, p.tl_pair);
+    }
+    if (p.n_single > 0) {
+        ss = ss < 1 ? 1 : (ss > p.n_tiles ? p.n_tiles : ss);
+        p.tl_single = ceil_div(p.n_tiles, ss);
+        p.s_single = ceil_div(p.n_tiles, p.tl_single);
+    }
+    p.ctas_per_head = p.n_pair * p.s_pair + p.n_single * p.s_single;
+    p.splits = p.s_pair > p.s_single ? p.s_pair : p.s_single;
     return p;
 }
 
 cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtensorMap &tq, const CUtensorMap &tk,
                                 const CUtensorMap &tv, cudaStream_t st) {
+    // setmaxnreg.inc waits until the block's register pool can serve it, so the
+    // split must fit the registers the block is launched with.
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa{};
+        cudaError_t e0 = cudaFuncGetAttributes(&fa, tree_attn_tc_kernel);
+        if (e0 != cudaSuccess) return e0;
+        launch_regs = fa.numRegs;
+    }
+    if (128 * CTRL_REGS + 256 * SOFTMAX_REGS > TC_THREADS * launch_regs) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)TC_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.splits, p.n_mpairs, a.Hkv);
-    tree_attn_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(tq, tk, tv, a, p.n_mtiles);
+    TcLaunch L{};
+    L.tpb = p.tpb;
+    L.n_mtiles = p.n_mtiles;
+    L.n_pair = p.n_pair;
+    L.s_pair = p.s_pair;
+    L.s_single = p.s_single;
+    L.tl_pair = p.tl_pair;
+    L.tl_single = p.tl_single;
+    L.n_tiles = p.n_tiles;
+    L.ctas_per_head = p.ctas_per_head;
+    L.direct = p.splits == 1 ? 1 : 0;
+    dim3 grid(p.ctas_per_head * a.Hkv);
+    tree_attn_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(tq, tk, tv, a, L);
     return cudaGetLastError();
 }
 

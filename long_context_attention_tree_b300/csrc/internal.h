@@ -42,7 +42,10 @@ struct MergeArgs {
     const float *ws_ml;
     __nv_bfloat16 *out;
     float *lse;
-    int T, Hq, splits;
+    int T, Hq;
+    int splits;      // partials of rows t < t_split
+    int t_split;     // first batch row whose partial count is splits_hi
+    int splits_hi;   // partials of rows t >= t_split
 };
 
 struct SimtPlan {
@@ -53,10 +56,21 @@ SimtPlan simt_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms);
 cudaError_t launch_tree_attn_simt(const AttnArgs &a, const SimtPlan &p, cudaStream_t st);
 cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st);
 
-// tensor-core (tcgen05) path, head_dim 128, 64 <= T <= 128
+// tensor-core (tcgen05) path, head_dim 128, 64 <= T <= 128.
+constexpr int TC_KV_TILE = 64;  // KV tokens per pipeline step (one 64-token scoring chunk)
+// Per KV head the M-tiles are grouped into n_pair two-tile streams (ping-pong
+// between the two tiles) and n_single one-tile streams (double-buffered S);
+// each stream's KV tiles are split into s_pair / s_single contiguous ranges.
 struct TcPlan {
     bool ok;
-    int tpb, n_mtiles, n_mpairs, n_tiles, splits, tiles_per_split;
+    int tpb;                  // whole batch rows per M-tile (floor(128 / G))
+    int n_mtiles;             // ceil(T / tpb)
+    int n_pair, n_single;     // streams per KV head
+    int s_pair, s_single;     // KV splits per stream kind
+    int tl_pair, tl_single;   // KV tiles per split
+    int n_tiles;              // ceil((N + T) / TC_KV_TILE)
+    int ctas_per_head;        // n_pair * s_pair + n_single * s_single
+    int splits;               // max(s_pair, s_single): workspace slices
 };
 TcPlan tc_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms);
 size_t tc_smem_bytes();

@@ -238,14 +238,13 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
     cudaError_t e;
     if (plan.tc) {
         const ts::TcPlan &p = plan.tcp;
-        a.tiles_per_split = p.tiles_per_split;
         a.n_tiles = p.n_tiles;
         a.tpb = p.tpb;
         CUtensorMap tq, tk, tv;
         const uint64_t row_bytes = (uint64_t)d * 2;
         if (!encode_map(&tq, q, d, Hq, T, row_bytes, row_bytes * Hq, 64, a.G, p.tpb) ||
-            !encode_map(&tk, k, d, N + T, Hkv, row_bytes, row_bytes * ld_kv, 64, 128, 1) ||
-            !encode_map(&tv, v, d, N + T, Hkv, row_bytes, row_bytes * ld_kv, 64, 128, 1))
+            !encode_map(&tk, k, d, N + T, Hkv, row_bytes, row_bytes * ld_kv, 64, ts::TC_KV_TILE, 1) ||
+            !encode_map(&tv, v, d, N + T, Hkv, row_bytes, row_bytes * ld_kv, 64, ts::TC_KV_TILE, 1))
             return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled failed (or the driver entry point is missing)");
         e = ts::launch_tree_attn_tc(a, p, tq, tk, tv, s);
         if (e != cudaSuccess) return cuda_fail(e, "tree_attn_tc launch");
@@ -259,7 +258,13 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
     }
     ts::note_launches(1);
     if (plan.splits > 1) {
-        ts::MergeArgs m{a.ws_o, a.ws_ml, a.out, a.lse, T, Hq, plan.splits};
+        ts::MergeArgs m{a.ws_o, a.ws_ml, a.out, a.lse, T, Hq, plan.splits, T, plan.splits};
+        if (plan.tc) {
+            // rows of pair streams have s_pair partials, rows of the single stream s_single
+            m.splits = plan.tcp.s_pair;
+            m.t_split = 2 * plan.tcp.n_pair * plan.tcp.tpb;
+            m.splits_hi = plan.tcp.s_single;
+        }
         e = ts::launch_lse_merge(m, d, s);
         if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
         ts::note_launches(1);

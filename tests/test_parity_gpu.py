@@ -2,7 +2,12 @@
 
 Bars: bit-exact for chunk scores on integer data, selected indices, gathered
 caches, targets, min-p counts and acceptance; bf16 attention outputs within
-max-abs 2e-2 and relative L2 1e-2 of the fp64 result; LSE within 1e-3."""
+max-abs 2e-2 and relative L2 1e-2 of the fp64 result; LSE within 4e-3.
+
+The LSE bar follows from the arithmetic: the tensor-core path rounds every
+softmax weight to bf16 (unit roundoff 2^-8) and normalises by the sum of the
+rounded weights, so its log-sum-exp may differ from the exact one by up to
+log(1 + 2^-8) = 3.9e-3."""
 import math
 
 import numpy as np
@@ -17,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 MAX_ABS = 2e-2
 REL_L2 = 1e-2
-LSE_ABS = 1e-3
+LSE_ABS = 4e-3  # log(1 + 2^-8): bf16 softmax weights
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,6 +50,8 @@ def run_attn(q, k, v, N, parent, scale, scores=False, score_row=0, stream=None):
     ts.ts_tree_attn(q, k, v, N, dev_mask(parent), out, lse=lse, chunk_scores=sc, score_row=score_row,
                     workspace=ws, scale=scale, stream=stream)
     torch.cuda.synchronize()
+    # no bounded device-side wait may have given up
+    assert ts.ts_device_error(True) == ts.TS_OK
     return out, lse, sc
 
 
