@@ -7,35 +7,37 @@
 // Rows of one KV head g are the T x G pairs (t, j), t-major; an M-tile is
 // tpb = floor(128/G) whole batch rows times the G query heads of the group,
 // so every K/V byte staged in shared memory serves all G heads.  A CTA owns
-// one or two M-tiles of one KV head (a "pair" or "single" stream; two tiles
-// share every K/V load) and a contiguous range of 64-token KV tiles.  The
-// split counts are chosen on the host so that every CTA carries about the
-// same tensor-core work; the partials are combined by the log-sum-exp merge.
+// one or two M-tiles of one KV head and a contiguous range of 128-token KV
+// tiles:
+//   pair stream   two M-tiles sharing every K/V load; the MMAs of one tile
+//                 run while the softmax of the other works (ping-pong).
+//                 TMEM: S_0 S_1 O_0 O_1 (128 columns each), P_m over S_m.
+//   single stream one M-tile; S is double-buffered so the MMA of the next
+//                 KV tile runs while the softmax works.  TMEM: S_a S_b O.
+// The split counts are chosen on the host so that every CTA carries about
+// the same tensor-core work; the partials are combined by the log-sum-exp
+// merge kernel.
 //
-// Per KV tile i and M-tile m (TMEM columns: S_m 64, P_m 2 x 32, O_m 128):
-//   S_m(i) = Q_m K_i^T            8 MMAs, M=128 N=64 K=16, operands K-major
-//   softmax_m(i)                  S_m -> registers; P = 2^(s*c - m) -> P_m
-//   O_m   += P_m(i) V_i           4 MMAs, M=128 N=128 K=16, P from TMEM,
-//                                 V MN-major in shared memory
-// P has columns of its own, so S_m(i+1) is issued as soon as softmax_m(i)
-// has read S_m(i): the tensor pipe computes the next scores while the
-// softmax works.  P is double-buffered (buffer i&1), so softmax_m(i) only
-// waits for O_m += P(i-2) V, issued a whole tile earlier: the MMA latency
-// stays off the softmax's critical path and the tensor pipe sets the pace.
+// Per KV tile and M-tile: S = Q K^T (8 MMAs, M=128 N=128 K=16, operands
+// K-major in shared memory), softmax, O += P V (8 MMAs, P read from TMEM,
+// V MN-major in shared memory).  Every MMA descriptor is precomputed, so the
+// issuing thread only adds constants: issue keeps up with the 64-cycle MMAs.
 //
 // Warp roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: Q once, then K and V tiles into rings;
+//   warp 0      TMA producer: Q once, then K and V tiles into 2-stage rings;
 //   warp 1      owns TMEM (512 columns); one thread issues every tcgen05.mma;
-//   warps 2-3   idle (they complete the control warpgroup, whose registers
-//               are handed to the softmax warpgroups with setmaxnreg);
+//   warps 2-3   idle;
 //   warps 4-7   softmax warpgroup 0 (thread = row of M-tile 0);
 //   warps 8-11  softmax warpgroup 1 (M-tile 1 of a pair stream).
-// The running max is lazy: O and l are rescaled only when a row's max grows
-// by more than 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so
-// the TMEM round trip of a rescale is rare.  The chunk importance of the
-// scoring row is summed from the same S values.  Every wait is bounded (see
-// tc_ptx.cuh): a wait that gives up raises the CTA's abort flag and the
-// sticky device status word, and the CTA winds down.
+// A softmax thread loads its row of S (128 fp32) into registers and writes
+// P = 2^(s*c - m) as bf16 over the first 64 columns of S.  The running max
+// is lazy: O and l are rescaled only when a row's max grows by more than
+// 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so the TMEM
+// round trip of a rescale is rare.  The normaliser l sums the bf16-rounded
+// weights that the P.V product uses.  The chunk importance of the scoring
+// row is summed from the same S values.
+// Every wait is bounded (see tc_ptx.cuh): a wait that gives up raises the
+// CTA's abort flag and the sticky device status word, and the CTA winds down.
 #include "internal.h"
 #include "tc_ptx.cuh"
 #include "ts_common.cuh"
@@ -46,44 +48,32 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int TC_THREADS = 384;
-// Register split (setmaxnreg): the control warpgroup drops to CTRL_REGS, the
-// two softmax warpgroups rise to SOFTMAX_REGS.  128*CTRL + 256*SOFTMAX must
-// not exceed 384 x the kernel's launch register count (checked on the host).
-constexpr int CTRL_REGS = 96;
-constexpr int SOFTMAX_REGS = 200;
-constexpr int KV_TILE = TC_KV_TILE;             // 64 tokens
-constexpr int Q_TILE_BYTES = 128 * 128 * 2;     // 128 rows x 128 dims (two 64-column swizzled halves)
-constexpr int Q_HALF_BYTES = Q_TILE_BYTES / 2;
-constexpr int KV_TILE_BYTES = KV_TILE * 128 * 2;  // 64 tokens x 128 dims
-constexpr int KV_HALF_BYTES = KV_TILE_BYTES / 2;
-constexpr int SMEM_DATA_BYTES = 224 * 1024;     // pair: 2 Q + 4+4 KV stages; single: 1 Q + 6+6 KV stages
-constexpr float RESCALE_THRESHOLD = 20.0f;      // log2 units
-// TMEM columns
-constexpr uint32_t COL_S = 0;    // S_m at m*64
-constexpr uint32_t COL_P = 128;  // P_m buffer b at 128 + m*64 + b*32 (bf16 pairs)
-constexpr uint32_t COL_O = 256;  // O_m at 256 + m*128
+constexpr int TC_THREADS = 384;  // 168 registers per thread (3 warps per SM sub-partition)
+constexpr int KV_TILE = TC_KV_TILE;         // 128 tokens
+constexpr int TILE_BYTES = 128 * 128 * 2;   // 128 rows x 128 dims, two 64-column swizzled halves
+constexpr int HALF_BYTES = TILE_BYTES / 2;
+constexpr int NSTAGE = 2;                   // K and V ring depth (pair: 2 Q + 2 K + 2 V = 192 KB)
+constexpr int SMEM_DATA_BYTES = 6 * TILE_BYTES;
+constexpr float RESCALE_THRESHOLD = 20.0f;  // log2 units
 
 struct __align__(8) TcSmemTail {
     uint64_t q_full;
-    uint64_t k_full[6], k_empty[6];
-    uint64_t v_full[6], v_empty[6];
-    uint64_t s_full[2], s_free[2];
-    // [M-tile][P buffer]: a tile's P written / its O += P V complete.  One
-    // barrier per buffer: with P double-buffered the softmax may run a whole
-    // tile ahead of the issuer, which a single barrier's parity cannot tell.
-    uint64_t p_full[2][2], o_done[2][2];
+    uint64_t k_full[NSTAGE], k_empty[NSTAGE];
+    uint64_t v_full[NSTAGE], v_empty[NSTAGE];
+    // [slot]: the M-tile (pair stream, phase = tile) or the S buffer tile & 1
+    // (single stream, phase = tile >> 1).  A single stream's warps may run a
+    // tile ahead of one another, so its barriers are per buffer: a parity
+    // wait must never be two phases behind.
+    uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t mma_done;
-    uint64_t score_bar[2];    // the G score rows arrive once per tile (by tile parity)
+    uint64_t score_bar[2][2];                   // [half][parity]: the G score rows of that chunk arrived
     uint32_t tmem_base;
     int abort_flag;
-    float score_part[2][32];  // [tile parity][head j]
+    float score_part[2][2][32];                 // [half][parity][head j]
 };
 
 constexpr size_t TC_SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)SMEM_DATA_BYTES + sizeof(TcSmemTail);
 static_assert(TC_SMEM_BYTES <= 232448, "shared memory above the 227 KB per-block limit");
-static_assert(2 * Q_TILE_BYTES + 8 * KV_TILE_BYTES <= SMEM_DATA_BYTES, "pair layout");
-static_assert(1 * Q_TILE_BYTES + 12 * KV_TILE_BYTES <= SMEM_DATA_BYTES, "single layout");
 
 // Per-launch constants derived from the host plan.
 struct TcLaunch {
@@ -96,22 +86,27 @@ __device__ __forceinline__ void raise_abort(TcSmemTail *tl) {
     atomicExch(&g_device_error, (int)TS_ERR_TIMEOUT);
 }
 
-// S[128 x 64] = Q[128 x 128] K^T: 8 MMAs with K = 16 over the head dim.
-__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem, uint32_t idesc) {
+// Descriptors of 128-row swizzled tile halves, as 64-bit values to which a
+// byte offset >> 4 is added directly (the 14-bit start field cannot overflow
+// inside the 227 KB shared-memory window).
+__device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return tc::smem_desc_sw128(addr, 16, 1024); }
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr) { return tc::smem_desc_sw128(addr, HALF_BYTES, 1024); }
+__device__ __forceinline__ uint64_t dplus(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
+// S[128 x 128] = Q[128 x 128] K^T: 8 MMAs with K = 16 over the head dim.
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t dq, uint64_t dk, uint32_t idesc) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint32_t in_row = (uint32_t)(k & 3) * 32;  // 16 bf16 = 32 bytes inside the 128-byte swizzled row
-        tc::mma_ss(d_tmem, tc::smem_desc_sw128(q_smem + (k >> 2) * Q_HALF_BYTES + in_row, 16, 1024),
-                   tc::smem_desc_sw128(k_smem + (k >> 2) * KV_HALF_BYTES + in_row, 16, 1024), idesc, k > 0);
+        const uint32_t off = (uint32_t)((k >> 2) * HALF_BYTES + (k & 3) * 32);
+        tc::mma_ss(d_tmem, dplus(dq, off), dplus(dk, off), idesc, k > 0);
     }
 }
-// O[128 x 128] += P[128 x 64 tokens] V[64 tokens x 128]: 4 MMAs with K = 16 tokens.
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t idesc,
+// O[128 x 128] += P[128 x 128 tokens] V[128 tokens x 128]: 8 MMAs with K = 16 tokens.
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t dv, uint32_t idesc,
                                          bool accumulate) {
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        tc::mma_ts(o_tmem, p_tmem + kk * 8, tc::smem_desc_sw128(v_smem + kk * 2048, KV_HALF_BYTES, 1024), idesc,
-                   (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < 8; ++kk)
+        tc::mma_ts(o_tmem, p_tmem + kk * 8, dplus(dv, (uint32_t)kk * 2048), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // Softmax helpers on one 32-token chunk of a row of S held in registers.
@@ -144,7 +139,7 @@ __device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
 }
 // P = 2^(x*c - m) for 32 tokens -> 16 packed bf16x2 words (even token in the
 // lower half); returns the fp32 sum of the 32 bf16-rounded values, so that the
-// normaliser l sums exactly the weights the P.V product uses (a row dominated
+// normaliser sums exactly the weights the P.V product uses (a row dominated
 // by one key then reproduces that key's value without the weight's rounding).
 __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], float2 c2, float2 nm2, uint32_t (&pk)[16]) {
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
@@ -197,12 +192,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tiles_per = L.tl_single;
     }
     const int nm = pair ? 2 : 1;
-    const int nst = pair ? 4 : 6;
     const int tile_begin = split * tiles_per;
     const int n_my = max(0, min(L.n_tiles, tile_begin + tiles_per) - tile_begin);
-    unsigned char *sQ = base;                                  // [nm][Q_TILE_BYTES]
-    unsigned char *sK = sQ + (size_t)nm * Q_TILE_BYTES;        // [nst][KV_TILE_BYTES]
-    unsigned char *sV = sK + (size_t)nst * KV_TILE_BYTES;      // [nst][KV_TILE_BYTES]
+    unsigned char *sQ = base;                          // [nm][TILE_BYTES]
+    unsigned char *sK = sQ + (size_t)nm * TILE_BYTES;  // [NSTAGE][TILE_BYTES]
+    unsigned char *sV = sK + (size_t)NSTAGE * TILE_BYTES;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.G, tpb = L.tpb;
@@ -210,7 +204,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&tl->q_full, 1);
-        for (int s = 0; s < 6; ++s) {
+        for (int s = 0; s < NSTAGE; ++s) {
             tc::mbar_init(&tl->k_full[s], 1);
             tc::mbar_init(&tl->k_empty[s], 1);
             tc::mbar_init(&tl->v_full[s], 1);
@@ -218,15 +212,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         for (int m = 0; m < 2; ++m) {
             tc::mbar_init(&tl->s_full[m], 1);
-            tc::mbar_init(&tl->s_free[m], 128);
-            for (int b = 0; b < 2; ++b) {
-                tc::mbar_init(&tl->p_full[m][b], 128);
-                tc::mbar_init(&tl->o_done[m][b], 1);
-            }
+            tc::mbar_init(&tl->p_full[m], 128);
+            tc::mbar_init(&tl->o_done[m], 1);
+            tc::mbar_init(&tl->score_bar[m][0], (uint32_t)G);
+            tc::mbar_init(&tl->score_bar[m][1], (uint32_t)G);
         }
         tc::mbar_init(&tl->mma_done, 1);
-        tc::mbar_init(&tl->score_bar[0], (uint32_t)G);
-        tc::mbar_init(&tl->score_bar[1], (uint32_t)G);
         tl->abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -236,7 +227,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int per_half = (128 - rows_loaded) * 8;  // 16-byte units
         for (int e = threadIdx.x; e < nm * 2 * per_half; e += TC_THREADS) {
             const int mh = e / per_half, u = e % per_half;
-            uint4 *dst = reinterpret_cast<uint4 *>(sQ + (size_t)mh * Q_HALF_BYTES + (size_t)rows_loaded * 128) + u;
+            uint4 *dst = reinterpret_cast<uint4 *>(sQ + (size_t)mh * HALF_BYTES + (size_t)rows_loaded * 128) + u;
             *dst = make_uint4(0u, 0u, 0u, 0u);
         }
         tc::fence_proxy_async();
@@ -251,7 +242,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t tbase = tl->tmem_base;
 
     if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
       if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n_my > 0) {
@@ -262,91 +252,107 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tc::mbar_arrive_expect_tx(&tl->q_full, qbytes * nm);
             for (int m = 0; m < nm; ++m)
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sQ + m * Q_TILE_BYTES + h * Q_HALF_BYTES, &tm_q, &tl->q_full, h * 64, g * G,
+                    tc::tma_load_3d(sQ + m * TILE_BYTES + h * HALF_BYTES, &tm_q, &tl->q_full, h * 64, g * G,
                                     (mt0 + m) * tpb);
             int nk = 0, nv = 0;  // K and V tiles issued
             int st = 0;
             uint32_t ph = 0;
             for (int it = 0; it < n_my; ++it) {
                 const int tok0 = (tile_begin + it) * KV_TILE;
-                if (it >= nst && !tc::mbar_wait(&tl->k_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
-                tc::mbar_arrive_expect_tx(&tl->k_full[st], KV_TILE_BYTES);
+                if (it >= NSTAGE && !tc::mbar_wait(&tl->k_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
+                tc::mbar_arrive_expect_tx(&tl->k_full[st], TILE_BYTES);
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sK + st * KV_TILE_BYTES + h * KV_HALF_BYTES, &tm_k, &tl->k_full[st], h * 64,
-                                    tok0, g);
+                    tc::tma_load_3d(sK + st * TILE_BYTES + h * HALF_BYTES, &tm_k, &tl->k_full[st], h * 64, tok0, g);
                 nk = it + 1;
-                if (it >= nst && !tc::mbar_wait(&tl->v_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
-                tc::mbar_arrive_expect_tx(&tl->v_full[st], KV_TILE_BYTES);
+                if (it >= NSTAGE && !tc::mbar_wait(&tl->v_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
+                tc::mbar_arrive_expect_tx(&tl->v_full[st], TILE_BYTES);
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sV + st * KV_TILE_BYTES + h * KV_HALF_BYTES, &tm_v, &tl->v_full[st], h * 64,
-                                    tok0, g);
+                    tc::tma_load_3d(sV + st * TILE_BYTES + h * HALF_BYTES, &tm_v, &tl->v_full[st], h * 64, tok0, g);
                 nv = it + 1;
-                if (++st == nst) { st = 0; ph ^= 1u; }
+                if (++st == NSTAGE) { st = 0; ph ^= 1u; }
             }
             // never leave with a copy in flight into this CTA's shared memory
             tc::mbar_wait(&tl->q_full, 0, nullptr);
-            for (int j = max(0, nk - nst); j < nk; ++j)
-                tc::mbar_wait(&tl->k_full[j % nst], (uint32_t)(j / nst) & 1u, nullptr);
-            for (int j = max(0, nv - nst); j < nv; ++j)
-                tc::mbar_wait(&tl->v_full[j % nst], (uint32_t)(j / nst) & 1u, nullptr);
+            for (int j = max(0, nk - NSTAGE); j < nk; ++j)
+                tc::mbar_wait(&tl->k_full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, nullptr);
+            for (int j = max(0, nv - NSTAGE); j < nv; ++j)
+                tc::mbar_wait(&tl->v_full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, nullptr);
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n_my > 0) {
-            const uint32_t id_s = tc::idesc_bf16_f32(128, KV_TILE, false);
+            const uint32_t id_s = tc::idesc_bf16_f32(128, 128, false);
             const uint32_t id_o = tc::idesc_bf16_f32(128, 128, true);
-            const uint32_t q_addr0 = tc::smem_u32(sQ), q_addr1 = tc::smem_u32(sQ + Q_TILE_BYTES);
+            const uint64_t dq0 = desc_k(tc::smem_u32(sQ)), dq1 = desc_k(tc::smem_u32(sQ + TILE_BYTES));
+            const uint64_t dk0 = desc_k(tc::smem_u32(sK)), dv0 = desc_mn(tc::smem_u32(sV));
             int kst = 0, vst = 0;
             uint32_t kph = 0, vph = 0;
             bool ok = tc::mbar_wait(&tl->q_full, 0, abort_flag);
             if (ok) ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag);
             if (ok) {
                 tc::fence_after_sync();
-                const uint32_t kb = tc::smem_u32(sK + kst * KV_TILE_BYTES);
-                issue_s(tbase + COL_S, q_addr0, kb, id_s);
+                const uint64_t dk = dplus(dk0, (uint32_t)kst * TILE_BYTES);
+                issue_s(tbase + 0, dq0, dk, id_s);
                 tc::mma_commit(&tl->s_full[0]);
                 if (pair) {
-                    issue_s(tbase + COL_S + 64, q_addr1, kb, id_s);
+                    issue_s(tbase + 128, dq1, dk, id_s);
                     tc::mma_commit(&tl->s_full[1]);
                 }
                 tc::mma_commit(&tl->k_empty[kst]);
-                if (++kst == nst) { kst = 0; kph ^= 1u; }
+                if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
             }
             for (int it = 0; ok && it < n_my; ++it) {
-                const uint32_t par = (uint32_t)it & 1u;
-                // next scores first (as soon as the softmax has read S_m(it)), then O += P V
-                if (it + 1 < n_my) {
-                    if (!(ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag))) break;
-                    const uint32_t kb = tc::smem_u32(sK + kst * KV_TILE_BYTES);
-                    if (!(ok = tc::mbar_wait(&tl->s_free[0], par, abort_flag))) break;
-                    tc::fence_after_sync();
-                    issue_s(tbase + COL_S, q_addr0, kb, id_s);
-                    tc::mma_commit(&tl->s_full[0]);
-                    if (pair) {
-                        if (!(ok = tc::mbar_wait(&tl->s_free[1], par, abort_flag))) break;
-                        tc::fence_after_sync();
-                        issue_s(tbase + COL_S + 64, q_addr1, kb, id_s);
-                        tc::mma_commit(&tl->s_full[1]);
-                    }
-                    tc::mma_commit(&tl->k_empty[kst]);
-                    if (++kst == nst) { kst = 0; kph ^= 1u; }
-                }
-                if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
-                const uint32_t vb = tc::smem_u32(sV + vst * KV_TILE_BYTES);
-                const uint32_t pb = 32u * (uint32_t)(it & 1);
-                const uint32_t ppar = (uint32_t)(it >> 1) & 1u;
-                if (!(ok = tc::mbar_wait(&tl->p_full[0][it & 1], ppar, abort_flag))) break;
-                tc::fence_after_sync();
-                issue_pv(tbase + COL_O, tbase + COL_P + pb, vb, id_o, it > 0);
-                tc::mma_commit(&tl->o_done[0][it & 1]);
+                const bool more = it + 1 < n_my;
                 if (pair) {
-                    if (!(ok = tc::mbar_wait(&tl->p_full[1][it & 1], ppar, abort_flag))) break;
+                    // PV_0(it), S_0(it+1), PV_1(it), S_1(it+1): while one M-tile's
+                    // softmax works, the tensor pipe runs the other tile's MMAs.
+                    const uint32_t par = (uint32_t)it & 1u;
+                    if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
+                    const uint64_t dv = dplus(dv0, (uint32_t)vst * TILE_BYTES);
+                    if (!(ok = tc::mbar_wait(&tl->p_full[0], par, abort_flag))) break;
                     tc::fence_after_sync();
-                    issue_pv(tbase + COL_O + 128, tbase + COL_P + 64 + pb, vb, id_o, it > 0);
-                    tc::mma_commit(&tl->o_done[1][it & 1]);
+                    issue_pv(tbase + 256, tbase + 0, dv, id_o, it > 0);
+                    tc::mma_commit(&tl->o_done[0]);
+                    uint64_t dk = 0;
+                    if (more) {
+                        if (!(ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag))) break;
+                        tc::fence_after_sync();
+                        dk = dplus(dk0, (uint32_t)kst * TILE_BYTES);
+                        issue_s(tbase + 0, dq0, dk, id_s);
+                        tc::mma_commit(&tl->s_full[0]);
+                    }
+                    if (!(ok = tc::mbar_wait(&tl->p_full[1], par, abort_flag))) break;
+                    tc::fence_after_sync();
+                    issue_pv(tbase + 384, tbase + 128, dv, id_o, it > 0);
+                    tc::mma_commit(&tl->o_done[1]);
+                    tc::mma_commit(&tl->v_empty[vst]);
+                    if (++vst == NSTAGE) { vst = 0; vph ^= 1u; }
+                    if (more) {
+                        issue_s(tbase + 128, dq1, dk, id_s);
+                        tc::mma_commit(&tl->s_full[1]);
+                        tc::mma_commit(&tl->k_empty[kst]);
+                        if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
+                    }
+                } else {
+                    // S(it+1) into the other S buffer, then PV(it).
+                    if (more) {
+                        if (!(ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag))) break;
+                        tc::fence_after_sync();
+                        const int b = (it + 1) & 1;
+                        issue_s(tbase + 128 * b, dq0, dplus(dk0, (uint32_t)kst * TILE_BYTES), id_s);
+                        tc::mma_commit(&tl->s_full[b]);
+                        tc::mma_commit(&tl->k_empty[kst]);
+                        if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
+                    }
+                    if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
+                    const int b = it & 1;
+                    if (!(ok = tc::mbar_wait(&tl->p_full[b], (uint32_t)(it >> 1) & 1u, abort_flag))) break;
+                    tc::fence_after_sync();
+                    issue_pv(tbase + 256, tbase + 128 * b, dplus(dv0, (uint32_t)vst * TILE_BYTES), id_o, it > 0);
+                    tc::mma_commit(&tl->o_done[b]);
+                    tc::mma_commit(&tl->v_empty[vst]);
+                    if (++vst == NSTAGE) { vst = 0; vph ^= 1u; }
                 }
-                tc::mma_commit(&tl->v_empty[vst]);
-                if (++vst == nst) { vst = 0; vph ^= 1u; }
             }
             if (!ok) raise_abort(tl);
             // drain: every issued MMA completes before TMEM is released
@@ -355,14 +361,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
       }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
         // ------------------------------------------------------------ softmax warpgroups
-        const int wg = (warp - 4) >> 2;  // 0 or 1
+        const int wm = (warp - 4) >> 2;  // M-tile slot 0 or 1
         const int quad = warp & 3;       // TMEM lane quadrant this warp may access
         const int r = quad * 32 + lane;  // row inside the M-tile
         const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
-        if (wg < nm && n_my > 0) {
-            const int mt = mt0 + wg;
+        if (wm < nm && n_my > 0) {
+            const int mt = mt0 + wm;
             const int t = mt * tpb + r / G;
             const int j = r % G;
             const bool row_valid = r < rows_loaded && t < a.T;
@@ -375,57 +380,64 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const bool is_score_row = score_wg && row_valid && t == a.score_row;
             const bool is_score_reducer = score_wg && r == (a.score_row % tpb) * G;
             const bool score_warp = __any_sync(0xffffffffu, is_score_row || is_score_reducer);
-            const uint32_t s_addr = lane_addr + COL_S + 64u * (uint32_t)wg;
-            const uint32_t p_addr = lane_addr + COL_P + 64u * (uint32_t)wg;
-            const uint32_t o_addr = lane_addr + COL_O + 128u * (uint32_t)wg;
+            const uint32_t o_addr = lane_addr + (pair ? 256u + 128u * (uint32_t)wm : 256u);
             const float c = a.scale_log2;
             const float2 c2 = make_float2(c, c);
             float m_run = -INFINITY, l_run = 0.f;
             bool ok = true;
             for (int it = 0; it < n_my; ++it) {
-                const uint32_t par = (uint32_t)it & 1u;
+                const int slot = pair ? wm : (it & 1);
+                const uint32_t spar = pair ? ((uint32_t)it & 1u) : ((uint32_t)(it >> 1) & 1u);
                 const int tile = tile_begin + it;
                 const int64_t tok0 = (int64_t)tile * KV_TILE;
-                ok = tc::mbar_wait(&tl->s_full[wg], par, abort_flag);
+                ok = tc::mbar_wait(&tl->s_full[slot], spar, abort_flag);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc::fence_after_sync();
-                uint32_t x0[32], x1[32];
+                const uint32_t s_addr = lane_addr + 128u * (uint32_t)slot;
+                uint32_t x0[32], x1[32], x2[32], x3[32];
                 tc::tmem_ld32(s_addr + 0, x0);
                 tc::tmem_ld32(s_addr + 32, x1);
+                tc::tmem_ld32(s_addr + 64, x2);
+                tc::tmem_ld32(s_addr + 96, x3);
                 tc::tmem_wait_ld();
-                // S_m is in registers: the next tile's scores may overwrite it
-                tc::fence_before_sync();
-                tc::mbar_arrive(&tl->s_free[wg]);
 
-                // ---- fused chunk importance of the scoring row (raw q.k, tokens < N)
+                // ---- fused chunk importance of the scoring row: chunks 2*tile and 2*tile+1
                 if (score_warp) {
+                    const int pb = it & 1;
                     if (is_score_row) {
                         const int64_t lim64 = a.N - tok0;
-                        const int lim = lim64 >= 64 ? 64 : (lim64 < 0 ? 0 : (int)lim64);
-                        tl->score_part[it & 1][j] = sum_chunk(x0, lim) + sum_chunk(x1, lim - 32);
-                        tc::mbar_arrive(&tl->score_bar[it & 1]);
+                        const int lim = lim64 >= 128 ? 128 : (lim64 < 0 ? 0 : (int)lim64);
+                        tl->score_part[0][pb][j] = sum_chunk(x0, lim) + sum_chunk(x1, lim - 32);
+                        tl->score_part[1][pb][j] = sum_chunk(x2, lim - 64) + sum_chunk(x3, lim - 96);
+                        tc::mbar_arrive(&tl->score_bar[0][pb]);
                     }
                     if (is_score_reducer) {
-                        if (tc::mbar_wait(&tl->score_bar[it & 1], (uint32_t)(it >> 1) & 1u, abort_flag)) {
-                            if (tok0 < a.N) {
-                                float best = tl->score_part[it & 1][0];
-                                for (int jj = 1; jj < G; ++jj) best = fmaxf(best, tl->score_part[it & 1][jj]);
-                                a.chunk_scores[(size_t)g * a.n_chunks + tile] = best;
+                        if (tc::mbar_wait(&tl->score_bar[0][pb], (uint32_t)(it >> 1) & 1u, abort_flag)) {
+                            for (int hh = 0; hh < 2; ++hh) {
+                                if (tok0 + 64 * hh < a.N) {
+                                    float best = tl->score_part[hh][pb][0];
+                                    for (int jj = 1; jj < G; ++jj) best = fmaxf(best, tl->score_part[hh][pb][jj]);
+                                    a.chunk_scores[(size_t)g * a.n_chunks + 2 * tile + hh] = best;
+                                }
                             }
                         } else {
                             raise_abort(tl);
                         }
                     }
+                    // reconverge before the warp-collective TMEM accesses below
+                    __syncwarp();
                 }
 
                 // ---- tiles that reach past the prefix: hide what this row may not see
                 if (tok0 + KV_TILE > a.N) {
                     mask_chunk(x0, tok0 + 0, a.N, a.T, mk0, mk1);
                     mask_chunk(x1, tok0 + 32, a.N, a.T, mk0, mk1);
+                    mask_chunk(x2, tok0 + 64, a.N, a.T, mk0, mk1);
+                    mask_chunk(x3, tok0 + 96, a.N, a.T, mk0, mk1);
                 }
 
                 // ---- row max (raw units), lazy running-max update
-                const float mx = fmaxf(max_chunk(x0), max_chunk(x1));
+                const float mx = fmaxf(fmaxf(max_chunk(x0), max_chunk(x1)), fmaxf(max_chunk(x2), max_chunk(x3)));
                 const float m_new = fmaxf(m_run, mx * c);
                 const bool resc = m_new > m_run + RESCALE_THRESHOLD;
                 const float alpha = resc ? tc::ex2(m_run - m_new) : 1.f;
@@ -434,23 +446,41 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     m_run = m_new;
                 }
 
-                // ---- P = 2^(s*c - m) in bf16 (token k -> P column k/2, even k in the lower half)
+                // ---- P = 2^(s*c - m) in bf16 over the first 64 columns of S
+                // (token k -> column k/2, even k in the lower half; S is in registers)
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 const float2 nm2 = make_float2(neg_m, neg_m);
-                uint32_t pk0[16], pk1[16];
-                const float lsum = exp_chunk(x0, c2, nm2, pk0) + exp_chunk(x1, c2, nm2, pk1);
-
-                // ---- P buffer it&1 was last read by O += P(it-2) V: wait for it
-                // (each buffer's barrier completes once per two tiles, phase it>>1)
-                const int pbuf = it & 1;
-                if (it >= 2) {
-                    ok = tc::mbar_wait(&tl->o_done[wg][pbuf], (uint32_t)((it >> 1) - 1) & 1u, abort_flag);
-                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                float lsum;
+                {
+                    uint32_t pk[16];
+                    lsum = exp_chunk(x0, c2, nm2, pk);
+                    tc::tmem_st16(s_addr + 0, pk);
                 }
-                // ---- rescale O_m by alpha: every earlier O += P V must be complete
+                {
+                    uint32_t pk[16];
+                    lsum += exp_chunk(x1, c2, nm2, pk);
+                    tc::tmem_st16(s_addr + 16, pk);
+                }
+                {
+                    uint32_t pk[16];
+                    lsum += exp_chunk(x2, c2, nm2, pk);
+                    tc::tmem_st16(s_addr + 32, pk);
+                }
+                {
+                    uint32_t pk[16];
+                    lsum += exp_chunk(x3, c2, nm2, pk);
+                    tc::tmem_st16(s_addr + 48, pk);
+                }
+                l_run += lsum;
+
+                // ---- rescale O by alpha (before this tile's P.V)
                 if (it > 0 && __any_sync(0xffffffffu, resc)) {
-                    ok = tc::mbar_wait(&tl->o_done[wg][pbuf ^ 1], (uint32_t)((it - 1) >> 1) & 1u, abort_flag);
-                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                    if (!pair) {
+                        // a single stream computes S ahead: wait for the previous P.V into O
+                        ok = tc::mbar_wait(&tl->o_done[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1u, abort_flag);
+                        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                    }
+                    // (a pair stream's S_m(it) was issued after P_m(it-1).V, so O_m is final here)
                     tc::fence_after_sync();
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
@@ -462,17 +492,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         tc::tmem_st32(o_addr + cc * 32, ov);
                     }
                 }
-                tc::fence_after_sync();
-                tc::tmem_st16(p_addr + 32 * pbuf + 0, pk0);
-                tc::tmem_st16(p_addr + 32 * pbuf + 16, pk1);
-                l_run += lsum;
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
-                tc::mbar_arrive(&tl->p_full[wg][pbuf]);
+                tc::mbar_arrive(&tl->p_full[slot]);
             }
 
             // ---- epilogue: O of this range
-            if (ok) ok = tc::mbar_wait(&tl->o_done[wg][(n_my - 1) & 1], (uint32_t)((n_my - 1) >> 1) & 1u, abort_flag);
+            // (completion of the last P.V implies every earlier one: MMAs complete in order)
+            if (ok) {
+                if (pair)
+                    ok = tc::mbar_wait(&tl->o_done[wm], (uint32_t)(n_my - 1) & 1u, abort_flag);
+                else
+                    ok = tc::mbar_wait(&tl->o_done[(n_my - 1) & 1], (uint32_t)((n_my - 1) >> 1) & 1u, abort_flag);
+            }
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 raise_abort(tl);
@@ -498,14 +530,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                             for (int i = 0; i < 4; ++i)
                                 dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                         } else {
-                            float4 *dst = reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * 128 +
-                                                                     cc * 32);
+                            float4 *dst =
+                                reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * 128 + cc * 32);
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
                                 dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
                                                      __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
                         }
                     }
+                    __syncwarp();
                 }
                 if (row_valid) {
                     if (L.direct) {
@@ -584,16 +617,6 @@ TcPlan tc_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms) {
 
 cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtensorMap &tq, const CUtensorMap &tk,
                                 const CUtensorMap &tv, cudaStream_t st) {
-    // setmaxnreg.inc waits until the block's register pool can serve it, so the
-    // split must fit the registers the block is launched with.
-    static int launch_regs = -1;
-    if (launch_regs < 0) {
-        cudaFuncAttributes fa{};
-        cudaError_t e0 = cudaFuncGetAttributes(&fa, tree_attn_tc_kernel);
-        if (e0 != cudaSuccess) return e0;
-        launch_regs = fa.numRegs;
-    }
-    if (128 * CTRL_REGS + 256 * SOFTMAX_REGS > TC_THREADS * launch_regs) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)TC_SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -57,7 +57,7 @@ cudaError_t launch_tree_attn_simt(const AttnArgs &a, const SimtPlan &p, cudaStre
 cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st);
 
 // tensor-core (tcgen05) path, head_dim 128, 64 <= T <= 128.
-constexpr int TC_KV_TILE = 64;  // KV tokens per pipeline step (one 64-token scoring chunk)
+constexpr int TC_KV_TILE = 128;  // KV tokens per pipeline step (two 64-token scoring chunks)
 // Per KV head the M-tiles are grouped into n_pair two-tile streams (ping-pong
 // between the two tiles) and n_single one-tile streams (double-buffered S);
 // each stream's KV tiles are split into s_pair / s_single contiguous ranges.

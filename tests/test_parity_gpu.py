@@ -354,3 +354,24 @@ def test_vocab_data_errors_reported_not_trapped():
     # the context is still usable
     t, _, r, _ = run_vocab(vi.logits, vi.history, vi.parent, vi.draft, vi.anchor)
     assert r[3] == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,N", [(4, 4, 102400), (10, 2, 40960)])
+def test_fused_scores_leave_attention_bitwise_unchanged(Hq, Hkv, N):
+    """The fused chunk scoring only reads S: outputs with and without it must be
+    bit-identical, on long KV ranges where warps drift apart (one-tile streams
+    with double-buffered S, and two-tile plus one-tile streams for group 5)."""
+    T, d = 120, 128
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=N + Hq, device="cuda")
+    parent = W.verify_parents()
+    scale = 1 / math.sqrt(d)
+    o1, l1, _ = run_attn(q, k, v, N, parent, scale)
+    for score_row in (0, 64, T - 1):
+        o2, l2, sc = run_attn(q, k, v, N, parent, scale, scores=True, score_row=score_row)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2), f"score_row {score_row}"
+    rows = np.unique(np.concatenate([np.arange(Hq), np.arange(T * Hq - Hq, T * Hq),
+                                     np.random.default_rng(N).integers(0, T * Hq, 24)])).astype(np.int32)
+    ro, rl = oracle.tree_attn(q.cpu(), k.cpu(), v.cpu(), N, parent, scale, rows=rows)
+    o = o1.reshape(-1, d)[rows].float().cpu().double().numpy()
+    assert np.abs(o - ro).max() <= MAX_ABS
+    assert np.abs(l1.reshape(-1)[rows].cpu().double().numpy() - rl).max() <= LSE_ABS
