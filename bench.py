@@ -240,30 +240,54 @@ def run_native(args, ws, rank, local):
             step.run(s)
     s.synchronize()
 
-    # ---- timed region: eager launches on one stream, events around every verify call
+    # ---- timed region: one CUDA graph per timed step (the whole step: every
+    # layer's verify, refresh and draft calls, then the vocab stage), with
+    # event-record nodes around each call so every kernel is timed on the
+    # stream it runs on, free of host launch gaps.
     nL = step.n_layers
-    ev_v = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
-            for _ in range(args.steps)]
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True, external=True)
+
+    graphs, marks = [], []
+    launches0 = ts.ts_launch_count()
+    for k in range(args.steps):
+        g = torch.cuda.CUDAGraph()
+        mk = {"layer": [], "vocab": None}
+        with torch.cuda.graph(g, stream=s):
+            for i in range(nL):
+                e = (ev(), ev(), ev(), ev())
+                e[0].record(s)
+                step.run_verify(i, s)
+                e[1].record(s)
+                step.run_refresh(i, s)
+                e[2].record(s)
+                step.run_draft(i, s)
+                e[3].record(s)
+                mk["layer"].append(e)
+            if step.vocab:
+                e = (ev(), ev())
+                e[0].record(s)
+                step.run_vocab(s)
+                e[1].record(s)
+                mk["vocab"] = e
+        graphs.append(g)
+        marks.append(mk)
+    launches = ts.ts_launch_count() - launches0  # kernels per replay x steps (counted at capture)
+    with torch.cuda.stream(s):
+        graphs[0].replay()  # first replay uploads the graph
+    s.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     time.sleep(0.3)
     barrier(ws)
     torch.cuda.synchronize()
-    launches0 = ts.ts_launch_count()
     with torch.cuda.stream(s):
         ev0.record(s)
-        for k in range(args.steps):
-            for i in range(nL):
-                ev_v[k][i][0].record(s)
-                step.run_verify(i, s)
-                ev_v[k][i][1].record(s)
-                step.run_refresh(i, s)
-                step.run_draft(i, s)
-            if step.vocab:
-                step.run_vocab(s)
+        for g in graphs:
+            g.replay()
         ev1.record(s)
     s.synchronize()
-    launches = ts.ts_launch_count() - launches0
     dev_status = ts.ts_device_error(True)
     torch.cuda.synchronize()
     barrier(ws)
@@ -273,7 +297,10 @@ def run_native(args, ws, rank, local):
     kv_step = step.kv_bytes_per_step()
     value_bps, t_max = aggregate(kv_step * args.steps, t_total, ws)
     ms_per_step = t_max / args.steps * 1e3
-    verify_ms = [ev_v[k][i][0].elapsed_time(ev_v[k][i][1]) for k in range(args.steps) for i in range(nL)]
+    verify_ms = [e[0].elapsed_time(e[1]) for mk in marks for e in mk["layer"]]
+    refresh_ms = [e[1].elapsed_time(e[2]) for mk in marks for e in mk["layer"]]
+    draft_ms = [e[2].elapsed_time(e[3]) for mk in marks for e in mk["layer"]]
+    vocab_ms = [mk["vocab"][0].elapsed_time(mk["vocab"][1]) for mk in marks if mk["vocab"] is not None]
     verify_avg_s = statistics.mean(verify_ms) / 1e3
 
     # ---- dominant kernel roofline: the verify attention call
@@ -296,6 +323,24 @@ def run_native(args, ws, rank, local):
     roof["verify_us_per_layer"] = verify_avg_s * 1e6
     roof["verify_kv_gbs"] = kv_layer / verify_avg_s / 1e9
     roof["verify_kv_frac_of_hbm"] = kv_layer / verify_avg_s / 1e9 / peaks["hbm"]
+
+    # ---- every row of the step, timed the same way (algorithmic bytes per call)
+    B, Td = step.B, step.Td
+    refresh_s = statistics.mean(refresh_ms) / 1e3
+    draft_s = statistics.mean(draft_ms) / 1e3
+    gather_bytes = 4 * cfg.Hkv * B * d * 2           # selected K and V chunks read, then written
+    draft_bytes = 2 * cfg.Hkv * (B + Td) * d * 2     # partial-cache K and V
+    kernels = {
+        "verify": {"us": verify_avg_s * 1e6, "kv_gbs": kv_layer / verify_avg_s / 1e9,
+                   "tflops": flops / verify_avg_s / 1e12},
+        "select_gather": {"us": refresh_s * 1e6, "gbs": gather_bytes / refresh_s / 1e9, "bytes": gather_bytes},
+        "draft_attention": {"us": draft_s * 1e6, "gbs": draft_bytes / draft_s / 1e9, "bytes": draft_bytes,
+                            "tflops": 4.0 * Td * Hq * (B + Td) * d / draft_s / 1e12},
+    }
+    if vocab_ms:
+        vocab_s = statistics.mean(vocab_ms) / 1e3
+        vbytes = T * cfg.vocab * 4
+        kernels["penalty_minp_verify"] = {"us": vocab_s * 1e6, "gbs": vbytes / vocab_s / 1e9, "bytes": vbytes}
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(step, s, args, ws)
@@ -322,9 +367,11 @@ def run_native(args, ws, rank, local):
             "kv_frac_of_hbm_peak": value / ws / peaks["hbm"],
             "kv_frac_of_hbm_nominal_8tbs": value / ws / 8000.0,
             "roofline": roof,
+            "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
+            "timing": "each timed step is one CUDA graph replay; per-call events are graph nodes",
             "device_status": dev_status,
             "clocks": clk,
             "peaks": peaks,

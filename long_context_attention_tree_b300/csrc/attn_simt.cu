@@ -269,7 +269,10 @@ tree_attn_simt_kernel(const AttnArgs a) {
     }
 }
 
-// Log-sum-exp merge over splits (log2 domain partials).  One warp per (t, h) row.
+// Log-sum-exp merge over splits (log2 domain partials).  One warp per (t, h)
+// row: the lanes read the splits' (m, l) pairs side by side, reduce the max
+// with shuffles, and then accumulate the weighted partial outputs with four
+// independent loads in flight per lane.
 template <int D>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeArgs a) {
     constexpr int DPL = D / 32;
@@ -281,27 +284,41 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeArgs a) {
     const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml);
     const int n_split = (warp / a.Hq) < a.t_split ? a.splits : a.splits_hi;
     float m = -INFINITY;
-    for (int s = 0; s < n_split; ++s) m = fmaxf(m, ml[s * stride + warp].x);
+    for (int s = lane; s < n_split; s += 32) m = fmaxf(m, ml[s * stride + warp].x);
+    m = warp_max(m);
     float l = 0.f;
+    for (int s = lane; s < n_split; s += 32) {
+        const float2 p = ml[s * stride + warp];
+        if (p.x != -INFINITY) l = fmaf(p.y, exp2f(p.x - m), l);  // -inf: the split saw no visible key
+    }
+    l = warp_sum(l);
     float acc[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) acc[c] = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-        const float2 p = ml[s * stride + warp];
-        if (p.x == -INFINITY) continue;  // split saw no visible key for this row
-        const float w = exp2f(p.x - m);
-        l = fmaf(p.y, w, l);
-        const float *src = a.ws_o + (s * stride + warp) * D + lane * DPL;
-        if constexpr (DPL == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] = fmaf(v.x, w, acc[0]); acc[1] = fmaf(v.y, w, acc[1]);
-            acc[2] = fmaf(v.z, w, acc[2]); acc[3] = fmaf(v.w, w, acc[3]);
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(src);
-            acc[0] = fmaf(v.x, w, acc[0]); acc[1] = fmaf(v.y, w, acc[1]);
+    const float *src0 = a.ws_o + (size_t)warp * D + lane * DPL;
+    for (int s0 = 0; s0 < n_split; s0 += 32) {
+        // this lane's weight for split s0 + lane, broadcast below
+        float wl = 0.f;
+        if (s0 + lane < n_split) {
+            const float mx = ml[(s0 + lane) * stride + warp].x;
+            wl = mx == -INFINITY ? 0.f : exp2f(mx - m);
+        }
+        const int n = min(32, n_split - s0);
+#pragma unroll 4
+        for (int i = 0; i < n; ++i) {
+            const float w = __shfl_sync(0xffffffffu, wl, i);
+            const float *src = src0 + (size_t)(s0 + i) * stride * D;
+            if constexpr (DPL == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                acc[0] = fmaf(v.x, w, acc[0]); acc[1] = fmaf(v.y, w, acc[1]);
+                acc[2] = fmaf(v.z, w, acc[2]); acc[3] = fmaf(v.w, w, acc[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                acc[0] = fmaf(v.x, w, acc[0]); acc[1] = fmaf(v.y, w, acc[1]);
+            }
         }
     }
-    const float inv = 1.f / l;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16 *dst = a.out + (size_t)warp * D + lane * DPL;
 #pragma unroll
     for (int c = 0; c < DPL; c += 2)
