@@ -64,7 +64,7 @@ struct __align__(8) TcSmemTail {
     // (single stream, phase = tile >> 1).  A single stream's warps may run a
     // tile ahead of one another, so its barriers are per buffer: a parity
     // wait must never be two phases behind.
-    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t s_full[2], p_half[2], p_full[2], o_done[2];  // p_half: P of tokens 0-63 written
     uint64_t mma_done;
     uint64_t score_bar[2][2];                   // [half][parity]: the G score rows of that chunk arrived
     uint32_t tmem_base;
@@ -101,11 +101,12 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t dq, uint64_t d
         tc::mma_ss(d_tmem, dplus(dq, off), dplus(dk, off), idesc, k > 0);
     }
 }
-// O[128 x 128] += P[128 x 128 tokens] V[128 tokens x 128]: 8 MMAs with K = 16 tokens.
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t dv, uint32_t idesc,
-                                         bool accumulate) {
+// O[128 x 128] += P[128 x 64 tokens] V[64 tokens x 128] for one half of the
+// tile (tokens 64h..64h+63): 4 MMAs with K = 16 tokens.
+__device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, uint64_t dv, uint32_t idesc, int h,
+                                              bool accumulate) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
+    for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
         tc::mma_ts(o_tmem, p_tmem + kk * 8, dplus(dv, (uint32_t)kk * 2048), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
@@ -212,6 +213,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         for (int m = 0; m < 2; ++m) {
             tc::mbar_init(&tl->s_full[m], 1);
+            tc::mbar_init(&tl->p_half[m], 128);
             tc::mbar_init(&tl->p_full[m], 128);
             tc::mbar_init(&tl->o_done[m], 1);
             tc::mbar_init(&tl->score_bar[m][0], (uint32_t)G);
@@ -309,9 +311,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     const uint32_t par = (uint32_t)it & 1u;
                     if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
                     const uint64_t dv = dplus(dv0, (uint32_t)vst * TILE_BYTES);
+                    // each half of P goes to the tensor pipe as soon as it is written
+                    if (!(ok = tc::mbar_wait(&tl->p_half[0], par, abort_flag))) break;
+                    tc::fence_after_sync();
+                    issue_pv_half(tbase + 256, tbase + 0, dv, id_o, 0, it > 0);
                     if (!(ok = tc::mbar_wait(&tl->p_full[0], par, abort_flag))) break;
                     tc::fence_after_sync();
-                    issue_pv(tbase + 256, tbase + 0, dv, id_o, it > 0);
+                    issue_pv_half(tbase + 256, tbase + 0, dv, id_o, 1, true);
                     tc::mma_commit(&tl->o_done[0]);
                     uint64_t dk = 0;
                     if (more) {
@@ -321,9 +327,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         issue_s(tbase + 0, dq0, dk, id_s);
                         tc::mma_commit(&tl->s_full[0]);
                     }
+                    if (!(ok = tc::mbar_wait(&tl->p_half[1], par, abort_flag))) break;
+                    tc::fence_after_sync();
+                    issue_pv_half(tbase + 384, tbase + 128, dv, id_o, 0, it > 0);
                     if (!(ok = tc::mbar_wait(&tl->p_full[1], par, abort_flag))) break;
                     tc::fence_after_sync();
-                    issue_pv(tbase + 384, tbase + 128, dv, id_o, it > 0);
+                    issue_pv_half(tbase + 384, tbase + 128, dv, id_o, 1, true);
                     tc::mma_commit(&tl->o_done[1]);
                     tc::mma_commit(&tl->v_empty[vst]);
                     if (++vst == NSTAGE) { vst = 0; vph ^= 1u; }
@@ -346,9 +355,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     }
                     if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
                     const int b = it & 1;
+                    // (a single stream's next S is already in flight: P.V goes as one piece)
+                    const uint64_t dv = dplus(dv0, (uint32_t)vst * TILE_BYTES);
                     if (!(ok = tc::mbar_wait(&tl->p_full[b], (uint32_t)(it >> 1) & 1u, abort_flag))) break;
                     tc::fence_after_sync();
-                    issue_pv(tbase + 256, tbase + 128 * b, dplus(dv0, (uint32_t)vst * TILE_BYTES), id_o, it > 0);
+                    issue_pv_half(tbase + 256, tbase + 128 * b, dv, id_o, 0, it > 0);
+                    issue_pv_half(tbase + 256, tbase + 128 * b, dv, id_o, 1, true);
                     tc::mma_commit(&tl->o_done[b]);
                     tc::mma_commit(&tl->v_empty[vst]);
                     if (++vst == NSTAGE) { vst = 0; vph ^= 1u; }
@@ -447,7 +459,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
 
                 // ---- P = 2^(s*c - m) in bf16 over the first 64 columns of S
-                // (token k -> column k/2, even k in the lower half; S is in registers)
+                // (token k -> column k/2, even k in the lower half; S is in registers).
+                // Tokens 0-63 first: their P.V is issued while tokens 64-127 are
+                // exponentiated.
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 const float2 nm2 = make_float2(neg_m, neg_m);
                 float lsum;
@@ -461,19 +475,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     lsum += exp_chunk(x1, c2, nm2, pk);
                     tc::tmem_st16(s_addr + 16, pk);
                 }
-                {
-                    uint32_t pk[16];
-                    lsum += exp_chunk(x2, c2, nm2, pk);
-                    tc::tmem_st16(s_addr + 32, pk);
-                }
-                {
-                    uint32_t pk[16];
-                    lsum += exp_chunk(x3, c2, nm2, pk);
-                    tc::tmem_st16(s_addr + 48, pk);
-                }
-                l_run += lsum;
 
-                // ---- rescale O by alpha (before this tile's P.V)
+                // ---- rescale O by alpha (before this tile's first P.V)
                 if (it > 0 && __any_sync(0xffffffffu, resc)) {
                     if (!pair) {
                         // a single stream computes S ahead: wait for the previous P.V into O
@@ -492,6 +495,20 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         tc::tmem_st32(o_addr + cc * 32, ov);
                     }
                 }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                tc::mbar_arrive(&tl->p_half[slot]);
+                {
+                    uint32_t pk[16];
+                    lsum += exp_chunk(x2, c2, nm2, pk);
+                    tc::tmem_st16(s_addr + 32, pk);
+                }
+                {
+                    uint32_t pk[16];
+                    lsum += exp_chunk(x3, c2, nm2, pk);
+                    tc::tmem_st16(s_addr + 48, pk);
+                }
+                l_run += lsum;
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 tc::mbar_arrive(&tl->p_full[slot]);

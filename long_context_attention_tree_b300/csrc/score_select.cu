@@ -235,22 +235,43 @@ select_gather_kernel(const float *__restrict__ scores, int n_chunks, int k_sel,
     }
     __syncthreads();
 
-    // --- gather this part's chunks (K then V), 16 bytes per thread per step
-    constexpr int U = D / 8;  // 16-byte units per row
+    // --- gather this part's chunks, K and V: every load of a pair of chunks is
+    // issued before the first store, so each thread keeps 8 x 16 bytes in flight
+    constexpr int U = D / 8;                     // 16-byte units per row
+    constexpr int PER = CHUNK * U / SG_THREADS;  // units per thread per chunk (2 for D = 128)
+    static_assert(CHUNK * U % SG_THREADS == 0, "chunk must split evenly over the threads");
     const int i0 = p * chunks_per_part, i1 = min(k_sel, i0 + chunks_per_part);
     const __nv_bfloat16 *kh = k + (size_t)g * ld_kv * D;
     const __nv_bfloat16 *vh = v + (size_t)g * ld_kv * D;
     __nv_bfloat16 *kp = k_part + (size_t)g * ld_part * D;
     __nv_bfloat16 *vp = v_part + (size_t)g * ld_part * D;
-    for (int i = i0; i < i1; ++i) {
-        const int c = min(max(list[i], 0), n_chunks - 1);
-        const size_t src_row = (size_t)c * CHUNK, dst_row = (size_t)i * CHUNK;
-        for (int e = tid; e < CHUNK * U; e += SG_THREADS) {
-            const int r = e / U, u = e % U;
-            const uint4 wk = *reinterpret_cast<const uint4 *>(kh + (src_row + r) * D + u * 8);
-            const uint4 wv = *reinterpret_cast<const uint4 *>(vh + (src_row + r) * D + u * 8);
-            *reinterpret_cast<uint4 *>(kp + (dst_row + r) * D + u * 8) = wk;
-            *reinterpret_cast<uint4 *>(vp + (dst_row + r) * D + u * 8) = wv;
+    for (int i = i0; i < i1; i += 2) {
+        const int nb = min(2, i1 - i);
+        uint4 wk[2][PER], wv[2][PER];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            if (b < nb) {
+                const int c = min(max(list[i + b], 0), n_chunks - 1);
+                const size_t src_row = (size_t)c * CHUNK;
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+                    const int e = tid + q * SG_THREADS, r = e / U, u = e % U;
+                    wk[b][q] = *reinterpret_cast<const uint4 *>(kh + (src_row + r) * D + u * 8);
+                    wv[b][q] = *reinterpret_cast<const uint4 *>(vh + (src_row + r) * D + u * 8);
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            if (b < nb) {
+                const size_t dst_row = (size_t)(i + b) * CHUNK;
+#pragma unroll
+                for (int q = 0; q < PER; ++q) {
+                    const int e = tid + q * SG_THREADS, r = e / U, u = e % U;
+                    *reinterpret_cast<uint4 *>(kp + (dst_row + r) * D + u * 8) = wk[b][q];
+                    *reinterpret_cast<uint4 *>(vp + (dst_row + r) * D + u * 8) = wv[b][q];
+                }
+            }
         }
     }
 }

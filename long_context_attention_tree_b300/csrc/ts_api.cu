@@ -68,7 +68,8 @@ bool force_simt() {
 // Which kernel runs and how the KV length is split; used both to size the
 // workspace and to launch, so the two always agree.
 struct AttnPlan {
-    bool tc;
+    bool tc;     // tensor cores (T >= 64, head dim 128)
+    bool small;  // CUDA cores, small batch (T * G <= 24, head dim 128)
     ts::TcPlan tcp;
     ts::SimtPlan sp;
     int splits;
@@ -79,8 +80,11 @@ AttnPlan plan_attention(int T, int Hq, int Hkv, int d, int64_t N) {
     const int sms = num_sms();
     p.tcp = ts::tc_plan(T, Hq, Hkv, d, N, sms);
     p.tc = p.tcp.ok && !force_simt();
+    p.small = !p.tc && ts::small_ok(T, Hq, Hkv, d);
     if (p.tc) {
         p.splits = p.tcp.splits;
+    } else if (p.small) {
+        p.splits = ts::small_splits(T, N);
     } else {
         p.sp = ts::simt_plan(T, Hq, Hkv, d, N, sms);
         p.splits = p.sp.splits;
@@ -248,6 +252,9 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
             return fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled failed (or the driver entry point is missing)");
         e = ts::launch_tree_attn_tc(a, p, tq, tk, tv, s);
         if (e != cudaSuccess) return cuda_fail(e, "tree_attn_tc launch");
+    } else if (plan.small) {
+        e = ts::launch_tree_attn_small(a, plan.splits, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tree_attn_small launch");
     } else {
         const ts::SimtPlan &p = plan.sp;
         a.tiles_per_split = p.tiles_per_split;
