@@ -55,6 +55,7 @@ constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int NSTAGE = 2;                   // K and V ring depth (pair: 2 Q + 2 K + 2 V = 192 KB)
 constexpr int SMEM_DATA_BYTES = 6 * TILE_BYTES;
 constexpr float RESCALE_THRESHOLD = 20.0f;  // log2 units
+constexpr int SCORE_RING = 4;               // chunk-score slots between the scoring rows and warp 2
 
 struct __align__(8) TcSmemTail {
     uint64_t q_full;
@@ -66,10 +67,12 @@ struct __align__(8) TcSmemTail {
     // wait must never be two phases behind.
     uint64_t s_full[2], p_half[2], p_full[2], o_done[2];  // p_half: P of tokens 0-63 written
     uint64_t mma_done;
-    uint64_t score_bar[2][2];                   // [half][parity]: the G score rows of that chunk arrived
+    // Chunk scores: the G scoring rows put their two chunk sums of a KV tile
+    // into a ring slot (tile & 3); warp 2 takes the max over the group's heads.
+    uint64_t score_full[SCORE_RING], score_empty[SCORE_RING];
+    float score_sum[SCORE_RING][2][32];          // [slot][chunk half][head j]
     uint32_t tmem_base;
     int abort_flag;
-    float score_part[2][2][32];                 // [half][parity][head j]
 };
 
 constexpr size_t TC_SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)SMEM_DATA_BYTES + sizeof(TcSmemTail);
@@ -157,12 +160,26 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], float2 c2, f
     }
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
-__device__ __forceinline__ float sum_chunk(const uint32_t (&x)[32], int lim) {
-    float s = 0.f;
+// Chunk sums of the scoring row.  A whole 64-token chunk (a[] and b[]) is a
+// tree of packed adds (32 instructions); the chunk at the end of the prefix
+// sums x[0..lim) (lim clamped to [0, 32]) with eight partial sums.
+__device__ __forceinline__ float sum64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
+    float2 p[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-        if (i < lim) s += __uint_as_float(x[i]);
-    return s;
+    for (int i = 0; i < 16; ++i)
+        p[i] = __fadd2_rn(make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1])),
+                          make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1])));
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) p[i] = __fadd2_rn(p[i], p[i + w]);
+    return p[0].x + p[0].y;
+}
+__device__ __forceinline__ float sum_chunk(const uint32_t (&x)[32], int lim) {
+    float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) p[i & 7] += (i < lim) ? __uint_as_float(x[i]) : 0.f;
+    return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
 }  // namespace
@@ -202,6 +219,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.G, tpb = L.tpb;
     const int rows_loaded = tpb * G;
+    // M-tile slot (0/1) holding the row whose chunk scores this pass produces, or -1
+    const int score_wm = (a.chunk_scores != nullptr && a.score_row / tpb >= mt0 && a.score_row / tpb < mt0 + nm)
+                             ? a.score_row / tpb - mt0 : -1;
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&tl->q_full, 1);
@@ -216,10 +236,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tc::mbar_init(&tl->p_half[m], 128);
             tc::mbar_init(&tl->p_full[m], 128);
             tc::mbar_init(&tl->o_done[m], 1);
-            tc::mbar_init(&tl->score_bar[m][0], (uint32_t)G);
-            tc::mbar_init(&tl->score_bar[m][1], (uint32_t)G);
         }
         tc::mbar_init(&tl->mma_done, 1);
+        for (int sl = 0; sl < SCORE_RING; ++sl) {
+            tc::mbar_init(&tl->score_full[sl], (uint32_t)G);
+            tc::mbar_init(&tl->score_empty[sl], 1);
+        }
         tl->abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -279,6 +301,29 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tc::mbar_wait(&tl->k_full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, nullptr);
             for (int j = max(0, nv - NSTAGE); j < nv; ++j)
                 tc::mbar_wait(&tl->v_full[j % NSTAGE], (uint32_t)(j / NSTAGE) & 1u, nullptr);
+        }
+      } else if (warp == 2) {
+        // ------------------------------------------------------------ chunk-score reducer
+        // Off the softmax's critical path: per KV tile, the max over the group's
+        // heads of the scoring rows' two chunk sums.
+        if (lane == 0 && score_wm >= 0) {
+            for (int it = 0; it < n_my; ++it) {
+                const int sl = it & (SCORE_RING - 1);
+                if (!tc::mbar_wait(&tl->score_full[sl], (uint32_t)(it / SCORE_RING) & 1u, abort_flag)) {
+                    raise_abort(tl);
+                    break;
+                }
+                float b0 = -INFINITY, b1 = -INFINITY;
+                for (int j = 0; j < G; ++j) {
+                    b0 = fmaxf(b0, tl->score_sum[sl][0][j]);
+                    b1 = fmaxf(b1, tl->score_sum[sl][1][j]);
+                }
+                tc::mbar_arrive(&tl->score_empty[sl]);
+                const int tile = tile_begin + it;
+                const int64_t tok0 = (int64_t)tile * KV_TILE;
+                if (tok0 < a.N) a.chunk_scores[(size_t)g * a.n_chunks + 2 * tile] = b0;
+                if (tok0 + 64 < a.N) a.chunk_scores[(size_t)g * a.n_chunks + 2 * tile + 1] = b1;
+            }
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -388,10 +433,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 mk0 = a.mask[2 * t];
                 mk1 = a.mask[2 * t + 1];
             }
-            const bool score_wg = a.chunk_scores != nullptr && a.score_row / tpb == mt;
-            const bool is_score_row = score_wg && row_valid && t == a.score_row;
-            const bool is_score_reducer = score_wg && r == (a.score_row % tpb) * G;
-            const bool score_warp = __any_sync(0xffffffffu, is_score_row || is_score_reducer);
+            const bool is_score_row = score_wm == wm && row_valid && t == a.score_row;
+            const bool score_warp = __any_sync(0xffffffffu, is_score_row);
             const uint32_t o_addr = lane_addr + (pair ? 256u + 128u * (uint32_t)wm : 256u);
             const float c = a.scale_log2;
             const float2 c2 = make_float2(c, c);
@@ -414,29 +457,29 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tc::tmem_wait_ld();
 
                 // ---- fused chunk importance of the scoring row: chunks 2*tile and 2*tile+1
+                // (raw q.k summed over the tokens < N of each chunk) into the ring for warp 2
                 if (score_warp) {
-                    const int pb = it & 1;
                     if (is_score_row) {
-                        const int64_t lim64 = a.N - tok0;
-                        const int lim = lim64 >= 128 ? 128 : (lim64 < 0 ? 0 : (int)lim64);
-                        tl->score_part[0][pb][j] = sum_chunk(x0, lim) + sum_chunk(x1, lim - 32);
-                        tl->score_part[1][pb][j] = sum_chunk(x2, lim - 64) + sum_chunk(x3, lim - 96);
-                        tc::mbar_arrive(&tl->score_bar[0][pb]);
-                    }
-                    if (is_score_reducer) {
-                        if (tc::mbar_wait(&tl->score_bar[0][pb], (uint32_t)(it >> 1) & 1u, abort_flag)) {
-                            for (int hh = 0; hh < 2; ++hh) {
-                                if (tok0 + 64 * hh < a.N) {
-                                    float best = tl->score_part[hh][pb][0];
-                                    for (int jj = 1; jj < G; ++jj) best = fmaxf(best, tl->score_part[hh][pb][jj]);
-                                    a.chunk_scores[(size_t)g * a.n_chunks + 2 * tile + hh] = best;
-                                }
-                            }
+                        float s0, s1;
+                        if (tok0 + KV_TILE <= a.N) {
+                            s0 = sum64(x0, x1);
+                            s1 = sum64(x2, x3);
+                        } else {
+                            const int64_t lim64 = a.N - tok0;
+                            const int lim = lim64 < 0 ? 0 : (int)lim64;
+                            s0 = sum_chunk(x0, lim) + sum_chunk(x1, lim - 32);
+                            s1 = sum_chunk(x2, lim - 64) + sum_chunk(x3, lim - 96);
+                        }
+                        const int sl = it & (SCORE_RING - 1);
+                        if (it < SCORE_RING ||
+                            tc::mbar_wait(&tl->score_empty[sl], (uint32_t)(it / SCORE_RING - 1) & 1u, abort_flag)) {
+                            tl->score_sum[sl][0][j] = s0;
+                            tl->score_sum[sl][1][j] = s1;
+                            tc::mbar_arrive(&tl->score_full[sl]);
                         } else {
                             raise_abort(tl);
                         }
                     }
-                    // reconverge before the warp-collective TMEM accesses below
                     __syncwarp();
                 }
 
