@@ -269,61 +269,108 @@ tree_attn_simt_kernel(const AttnArgs a) {
     }
 }
 
-// Log-sum-exp merge over splits (log2 domain partials).  One warp per (t, h)
-// row: the lanes read the splits' (m, l) pairs side by side, reduce the max
-// with shuffles, and then accumulate the weighted partial outputs with four
-// independent loads in flight per lane.
-template <int D>
+// Log-sum-exp merge over splits (log2 domain partials).  WPR warps per
+// (t, h) row (1 when there are many rows, 4 when there are few): each warp
+// issues its first eight partial-output loads, reads the splits' (m, l)
+// pairs side by side (two per lane) and reduces max and normaliser with
+// shuffles while those loads are in flight; warp w then accumulates splits
+// w, w+WPR, ... with eight loads in flight per lane, and the row's warps add
+// their sums through shared memory.  A row costs about two dependent memory
+// round trips.
+template <int D, int WPR>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeArgs a) {
-    constexpr int DPL = D / 32;
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
+    constexpr int DPL = D / 32;  // dims per lane
+    constexpr int BATCH = 8;     // splits in flight per warp
+    constexpr int RPC = 4 / WPR; // rows per CTA
+    __shared__ __align__(16) float part[4][D];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row = blockIdx.x * RPC + warp / WPR, sub = warp % WPR;
     const int rows = a.T * a.Hq;
-    if (warp >= rows) return;
+    const bool live = row < rows;  // uniform per CTA when WPR == 4
     const size_t stride = (size_t)rows;
-    const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml);
-    const int n_split = (warp / a.Hq) < a.t_split ? a.splits : a.splits_hi;
-    float m = -INFINITY;
-    for (int s = lane; s < n_split; s += 32) m = fmaxf(m, ml[s * stride + warp].x);
+    const int n_split = !live ? 0 : ((row / a.Hq) < a.t_split ? a.splits : a.splits_hi);
+    const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml) + row;
+    const float *src0 = a.ws_o + (size_t)row * D + lane * DPL;
+
+    float v[BATCH][DPL];
+    auto load_batch = [&](int s0) {
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            const int s = s0 + WPR * i;
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) v[i][c] = 0.f;
+            if (s < n_split) {
+                const float *src = src0 + (size_t)s * stride * D;
+                if constexpr (DPL == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src);
+                    v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(src);
+                    v[i][0] = x.x; v[i][1] = x.y;
+                }
+            }
+        }
+    };
+    load_batch(sub);
+
+    // (m, l) of splits lane and lane + 32 in registers, the rest re-read
+    const float2 none = make_float2(-INFINITY, 0.f);
+    const float2 p0 = lane < n_split ? ml[(size_t)lane * stride] : none;
+    const float2 p1 = lane + 32 < n_split ? ml[(size_t)(lane + 32) * stride] : none;
+    float m = fmaxf(p0.x, p1.x);
+    for (int s = lane + 64; s < n_split; s += 32) m = fmaxf(m, ml[(size_t)s * stride].x);
     m = warp_max(m);
-    float l = 0.f;
-    for (int s = lane; s < n_split; s += 32) {
-        const float2 p = ml[s * stride + warp];
-        if (p.x != -INFINITY) l = fmaf(p.y, exp2f(p.x - m), l);  // -inf: the split saw no visible key
+    // -inf: the split saw no visible key
+    const float w0 = p0.x == -INFINITY ? 0.f : exp2f(p0.x - m);
+    const float w1 = p1.x == -INFINITY ? 0.f : exp2f(p1.x - m);
+    float l = p0.y * w0 + p1.y * w1;
+    for (int s = lane + 64; s < n_split; s += 32) {
+        const float2 p = ml[(size_t)s * stride];
+        if (p.x != -INFINITY) l = fmaf(p.y, exp2f(p.x - m), l);
     }
     l = warp_sum(l);
+
     float acc[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) acc[c] = 0.f;
-    const float *src0 = a.ws_o + (size_t)warp * D + lane * DPL;
-    for (int s0 = 0; s0 < n_split; s0 += 32) {
-        // this lane's weight for split s0 + lane, broadcast below
-        float wl = 0.f;
-        if (s0 + lane < n_split) {
-            const float mx = ml[(s0 + lane) * stride + warp].x;
-            wl = mx == -INFINITY ? 0.f : exp2f(mx - m);
-        }
-        const int n = min(32, n_split - s0);
-#pragma unroll 4
-        for (int i = 0; i < n; ++i) {
-            const float w = __shfl_sync(0xffffffffu, wl, i);
-            const float *src = src0 + (size_t)(s0 + i) * stride * D;
-            if constexpr (DPL == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                acc[0] = fmaf(v.x, w, acc[0]); acc[1] = fmaf(v.y, w, acc[1]);
-                acc[2] = fmaf(v.z, w, acc[2]); acc[3] = fmaf(v.w, w, acc[3]);
+    for (int s0 = sub; s0 < n_split; s0 += WPR * BATCH) {
+        if (s0 != sub) load_batch(s0);
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            const int s = s0 + WPR * i;  // warp-uniform
+            float w;
+            if (s < 32) {
+                w = __shfl_sync(0xffffffffu, w0, s);
+            } else if (s < 64) {
+                w = __shfl_sync(0xffffffffu, w1, s - 32);
             } else {
-                const float2 v = *reinterpret_cast<const float2 *>(src);
-                acc[0] = fmaf(v.x, w, acc[0]); acc[1] = fmaf(v.y, w, acc[1]);
+                const float mx = s < n_split ? ml[(size_t)s * stride].x : -INFINITY;
+                w = mx == -INFINITY ? 0.f : exp2f(mx - m);
             }
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) acc[c] = fmaf(v[i][c], w, acc[c]);
         }
     }
+    if constexpr (WPR > 1) {
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) part[warp][lane * DPL + c] = acc[c];
+        __syncthreads();
+        if (warp != 0) return;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) {
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPR; ++w) t += part[w][lane * DPL + c];
+            acc[c] = t;
+        }
+    }
+    if (!live) return;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16 *dst = a.out + (size_t)warp * D + lane * DPL;
+    __nv_bfloat16 *dst = a.out + (size_t)row * D + lane * DPL;
 #pragma unroll
     for (int c = 0; c < DPL; c += 2)
         *reinterpret_cast<__nv_bfloat162 *>(dst + c) = __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
-    if (a.lse != nullptr && lane == 0) a.lse[warp] = (m + log2f(l)) * TS_LN2;
+    if (a.lse != nullptr && lane == 0) a.lse[row] = (m + log2f(l)) * TS_LN2;
 }
 
 // ----------------------------------------------------------------------------
@@ -378,11 +425,18 @@ cudaError_t launch_tree_attn_simt(const AttnArgs &a, const SimtPlan &p, cudaStre
 
 cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st) {
     const int rows = m.T * m.Hq;
-    const int blocks = (rows + 3) / 4;
-    if (d == 128)
-        lse_merge_kernel<128><<<blocks, 128, 0, st>>>(m);
-    else
-        lse_merge_kernel<64><<<blocks, 128, 0, st>>>(m);
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // few rows: four warps share a row's splits; many rows: a warp per row
+    const bool few = (int64_t)rows * 4 <= (int64_t)sms * 32;
+    const int blocks = few ? rows : (rows + 3) / 4;
+    if (d == 128) {
+        if (few) lse_merge_kernel<128, 4><<<blocks, 128, 0, st>>>(m);
+        else lse_merge_kernel<128, 1><<<blocks, 128, 0, st>>>(m);
+    } else {
+        if (few) lse_merge_kernel<64, 4><<<blocks, 128, 0, st>>>(m);
+        else lse_merge_kernel<64, 1><<<blocks, 128, 0, st>>>(m);
+    }
     return cudaGetLastError();
 }
 

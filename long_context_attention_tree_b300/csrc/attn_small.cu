@@ -4,263 +4,270 @@
 // target model with a partial KV cache drafts the next tokens), e.g. 4 chain
 // rows x 5 query heads over a 4096-token partial cache.
 //
-// CTA = (KV head g, 256-token KV range), 512 threads.  Rows r = (t, j)
-// t-major, R = T*G, padded to RP = 4*R4.
-//   S:  thread = (token, half of the head dim); each thread streams its half
-//       K row (128 B) from global memory and forms all R partial dot products
-//       with Q held in shared memory as [d][RP] fp32 (one broadcast 16-byte
-//       read feeds four rows), packed fp32x2 FMAs; the two halves are added
-//       through shared memory.
-//   softmax over the CTA's 256 tokens per row: warp shuffles, then shared
-//       memory across the 8 warps; P = 2^(s*c - m) goes to shared memory as
-//       [token][RP].
-//   O:  lane = 4 dims, warp = 16 tokens; each lane reads V[token][4 dims]
-//       (coalesced 256 B per token) and accumulates R x 4 outputs; the
-//       sixteen warps' partial sums are added through shared memory.
+// CTA = (KV head g, 128-token KV range); rows r = (t, j) t-major, R = T*G,
+// in groups of four.  The range's K and V (32 KB each) are copied into
+// shared memory with 16-byte cp.async at the start, so every byte of the
+// range is in flight at once (K rows XOR-swizzled by 16-byte chunk so that
+// lanes reading different rows hit different banks).  Warp w owns rows
+// 4w..4w+3 for the whole range, so the softmax of its rows never leaves the
+// warp:
+//   S:  lane l takes tokens l, l+32, l+64, l+96 (16 scores in registers),
+//       8 dims at a time; Q sits in shared memory as [d][row][2] fp32 (each
+//       value twice), so one broadcast 16-byte read gives two rows as pairs
+//       and the products are packed fp32x2 FMAs over token pairs.
+//   softmax over the range: max and sum per row with warp shuffles; P goes
+//       to the warp's own shared-memory slab as [token][row][2].
+//   O:  lane l owns dims 4l..4l+3; per token one 8-byte V read (the warp
+//       reads the whole 256-byte row) and two broadcast reads of P feed 16
+//       FMAs.
 // The partial (O, m, l) of each range goes to the split workspace and the
 // log-sum-exp merge kernel combines the ranges (a single range writes the
 // normalised output directly).  The chunk importance of the scoring row can
-// be produced by the same pass.
+// be produced by the same pass (a range is two 64-token chunks).
 #include "internal.h"
 #include "ts_common.cuh"
 
 namespace ts {
 
 namespace {
-constexpr int SM_THREADS = 512;
-constexpr int SM_TOKENS = 256;  // tokens per CTA (two threads each in the S phase)
+constexpr int SM_TOKENS = 128;  // tokens per CTA: 4 per lane
 constexpr int D = 128;
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 }  // namespace
 
 template <int R4>
-__global__ void __launch_bounds__(SM_THREADS, 1) tree_attn_small_kernel(const AttnArgs a, int n_splits) {
+__global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs a, int n_splits) {
     constexpr int RP = 4 * R4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float *qs = reinterpret_cast<float *>(smem_raw);   // [D][RP]
-    float *ps = qs + D * RP;                            // [SM_TOKENS][RP]
-    float *xs = ps + SM_TOKENS * RP;                    // [SM_TOKENS][RP] upper-half partial S
-    float *ob = xs + SM_TOKENS * RP;                    // [8 warps][RP][D] partial O
-    float *red = ob + 8 * RP * D;                       // [8 warps][RP] partial max, then partial sum
-    float *fin = red + 8 * RP;                          // [RP] final max, then [RP] final sum
-    float *scs = fin + 2 * RP;                          // [8 warps][32] score partials
+    unsigned char *sk = smem_raw;                      // [SM_TOKENS][D] bf16, 16-byte chunks swizzled
+    unsigned char *sv = sk + SM_TOKENS * D * 2;        // [SM_TOKENS][D] bf16
+    float *qs = reinterpret_cast<float *>(sv + SM_TOKENS * D * 2);  // [D][RP][2]
+    float *ps = qs + D * RP * 2;                       // [R4][SM_TOKENS][4][2]
+    __shared__ float scs[2][32];                       // chunk sums of the scoring rows, [chunk][head]
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int split = blockIdx.x, g = blockIdx.y;
     const int G = a.G, R = a.T * G;
     const int64_t L = a.N + a.T;
     const int64_t t0 = (int64_t)split * SM_TOKENS;
+    const int n_tok = (int)max((int64_t)0, min((int64_t)SM_TOKENS, L - t0));
 
-    // ---- Q of the group -> shared memory, transposed to [d][row] (zero padding rows)
-    for (int e = tid; e < RP * (D / 8); e += SM_THREADS) {
-        const int r = e / (D / 8), c8 = (e % (D / 8)) * 8;
-        float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (r < R) {
-            const int t = r / G, j = r % G;
-            const uint4 w = *reinterpret_cast<const uint4 *>(a.q + ((size_t)t * a.Hq + g * G + j) * D + c8);
-            f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
-            f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
-        }
+    // ---- Q of the group: global loads first (they must not queue behind the
+    // range's K/V copies); rows vary fastest across the threads so that the
+    // transposed shared-memory stores do not collide in one bank
+    constexpr int QITER = (RP * (D / 8) + R4 * 32 - 1) / (R4 * 32);
+    uint4 qw[QITER];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) qs[(c8 + i) * RP + r] = f[i];
+    for (int u = 0; u < QITER; ++u) {
+        const int e = threadIdx.x + u * R4 * 32;
+        const int r = e % RP, c8 = (e / RP) * 8;
+        qw[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < RP * (D / 8) && r < R) {
+            const int t = r / G, j = r % G;
+            qw[u] = *reinterpret_cast<const uint4 *>(a.q + ((size_t)t * a.Hq + g * G + j) * D + c8);
+        }
     }
+
+    // ---- the range's K (group 0) and V (group 1) -> shared memory; rows past
+    // the range are zero-filled
+    {
+        const __nv_bfloat16 *kg = a.k + ((size_t)g * a.ld_kv + (size_t)t0) * D;
+        const __nv_bfloat16 *vg = a.v + ((size_t)g * a.ld_kv + (size_t)t0) * D;
+        for (int e = threadIdx.x; e < SM_TOKENS * (D / 8); e += R4 * 32) {
+            const int row = e / (D / 8), c = e % (D / 8);
+            const bool ok = row < n_tok;
+            cp_async16_zfill(sk + row * (D * 2) + ((c ^ (row & 7)) * 16), kg + (ok ? (size_t)row * D + c * 8 : 0), ok);
+        }
+        cp_async_commit();
+        for (int e = threadIdx.x; e < SM_TOKENS * (D / 8); e += R4 * 32) {
+            const int row = e / (D / 8), c = e % (D / 8);
+            const bool ok = row < n_tok;
+            cp_async16_zfill(sv + row * (D * 2) + c * 16, vg + (ok ? (size_t)row * D + c * 8 : 0), ok);
+        }
+        cp_async_commit();
+    }
+
+    // ---- Q -> shared memory as [d][row][2] (padding rows zero)
+#pragma unroll
+    for (int u = 0; u < QITER; ++u) {
+        const int e = threadIdx.x + u * R4 * 32;
+        if (e < RP * (D / 8)) {
+            const int r = e % RP, c8 = (e / RP) * 8;
+            const uint4 w = qw[u];
+            const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float2 *>(qs + ((c8 + i) * RP + r) * 2) = make_float2(f[i], f[i]);
+        }
+    }
+    cp_async_wait<1>();  // K has landed
     __syncthreads();
 
-    // ---- S: this thread's token and half of the head dim, against every row
-    const int hd = tid >> 8;                 // head-dim half (warp-uniform)
-    const int tl = tid & (SM_TOKENS - 1);    // token inside the range
-    const int64_t tok = t0 + tl;
-    const bool in_range = tok < L;
-    float2 s[R4][2];
+    // ---- S for tokens tok[i] = t0 + lane + 32 i and rows 4 warp + jr:
+    // acc[jr][0] = (tokens 0, 1), acc[jr][1] = (tokens 2, 3)
+    int64_t tok[4];
+    bool in_range[4];
 #pragma unroll
-    for (int i = 0; i < R4; ++i) s[i][0] = s[i][1] = make_float2(0.f, 0.f);
-    if (in_range) {
-        const uint4 *krow = reinterpret_cast<const uint4 *>(a.k + ((size_t)g * a.ld_kv + (size_t)tok) * D) + hd * 8;
-        uint4 kw[8];
+    for (int i = 0; i < 4; ++i) {
+        tok[i] = t0 + lane + 32 * i;
+        in_range[i] = tok[i] < L;
+    }
+    float2 acc[4][2];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) kw[c] = krow[c];
+    for (int jr = 0; jr < 4; ++jr) acc[jr][0] = acc[jr][1] = make_float2(0.f, 0.f);
+    {
+        const float4 *q4 = reinterpret_cast<const float4 *>(qs) + warp * 2;  // rows 4w..4w+3 of dim 0
+        const unsigned char *krow = sk + lane * (D * 2);                     // token lane; + 32 i rows
+        const int sw = lane & 7;                                             // (lane + 32 i) & 7
+#pragma unroll 2
+        for (int c = 0; c < D / 8; ++c) {
+            uint4 kw[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint32_t wv[4] = {kw[c].x, kw[c].y, kw[c].z, kw[c].w};
+            for (int i = 0; i < 4; ++i)
+                kw[i] = *reinterpret_cast<const uint4 *>(krow + i * 32 * (D * 2) + ((c ^ sw) * 16));
+            const uint32_t w[4][4] = {{kw[0].x, kw[0].y, kw[0].z, kw[0].w},
+                                      {kw[1].x, kw[1].y, kw[1].z, kw[1].w},
+                                      {kw[2].x, kw[2].y, kw[2].z, kw[2].w},
+                                      {kw[3].x, kw[3].y, kw[3].z, kw[3].w}};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float kv = (e & 1) ? bf16_hi(wv[e >> 1]) : bf16_lo(wv[e >> 1]);
-                const float2 k2 = make_float2(kv, kv);
-                const float4 *q4 = reinterpret_cast<const float4 *>(qs + (hd * 64 + c * 8 + e) * RP);
+                const float4 qa = q4[(c * 8 + e) * (RP / 2)];      // (q0, q0, q1, q1)
+                const float4 qb = q4[(c * 8 + e) * (RP / 2) + 1];  // (q2, q2, q3, q3)
+                float kv[4];
 #pragma unroll
-                for (int i = 0; i < R4; ++i) {
-                    const float4 q = q4[i];
-                    s[i][0] = ffma2(make_float2(q.x, q.y), k2, s[i][0]);
-                    s[i][1] = ffma2(make_float2(q.z, q.w), k2, s[i][1]);
-                }
+                for (int i = 0; i < 4; ++i) kv[i] = (e & 1) ? bf16_hi(w[i][e >> 1]) : bf16_lo(w[i][e >> 1]);
+                const float2 k01 = make_float2(kv[0], kv[1]), k23 = make_float2(kv[2], kv[3]);
+                acc[0][0] = ffma2(k01, make_float2(qa.x, qa.y), acc[0][0]);
+                acc[0][1] = ffma2(k23, make_float2(qa.x, qa.y), acc[0][1]);
+                acc[1][0] = ffma2(k01, make_float2(qa.z, qa.w), acc[1][0]);
+                acc[1][1] = ffma2(k23, make_float2(qa.z, qa.w), acc[1][1]);
+                acc[2][0] = ffma2(k01, make_float2(qb.x, qb.y), acc[2][0]);
+                acc[2][1] = ffma2(k23, make_float2(qb.x, qb.y), acc[2][1]);
+                acc[3][0] = ffma2(k01, make_float2(qb.z, qb.w), acc[3][0]);
+                acc[3][1] = ffma2(k23, make_float2(qb.z, qb.w), acc[3][1]);
             }
         }
     }
-    if (hd == 1) {
+    float s[4][4];  // [token i][row jr], raw q.k
 #pragma unroll
-        for (int i = 0; i < R4; ++i)
-            reinterpret_cast<float4 *>(xs + tl * RP)[i] = make_float4(s[i][0].x, s[i][0].y, s[i][1].x, s[i][1].y);
-    }
-    __syncthreads();
-    float sv[RP];
-#pragma unroll
-    for (int i = 0; i < R4; ++i) {
-        const float4 u = reinterpret_cast<const float4 *>(xs + tl * RP)[i];
-        sv[4 * i + 0] = s[i][0].x + u.x; sv[4 * i + 1] = s[i][0].y + u.y;
-        sv[4 * i + 2] = s[i][1].x + u.z; sv[4 * i + 3] = s[i][1].y + u.w;
+    for (int jr = 0; jr < 4; ++jr) {
+        s[0][jr] = acc[jr][0].x; s[1][jr] = acc[jr][0].y;
+        s[2][jr] = acc[jr][1].x; s[3][jr] = acc[jr][1].y;
     }
 
-    // ---- fused chunk importance of the scoring row (raw q.k over tokens < N);
-    // a 64-token chunk is two warps of this CTA
-    if (hd == 0 && a.chunk_scores != nullptr && a.score_row >= 0 && a.score_row < a.T) {
-        const int r0 = a.score_row * G;
+    // ---- fused chunk importance of the scoring row (raw q.k over tokens < N):
+    // chunk 2*split takes tokens i = 0, 1, chunk 2*split+1 tokens i = 2, 3
+    if (a.chunk_scores != nullptr) {
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
-            if (r >= r0 && r < r0 + G) {
-                float x = (tok < a.N) ? sv[r] : 0.f;
-                x = warp_sum(x);
-                if (lane == 0) scs[warp * 32 + (r - r0)] = x;
+        for (int jr = 0; jr < 4; ++jr) {
+            const int r = 4 * warp + jr;
+            if (r < R && r / G == a.score_row) {  // warp-uniform
+                float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float v = tok[i] < a.N ? s[i][jr] : 0.f;
+                    if (i < 2) x0 += v; else x1 += v;
+                }
+                x0 = warp_sum(x0);
+                x1 = warp_sum(x1);
+                if (lane == 0) {
+                    scs[0][r % G] = x0;
+                    scs[1][r % G] = x1;
+                }
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < 2) {
+            const int64_t ch0 = t0 + 64 * threadIdx.x;
+            if (ch0 < a.N) {
+                float best = -INFINITY;
+                for (int j = 0; j < G; ++j) best = fmaxf(best, scs[threadIdx.x][j]);
+                a.chunk_scores[(size_t)g * a.n_chunks + (size_t)(ch0 / 64)] = best;
             }
         }
     }
 
     // ---- visibility: prefix tokens for every row, batch tokens by ancestry
     const float c = a.scale_log2;
+    float m[4], l[4];
 #pragma unroll
-    for (int r = 0; r < RP; ++r) {
-        bool vis = false;
-        if (in_range && r < R) {
-            if (tok < a.N) {
-                vis = true;
-            } else {
-                const int t = r / G;
-                vis = mask_bit(a.mask, t, (int)(tok - a.N));
-            }
+    for (int jr = 0; jr < 4; ++jr) {
+        const int r = 4 * warp + jr;
+        const int t = r < R ? r / G : 0;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            bool vis = in_range[i] && r < R;
+            if (vis && tok[i] >= a.N) vis = mask_bit(a.mask, t, (int)(tok[i] - a.N));
+            s[i][jr] = vis ? s[i][jr] * c : -INFINITY;
+            mx = fmaxf(mx, s[i][jr]);
         }
-        sv[r] = vis ? sv[r] * c : -INFINITY;
+        m[jr] = warp_max(mx);
     }
+    // ---- P = 2^(s*c - m) into this warp's slab [token][row][2], row sums
+    float *pw = ps + (size_t)warp * SM_TOKENS * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float p[4];
+#pragma unroll
+        for (int jr = 0; jr < 4; ++jr) p[jr] = (m[jr] == -INFINITY) ? 0.f : exp2f(s[i][jr] - m[jr]);
+        float4 *dst = reinterpret_cast<float4 *>(pw + (lane + 32 * i) * 8);
+        dst[0] = make_float4(p[0], p[0], p[1], p[1]);
+        dst[1] = make_float4(p[2], p[2], p[3], p[3]);
+#pragma unroll
+        for (int jr = 0; jr < 4; ++jr) s[i][jr] = p[jr];
+    }
+#pragma unroll
+    for (int jr = 0; jr < 4; ++jr) l[jr] = warp_sum((s[0][jr] + s[1][jr]) + (s[2][jr] + s[3][jr]));
+    cp_async_wait<0>();  // V has landed (this thread's copies) ...
+    __syncthreads();     // ... and every thread's; P of this warp is visible too
 
-    // ---- row max over the CTA's tokens (warps 0-7 own one token per lane)
-    if (hd == 0) {
+    // ---- O: lane = dims [4 lane, 4 lane + 4), every token of the range
+    float2 o[4][2];
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
-            const float m = warp_max(sv[r]);
-            if (lane == 0) red[warp * RP + r] = m;
-        }
-    }
-    __syncthreads();
-    if (a.chunk_scores != nullptr && a.score_row >= 0 && a.score_row < a.T && tid < 4) {
-        // chunk (2 warps) tid of this CTA: max over the group's heads
-        const int64_t ch_tok0 = t0 + 64 * tid;
-        if (ch_tok0 < a.N) {
-            float best = -INFINITY;
-            for (int j = 0; j < G; ++j) best = fmaxf(best, scs[(2 * tid) * 32 + j] + scs[(2 * tid + 1) * 32 + j]);
-            a.chunk_scores[(size_t)g * a.n_chunks + (size_t)(ch_tok0 / 64)] = best;
-        }
-    }
-    if (tid < RP) {
-        float m = -INFINITY;
+    for (int jr = 0; jr < 4; ++jr) o[jr][0] = o[jr][1] = make_float2(0.f, 0.f);
+    const uint2 *vcol = reinterpret_cast<const uint2 *>(sv) + lane;
+    for (int i0 = 0; i0 < n_tok; i0 += 16) {
+        uint2 vw[16];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) m = fmaxf(m, red[w * RP + tid]);
-        fin[tid] = m;
-    }
-    __syncthreads();
-
-    // ---- P -> shared memory [token][row], partial row sums
-    if (hd == 0) {
-        float pv[RP];
+        for (int i = 0; i < 16; ++i) vw[i] = vcol[(i0 + i) * (D / 4)];  // zero past the range
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
-            const float m = fin[r];
-            pv[r] = (m == -INFINITY) ? 0.f : exp2f(sv[r] - m);
-        }
-#pragma unroll
-        for (int i = 0; i < R4; ++i)
-            reinterpret_cast<float4 *>(ps + tl * RP)[i] =
-                make_float4(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
-#pragma unroll
-        for (int r = 0; r < RP; ++r) {
-            const float l = warp_sum(pv[r]);
-            if (lane == 0) red[warp * RP + r] = l;
-        }
-    }
-    __syncthreads();
-    if (tid < RP) {
-        float l = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) l += red[w * RP + tid];
-        fin[RP + tid] = l;
-    }
-
-    // ---- O: lane = dims [4 lane, 4 lane + 4), warp = tokens [16 warp, 16 warp + 16)
-    float2 o[RP][2];
-#pragma unroll
-    for (int r = 0; r < RP; ++r) o[r][0] = o[r][1] = make_float2(0.f, 0.f);
-    const int64_t wt0 = t0 + 16 * warp;
-    const int n_tok = (int)max((int64_t)0, min((int64_t)16, L - wt0));
-    const uint2 *vcol = reinterpret_cast<const uint2 *>(a.v + ((size_t)g * a.ld_kv + (size_t)wt0) * D) + lane;
-    for (int i0 = 0; i0 < n_tok; i0 += 8) {
-        uint2 vw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vw[i] = (i0 + i < n_tok) ? vcol[(size_t)(i0 + i) * (D / 4)] : make_uint2(0u, 0u);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 16; ++i) {
             const float2 v01 = make_float2(bf16_lo(vw[i].x), bf16_hi(vw[i].x));
             const float2 v23 = make_float2(bf16_lo(vw[i].y), bf16_hi(vw[i].y));
-            const float4 *p4 = reinterpret_cast<const float4 *>(ps + (16 * warp + i0 + i) * RP);
-#pragma unroll
-            for (int q = 0; q < R4; ++q) {
-                const float4 p = p4[q];  // zero past the range: tokens beyond L have P = 0
-                const float pr[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 pp = make_float2(pr[e], pr[e]);
-                    o[4 * q + e][0] = ffma2(pp, v01, o[4 * q + e][0]);
-                    o[4 * q + e][1] = ffma2(pp, v23, o[4 * q + e][1]);
-                }
-            }
+            const float4 *p4 = reinterpret_cast<const float4 *>(pw + (i0 + i) * 8);
+            const float4 pa = p4[0], pb = p4[1];  // zero past the range
+            o[0][0] = ffma2(make_float2(pa.x, pa.y), v01, o[0][0]);
+            o[0][1] = ffma2(make_float2(pa.x, pa.y), v23, o[0][1]);
+            o[1][0] = ffma2(make_float2(pa.z, pa.w), v01, o[1][0]);
+            o[1][1] = ffma2(make_float2(pa.z, pa.w), v23, o[1][1]);
+            o[2][0] = ffma2(make_float2(pb.x, pb.y), v01, o[2][0]);
+            o[2][1] = ffma2(make_float2(pb.x, pb.y), v23, o[2][1]);
+            o[3][0] = ffma2(make_float2(pb.z, pb.w), v01, o[3][0]);
+            o[3][1] = ffma2(make_float2(pb.z, pb.w), v23, o[3][1]);
         }
     }
-    // ---- add the sixteen warps' partial O: 16 -> 8 -> 4 -> 2 -> 1
+
+    // ---- this range's result for the warp's rows
 #pragma unroll
-    for (int step = 8; step >= 1; step >>= 1) {
-        if (warp >= step && warp < 2 * step) {
-            float4 *dst = reinterpret_cast<float4 *>(ob + (size_t)(warp - step) * RP * D) + lane;
-#pragma unroll
-            for (int r = 0; r < RP; ++r)
-                dst[r * (D / 4)] = make_float4(o[r][0].x, o[r][0].y, o[r][1].x, o[r][1].y);
-        }
-        __syncthreads();
-        if (warp < step) {
-            const float4 *src = reinterpret_cast<const float4 *>(ob + (size_t)warp * RP * D) + lane;
-#pragma unroll
-            for (int r = 0; r < RP; ++r) {
-                const float4 x = src[r * (D / 4)];
-                o[r][0].x += x.x; o[r][0].y += x.y; o[r][1].x += x.z; o[r][1].y += x.w;
-            }
-        }
-        __syncthreads();
-    }
-    if (warp == 0) {
-#pragma unroll
-        for (int r = 0; r < RP; ++r) {
-            if (r >= R) break;
-            const int t = r / G, j = r % G;
-            const size_t row = (size_t)t * a.Hq + g * G + j;
-            const float m = fin[r], l = fin[RP + r];
-            if (n_splits == 1) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(a.out + row * D) + 2 * lane;
-                dst[0] = __floats2bfloat162_rn(o[r][0].x * inv, o[r][0].y * inv);
-                dst[1] = __floats2bfloat162_rn(o[r][1].x * inv, o[r][1].y * inv);
-                if (a.lse != nullptr && lane == 0) a.lse[row] = (m + log2f(l)) * TS_LN2;
-            } else {
-                float4 *dst = reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * D) + lane;
-                *dst = make_float4(o[r][0].x, o[r][0].y, o[r][1].x, o[r][1].y);
-                if (lane == 0)
-                    reinterpret_cast<float2 *>(a.ws_ml)[(size_t)split * a.T * a.Hq + row] = make_float2(m, l);
-            }
+    for (int jr = 0; jr < 4; ++jr) {
+        const int r = 4 * warp + jr;
+        if (r >= R) break;
+        const int t = r / G, j = r % G;
+        const size_t row = (size_t)t * a.Hq + g * G + j;
+        if (n_splits == 1) {
+            const float inv = l[jr] > 0.f ? 1.f / l[jr] : 0.f;
+            __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(a.out + row * D) + 2 * lane;
+            dst[0] = __floats2bfloat162_rn(o[jr][0].x * inv, o[jr][0].y * inv);
+            dst[1] = __floats2bfloat162_rn(o[jr][1].x * inv, o[jr][1].y * inv);
+            if (a.lse != nullptr && lane == 0) a.lse[row] = (m[jr] + log2f(l[jr])) * TS_LN2;
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * D) + lane;
+            *dst = make_float4(o[jr][0].x, o[jr][0].y, o[jr][1].x, o[jr][1].y);
+            if (lane == 0)
+                reinterpret_cast<float2 *>(a.ws_ml)[(size_t)split * a.T * a.Hq + row] = make_float2(m[jr], l[jr]);
         }
     }
 }
@@ -275,7 +282,7 @@ int small_splits(int T, int64_t N) { return (int)((N + T + SM_TOKENS - 1) / SM_T
 template <int R4>
 static size_t small_smem() {
     constexpr int RP = 4 * R4;
-    return sizeof(float) * ((size_t)D * RP + 2 * (size_t)SM_TOKENS * RP + 8 * (size_t)RP * D + 8 * RP + 2 * RP + 8 * 32);
+    return 2 * (size_t)SM_TOKENS * D * 2 + sizeof(float) * ((size_t)D * RP * 2 + (size_t)R4 * SM_TOKENS * 8);
 }
 
 template <int R4>
@@ -285,7 +292,7 @@ static cudaError_t launch_small_t(const AttnArgs &a, int splits, cudaStream_t st
                                          (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(splits, a.Hkv);
-    tree_attn_small_kernel<R4><<<grid, SM_THREADS, smem, st>>>(a, splits);
+    tree_attn_small_kernel<R4><<<grid, R4 * 32, smem, st>>>(a, splits);
     return cudaGetLastError();
 }
 

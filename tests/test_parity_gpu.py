@@ -175,6 +175,22 @@ def test_fused_scores_any_row(score_row):
     np.testing.assert_array_equal(fs.cpu().numpy(), rs.astype(np.float32))
 
 
+@pytest.mark.parametrize("T,Hq,Hkv,N,score_row", [(4, 40, 8, 4100, 3), (4, 32, 8, 1000, 0), (1, 8, 8, 63, 0),
+                                                   (6, 16, 4, 130, 5), (4, 32, 32, 257, 2)])
+def test_small_batch_fused_scores_and_attention(T, Hq, Hkv, N, score_row):
+    """Batches of at most 24 (row, head) pairs per KV head run on the CUDA-core
+    small-batch kernel: its fused chunk scores are bit-exact, its output within
+    the attention bars, including a ragged last KV range."""
+    d = 128
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=300 + N, device="cuda")
+    parent = verify_parent(T)
+    out, lse, fs = run_attn(q, k, v, N, parent, 1 / math.sqrt(d), scores=True, score_row=score_row)
+    rs = oracle.score_chunks(q[score_row].cpu(), k.cpu(), N)
+    np.testing.assert_array_equal(fs.cpu().numpy(), rs.astype(np.float32))
+    ro, rl = oracle.tree_attn(q.cpu(), k.cpu(), v.cpu(), N, parent, 1 / math.sqrt(d))
+    check_attn(out, lse, ro, rl, "small batch")
+
+
 @pytest.mark.parametrize("N,budget,d", [(4096, 1024, 64), (20480, 4096, 128), (64 * 70, 4096, 128),
                                         (102400, 4096, 128), (640, 4096, 128)])
 def test_select_gather_bit_exact(N, budget, d):
