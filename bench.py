@@ -10,7 +10,7 @@ over it; then the vocabulary stage on 120 x 152064 fp32 logits (penalty 1.2
 over a 1024-token window, min-p 0.1, greedy target, acceptance).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                    [--workload qwen14b-100k|llama8b-<N>|llama2-7b-100k] [--no-cpu-baseline]
+                    [--workload qwen14b-100k|qwen14b-<N>|llama8b-<N>|llama2-7b-100k] [--no-cpu-baseline]
 
 Prints one JSON line (rank 0).  Metric: verify-attention KV throughput
 (prefix K+V bytes read by the verify pass, per second of the whole step).
@@ -39,12 +39,36 @@ METRIC = "tree-verify attn KV GB/s (% of HBM peak) at 100K ctx; µs/layer/spec s
 UNIT = "GB/s"
 
 
+# DRAM traffic of the tcgen05 verify kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum of one launch, Qwen2.5-14B
+# shape at 40960 tokens: 247.38 + 3.65 MB for 167.77 MB of prefix K/V), scaled
+# to a launch by its prefix K/V bytes.  It holds only for the kernel source it
+# was taken on (the hash below); for any other source the traffic is unknown.
+VERIFY_TRAFFIC_PER_KV_BYTE = (247.375104 + 3.650304) / 167.772160
+VERIFY_TRAFFIC_SOURCE_SHA1 = "68d3212966bddeb07a876c9f037b5c68cb2a5186"
+
+
+def verify_traffic(kv_bytes: float):
+    import hashlib
+    csrc = os.path.join(ROOT, "long_context_attention_tree_b300", "csrc")
+    h = hashlib.sha1()
+    for f in ("attn_tc.cu", "tc_ptx.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != VERIFY_TRAFFIC_SOURCE_SHA1:
+        return None
+    return kv_bytes * VERIFY_TRAFFIC_PER_KV_BYTE
+
+
 def workload_config(name: str):
     from long_context_attention_tree_b300 import workloads as W
     if name == "qwen14b-100k":
         return W.CONFIGS[5]
     if name == "llama2-7b-100k":
         return W.CONFIGS[4]
+    if name.startswith("qwen14b-"):  # the Qwen2.5-14B shape at another context length (profiling)
+        N = int(name.split("-")[1].lower().replace("k", "")) * 1024 if name.lower().endswith("k") else int(name.split("-")[1])
+        return W.CONFIGS[5].with_N(N)
     if name.startswith("llama8b-"):
         N = int(name.split("-")[1].lower().replace("k", "")) * 1024 if name.lower().endswith("k") else int(name.split("-")[1])
         return W.CONFIGS[3].with_N(N)
@@ -317,7 +341,7 @@ def run_native(args, ws, rank, local):
         roof = {"bound": "alu", "achieved": flops / verify_avg_s / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
                 "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 flop x 2032 MHz"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = verify_traffic(kv_layer) if tensor_path else None
     roof["kernel"] = "ts_tree_attn (verify, T=%d)" % T
     roof["algorithmic_per_launch"] = {"kv_bytes": kv_layer, "flops": flops}
     roof["verify_us_per_layer"] = verify_avg_s * 1e6
