@@ -60,6 +60,28 @@ def verify_traffic(kv_bytes: float):
     return kv_bytes * VERIFY_TRAFFIC_PER_KV_BYTE
 
 
+def time_commit(step, s, reps: int = 20) -> dict:
+    """ts_commit_path on layer 0 with the step's device-side result and path."""
+    import long_context_attention_tree_b300 as ts
+    L0 = step.layers[0]
+    cfg = step.cfg
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(reps + 1)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(reps):
+            evs[i].record(s)
+            ts.ts_commit_path(L0.k, L0.v, cfg.N, step.result, step.path, stream=s)
+        evs[reps].record(s)
+    with torch.cuda.stream(s):
+        g.replay()
+        g.replay()
+    s.synchronize()
+    us = statistics.mean(evs[i].elapsed_time(evs[i + 1]) for i in range(reps)) * 1e3
+    Lacc = int(step.result[0].item())
+    nbytes = 2 * 2 * cfg.Hkv * Lacc * cfg.d * 2  # K and V rows of the path, read then written
+    return {"us": us, "accepted": Lacc, "bytes": nbytes, "gbs": nbytes / us / 1e3}
+
+
 def workload_config(name: str):
     from long_context_attention_tree_b300 import workloads as W
     if name == "qwen14b-100k":
@@ -366,6 +388,12 @@ def run_native(args, ws, rank, local):
         vbytes = T * cfg.vocab * 4
         kernels["penalty_minp_verify"] = {"us": vocab_s * 1e6, "gbs": vbytes / vocab_s / 1e9, "bytes": vbytes}
 
+    # ---- next row: commit of the accepted path into layer 0's cache (after the
+    # timed region; moves the rows the last vocab stage accepted), one CUDA graph
+    # of event-separated calls
+    if step.vocab:
+        kernels["commit_path"] = time_commit(step, s)
+
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(step, s, args, ws)
 
@@ -476,7 +504,7 @@ def main():
     ap.add_argument("--workload", default="qwen14b-100k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None, help="run only this many layers (profiling)")
-    ap.add_argument("--cpu-row-fraction", type=float, default=0.25,
+    ap.add_argument("--cpu-row-fraction", type=float, default=1.0,
                     help="fraction of verify rows the CPU oracle baseline computes")
     ap.add_argument("--ref-row-fraction", type=float, default=1.0 / 32,
                     help="fraction of verify rows per reference-arm step")

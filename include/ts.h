@@ -17,6 +17,8 @@
  *                            into a compact partial cache;
  *   ts_penalty_minp_verify   windowed contextual penalty, temperature, min-p,
  *                            greedy target and exact-match acceptance.
+ *   ts_commit_path           the accepted path's K/V rows become the
+ *                            continuation of the full cache.
  *
  * Conventions shared by every call:
  *   - Pointers without a _host suffix are device memory owned by the caller.
@@ -224,6 +226,26 @@ ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_
                                  const int32_t *draft, const int32_t *parent, int32_t anchor,
                                  int32_t *target, int32_t *kept, int32_t *result, int32_t *path,
                                  void *workspace, size_t ws_bytes, ts_stream_t stream);
+
+/*
+ * Commit of the accepted path into the full cache, the step after
+ * verification ("How it works" on the TokenSwift tool listing: the longest
+ * valid draft is kept and generation continues from it).  Reads L =
+ * result[0] and path[0..L) as ts_penalty_minp_verify wrote them (device
+ * memory: no host round trip) and moves the accepted batch rows to the front
+ * of the batch region, for every KV head g:
+ *     k[g][N + i] = k[g][N + path[i]]   (same for v),   i < L,
+ * so rows [0, N + L) of the cache are the sequence afterwards; rows
+ * N + L .. N + T - 1 keep stale values.  path must be strictly increasing
+ * with values in [0, T) (root..best of a topologically ordered forest) and
+ * 0 <= L <= T; otherwise nothing moves and result[3] is set to TS_ERR_DATA.
+ *   k, v    bf16 [Hkv][ld_kv][d], ld_kv >= N + T (updated in place)
+ *   result  int32[4] device (result[0] read, result[3] written on a data error)
+ *   path    int32[T] device
+ * Supported: 1 <= T <= 128, d in {64, 128}.
+ */
+ts_status ts_commit_path(void *k, void *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d, int32_t *result,
+                         const int32_t *path, ts_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -62,8 +62,9 @@ def lib() -> ctypes.CDLL:
         L.ts_select_gather.argtypes = [P, i32, i64, i32, i32, P, P, i64, i32, P, P, P, i64, P]
         L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
                                              P, P, P, P, P, sz, P]
+        L.ts_commit_path.argtypes = [P, P, i64, i64, i32, i32, i32, P, P, P]
         for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_noalloc", "ts_score_chunks",
-                     "ts_select_gather", "ts_penalty_minp_verify"):
+                     "ts_select_gather", "ts_penalty_minp_verify", "ts_commit_path"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -172,3 +173,10 @@ def ts_penalty_minp_verify(logits, history, theta: float, min_p: float, temperat
     _check(lib().ts_penalty_minp_verify(_ptr(logits), T, V, _ptr(history) if W else None, W, theta, min_p,
                                         temperature, _ptr(draft), _ptr(parent), int(anchor), _ptr(target),
                                         _ptr(kept), _ptr(result), _ptr(path), None, 0, _stream(stream)))
+
+
+def ts_commit_path(k, v, N: int, result, path, stream=None) -> None:
+    """Move the accepted rows N + path[i] to N + i (i < result[0]) in place."""
+    Hkv, ld, d = k.shape
+    T = path.numel()
+    _check(lib().ts_commit_path(_ptr(k), _ptr(v), ld, N, T, Hkv, d, _ptr(result), _ptr(path), _stream(stream)))

@@ -108,4 +108,8 @@ struct VocabArgs {
 };
 cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st);
 
+// commit of the accepted path into the full cache (T <= 128)
+cudaError_t launch_commit_path(__nv_bfloat16 *k, __nv_bfloat16 *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d,
+                               int32_t *result, const int32_t *path, cudaStream_t st);
+
 }  // namespace ts

@@ -371,3 +371,20 @@ ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_
 }
 
 }  // extern "C"
+
+ts_status ts_commit_path(void *k, void *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d, int32_t *result,
+                         const int32_t *path, ts_stream_t stream) {
+    if (T < 1 || T > 128) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [1, 128]", T);
+    if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    if (Hkv <= 0) return fail(TS_ERR_INVALID_ARG, "Hkv=%d", Hkv);
+    if (N < 0) return fail(TS_ERR_INVALID_ARG, "N=%lld < 0", (long long)N);
+    if (!k || !v || !result || !path) return fail(TS_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned4(result) || !aligned4(path))
+        return fail(TS_ERR_INVALID_ARG, "misaligned pointer");
+    if (ld_kv < N + T) return fail(TS_ERR_INVALID_ARG, "ld_kv=%lld < N + T", (long long)ld_kv);
+    cudaError_t e = ts::launch_commit_path(static_cast<__nv_bfloat16 *>(k), static_cast<__nv_bfloat16 *>(v), ld_kv, N,
+                                           T, Hkv, d, result, path, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "commit_path launch");
+    ts::note_launches(1);
+    return TS_OK;
+}

@@ -13,6 +13,7 @@ Functions, each following the definition stated in ``oracle.c``:
   gather             -- compact partial cache
   penalty_minp       -- windowed penalty, temperature, min-p count, greedy target
   accept             -- exact-match acceptance, longest path
+  commit_path        -- the accepted path's K/V rows moved to the end of the sequence
 """
 from __future__ import annotations
 
@@ -53,6 +54,7 @@ def _load():
         lib.oracle_gather.argtypes = [P, i32, i32, i32, i64, P, i64, i32, P, i64]
         lib.oracle_penalty_minp.argtypes = [P, i32, i32, P, i32, flt, flt, dbl, P, P, P]
         lib.oracle_accept.argtypes = [P, P, P, i32, i32, P, P]
+        lib.oracle_commit.argtypes = [P, i64, i64, i32, i32, i32, P, P, P]
         lib.oracle_set_threads.argtypes = [i32]
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -183,3 +185,24 @@ def accept(draft, parent, target, anchor: int):
     path = np.zeros(max(T, 1), dtype=np.int32)
     _load().oracle_accept(_ptr(dr), _ptr(p), _ptr(tg), T, int(anchor), _ptr(res), _ptr(path))
     return res, path[:T]
+
+
+def commit_path(k, v, N: int, result, path):
+    """(k', v', status): bf16 caches after moving the accepted rows
+    N + path[i] to N + i (i < result[0]); status 5 (and no move) on a bad path."""
+    import torch
+    res = np.ascontiguousarray(np.asarray(result, dtype=np.int32))
+    pth = np.ascontiguousarray(np.asarray(path, dtype=np.int32))
+    T = pth.size
+    out = []
+    status = 0
+    for x in (k, v):
+        Hkv, ld, d = x.shape
+        xb = _bf16_bits(x).copy()
+        st = np.zeros(1, dtype=np.int32)
+        rc = _load().oracle_commit(_ptr(xb), ld, N, T, Hkv, d, _ptr(res), _ptr(pth), _ptr(st))
+        if rc:
+            raise ValueError(f"oracle_commit failed ({rc})")
+        status = int(st[0])
+        out.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16))
+    return out[0], out[1], status

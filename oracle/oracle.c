@@ -339,3 +339,36 @@ int oracle_accept(const int32_t *draft, const int32_t *parent, const int32_t *ta
     free(depth);
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Commit of the accepted path (the kept draft becomes the continuation of */
+/* the sequence, "How it works" on the TokenSwift tool listing).            */
+/*   L = result[0]; for i < L and every KV head g:                          */
+/*     cache'[g][N + i] = cache[g][N + path[i]]                              */
+/*   (all sources read before any row is written).  0 <= L <= T and a path  */
+/*   strictly increasing inside [0, T) are required; otherwise nothing moves */
+/*   and *status = 5 (data error).  cache is one of K or V, bf16 bits.      */
+int oracle_commit(uint16_t *cache, int64_t ld, int64_t N, int T, int Hkv, int d,
+                  const int32_t *result, const int32_t *path, int32_t *status)
+{
+    const int L = result[0];
+    *status = 0;
+    int ok = L >= 0 && L <= T;
+    for (int i = 0; ok && i < L; ++i)
+        if (path[i] < 0 || path[i] >= T || (i > 0 && path[i - 1] >= path[i])) ok = 0;
+    if (!ok) {
+        *status = 5;
+        return 0;
+    }
+    if (L == 0) return 0;
+    uint16_t *tmp = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)L * d);
+    if (!tmp) return 1;
+    for (int g = 0; g < Hkv; ++g) {
+        uint16_t *base = cache + ((size_t)g * ld + (size_t)N) * d;
+        for (int i = 0; i < L; ++i)
+            memcpy(tmp + (size_t)i * d, base + (size_t)path[i] * d, sizeof(uint16_t) * (size_t)d);
+        memcpy(base, tmp, sizeof(uint16_t) * (size_t)L * d);
+    }
+    free(tmp);
+    return 0;
+}

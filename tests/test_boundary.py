@@ -150,3 +150,24 @@ def test_product_does_not_import_oracle():
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
                 assert "liboracle" not in text, fn
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), ts.TS_ERR_UNSUPPORTED),
+    (dict(T=129), ts.TS_ERR_UNSUPPORTED),
+    (dict(d=96), ts.TS_ERR_UNSUPPORTED),
+    (dict(Hkv=0), ts.TS_ERR_INVALID_ARG),
+    (dict(N=-1), ts.TS_ERR_INVALID_ARG),
+    (dict(ld=100), ts.TS_ERR_INVALID_ARG),
+    (dict(k=0x10008), ts.TS_ERR_INVALID_ARG),
+    (dict(path=0x10002), ts.TS_ERR_INVALID_ARG),
+    (dict(result=None), ts.TS_ERR_INVALID_ARG),
+])
+def test_commit_path_rejects_bad_arguments(kw, status):
+    """ts_commit_path validates on the host (fake, never dereferenced pointers)."""
+    P = 0x10000
+    a = dict(k=P, v=P, ld=4096 + 120, N=4096, T=120, Hkv=8, d=128, result=P, path=P)
+    a.update(kw)
+    rc = ts.lib().ts_commit_path(a["k"], a["v"], a["ld"], a["N"], a["T"], a["Hkv"], a["d"], a["result"], a["path"],
+                                 None)
+    assert rc == status, ts.lib().ts_last_error()

@@ -395,3 +395,52 @@ def test_planted_targets_are_the_oracle_targets():
     # without the penalty the flipped rows pick the history token instead
     t0, _ = oracle.penalty_minp(vi.logits.numpy(), vi.history.numpy(), 1.0, 0.1, 1.0)
     assert (t0 != t).sum() > 10
+
+
+# --------------------------------------------------------------------------
+# commit of the accepted path
+# --------------------------------------------------------------------------
+def _ancestors(parent, row):
+    out = []
+    while row >= 0:
+        out.append(row)
+        row = parent[row]
+    return out[::-1]
+
+
+@pytest.mark.parametrize("best", [0, 5, 20, 39, 41, 119])
+def test_commit_makes_the_path_the_sequence(best):
+    """After the commit, plain attention of the accepted row over the first
+    N + L cache rows equals its tree attention before the commit: the row saw
+    exactly the prefix and its ancestors, which the commit lays out in order."""
+    parent = W.verify_parents()
+    T, Hq, Hkv, d, N = len(parent), 4, 2, 64, 100
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=best, value_kind="normal")
+    scale = 1.0 / math.sqrt(d)
+    path = _ancestors(parent, best)
+    L = len(path)
+    pth = np.full(T, -1, dtype=np.int32)
+    pth[:L] = path
+    k2, v2, st = oracle.commit_path(k, v, N, [L, best, 0, 0], pth)
+    assert st == 0
+    before, lse_b = oracle.tree_attn(q, k, v, N, parent, scale, rows=list(range(best * Hq, best * Hq + Hq)))
+    after, lse_a = oracle.tree_attn(q[best:best + 1], k2, v2, N + L - 1, [-1], scale)
+    np.testing.assert_allclose(after.reshape(-1), before.reshape(-1), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse_a.reshape(-1), lse_b.reshape(-1), rtol=0, atol=1e-12)
+    # rows past the committed ones are untouched
+    assert torch.equal(k2[:, N + L:], k[:, N + L:]) and torch.equal(v2[:, :N], v[:, :N])
+
+
+def test_commit_identity_and_data_errors():
+    T, Hkv, d, N = 12, 2, 64, 8
+    _, k, v = W.make_qkv(T, 2, Hkv, d, N, seed=3)
+    chain = np.arange(T, dtype=np.int32)
+    for L in (0, 1, 5, T):  # a path 0, 1, ..., L-1 leaves the cache as it is
+        k2, v2, st = oracle.commit_path(k, v, N, [L, L - 1, 0, 0], chain)
+        assert st == 0 and torch.equal(k2, k) and torch.equal(v2, v)
+    for res, pth in (([3, 0, 0, 0], [0, 2, 2] + [-1] * 9),     # not increasing
+                     ([2, 0, 0, 0], [0, T] + [-1] * 10),       # outside the batch
+                     ([T + 1, 0, 0, 0], list(range(T))),       # L > T
+                     ([-1, 0, 0, 0], list(range(T)))):
+        k2, v2, st = oracle.commit_path(k, v, N, res, np.asarray(pth, dtype=np.int32))
+        assert st == 5 and torch.equal(k2, k) and torch.equal(v2, v)

@@ -391,3 +391,73 @@ def test_fused_scores_leave_attention_bitwise_unchanged(Hq, Hkv, N):
     o = o1.reshape(-1, d)[rows].float().cpu().double().numpy()
     assert np.abs(o - ro).max() <= MAX_ABS
     assert np.abs(l1.reshape(-1)[rows].cpu().double().numpy() - rl).max() <= LSE_ABS
+
+
+# --------------------------------------------------------------------------
+# commit of the accepted path (next row: the step after verification)
+# --------------------------------------------------------------------------
+def _ancestors(parent, row):
+    out = []
+    while row >= 0:
+        out.append(int(row))
+        row = parent[row]
+    return out[::-1]
+
+
+@pytest.mark.parametrize("Hkv,d,N,T,seed", [(8, 128, 20480, 120, 0), (2, 64, 4096, 40, 1), (32, 128, 1000, 64, 2),
+                                            (1, 128, 0, 1, 3)])
+def test_commit_path_bit_exact(Hkv, d, N, T, seed):
+    parent = verify_parent(T)
+    _, k, v = W.make_qkv(T, Hkv, Hkv, d, N, seed=500 + seed, device="cuda", value_kind="normal", ld_extra=3)
+    rng = np.random.default_rng(seed)
+    for best in list(rng.choice(T, size=min(T, 4), replace=False)) + [T - 1]:
+        path = _ancestors(parent, int(best))
+        L = len(path)
+        pth = np.full(T, -1, dtype=np.int32)
+        pth[:L] = path
+        res = np.array([L, best, 0, 0], dtype=np.int32)
+        kr, vr, st = oracle.commit_path(k.cpu(), v.cpu(), N, res, pth)
+        kg, vg = k.clone(), v.clone()
+        rd = torch.from_numpy(res).cuda()
+        ts.ts_commit_path(kg, vg, N, rd, torch.from_numpy(pth).cuda())
+        torch.cuda.synchronize()
+        assert st == 0 and int(rd[3]) == 0
+        assert torch.equal(kg.cpu(), kr) and torch.equal(vg.cpu(), vr)
+
+
+def test_commit_path_from_the_vocab_stage_on_device():
+    """Verify then commit with no host round trip: L and the path come from the
+    vocab stage's device outputs."""
+    parent = W.verify_parents()
+    T, Hkv, d, N = len(parent), 8, 128, 4096
+    vi = W.make_vocab_inputs(parent, 152064, 1024, seed=11, device="cuda", flip_rows=0.25)
+    target = torch.empty((T,), dtype=torch.int32, device="cuda")
+    kept = torch.empty_like(target)
+    result = torch.empty((4,), dtype=torch.int32, device="cuda")
+    path = torch.empty_like(target)
+    _, k, v = W.make_qkv(T, Hkv, Hkv, d, N, seed=12, device="cuda", value_kind="normal")
+    kg, vg = k.clone(), v.clone()
+    ts.ts_penalty_minp_verify(vi.logits, vi.history, 1.2, 0.1, 1.0, vi.draft, vi.parent, vi.anchor, target, kept,
+                              result, path)
+    ts.ts_commit_path(kg, vg, N, result, path)
+    torch.cuda.synchronize()
+    res, pth = result.cpu().numpy(), path.cpu().numpy()
+    assert res[0] > 0 and res[3] == 0
+    kr, vr, st = oracle.commit_path(k.cpu(), v.cpu(), N, res, pth)
+    assert st == 0 and torch.equal(kg.cpu(), kr) and torch.equal(vg.cpu(), vr)
+
+
+def test_commit_path_data_errors_reported_not_trapped():
+    T, Hkv, d, N = 16, 2, 128, 256
+    _, k, v = W.make_qkv(T, Hkv, Hkv, d, N, seed=13, device="cuda", value_kind="normal")
+    for res, pth in (([3, 0, 0, 0], [0, 4, 4]), ([2, 0, 0, 0], [1, T]), ([T + 1, 0, 0, 0], list(range(T))),
+                     ([0, -1, 0, 0], [])):
+        p = np.full(T, -1, dtype=np.int32)
+        p[:len(pth)] = pth
+        kg, vg = k.clone(), v.clone()
+        rd = torch.tensor(res, dtype=torch.int32, device="cuda")
+        ts.ts_commit_path(kg, vg, N, rd, torch.from_numpy(p).cuda())
+        torch.cuda.synchronize()
+        assert int(rd[3]) == (0 if res[0] == 0 else 5)
+        assert torch.equal(kg, k) and torch.equal(vg, v)
+    assert ts.ts_device_error(True) == 0
