@@ -82,6 +82,29 @@ def time_commit(step, s, reps: int = 20) -> dict:
     return {"us": us, "accepted": Lacc, "bytes": nbytes, "gbs": nbytes / us / 1e3}
 
 
+def time_sampled_vocab(step, s, reps: int = 5) -> dict:
+    """The vocab stage with min-p sampled targets (seeded Philox stream), one
+    CUDA graph of event-separated calls on the step's inputs."""
+    import long_context_attention_tree_b300 as ts
+    cfg, vi = step.cfg, step.vocab_inputs
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(reps + 1)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(reps):
+            evs[i].record(s)
+            ts.ts_penalty_minp_sample_verify(vi.logits, vi.history, cfg.theta, cfg.min_p, cfg.temperature, 2024, i,
+                                             vi.draft, vi.parent, vi.anchor, step.target, step.kept, step.result,
+                                             step.path, stream=s)
+        evs[reps].record(s)
+    with torch.cuda.stream(s):
+        g.replay()
+        g.replay()
+    s.synchronize()
+    us = statistics.mean(evs[i].elapsed_time(evs[i + 1]) for i in range(reps)) * 1e3
+    nbytes = vi.logits.numel() * 4
+    return {"us": us, "gbs": nbytes / us / 1e3, "bytes": nbytes}
+
+
 def workload_config(name: str):
     from long_context_attention_tree_b300 import workloads as W
     if name == "qwen14b-100k":
@@ -393,6 +416,7 @@ def run_native(args, ws, rank, local):
     # of event-separated calls
     if step.vocab:
         kernels["commit_path"] = time_commit(step, s)
+        kernels["penalty_minp_sample_verify"] = time_sampled_vocab(step, s)
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(step, s, args, ws)

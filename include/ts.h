@@ -17,6 +17,7 @@
  *                            into a compact partial cache;
  *   ts_penalty_minp_verify   windowed contextual penalty, temperature, min-p,
  *                            greedy target and exact-match acceptance.
+ *   ts_penalty_minp_sample_verify  the same with min-p sampled targets;
  *   ts_commit_path           the accepted path's K/V rows become the
  *                            continuation of the full cache.
  *
@@ -226,6 +227,28 @@ ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_
                                  const int32_t *draft, const int32_t *parent, int32_t anchor,
                                  int32_t *target, int32_t *kept, int32_t *result, int32_t *path,
                                  void *workspace, size_t ws_bytes, ts_stream_t stream);
+
+/*
+ * The same step with sampled targets (model card: --min_p 0.1 with
+ * --temperature 1.0 samples; "How it works": drafts are checked against the
+ * target tokens).  Identical to ts_penalty_minp_verify except that
+ *   target[i] = argmax over the min-p kept ids v of (l_v + G_v),
+ *   G_v = -ln(-ln U_v)   (Gumbel-max: v is drawn with probability
+ *                         proportional to exp(l_v) over the kept ids),
+ * lowest id on equal keys, where l are the final (penalised, tempered) fp32
+ * logits, U_v = (2 (x >> 41) + 1) * 2^-24 and x is word (v % 4) of
+ * Philox4x64-10 (Salmon et al., SC 2011) at counter (v / 4, i, offset, 0)
+ * under key (seed, 0); ln is evaluated in fp32 as ln x = e ln 2 + 2 atanh(s),
+ * s = (m - 1)/(m + 1), x = 2^e m, m in [sqrt(1/2), sqrt(2)), with the series
+ * s (1 + s^2/3 + ... + s^10/11), every operation an IEEE fp32 one.
+ * Acceptance then uses these sampled targets.  kept, result and path as for
+ * ts_penalty_minp_verify.
+ */
+ts_status ts_penalty_minp_sample_verify(const float *logits, int T, int V, const int32_t *history, int W,
+                                        float theta, float min_p, float temperature, uint64_t seed,
+                                        uint64_t offset, const int32_t *draft, const int32_t *parent,
+                                        int32_t anchor, int32_t *target, int32_t *kept, int32_t *result,
+                                        int32_t *path, ts_stream_t stream);
 
 /*
  * Commit of the accepted path into the full cache, the step after

@@ -63,8 +63,12 @@ def lib() -> ctypes.CDLL:
         L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
                                              P, P, P, P, P, sz, P]
         L.ts_commit_path.argtypes = [P, P, i64, i64, i32, i32, i32, P, P, P]
+        u64 = ctypes.c_uint64
+        L.ts_penalty_minp_sample_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, u64, u64, P, P,
+                                                    ctypes.c_int32, P, P, P, P, P]
         for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_noalloc", "ts_score_chunks",
-                     "ts_select_gather", "ts_penalty_minp_verify", "ts_commit_path"):
+                     "ts_select_gather", "ts_penalty_minp_verify", "ts_commit_path",
+                     "ts_penalty_minp_sample_verify"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -180,3 +184,15 @@ def ts_commit_path(k, v, N: int, result, path, stream=None) -> None:
     Hkv, ld, d = k.shape
     T = path.numel()
     _check(lib().ts_commit_path(_ptr(k), _ptr(v), ld, N, T, Hkv, d, _ptr(result), _ptr(path), _stream(stream)))
+
+
+def ts_penalty_minp_sample_verify(logits, history, theta: float, min_p: float, temperature: float, seed: int,
+                                  offset: int, draft, parent, anchor: int, target, kept, result, path,
+                                  stream=None) -> None:
+    """ts_penalty_minp_verify with min-p sampled targets (Gumbel-max, Philox4x64-10)."""
+    T, V = logits.shape
+    W = 0 if history is None else history.numel()
+    _check(lib().ts_penalty_minp_sample_verify(_ptr(logits), T, V, _ptr(history) if W else None, W, theta, min_p,
+                                               temperature, int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                               _ptr(draft), _ptr(parent), int(anchor), _ptr(target), _ptr(kept),
+                                               _ptr(result), _ptr(path), _stream(stream)))

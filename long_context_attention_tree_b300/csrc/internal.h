@@ -105,6 +105,8 @@ struct VocabArgs {
     const int32_t *parent;
     int32_t anchor;
     int32_t *target, *kept, *result, *path;
+    int sample;                      // 1: target = min-p sample (Gumbel-max), 0: greedy
+    unsigned long long seed, offset; // Philox4x64-10 key word 0 and counter word 2
 };
 cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st);
 

@@ -328,13 +328,10 @@ ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_t
     return TS_OK;
 }
 
-ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_t *history, int W,
-                                 float theta, float min_p, float temperature,
-                                 const int32_t *draft, const int32_t *parent, int32_t anchor,
-                                 int32_t *target, int32_t *kept, int32_t *result, int32_t *path,
-                                 void *workspace, size_t ws_bytes, ts_stream_t stream) {
-    (void)workspace;
-    (void)ws_bytes;
+static ts_status vocab_stage(const float *logits, int T, int V, const int32_t *history, int W, float theta,
+                             float min_p, float temperature, int sample, uint64_t seed, uint64_t offset,
+                             const int32_t *draft, const int32_t *parent, int32_t anchor, int32_t *target,
+                             int32_t *kept, int32_t *result, int32_t *path, ts_stream_t stream) {
     if (T < 1 || T > 1024) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [1, 1024]", T);
     if (V < 1 || V > 163840) return fail(TS_ERR_UNSUPPORTED, "V=%d outside [1, 163840]", V);
     if (W < 0) return fail(TS_ERR_INVALID_ARG, "W=%d < 0", W);
@@ -364,6 +361,9 @@ ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_
     a.kept = kept;
     a.result = result;
     a.path = path;
+    a.sample = sample;
+    a.seed = seed;
+    a.offset = offset;
     cudaError_t e = ts::launch_vocab(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "vocab launch");
     ts::note_launches(2);
@@ -371,6 +371,26 @@ ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_
 }
 
 }  // extern "C"
+
+ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_t *history, int W,
+                                 float theta, float min_p, float temperature,
+                                 const int32_t *draft, const int32_t *parent, int32_t anchor,
+                                 int32_t *target, int32_t *kept, int32_t *result, int32_t *path,
+                                 void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    return vocab_stage(logits, T, V, history, W, theta, min_p, temperature, 0, 0, 0, draft, parent, anchor, target,
+                       kept, result, path, stream);
+}
+
+ts_status ts_penalty_minp_sample_verify(const float *logits, int T, int V, const int32_t *history, int W,
+                                        float theta, float min_p, float temperature, uint64_t seed,
+                                        uint64_t offset, const int32_t *draft, const int32_t *parent,
+                                        int32_t anchor, int32_t *target, int32_t *kept, int32_t *result,
+                                        int32_t *path, ts_stream_t stream) {
+    return vocab_stage(logits, T, V, history, W, theta, min_p, temperature, 1, seed, offset, draft, parent, anchor,
+                       target, kept, result, path, stream);
+}
 
 ts_status ts_commit_path(void *k, void *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d, int32_t *result,
                          const int32_t *path, ts_stream_t stream) {

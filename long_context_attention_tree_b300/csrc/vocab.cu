@@ -37,6 +37,63 @@ __device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
     return a;
 }
 
+// ---- min-p sampling (model card: --min_p 0.1 --temperature 1.0 sample the
+// target).  Gumbel-max over the kept set: target = argmax_{l_v >= threshold}
+// (l_v + G_v), G_v = -ln(-ln U_v), which draws v with probability
+// proportional to exp(l_v) over the kept ids.  U_v comes from Philox4x64-10
+// (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+// SC 2011) at counter (v / 4, row, offset, 0) under key (seed, 0), word v % 4:
+// U = (2 (x >> 41) + 1) 2^-24, exact in fp32 and inside (0, 1).
+__device__ __forceinline__ uint64_t philox_word(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3, uint64_t k0,
+                                                uint64_t k1, int word) {
+    constexpr uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    constexpr uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+        const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return word == 0 ? c0 : word == 1 ? c1 : word == 2 ? c2 : c3;
+}
+// Natural logarithm for normal x > 0 as a fixed sequence of IEEE fp32
+// operations (explicitly rounded, never contracted), so that every platform
+// computing the same steps gets the same bits: x = 2^e m with m in
+// [sqrt(1/2), sqrt(2)), ln m = 2 atanh(s) = 2s (1 + s^2/3 + ... + s^10/11)
+// with s = (m - 1)/(m + 1), |s| <= 0.1716; ln x = e ln 2 + ln m.
+__device__ __forceinline__ float ln_f32(float x) {
+    const uint32_t b = __float_as_uint(x);
+    int e = (int)((b >> 23) & 0xffu) - 127;
+    float m = __uint_as_float((b & 0x7fffffu) | 0x3f800000u);
+    if (m > 0x1.6a09e6p+0f) {
+        m = __fmul_rn(m, 0.5f);
+        e += 1;
+    }
+    const float s = __fdiv_rn(__fsub_rn(m, 1.0f), __fadd_rn(m, 1.0f));
+    const float z = __fmul_rn(s, s);
+    float p = __fmaf_rn(z, 0x1.745d18p-4f, 0x1.c71c72p-4f);
+    p = __fmaf_rn(z, p, 0x1.24924ap-3f);
+    p = __fmaf_rn(z, p, 0x1.99999ap-3f);
+    p = __fmaf_rn(z, p, 0x1.555556p-2f);
+    p = __fmaf_rn(z, p, 1.0f);
+    const float lm = __fmul_rn(__fmul_rn(2.0f, s), p);
+    return __fmaf_rn(__int2float_rn(e), 0x1.62e430p-1f, lm);
+}
+__device__ __forceinline__ float gumbel(int v, int row, const VocabArgs &a) {
+    const uint64_t x = philox_word((uint64_t)(v >> 2), (uint64_t)row, a.offset, 0ull, a.seed, 0ull, v & 3);
+    const float u = __fmul_rn(__uint2float_rn(2u * (uint32_t)(x >> 41) + 1u), 0x1p-24f);
+    return -ln_f32(-ln_f32(u));
+}
+
+template <bool SAMPLE>
 __global__ void __cluster_dims__(VOCAB_CLUSTER, 1, 1) __launch_bounds__(VOCAB_THREADS)
 penalty_minp_kernel(const VocabArgs a, int slice) {
     cg::cluster_group cluster = cg::this_cluster();
@@ -45,6 +102,8 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
     __shared__ ArgMax cta_best;
     __shared__ int warp_cnt[VOCAB_THREADS / 32];
     __shared__ int cta_cnt;
+    __shared__ ArgMax warp_samp[SAMPLE ? VOCAB_THREADS / 32 : 1];
+    __shared__ ArgMax cta_samp;
 
     const int row = blockIdx.y;
     const unsigned rank = cluster.block_rank();
@@ -116,11 +175,36 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
         for (int w = 0; w < VOCAB_THREADS / 32; ++w) c += warp_cnt[w];
         cta_cnt = c;
     }
+    if constexpr (SAMPLE) {
+        // Gumbel-max draw over this slice's kept ids
+        ArgMax sb{-INFINITY, -1};
+#pragma unroll
+        for (int i = 0; i < VOCAB_CACHE; ++i) {
+            const int vv = v0 + i * VOCAB_THREADS + tid;
+            if (vv < v1 && x[i] >= f) sb = better(sb, ArgMax{__fadd_rn(x[i], gumbel(vv, row, a)), vv});
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ArgMax other{__shfl_xor_sync(0xffffffffu, sb.v, o), __shfl_xor_sync(0xffffffffu, sb.i, o)};
+            sb = better(sb, other);
+        }
+        if (lane == 0) warp_samp[warp] = sb;
+        __syncthreads();
+        if (tid == 0) {
+            ArgMax b = warp_samp[0];
+            for (int w = 1; w < VOCAB_THREADS / 32; ++w) b = better(b, warp_samp[w]);
+            cta_samp = b;
+        }
+    }
     cluster.sync();
     if (rank == 0 && tid == 0) {
         int total = 0;
-        for (int r = 0; r < VOCAB_CLUSTER; ++r) total += *cluster.map_shared_rank(&cta_cnt, r);
-        a.target[row] = gbest.i;
+        ArgMax sbest{-INFINITY, -1};
+        for (int r = 0; r < VOCAB_CLUSTER; ++r) {
+            total += *cluster.map_shared_rank(&cta_cnt, r);
+            if constexpr (SAMPLE) sbest = better(sbest, *cluster.map_shared_rank(&cta_samp, r));
+        }
+        a.target[row] = SAMPLE ? sbest.i : gbest.i;
         a.kept[row] = total;
     }
     cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
@@ -190,7 +274,10 @@ cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st) {
     slice = (slice + 31) & ~31;
     if (slice > VOCAB_MAX_SLICE) return cudaErrorInvalidValue;
     dim3 grid(VOCAB_CLUSTER, a.T);
-    penalty_minp_kernel<<<grid, VOCAB_THREADS, 0, st>>>(a, slice);
+    if (a.sample)
+        penalty_minp_kernel<true><<<grid, VOCAB_THREADS, 0, st>>>(a, slice);
+    else
+        penalty_minp_kernel<false><<<grid, VOCAB_THREADS, 0, st>>>(a, slice);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     accept_kernel<<<1, 1024, 0, st>>>(a);

@@ -14,6 +14,8 @@ Functions, each following the definition stated in ``oracle.c``:
   penalty_minp       -- windowed penalty, temperature, min-p count, greedy target
   accept             -- exact-match acceptance, longest path
   commit_path        -- the accepted path's K/V rows moved to the end of the sequence
+  philox4x64, ln_f32 -- Philox4x64-10 and the fp32 logarithm the sampler uses
+  sample             -- min-p sampling (Gumbel-max over the kept set)
 """
 from __future__ import annotations
 
@@ -55,6 +57,10 @@ def _load():
         lib.oracle_penalty_minp.argtypes = [P, i32, i32, P, i32, flt, flt, dbl, P, P, P]
         lib.oracle_accept.argtypes = [P, P, P, i32, i32, P, P]
         lib.oracle_commit.argtypes = [P, i64, i64, i32, i32, i32, P, P, P]
+        lib.oracle_philox4x64.argtypes = [P, P, P]
+        lib.oracle_ln_f32.argtypes = [flt]
+        lib.oracle_ln_f32.restype = flt
+        lib.oracle_sample.argtypes = [P, i32, i32, dbl, ctypes.c_uint64, ctypes.c_uint64, P]
         lib.oracle_set_threads.argtypes = [i32]
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -206,3 +212,31 @@ def commit_path(k, v, N: int, result, path):
         status = int(st[0])
         out.append(torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16))
     return out[0], out[1], status
+
+
+def philox4x64(counter, key) -> np.ndarray:
+    """uint64[4]: Philox4x64-10 of a 4-word counter under a 2-word key."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint64))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64))
+    out = np.zeros(4, dtype=np.uint64)
+    _load().oracle_philox4x64(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def ln_f32(x: float) -> float:
+    """The sampler's fp32 natural logarithm (normal positive inputs)."""
+    return float(_load().oracle_ln_f32(float(np.float32(x))))
+
+
+def sample(pen_logits, min_p: float, seed: int, offset: int = 0) -> np.ndarray:
+    """int32 [T]: min-p sampled targets from final fp32 logits [T][V] (Gumbel-max
+    over the kept set, Philox4x64-10 uniforms keyed by (seed, 0) at counter
+    (v / 4, row, offset, 0))."""
+    lg = np.ascontiguousarray(np.asarray(pen_logits, dtype=np.float32))
+    T, V = lg.shape
+    out = np.zeros(T, dtype=np.int32)
+    rc = _load().oracle_sample(_ptr(lg), T, V, log_min_p(min_p), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                               _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_sample failed ({rc})")
+    return out

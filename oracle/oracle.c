@@ -372,3 +372,92 @@ int oracle_commit(uint16_t *cache, int64_t ld, int64_t N, int T, int Hkv, int d,
     free(tmp);
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Min-p sampling at a temperature (model card flags --min_p 0.1           */
+/* --temperature 1.0: the method samples its target tokens).               */
+/*                                                                          */
+/* Random numbers: Philox4x64-10, the counter-based generator of Salmon,   */
+/* Moraes, Dror and Shaw ("Parallel random numbers: as easy as 1, 2, 3",    */
+/* SC 2011): ten rounds of                                                  */
+/*   (hi0, lo0) = M0 * c0, (hi1, lo1) = M1 * c2   (128-bit products)        */
+/*   c = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0)                           */
+/* with the key advanced by the Weyl increments (W0, W1) before every round */
+/* after the first.                                                         */
+void oracle_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) { k0 += W0; k1 += W1; }
+        const unsigned __int128 p0 = (unsigned __int128)M0 * c0, p1 = (unsigned __int128)M1 * c2;
+        const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Natural logarithm in fp32 for normal x > 0, every step an IEEE fp32      */
+/* operation (no contraction): x = 2^e m, m in [sqrt(1/2), sqrt(2));         */
+/* ln m = 2 atanh(s), s = (m - 1)/(m + 1), by the series                    */
+/* 2s (1 + s^2/3 + s^4/5 + ... + s^10/11) (|s| <= 0.1716, truncation below  */
+/* 1e-10 relative); ln x = e ln 2 + ln m.                                   */
+float oracle_ln_f32(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    int e = (int)((b >> 23) & 0xff) - 127;
+    const uint32_t mb = (b & 0x7fffffu) | 0x3f800000u;
+    float m;
+    memcpy(&m, &mb, 4);
+    if (m > 0x1.6a09e6p+0f) { m = m * 0.5f; e += 1; }
+    const float s = (m - 1.0f) / (m + 1.0f);
+    const float z = s * s;
+    float p = fmaf(z, 0x1.745d18p-4f, 0x1.c71c72p-4f);
+    p = fmaf(z, p, 0x1.24924ap-3f);
+    p = fmaf(z, p, 0x1.99999ap-3f);
+    p = fmaf(z, p, 0x1.555556p-2f);
+    p = fmaf(z, p, 1.0f);
+    const float lm = (2.0f * s) * p;
+    return fmaf((float)e, 0x1.62e430p-1f, lm);
+}
+
+/* Sampled target of every row from its final (penalised, tempered) fp32    */
+/* logits l[0..V): the min-p kept set K = {v : (double)l_v >= m + ln min_p}  */
+/* (m = max l), and the Gumbel-max draw                                      */
+/*   target = argmax_{v in K} (l_v + G_v),  G_v = -ln(-ln U_v)               */
+/* (lowest id on equal keys), which draws v with probability proportional to */
+/* exp(l_v) over K.  U_v = (2 (x >> 41) + 1) 2^-24 (exact in fp32, inside    */
+/* (0, 1)) with x = word (v mod 4) of Philox4x64-10 at counter               */
+/* (v / 4, row, offset, 0) and key (seed, 0).                                */
+int oracle_sample(const float *pen, int T, int V, double log_min_p, uint64_t seed, uint64_t offset,
+                  int32_t *sampled)
+{
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < T; ++i) {
+        const float *row = pen + (size_t)i * V;
+        float m = -INFINITY;
+        for (int vv = 0; vv < V; ++vv)
+            if (row[vv] > m) m = row[vv];
+        const double thr = (double)m + log_min_p;
+        float best = -INFINITY;
+        int arg = -1;
+        for (int vv = 0; vv < V; ++vv) {
+            if (!((double)row[vv] >= thr)) continue;
+            const uint64_t ctr[4] = {(uint64_t)(vv >> 2), (uint64_t)i, offset, 0};
+            const uint64_t key[2] = {seed, 0};
+            uint64_t out[4];
+            oracle_philox4x64(ctr, key, out);
+            const uint64_t x = out[vv & 3];
+            const float u = (float)(2u * (uint32_t)(x >> 41) + 1u) * 0x1p-24f;
+            const float g = -oracle_ln_f32(-oracle_ln_f32(u));
+            const float k = row[vv] + g;
+            if (arg < 0 || k > best) { best = k; arg = vv; }
+        }
+        sampled[i] = arg;
+    }
+    return 0;
+}

@@ -23,6 +23,7 @@ import networkx as nx
 import numpy as np
 import pytest
 import scipy.special
+import scipy.stats
 import torch
 import torch.nn.functional as F
 
@@ -444,3 +445,57 @@ def test_commit_identity_and_data_errors():
                      ([-1, 0, 0, 0], list(range(T)))):
         k2, v2, st = oracle.commit_path(k, v, N, res, np.asarray(pth, dtype=np.int32))
         assert st == 5 and torch.equal(k2, k) and torch.equal(v2, v)
+
+
+# --------------------------------------------------------------------------
+# min-p sampling: Philox4x64-10, the fp32 logarithm, the Gumbel-max draw
+# --------------------------------------------------------------------------
+def test_philox_matches_numpy():
+    """numpy's Philox bit generator is Philox4x64-10; it advances its counter
+    before each block, so its block from counter c - 1 is ours at counter c."""
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        c = [int(rng.integers(1, 2**63)), int(rng.integers(0, 2**63)), int(rng.integers(0, 2**63)), 0]
+        k = [int(rng.integers(0, 2**63)), int(rng.integers(0, 2**63))]
+        bg = np.random.Philox(counter=[c[0] - 1, c[1], c[2], c[3]], key=k)
+        np.testing.assert_array_equal(oracle.philox4x64(c, k), bg.random_raw(4).astype(np.uint64))
+
+
+def test_ln_f32_within_four_ulp():
+    rng = np.random.default_rng(6)
+    xs = np.concatenate([np.exp(rng.uniform(-60, 60, 4000)), 1 + rng.uniform(-0.3, 0.3, 2000),
+                         (2.0 * np.arange(1, 2000) + 1) * 2.0 ** -24]).astype(np.float32)
+    for x in xs:
+        got = oracle.ln_f32(float(x))
+        ref = math.log(float(x))
+        ulp = np.spacing(np.float32(abs(ref))) if ref != 0 else np.float32(2.0 ** -149)
+        assert abs(got - ref) <= 4 * float(ulp), (x, got, ref)
+
+
+@pytest.mark.parametrize("min_p", [0.0, 0.3])
+def test_gumbel_max_draws_the_min_p_distribution(min_p):
+    """Each row draws independently (its own counter); over many rows the
+    frequencies match softmax(l) renormalised over the min-p kept set."""
+    logits = np.array([0.0, 0.5, 1.0, 1.5, -3.0, 2.0, 1.9], dtype=np.float32)
+    R = 40000
+    s = oracle.sample(np.tile(logits, (R, 1)), min_p, seed=1234)
+    p = np.exp(logits - logits.max())
+    keep = p >= min_p * p.max()
+    p = np.where(keep, p, 0.0)
+    p /= p.sum()
+    counts = np.bincount(s, minlength=logits.size)
+    assert counts[~keep].sum() == 0
+    exp = p[keep] * R
+    chi2 = (((counts[keep] - exp) ** 2) / exp).sum()
+    assert scipy.stats.chi2.sf(chi2, keep.sum() - 1) > 1e-4, (counts, exp)
+
+
+def test_sampling_edge_cases():
+    lg = np.array([[0.0, 5.0, 1.0], [3.0, 3.0, -1.0]], dtype=np.float32)
+    # min_p = 1: only the maximum is kept, so the draw is the argmax (ties: both kept)
+    s = oracle.sample(lg, 1.0, seed=9)
+    assert s[0] == 1 and s[1] in (0, 1)
+    # the same seed and offset reproduce; another offset draws anew
+    big = np.random.default_rng(0).normal(0, 3, (64, 1000)).astype(np.float32)
+    a, b, c = (oracle.sample(big, 0.0, seed=3, offset=o) for o in (0, 0, 1))
+    assert np.array_equal(a, b) and not np.array_equal(a, c)

@@ -461,3 +461,34 @@ def test_commit_path_data_errors_reported_not_trapped():
         assert int(rd[3]) == (0 if res[0] == 0 else 5)
         assert torch.equal(kg, k) and torch.equal(vg, v)
     assert ts.ts_device_error(True) == 0
+
+
+# --------------------------------------------------------------------------
+# min-p sampled targets (next row): Gumbel-max with Philox4x64-10
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("V,W_,flip,seed,min_p,temp", [(152064, 1024, 0.25, 0, 0.1, 1.0),
+                                                       (152064, 1024, 0.0, 1, 0.02, 1.0),
+                                                       (1000, 50, 0.5, 2, 0.0, 1.0),
+                                                       (33, 5, 0.0, 3, 0.3, 0.7),
+                                                       (163840, 2048, 0.3, 5, 0.1, 2.0)])
+def test_sampled_vocab_stage_bit_exact(V, W_, flip, seed, min_p, temp):
+    """Sampled targets, kept counts, accepted length and path agree bit for bit
+    with the oracle's Gumbel-max draw from the same Philox stream."""
+    parent = W.verify_parents()
+    T = len(parent)
+    vi = W.make_vocab_inputs(parent, V, W_, seed=seed, device="cuda", flip_rows=flip)
+    target = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    kept = torch.full_like(target, -7)
+    result = torch.full((4,), -7, dtype=torch.int32, device="cuda")
+    path = torch.full_like(target, -7)
+    ts.ts_penalty_minp_sample_verify(vi.logits, vi.history, 1.2, min_p, temp, 77 + seed, 5, vi.draft, vi.parent,
+                                     vi.anchor, target, kept, result, path)
+    torch.cuda.synchronize()
+    _, rk, pen = oracle.penalty_minp(vi.logits.cpu().numpy(), vi.history.cpu().numpy(), 1.2, min_p, temp,
+                                     return_logits=True)
+    rs = oracle.sample(pen, min_p, 77 + seed, 5)
+    np.testing.assert_array_equal(target.cpu().numpy(), rs)
+    np.testing.assert_array_equal(kept.cpu().numpy(), rk)
+    rr, rp = oracle.accept(vi.draft.cpu().numpy(), parent, rs, vi.anchor)
+    np.testing.assert_array_equal(result.cpu().numpy(), rr)
+    np.testing.assert_array_equal(path.cpu().numpy(), rp)
