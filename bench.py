@@ -108,15 +108,15 @@ def time_sampled_vocab(step, s, reps: int = 5) -> dict:
 def workload_config(name: str):
     from long_context_attention_tree_b300 import workloads as W
     if name == "qwen14b-100k":
-        return W.CONFIGS[5]
+        return W.WORKLOADS["qwen14b-100k"]
     if name == "llama2-7b-100k":
-        return W.CONFIGS[4]
+        return W.WORKLOADS["llama2-7b-100k"]
     if name.startswith("qwen14b-"):  # the Qwen2.5-14B shape at another context length (profiling)
         N = int(name.split("-")[1].lower().replace("k", "")) * 1024 if name.lower().endswith("k") else int(name.split("-")[1])
-        return W.CONFIGS[5].with_N(N)
+        return W.WORKLOADS["qwen14b-100k"].with_N(N)
     if name.startswith("llama8b-"):
         N = int(name.split("-")[1].lower().replace("k", "")) * 1024 if name.lower().endswith("k") else int(name.split("-")[1])
-        return W.CONFIGS[3].with_N(N)
+        return W.WORKLOADS["llama8b-sweep"].with_N(N)
     raise SystemExit(f"unknown workload {name}")
 
 

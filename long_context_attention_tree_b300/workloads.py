@@ -130,13 +130,13 @@ class Config:
         return 2 * self.Hkv * self.N * self.d * 2
 
 
-CONFIGS = {
-    1: Config(1, "tiny-1layer", Hq=4, Hkv=1, d=64, N=4096, n_chains=0, budget=1024),
-    2: Config(2, "llama3.1-8b-20k-1layer", Hq=32, Hkv=8, d=128, N=20480),
-    3: Config(3, "llama3.1-8b-sweep-32layer", Hq=32, Hkv=8, d=128, N=102400, layers=32),
-    4: Config(4, "llama2-7b-mha-100k-1layer", Hq=32, Hkv=32, d=128, N=102400),
-    5: Config(5, "qwen2.5-14b-100k-48layer-step", Hq=40, Hkv=8, d=128, N=102400, layers=48,
-              vocab=152064),
+WORKLOADS = {
+    "tiny": Config(1, "tiny-1layer", Hq=4, Hkv=1, d=64, N=4096, n_chains=0, budget=1024),
+    "llama8b-20k": Config(2, "llama3.1-8b-20k-1layer", Hq=32, Hkv=8, d=128, N=20480),
+    "llama8b-sweep": Config(3, "llama3.1-8b-sweep-32layer", Hq=32, Hkv=8, d=128, N=102400, layers=32),
+    "llama2-7b-100k": Config(4, "llama2-7b-mha-100k-1layer", Hq=32, Hkv=32, d=128, N=102400),
+    "qwen14b-100k": Config(5, "qwen2.5-14b-100k-48layer-step", Hq=40, Hkv=8, d=128, N=102400, layers=48,
+                           vocab=152064),
 }
 SWEEP_N = (20480, 40960, 61440, 81920, 102400)
 

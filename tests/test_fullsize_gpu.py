@@ -55,7 +55,7 @@ def _check_step(step: SpecStep, layers, rows_per_layer=6):
 
 
 def test_qwen14b_full_step_all_layers():
-    cfg = W.CONFIGS[5]
+    cfg = W.WORKLOADS["qwen14b-100k"]
     step = SpecStep(cfg)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -74,7 +74,7 @@ def test_qwen14b_full_step_all_layers():
 
 
 def test_step_graph_replay_matches_eager():
-    cfg = W.CONFIGS[5]
+    cfg = W.WORKLOADS["qwen14b-100k"]
     step = SpecStep(cfg, layers=3)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -97,7 +97,7 @@ def test_step_graph_replay_matches_eager():
 
 @pytest.mark.parametrize("N", [20480, 102400])
 def test_llama8b_sweep_layers(N):
-    cfg = W.CONFIGS[3].with_N(N)
+    cfg = W.WORKLOADS["llama8b-sweep"].with_N(N)
     step = SpecStep(cfg, layers=2)
     step.run()
     torch.cuda.synchronize()
@@ -105,7 +105,7 @@ def test_llama8b_sweep_layers(N):
 
 
 def test_llama2_7b_mha_layer():
-    cfg = W.CONFIGS[4]
+    cfg = W.WORKLOADS["llama2-7b-100k"]
     step = SpecStep(cfg)
     step.run()
     torch.cuda.synchronize()

@@ -135,10 +135,10 @@ def test_tree_attn_forced_cuda_core_path_matches(monkeypatch):
     check_attn(out, lse, ro, rl)
 
 
-@pytest.mark.parametrize("cid", [1, 2])
-def test_config_full_parity(cid):
-    """The tiny config and the LLaMA3.1-8B 20K layer, every output row."""
-    cfg = W.CONFIGS[cid]
+@pytest.mark.parametrize("name", ["tiny", "llama8b-20k"])
+def test_workload_full_parity(name):
+    """The tiny workload and the LLaMA3.1-8B 20K layer, every output row."""
+    cfg = W.WORKLOADS[name]
     x = W.make_layer_inputs(cfg, 0, device="cuda")
     out, lse, sc = run_attn(x.q, x.k, x.v, cfg.N, cfg.parents, cfg.scale, scores=True)
     ro, rl = oracle.tree_attn(x.q.cpu(), x.k.cpu(), x.v.cpu(), cfg.N, cfg.parents, cfg.scale)
@@ -234,7 +234,7 @@ def test_select_ties_and_signed_zero():
 
 
 def test_draft_attention_over_partial_cache():
-    cfg = W.CONFIGS[2]
+    cfg = W.WORKLOADS["llama8b-20k"]
     x = W.make_layer_inputs(cfg, 0, device="cuda")
     N = cfg.N
     sc = torch.empty((cfg.Hkv, cfg.n_chunks), dtype=torch.float32, device="cuda")
