@@ -56,8 +56,8 @@ SimtPlan simt_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms);
 cudaError_t launch_tree_attn_simt(const AttnArgs &a, const SimtPlan &p, cudaStream_t st);
 cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st);
 
-// CUDA-core path for small batches (T * G <= 24, head dim 128): one 256-token
-// KV range per CTA, splits = ceil((N + T) / 256)
+// CUDA-core path for small batches (T * G <= 24, head dim 128): one 128-token
+// KV range per CTA, splits = ceil((N + T) / 128)
 bool small_ok(int T, int Hq, int Hkv, int d);
 int small_splits(int T, int64_t N);
 cudaError_t launch_tree_attn_small(const AttnArgs &a, int splits, cudaStream_t st);
