@@ -141,6 +141,29 @@ def test_vocab_rejects():
     assert call(logits=0x10002) == ts.TS_ERR_INVALID_ARG
 
 
+def test_sampled_vocab_rejects():
+    """The sampled entry point validates exactly like the greedy one."""
+    L = ts.lib()
+    P = 0x10000
+    f = L.ts_penalty_minp_sample_verify
+    ok = dict(logits=P, T=120, V=152064, history=P, W=1024, theta=1.2, min_p=0.1, temp=1.0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["logits"], a["T"], a["V"], a["history"], a["W"], a["theta"], a["min_p"], a["temp"],
+                 2**64 - 1, 7, P, P, 0, P, P, P, P, None)
+    assert call(T=0) == ts.TS_ERR_UNSUPPORTED
+    assert call(T=1025) == ts.TS_ERR_UNSUPPORTED
+    assert call(V=200000) == ts.TS_ERR_UNSUPPORTED
+    assert call(theta=float("nan")) == ts.TS_ERR_INVALID_ARG
+    assert call(temp=0.0) == ts.TS_ERR_INVALID_ARG
+    assert call(min_p=-0.1) == ts.TS_ERR_INVALID_ARG
+    assert call(W=-1) == ts.TS_ERR_INVALID_ARG
+    assert call(history=None) == ts.TS_ERR_INVALID_ARG
+    assert call(logits=0x10002) == ts.TS_ERR_INVALID_ARG
+
+
 def test_product_does_not_import_oracle():
     """The product package and its sources never reference the oracle."""
     pkg = os.path.join(ROOT, "long_context_attention_tree_b300")
