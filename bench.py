@@ -42,20 +42,29 @@ UNIT = "GB/s"
 # DRAM traffic of the tcgen05 verify kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum of one launch, Qwen2.5-14B
 # shape at 40960 tokens: 247.38 + 3.65 MB for 167.77 MB of prefix K/V), scaled
-# to a launch by its prefix K/V bytes.  It holds only for the kernel source it
-# was taken on (the hash below); for any other source the traffic is unknown.
+# to a launch by its prefix K/V bytes.  It holds only for the kernel code it
+# was taken on: the fingerprint below is of that code with comments and
+# whitespace removed; for any other code the traffic is unknown (null).
 VERIFY_TRAFFIC_PER_KV_BYTE = (247.375104 + 3.650304) / 167.772160
-VERIFY_TRAFFIC_SOURCE_SHA1 = "68d3212966bddeb07a876c9f037b5c68cb2a5186"
+VERIFY_TRAFFIC_CODE_SHA1 = "8ca1a49f8b8f972d773faf4abffc4b6cedf060e7"
+
+
+def _code_fingerprint(paths) -> str:
+    import hashlib
+    import re
+    h = hashlib.sha1()
+    for p in paths:
+        with open(p) as fh:
+            t = fh.read()
+        t = re.sub(r"/\*.*?\*/", " ", t, flags=re.S)
+        t = re.sub(r"//[^\n]*", " ", t)
+        h.update(" ".join(t.split()).encode())
+    return h.hexdigest()
 
 
 def verify_traffic(kv_bytes: float):
-    import hashlib
     csrc = os.path.join(ROOT, "long_context_attention_tree_b300", "csrc")
-    h = hashlib.sha1()
-    for f in ("attn_tc.cu", "tc_ptx.cuh"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest() != VERIFY_TRAFFIC_SOURCE_SHA1:
+    if _code_fingerprint([os.path.join(csrc, "attn_tc.cu"), os.path.join(csrc, "tc_ptx.cuh")]) != VERIFY_TRAFFIC_CODE_SHA1:
         return None
     return kv_bytes * VERIFY_TRAFFIC_PER_KV_BYTE
 

@@ -26,7 +26,9 @@
 // Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q once, then K and V tiles into 2-stage rings;
 //   warp 1      owns TMEM (512 columns); one thread issues every tcgen05.mma;
-//   warps 2-3   idle;
+//   warp 2      chunk-score reducer: takes the scoring rows' chunk sums from a
+//               shared-memory ring and writes the max over the group's heads;
+//   warp 3      idle;
 //   warps 4-7   softmax warpgroup 0 (thread = row of M-tile 0);
 //   warps 8-11  softmax warpgroup 1 (M-tile 1 of a pair stream).
 // A softmax thread loads its row of S (128 fp32) into registers and writes
@@ -35,7 +37,8 @@
 // 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so the TMEM
 // round trip of a rescale is rare.  The normaliser l sums the bf16-rounded
 // weights that the P.V product uses.  The chunk importance of the scoring
-// row is summed from the same S values.
+// row is summed from the same S values (packed adds) and handed to warp 2,
+// so the softmax warps never wait for the reduction.
 // Every wait is bounded (see tc_ptx.cuh): a wait that gives up raises the
 // CTA's abort flag and the sticky device status word, and the CTA winds down.
 #include "internal.h"
