@@ -115,8 +115,9 @@ size_t ts_tree_attn_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t N);
  *            or NULL when that is 0.
  * Supported: d in {64, 128}; Hq % Hkv == 0; Hq/Hkv <= 32; 0 <= T <= 128;
  * N >= 0; N + T >= 1 when T >= 1.  T >= 64 with d == 128 runs on the tensor
- * cores (tcgen05, TMEM accumulators); other shapes run on the CUDA cores.
- * T == 0 is a no-op.
+ * cores (tcgen05, TMEM accumulators); other shapes run on the CUDA cores
+ * (batches of at most 24 (row, head) pairs per KV head with d == 128, such as
+ * the 4-row drafting pass, on a kernel built for them).  T == 0 is a no-op.
  */
 ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_kv,
                        int64_t N, int T, int Hq, int Hkv, int d, float scale,
