@@ -16,6 +16,7 @@ Functions, each following the definition stated in ``oracle.c``:
   commit_path        -- the accepted path's K/V rows moved to the end of the sequence
   philox4x64, ln_f32 -- Philox4x64-10 and the fp32 logarithm the sampler uses
   sample             -- min-p sampling (Gumbel-max over the kept set)
+  ngram_topk         -- top-k 4-grams of the generated text that start with the anchor
 """
 from __future__ import annotations
 
@@ -61,6 +62,7 @@ def _load():
         lib.oracle_ln_f32.argtypes = [flt]
         lib.oracle_ln_f32.restype = flt
         lib.oracle_sample.argtypes = [P, i32, i32, dbl, ctypes.c_uint64, ctypes.c_uint64, P]
+        lib.oracle_ngram_topk.argtypes = [P, i64, i32, i32, P, P, P]
         lib.oracle_set_threads.argtypes = [i32]
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -240,3 +242,17 @@ def sample(pen_logits, min_p: float, seed: int, offset: int = 0) -> np.ndarray:
     if rc:
         raise ValueError(f"oracle_sample failed ({rc})")
     return out
+
+
+def ngram_topk(seq, anchor: int, k: int):
+    """(chains int32 [m][4], counts int32 [m]), m <= k: the 4-grams of seq that
+    start with anchor, most frequent first, then by their last three tokens."""
+    sq = np.ascontiguousarray(np.asarray(seq, dtype=np.int32))
+    chains = np.zeros((max(k, 1), 4), dtype=np.int32)
+    counts = np.zeros(max(k, 1), dtype=np.int32)
+    found = np.zeros(1, dtype=np.int32)
+    rc = _load().oracle_ngram_topk(_ptr(sq), sq.size, int(anchor), int(k), _ptr(chains), _ptr(counts), _ptr(found))
+    if rc:
+        raise ValueError(f"oracle_ngram_topk failed ({rc})")
+    m = int(found[0])
+    return chains[:m], counts[:m]

@@ -461,3 +461,60 @@ int oracle_sample(const float *pen, int T, int V, double log_min_p, uint64_t see
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* 4-gram table of the generated text and top-k retrieval ("How it works"  */
+/* on the TokenSwift tool listing: the top-k candidate 4-grams form draft  */
+/* tokens and the n-gram table is updated after every step; the summary's */
+/* "Approach": n-gram retrieval from the generated text).                   */
+/*   count(w) = #{p in [3, n) : seq[p-3..p] = w}  (the table after seq).     */
+/*   For an anchor a (the next token, which every draft root must equal):   */
+/*   the 4-grams w with w0 = a and count(w) > 0, by count descending, then   */
+/*   (w1, w2, w3) ascending; the first k of them.  Returns how many were     */
+/*   found (<= k) in *found; chains[i][0..4) = w, counts[i] = count(w).      */
+typedef struct { int32_t w[3]; int32_t c; } ngram3_t;
+
+static int by_tail(const void *x, const void *y)
+{
+    const int32_t *a = ((const ngram3_t *)x)->w, *b = ((const ngram3_t *)y)->w;
+    for (int i = 0; i < 3; ++i)
+        if (a[i] != b[i]) return a[i] < b[i] ? -1 : 1;
+    return 0;
+}
+static int by_count_then_tail(const void *x, const void *y)
+{
+    const ngram3_t *a = (const ngram3_t *)x, *b = (const ngram3_t *)y;
+    if (a->c != b->c) return a->c > b->c ? -1 : 1;
+    return by_tail(x, y);
+}
+
+int oracle_ngram_topk(const int32_t *seq, int64_t n, int32_t anchor, int k, int32_t *chains, int32_t *counts,
+                      int32_t *found)
+{
+    *found = 0;
+    if (n < 4 || k <= 0) return 0;
+    ngram3_t *g = (ngram3_t *)malloc(sizeof(ngram3_t) * (size_t)(n - 3));
+    if (!g) return 1;
+    int64_t m = 0;
+    for (int64_t p = 3; p < n; ++p)
+        if (seq[p - 3] == anchor) {
+            g[m].w[0] = seq[p - 2]; g[m].w[1] = seq[p - 1]; g[m].w[2] = seq[p]; g[m].c = 1;
+            ++m;
+        }
+    qsort(g, (size_t)m, sizeof(ngram3_t), by_tail);
+    int64_t u = 0;  /* distinct tails with their counts */
+    for (int64_t i = 0; i < m; ++i) {
+        if (u > 0 && by_tail(&g[u - 1], &g[i]) == 0) ++g[u - 1].c;
+        else g[u++] = g[i];
+    }
+    qsort(g, (size_t)u, sizeof(ngram3_t), by_count_then_tail);
+    const int take = (int)(u < k ? u : k);
+    for (int i = 0; i < take; ++i) {
+        chains[4 * i] = anchor;
+        for (int j = 0; j < 3; ++j) chains[4 * i + 1 + j] = g[i].w[j];
+        counts[i] = g[i].c;
+    }
+    *found = take;
+    free(g);
+    return 0;
+}

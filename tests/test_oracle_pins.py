@@ -499,3 +499,47 @@ def test_sampling_edge_cases():
     big = np.random.default_rng(0).normal(0, 3, (64, 1000)).astype(np.float32)
     a, b, c = (oracle.sample(big, 0.0, seed=3, offset=o) for o in (0, 0, 1))
     assert np.array_equal(a, b) and not np.array_equal(a, c)
+
+
+# --------------------------------------------------------------------------
+# n-gram table: top-k 4-grams of the generated text that start with the anchor
+# --------------------------------------------------------------------------
+def _ngram_brute(seq, anchor, k):
+    from collections import Counter
+    c = Counter(tuple(seq[p - 3:p + 1]) for p in range(3, len(seq)))
+    cand = sorted(((-n, w[1:], w) for w, n in c.items() if w[0] == anchor))
+    return [list(w) for _, _, w in cand[:k]], [-n for n, _, _ in cand[:k]]
+
+
+def test_ngram_hand_examples(golden_dir):
+    for line in open(os.path.join(golden_dir, "ngram_hand.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, seq, anchor, k, want = [x.strip() for x in line.split("|")]
+        chains, counts = oracle.ngram_topk([int(x) for x in seq.split()], int(anchor), int(k))
+        got = "-" if len(chains) == 0 else " ; ".join(
+            " ".join(str(int(x)) for x in c) + f" : {int(n)}" for c, n in zip(chains, counts))
+        assert got == want, name
+
+
+@pytest.mark.parametrize("vocab,n,k", [(3, 200, 5), (6, 1000, 20), (50, 3000, 20), (2, 40, 30)])
+def test_ngram_topk_matches_a_counter(vocab, n, k):
+    """Against collections.Counter over every window, for every anchor."""
+    seq = np.random.default_rng(vocab * n).integers(0, vocab, n).tolist()
+    total = 0
+    for a in range(vocab + 1):
+        chains, counts = oracle.ngram_topk(seq, a, k)
+        want_c, want_n = _ngram_brute(seq, a, k)
+        assert chains.tolist() == want_c and counts.tolist() == want_n
+        total += oracle.ngram_topk(seq, a, 10 ** 6)[1].sum()
+    assert total == n - 3  # every window counted once
+
+
+def test_ngram_update_adds_exactly_the_new_window():
+    seq = [3, 1, 4, 1, 5, 9, 2, 6, 5, 3, 5, 8, 9, 7, 9, 3, 2, 3, 8, 4]
+    for n in range(4, len(seq)):
+        before = {tuple(c): m for c, m in zip(*oracle.ngram_topk(seq[:n], seq[n - 3], 10 ** 6))}
+        after = {tuple(c): m for c, m in zip(*oracle.ngram_topk(seq[:n + 1], seq[n - 3], 10 ** 6))}
+        w = tuple(seq[n - 3:n + 1])
+        assert after[w] == before.get(w, 0) + 1
+        assert all(after[x] == before[x] for x in before if x != w)
