@@ -51,10 +51,10 @@ def _load():
         P = ctypes.c_void_p
         i32, i64, dbl, flt = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_float
         lib.oracle_visible.argtypes = [P, i32, P]
-        lib.oracle_tree_attn_rows.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, dbl, P, P, i32, P, P]
+        lib.oracle_tree_attn_rows.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, dbl, P, P, P, i32, P, P]
         lib.oracle_score_chunks.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P]
         lib.oracle_select.argtypes = [P, i32, i32, i32, P]
-        lib.oracle_gather.argtypes = [P, i32, i32, i32, i64, P, i64, i32, P, i64]
+        lib.oracle_gather.argtypes = [P, i32, i32, i32, i64, P, i64, i32, P, i64, P]
         lib.oracle_penalty_minp.argtypes = [P, i32, i32, P, i32, flt, flt, dbl, P, P, P]
         lib.oracle_accept.argtypes = [P, P, P, i32, i32, P, P]
         lib.oracle_commit.argtypes = [P, i64, i64, i32, i32, i32, P, P, P]
@@ -98,21 +98,24 @@ def visible(parent) -> np.ndarray:
     return vis.astype(bool)
 
 
-def tree_attn(q, k, v, N: int, parent, scale: float, rows=None):
+def tree_attn(q, k, v, N: int, parent, scale: float, rows=None, prefix_len=None):
     """Tree-masked attention in fp64.
 
     q: bf16 [T][Hq][d]; k, v: bf16 [Hkv][ld][d] (prefix [0,N), batch rows [N,N+T)).
     rows: None for every (t, h), else an int array of row ids t*Hq + h.
+    prefix_len: None, or int [Hkv]: KV head g sees prefix rows [0, prefix_len[g]) only.
     Returns (out float64 [n_rows][d] or [T][Hq][d] when rows is None, lse float64)."""
     T, Hq, d = q.shape
     Hkv, ld, _ = k.shape
     qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
     p = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+    pl = None if prefix_len is None else np.ascontiguousarray(np.asarray(prefix_len, dtype=np.int32))
     rid = np.arange(T * Hq, dtype=np.int32) if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     out = np.zeros((rid.size, d), dtype=np.float64)
     lse = np.zeros(rid.size, dtype=np.float64)
     rc = _load().oracle_tree_attn_rows(_ptr(qb), _ptr(kb), _ptr(vb), ld, N, T, Hq, Hkv, d,
-                                       float(scale), _ptr(p), _ptr(rid), rid.size, _ptr(out), _ptr(lse))
+                                       float(scale), _ptr(p), _ptr(pl) if pl is not None else None,
+                                       _ptr(rid), rid.size, _ptr(out), _ptr(lse))
     if rc:
         raise ValueError(f"oracle_tree_attn_rows failed ({rc})")
     if rows is None:
@@ -146,19 +149,22 @@ def select(scores_f32, k: int) -> np.ndarray:
     return sel
 
 
-def gather(sel, src, N: int, chunk: int, ld_dst: int, fill=None):
+def gather(sel, src, N: int, chunk: int, ld_dst: int, fill=None, return_len=False):
     """bf16 [Hkv][ld_dst][d] compact cache holding the selected chunks (rows past
-    k*chunk, and rows of a partial last chunk past N, keep ``fill`` (zeros))."""
+    k*chunk, and rows of a partial last chunk past N, keep ``fill`` (zeros)).
+    With return_len, also the int32 [Hkv] count of tokens gathered per head."""
     import torch
     Hkv, ld_src, d = src.shape
     s = np.ascontiguousarray(np.asarray(sel, dtype=np.int32))
     kk = s.shape[1]
     srcb = _bf16_bits(src)
     dst = np.zeros((Hkv, ld_dst, d), dtype=np.uint16) if fill is None else _bf16_bits(fill).copy()
-    rc = _load().oracle_gather(_ptr(s), Hkv, kk, chunk, N, _ptr(srcb), ld_src, d, _ptr(dst), ld_dst)
+    plen = np.zeros(Hkv, dtype=np.int32)
+    rc = _load().oracle_gather(_ptr(s), Hkv, kk, chunk, N, _ptr(srcb), ld_src, d, _ptr(dst), ld_dst, _ptr(plen))
     if rc:
         raise ValueError(f"oracle_gather failed ({rc})")
-    return torch.from_numpy(dst.view(np.int16)).view(torch.bfloat16)
+    out = torch.from_numpy(dst.view(np.int16)).view(torch.bfloat16)
+    return (out, plen) if return_len else out
 
 
 def log_min_p(min_p: float) -> float:

@@ -82,7 +82,9 @@ int oracle_visible(const int32_t *parent, int T, uint8_t *vis)
 /*   q: bf16 [T][Hq][d];  k, v: bf16 [Hkv][ld_kv][d]; prefix rows [0,N),   */
 /*   the batch's own rows at [N, N+T).  Row id r = t*Hq + h.               */
 /*   For row (t,h), KV head g = h / (Hq/Hkv).  Visible keys: every prefix  */
-/*   token, and batch token N+u when u is t itself or an ancestor of t.    */
+/*   token j < P_g, and batch token N+u when u is t itself or an ancestor  */
+/*   of t.  P_g = N, or prefix_len[g] when prefix_len is given (a compact  */
+/*   partial cache whose heads hold different numbers of valid rows).      */
 /*   s_j = scale * (q . k_j)   (fp64 from the bf16 values)                  */
 /*   o   = sum_j softmax(s)_j v_j,   lse = log sum_j exp(s_j)               */
 /*   out: double [n_rows][d];  lse_out: double [n_rows] (nullable).         */
@@ -90,12 +92,15 @@ int oracle_visible(const int32_t *parent, int T, uint8_t *vis)
 /* ---------------------------------------------------------------------- */
 int oracle_tree_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                           int64_t ld_kv, int64_t N, int T, int Hq, int Hkv, int d,
-                          double scale, const int32_t *parent,
+                          double scale, const int32_t *parent, const int32_t *prefix_len,
                           const int32_t *row_ids, int n_rows,
                           double *out, double *lse_out)
 {
     if (T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || N < 0 || ld_kv < N + T)
         return 2;
+    if (prefix_len)
+        for (int g = 0; g < Hkv; ++g)
+            if (prefix_len[g] < 0 || prefix_len[g] > N) return 2;
     uint8_t *vis = (uint8_t *)malloc((size_t)(T > 0 ? T : 1) * (size_t)(T > 0 ? T : 1));
     if (!vis) return 2;
     if (T > 0 && oracle_visible(parent, T, vis)) { free(vis); return 1; }
@@ -123,9 +128,10 @@ int oracle_tree_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
             const uint16_t *qr = q + ((size_t)t * Hq + h) * d;
             const uint16_t *kh = k + (size_t)g * ld_kv * d;
             const uint16_t *vh = v + (size_t)g * ld_kv * d;
+            const int64_t P = prefix_len ? prefix_len[g] : N;
             double m = -INFINITY;
             for (int64_t j = 0; j < L; ++j) {
-                seen[j] = (j < N) ? 1 : vis[(size_t)t * T + (j - N)];
+                seen[j] = (j < N) ? (j < P) : vis[(size_t)t * T + (j - N)];
                 if (!seen[j]) continue;
                 double dot = 0.0;
                 for (int c = 0; c < d; ++c)
@@ -233,11 +239,17 @@ int oracle_select(const float *scores, int Hkv, int nc, int k, int32_t *sel)
 /*   dst[g][i*chunk + t] = src[g][sel[g][i]*chunk + t] for i<k, t<chunk,    */
 /* rows of d bf16 elements; tokens at or past N are not copied (a partial  */
 /* last chunk leaves its trailing rows of dst untouched).                  */
+/* part_len (nullable): int32 [Hkv], the number of tokens gathered for     */
+/* head g -- the rows [0, part_len[g]) of dst hold real tokens when the    */
+/* selection is ascending (only the last chunk of the prefix can be short, */
+/* and it is the largest index, so it sits last).                          */
 int oracle_gather(const int32_t *sel, int Hkv, int k, int chunk, int64_t N,
-                  const uint16_t *src, int64_t ld_src, int d, uint16_t *dst, int64_t ld_dst)
+                  const uint16_t *src, int64_t ld_src, int d, uint16_t *dst, int64_t ld_dst,
+                  int32_t *part_len)
 {
     if ((int64_t)k * chunk > ld_dst) return 2;
-    for (int g = 0; g < Hkv; ++g)
+    for (int g = 0; g < Hkv; ++g) {
+        int32_t copied = 0;
         for (int i = 0; i < k; ++i) {
             int64_t c = sel[(size_t)g * k + i];
             for (int t = 0; t < chunk; ++t) {
@@ -245,8 +257,11 @@ int oracle_gather(const int32_t *sel, int Hkv, int k, int chunk, int64_t N,
                 if (s >= N) break;
                 memcpy(dst + ((size_t)g * ld_dst + (size_t)i * chunk + t) * d,
                        src + ((size_t)g * ld_src + s) * d, sizeof(uint16_t) * (size_t)d);
+                ++copied;
             }
         }
+        if (part_len) part_len[g] = copied;
+    }
     return 0;
 }
 

@@ -232,6 +232,36 @@ def test_sampled_rows_equal_full():
     np.testing.assert_array_equal(ls_, lse.reshape(-1)[rows])
 
 
+@pytest.mark.parametrize("prefix_len", [[0, 5, 77], [77, 77, 77], [64, 1, 30]])
+def test_ragged_prefix_matches_sdpa_per_head(prefix_len):
+    """KV head g sees prefix rows [0, prefix_len[g]) only: torch SDPA per KV head
+    with a mask that hides the rest of the prefix."""
+    T, Hq, Hkv, d, N = 4, 6, 3, 64, 77
+    parent = [-1, 0, 1, 2]
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=31, value_kind="normal")
+    o, lse = oracle.tree_attn(q, k, v, N, parent, 0.125, prefix_len=prefix_len)
+    G = Hq // Hkv
+    vis = closure_mask(parent)
+    for g in range(Hkv):
+        mask = torch.zeros((T, N + T), dtype=torch.bool)
+        mask[:, :prefix_len[g]] = True
+        mask[:, N:] = torch.from_numpy(vis)
+        qq = q[:, g * G:(g + 1) * G].double().permute(1, 0, 2)
+        kk = k[g:g + 1, :N + T].double().expand(G, -1, -1)
+        vv = v[g:g + 1, :N + T].double().expand(G, -1, -1)
+        ref = F.scaled_dot_product_attention(qq[None], kk[None], vv[None], attn_mask=mask, scale=0.125)[0]
+        np.testing.assert_allclose(o[:, g * G:(g + 1) * G], ref.permute(1, 0, 2).numpy(), atol=1e-10, rtol=0)
+        sc = (torch.einsum("htd,hld->htl", qq, kk) * 0.125).masked_fill(~mask, -math.inf).numpy()
+        np.testing.assert_allclose(lse[:, g * G:(g + 1) * G], scipy.special.logsumexp(sc, axis=-1).T,
+                                   atol=1e-10, rtol=0)
+
+
+def test_ragged_prefix_rejects_out_of_range():
+    q, k, v = W.make_qkv(1, 2, 2, 64, 10, seed=1)
+    with pytest.raises(ValueError):
+        oracle.tree_attn(q, k, v, 10, [-1], 0.125, prefix_len=[3, 11])
+
+
 # ---------------------------------------------------------------- chunk scores
 @pytest.mark.parametrize("N", [1, 63, 64, 65, 300])
 def test_chunk_scores_int64_brute_force(N):
@@ -294,6 +324,39 @@ def test_gather_moves_the_named_chunk():
     _, k, _ = W.make_qkv(1, 1, Hkv, d, N, seed=12)
     kp = oracle.gather(np.array([[3, 1]], dtype=np.int32), k, N, 64, ld_dst=128)
     assert torch.equal(kp[0, :64], k[0, 192:256]) and torch.equal(kp[0, 64:128], k[0, 64:128])
+
+
+@pytest.mark.parametrize("N", [4100, 130, 64 * 9])
+def test_partial_cache_attention_equals_attention_over_the_selected_tokens(N):
+    """A ragged last chunk: the gathered rows [0, part_len[g]) of head g, with the
+    draft batch's own rows after the budget, give the same attention as the
+    selected token positions indexed straight out of the full cache."""
+    Hq, Hkv, d, Td, chunk, kk = 4, 2, 64, 3, 64, 3
+    q, k, v = W.make_qkv(Td, Hq, Hkv, d, N, seed=N, value_kind="normal")
+    nc = (N + chunk - 1) // chunk
+    rng = np.random.default_rng(N)
+    sel = np.stack([np.sort(rng.choice(nc, size=kk, replace=False)) for _ in range(Hkv)]).astype(np.int32)
+    sel[0, -1] = nc - 1   # head 0 always holds the (possibly short) last chunk
+    B = kk * chunk
+    kp, plen = oracle.gather(sel, k, N, chunk, B + Td, return_len=True)
+    vp = oracle.gather(sel, v, N, chunk, B + Td)
+    kp[:, B:] = k[:, N:N + Td]
+    vp[:, B:] = v[:, N:N + Td]
+    parent = [-1] + list(range(Td - 1))
+    o, lse = oracle.tree_attn(q, kp, vp, B, parent, 0.125, prefix_len=plen)
+    G = Hq // Hkv
+    for g in range(Hkv):
+        idx = np.concatenate([np.arange(c * chunk, min((c + 1) * chunk, N)) for c in sel[g]])
+        assert plen[g] == idx.size
+        for t in range(Td):
+            keys = np.concatenate([idx, N + np.arange(t + 1)])
+            kk_ = k[g, keys].double()
+            vv_ = v[g, keys].double()
+            for j in range(G):
+                s_ = 0.125 * (kk_ @ q[t, g * G + j].double())
+                p_ = torch.softmax(s_, 0)
+                np.testing.assert_allclose(o[t, g * G + j], (p_ @ vv_).numpy(), atol=1e-10, rtol=0)
+                assert abs(lse[t, g * G + j] - torch.logsumexp(s_, 0).item()) < 1e-10
 
 
 # ---------------------------------------------------------------- penalty / min-p
