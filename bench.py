@@ -114,6 +114,64 @@ def time_sampled_vocab(step, s, reps: int = 5) -> dict:
     return {"us": us, "gbs": nbytes / us / 1e3, "bytes": nbytes}
 
 
+def time_verify_configs(peaks, s, reps: int = 12) -> dict:
+    """The verify call on every other workload of the pages' evaluation, each on
+    enough layers that consecutive calls read cold HBM: the LLaMA2-7B MHA layer
+    at 102400 tokens (HBM-bound) and the LLaMA3.1-8B layer at 20K-100K
+    (tensor-bound).  One CUDA graph of event-separated calls per workload,
+    rotating over the layers; the first replay uploads the graph, the second is
+    timed."""
+    import long_context_attention_tree_b300 as ts
+    from long_context_attention_tree_b300 import workloads as W
+    out = {}
+    l2 = 126e6
+    todo = [("llama2-7b-100k", W.WORKLOADS["llama2-7b-100k"])]
+    todo += [(f"llama8b-{n // 1024}k", W.WORKLOADS["llama8b-sweep"].with_N(n)) for n in W.SWEEP_N]
+    for name, cfg in todo:
+        n_layers = max(2, math.ceil(3 * l2 / cfg.kv_bytes_per_layer()))
+        layers = [W.make_layer_inputs(cfg, i, device="cuda") for i in range(n_layers)]
+        mask = torch.from_numpy(ts.ts_tree_mask_from_parents(cfg.parents).view(np.int64)).cuda()
+        ws = torch.empty(max(16, ts.ts_tree_attn_workspace_bytes(cfg.T, cfg.Hq, cfg.Hkv, cfg.d, cfg.N)),
+                         dtype=torch.uint8, device="cuda")
+        o = torch.empty((cfg.T, cfg.Hq, cfg.d), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((cfg.T, cfg.Hq), dtype=torch.float32, device="cuda")
+        sc = torch.empty((cfg.Hkv, cfg.n_chunks), dtype=torch.float32, device="cuda")
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(reps + 1)]
+        with torch.cuda.stream(s):
+            for x in layers:  # warm-up outside the graph (kernel attributes)
+                ts.ts_tree_attn(x.q, x.k, x.v, cfg.N, mask, o, lse=lse, chunk_scores=sc, workspace=ws,
+                                scale=cfg.scale, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(reps):
+                x = layers[i % n_layers]
+                evs[i].record(s)
+                ts.ts_tree_attn(x.q, x.k, x.v, cfg.N, mask, o, lse=lse, chunk_scores=sc, workspace=ws,
+                                scale=cfg.scale, stream=s)
+            evs[reps].record(s)
+        with torch.cuda.stream(s):
+            g.replay()
+            g.replay()
+        s.synchronize()
+        us = statistics.mean(evs[i].elapsed_time(evs[i + 1]) for i in range(reps)) * 1e3
+        kv = cfg.kv_bytes_per_layer()
+        flops = 4.0 * cfg.T * cfg.Hq * cfg.N * cfg.d
+        gbs = kv / us / 1e3
+        tf = flops / us / 1e6
+        t_hbm = kv / (peaks["hbm"] * 1e9)
+        t_tc = flops / (peaks["bf16"] * 1e12)
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        out[name] = {"N": cfg.N, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "T": cfg.T, "layers_rotated": n_layers,
+                     "us_per_call": us, "kv_gbs": gbs, "kv_frac_of_hbm": gbs / peaks["hbm"], "tflops": tf,
+                     "bound": bound,
+                     "roofline_frac": (t_hbm if bound == "hbm" else t_tc) / (us * 1e-6),
+                     "tensor_frac_of_burst": tf / peaks["bf16"]}
+        del layers, g
+        torch.cuda.empty_cache()
+    return out
+
+
 def workload_config(name: str):
     from long_context_attention_tree_b300 import workloads as W
     if name == "qwen14b-100k":
@@ -387,8 +445,14 @@ def run_native(args, ws, rank, local):
     kv_layer = cfg.kv_bytes_per_layer()
     tensor_path = ts.ts_tree_attn_uses_tensor_cores(T, Hq, cfg.Hkv, d, N)
     if tensor_path:
-        roof = {"bound": "tensor", "achieved": flops / verify_avg_s / 1e12, "peak": peaks["bf16_sus"],
-                "unit": "TFLOP/s", "peak_source": f"bf16 sustained, {peaks['source']}"}
+        # The verify kernel runs at the full SM clock (about 600 W, far below the
+        # power cap) inside a timed region well under a second, so the burst
+        # cuBLAS peak is its denominator; the sustained figure (measured at a
+        # power-capped ~1155 MHz) is reported beside it.
+        achieved = flops / verify_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "peak_source": f"bf16 burst, {peaks['source']}",
+                "peak_sustained": peaks["bf16_sus"], "frac_of_sustained": achieved / peaks["bf16_sus"]}
     else:
         # CUDA-core fp32 FMA path: 148 SMs x 128 lanes x 2 flop x max SM clock
         alu_peak = 148 * 128 * 2 * peaks["sm_max"] * 1e6 / 1e12
@@ -430,6 +494,11 @@ def run_native(args, ws, rank, local):
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(step, s, args, ws)
 
+    # ---- the verify call on the other workloads (MHA 100K, LLaMA3.1-8B sweep)
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = time_verify_configs(peaks, s)
+
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if ws == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -453,6 +522,7 @@ def run_native(args, ws, rank, local):
             "kv_frac_of_hbm_nominal_8tbs": value / ws / 8000.0,
             "roofline": roof,
             "kernels": kernels,
+            "configs": configs,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -560,6 +630,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="qwen14b-100k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip timing the verify call on the other workloads")
     ap.add_argument("--layers", type=int, default=None, help="run only this many layers (profiling)")
     ap.add_argument("--cpu-row-fraction", type=float, default=1.0,
                     help="fraction of verify rows the CPU oracle baseline computes")

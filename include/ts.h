@@ -12,7 +12,10 @@
  *                            (verify pass over the full cache; draft pass over
  *                            the partial cache), split over the KV length with
  *                            a log-sum-exp merge, optional fused chunk scores;
+ *   ts_tree_attn_partial     the drafting pass over the compact partial cache
+ *                            (per-KV-head count of gathered tokens);
  *   ts_score_chunks          query-key importance of every 64-token KV chunk;
+ *   ts_rescore_tail          the same for the chunks a commit touched only;
  *   ts_select_gather         top-k chunks up to the retrieval budget, gathered
  *                            into a compact partial cache;
  *   ts_penalty_minp_verify   windowed contextual penalty, temperature, min-p,
@@ -90,7 +93,8 @@ size_t ts_tree_attn_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t N);
 
 /*
  * Tree-masked grouped-query attention over a bf16 KV cache: the verify pass
- * ("fed into the LLM with a full KV cache", "How it works") when k/v are the
+ * (TokenSwift tool listing, "How it works": the drafted candidates go through
+ * the target model, which attends over the whole KV cache) when k/v are the
  * full cache, and the self-drafting pass when they are the partial cache.
  *
  * For batch row t and query head h, with g = h / (Hq/Hkv):
@@ -126,6 +130,25 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
                        void *workspace, size_t ws_bytes, ts_stream_t stream);
 
 /*
+ * The self-drafting pass over the compact partial cache that ts_select_gather
+ * wrote (tool listing, "How it works": the target model drafts from a partial
+ * KV cache).  Same as ts_tree_attn over k_part/v_part with N = B, except that
+ * KV head g sees only the prefix rows [0, part_len[g]): when the last chunk of
+ * the full cache is short (N not a multiple of 64) and head g selected it, its
+ * partial cache holds fewer than B real tokens.
+ *   k_part, v_part  bf16 [Hkv][ld_part][d]: rows [0, B) the gathered tokens
+ *            (valid up to part_len[g]), rows [B, B+T) the draft batch's own K/V
+ *   part_len device int32 [Hkv] as ts_select_gather wrote it (values outside
+ *            [0, B] are clamped to it)
+ * No chunk scores.  Other arguments, sizes and errors as for ts_tree_attn;
+ * the workspace size is ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, B).
+ */
+ts_status ts_tree_attn_partial(const void *q, const void *k_part, const void *v_part, int64_t ld_part,
+                               int64_t B, int T, int Hq, int Hkv, int d, float scale,
+                               const uint64_t *mask, const int32_t *part_len, void *out, float *lse,
+                               void *workspace, size_t ws_bytes, ts_stream_t stream);
+
+/*
  * 1 when ts_tree_attn runs these sizes on the tensor cores (tcgen05), 0 when
  * on the CUDA cores (or the sizes are unsupported).  Setting the environment
  * variable TS_FORCE_SIMT=1 before the call forces the CUDA-core kernel.
@@ -143,6 +166,25 @@ int ts_tree_attn_uses_tensor_cores(int T, int Hq, int Hkv, int d, int64_t N);
 ts_status ts_device_error(int clear);
 
 /*
+ * Self-tests of the failure paths, for tests and health checks; neither
+ * faults, traps or hangs the GPU.
+ *
+ * ts_selftest_bounded_wait launches one warp that waits on an mbarrier no
+ * thread ever arrives at, with no copy or MMA in flight.  Its bounded wait
+ * gives up after budget_ns of wall-clock time (0 < budget_ns <= 1e9), records
+ * TS_ERR_TIMEOUT in the sticky status that ts_device_error reads, and the
+ * kernel returns: the path a stalled attention pipeline takes, exercised on
+ * purpose.  The context stays usable.
+ *
+ * ts_selftest_fail_launches(n) makes the next n kernel launches of this
+ * library fail on the host without launching (the launch reports
+ * cudaErrorInvalidValue, the call returns TS_ERR_CUDA); n = 0 turns it off.
+ * Process-wide; not for concurrent use with real work.
+ */
+ts_status ts_selftest_bounded_wait(uint64_t budget_ns, ts_stream_t stream);
+void ts_selftest_fail_launches(int n);
+
+/*
  * Allocation-free ts_tree_attn.  The pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory -- code running
  * inside another runtime's execution callback (an inference-server plugin, a
@@ -155,7 +197,8 @@ ts_status ts_device_error(int clear);
  *   - Sizes whose ts_tree_attn_workspace_bytes exceeds the array return
  *     TS_ERR_UNSUPPORTED.
  *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current); make that first call before any stream capture:
+ *     a first call whose stream is capturing returns TS_ERR_UNSUPPORTED.
  *   - All calls share the array: calls whose kernels overlap on the GPU race
  *     on it; calls ordered on one stream are safe.  Its contents carry over
  *     between calls and nothing in it needs clearing.
@@ -167,8 +210,8 @@ ts_status ts_tree_attn_noalloc(const void *q, const void *k, const void *v, int6
                                float *chunk_scores, int score_row, ts_stream_t stream);
 
 /*
- * Query-key importance of every KV chunk ("a dynamically updated partial KV
- * cache ranked by query-key importance", ICML 2025 summary, "Approach"):
+ * Query-key importance of every KV chunk (ICML 2025 summary, "Approach": the
+ * partial cache keeps the chunks whose keys score highest against the query):
  *   scores[g][c] = max over the query heads h of group g of
  *                  q_row[h] . sum_{t in chunk c, t < N} k[g][t]     (unscaled fp32)
  *   q_row   bf16 [Hq][d]   (the scoring query: one row of the verify batch)
@@ -180,6 +223,26 @@ ts_status ts_score_chunks(const void *q_row, const void *k, int64_t ld_kv, int64
                           int Hq, int Hkv, int d, int chunk, float *scores, ts_stream_t stream);
 
 /*
+ * Incremental re-scoring after a commit (tool listing, "How it works": the KV
+ * cache is updated after each step; ICML 2025 summary, ablation table: the
+ * partial cache is refreshed every step).  The commit appends tokens
+ * [N_old, N_new) to the full cache and leaves rows below N_old untouched, so
+ * the chunks that were complete at N_old keep their scores; only the chunks
+ * from floor(N_old/64) on are scored again.  Afterwards scores_new equals
+ * ts_score_chunks(q_row, k, N_new) exactly.
+ *   scores_old  fp32 [Hkv][ceil(N_old/64)]: the scores of the same q_row over
+ *               the first N_old tokens (e.g. the verify pass's fused scores,
+ *               q_row = its scoring row); may be NULL when N_old < 64
+ *   scores_new  fp32 [Hkv][ceil(N_new/64)]; it may be scores_old itself only
+ *               when both have the same number of chunks, and must not
+ *               otherwise overlap it
+ * Supported: chunk == 64, d in {64, 128}, Hq/Hkv <= 32, 0 <= N_old <= N_new.
+ */
+ts_status ts_rescore_tail(const float *scores_old, int64_t N_old, const void *q_row, const void *k, int64_t ld_kv,
+                          int64_t N_new, int Hq, int Hkv, int d, int chunk, float *scores_new,
+                          ts_stream_t stream);
+
+/*
  * Top-k chunk selection and gather into the compact partial cache
  * (retrieval budget of the model card's command line, 4096 tokens; the
  * partial cache the drafting pass reads, "How it works").
@@ -187,17 +250,26 @@ ts_status ts_score_chunks(const void *q_row, const void *k, int64_t ld_kv, int64
  *   with the largest scores[g][.]; equal scores (-0 equals +0) go to the
  *   lower chunk index; sel[g][0..k) lists them in ascending order.  Then
  *     k_part[g][i*chunk + t] = k[g][sel[g][i]*chunk + t]  (same for v)
- *   for i < k, t < chunk.
+ *   for i < k, t < chunk and sel[g][i]*chunk + t < N: the last chunk of the
+ *   cache holds N - 64*floor(N/64) tokens when N is not a multiple of 64, and
+ *   the rows past them are not written.  That chunk has the largest index, so
+ *   when selected it is the last in the partial cache and the gathered tokens
+ *   of head g are the rows [0, part_len[g]).
+ *   The call takes N rather than the chunk count because the length of the
+ *   last chunk matters.
  *   scores  fp32 [Hkv][ceil(N/chunk)], finite
  *   k, v    bf16 [Hkv][ld_kv][d], ld_kv >= N
  *   sel     int32 [Hkv][k]
+ *   part_len int32 [Hkv] or NULL: tokens gathered for head g (k*chunk, less
+ *           the missing rows of a short last chunk it selected); pass it to
+ *           ts_tree_attn_partial
  *   k_part, v_part  bf16 [Hkv][ld_part][d], ld_part >= k*chunk
  * Supported: chunk == 64, d in {64, 128}, budget_tokens % chunk == 0,
- * N % chunk == 0, ceil(N/chunk) <= 16384.
+ * ceil(N/chunk) <= 16384.
  */
 ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
                            const void *k, const void *v, int64_t ld_kv, int d,
-                           int32_t *sel, void *k_part, void *v_part, int64_t ld_part,
+                           int32_t *sel, int32_t *part_len, void *k_part, void *v_part, int64_t ld_part,
                            ts_stream_t stream);
 
 /*

@@ -25,7 +25,10 @@ _STATUS = {0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_UNSUPPORTED", 3: "TS_
            4: "TS_ERR_TIMEOUT", 5: "TS_ERR_DATA"}
 
 __all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree_attn_workspace_bytes",
-           "ts_launch_count", "ts_tree_attn_uses_tensor_cores", "ts_device_error", "ts_tree_attn", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_select_gather", "ts_penalty_minp_verify"]
+           "ts_launch_count", "ts_tree_attn_uses_tensor_cores", "ts_device_error", "ts_selftest_bounded_wait",
+           "ts_selftest_fail_launches", "ts_tree_attn",
+           "ts_tree_attn_partial", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_rescore_tail",
+           "ts_select_gather", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path"]
 
 
 class TSError(RuntimeError):
@@ -56,19 +59,25 @@ def lib() -> ctypes.CDLL:
         L.ts_tree_attn_uses_tensor_cores.restype = i32
         L.ts_device_error.argtypes = [i32]
         L.ts_device_error.restype = i32
+        L.ts_selftest_bounded_wait.argtypes = [ctypes.c_uint64, P]
+        L.ts_selftest_bounded_wait.restype = i32
+        L.ts_selftest_fail_launches.argtypes = [i32]
+        L.ts_selftest_fail_launches.restype = None
         L.ts_tree_attn.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P, sz, P]
+        L.ts_tree_attn_partial.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, P, sz, P]
         L.ts_tree_attn_noalloc.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P]
         L.ts_score_chunks.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P, P]
-        L.ts_select_gather.argtypes = [P, i32, i64, i32, i32, P, P, i64, i32, P, P, P, i64, P]
+        L.ts_rescore_tail.argtypes = [P, i64, P, P, i64, i64, i32, i32, i32, i32, P, P]
+        L.ts_select_gather.argtypes = [P, i32, i64, i32, i32, P, P, i64, i32, P, P, P, P, i64, P]
         L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
                                              P, P, P, P, P, sz, P]
         L.ts_commit_path.argtypes = [P, P, i64, i64, i32, i32, i32, P, P, P]
         u64 = ctypes.c_uint64
         L.ts_penalty_minp_sample_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, u64, u64, P, P,
                                                     ctypes.c_int32, P, P, P, P, P]
-        for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_noalloc", "ts_score_chunks",
-                     "ts_select_gather", "ts_penalty_minp_verify", "ts_commit_path",
-                     "ts_penalty_minp_sample_verify"):
+        for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_partial", "ts_tree_attn_noalloc",
+                     "ts_score_chunks", "ts_rescore_tail", "ts_select_gather", "ts_penalty_minp_verify",
+                     "ts_commit_path", "ts_penalty_minp_sample_verify"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -127,6 +136,17 @@ def ts_device_error(clear: bool = True) -> int:
     return int(st)
 
 
+def ts_selftest_bounded_wait(budget_ns: int, stream=None) -> None:
+    """One warp whose bounded wait on an mbarrier nobody arrives at gives up
+    after budget_ns and records TS_ERR_TIMEOUT (read it with ts_device_error)."""
+    _check(lib().ts_selftest_bounded_wait(int(budget_ns), _stream(stream)))
+
+
+def ts_selftest_fail_launches(n: int) -> None:
+    """Make the next n kernel launches fail on the host (TS_ERR_CUDA); 0 = off."""
+    lib().ts_selftest_fail_launches(int(n))
+
+
 def ts_tree_attn(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_row: int = 0,
                  workspace=None, scale: Optional[float] = None, stream=None) -> None:
     """Tree-masked GQA attention.  q [T][Hq][d], k/v [Hkv][ld][d] (bf16, CUDA),
@@ -140,6 +160,20 @@ def ts_tree_attn(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_
     _check(lib().ts_tree_attn(_ptr(q), _ptr(k), _ptr(v), ld, N, T, Hq, Hkv, d, scale, _ptr(mask), _ptr(out),
                               _ptr(lse), _ptr(chunk_scores), score_row, _ptr(workspace), ws_bytes,
                               _stream(stream)))
+
+
+def ts_tree_attn_partial(q, k_part, v_part, B: int, mask, part_len, out, lse=None, workspace=None,
+                         scale: Optional[float] = None, stream=None) -> None:
+    """Drafting attention over the compact partial cache: KV head g sees the
+    gathered rows [0, part_len[g]) and the batch rows [B, B+T) by the mask."""
+    T, Hq, d = q.shape
+    Hkv, ld, _ = k_part.shape
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ts_tree_attn_partial(_ptr(q), _ptr(k_part), _ptr(v_part), ld, B, T, Hq, Hkv, d, scale, _ptr(mask),
+                                      _ptr(part_len), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                      _stream(stream)))
 
 
 def ts_tree_attn_noalloc(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_row: int = 0,
@@ -162,12 +196,23 @@ def ts_score_chunks(q_row, k, N: int, scores, chunk: int = 64, stream=None) -> N
     _check(lib().ts_score_chunks(_ptr(q_row), _ptr(k), ld, N, Hq, Hkv, d, chunk, _ptr(scores), _stream(stream)))
 
 
+def ts_rescore_tail(scores_old, N_old: int, q_row, k, N_new: int, scores_new, chunk: int = 64,
+                    stream=None) -> None:
+    """Chunk scores at N_new from the scores at N_old: only the chunks from
+    floor(N_old/64) on are scored again."""
+    Hq, d = q_row.shape
+    Hkv, ld, _ = k.shape
+    _check(lib().ts_rescore_tail(_ptr(scores_old), N_old, _ptr(q_row), _ptr(k), ld, N_new, Hq, Hkv, d, chunk,
+                                 _ptr(scores_new), _stream(stream)))
+
+
 def ts_select_gather(scores, N: int, budget_tokens: int, k, v, sel, k_part, v_part, chunk: int = 64,
-                     stream=None) -> None:
+                     part_len=None, stream=None) -> None:
     Hkv, ld, d = k.shape
     ld_part = k_part.shape[1]
     _check(lib().ts_select_gather(_ptr(scores), Hkv, N, budget_tokens, chunk, _ptr(k), _ptr(v), ld, d,
-                                  _ptr(sel), _ptr(k_part), _ptr(v_part), ld_part, _stream(stream)))
+                                  _ptr(sel), _ptr(part_len), _ptr(k_part), _ptr(v_part), ld_part,
+                                  _stream(stream)))
 
 
 def ts_penalty_minp_verify(logits, history, theta: float, min_p: float, temperature: float, draft, parent,

@@ -90,6 +90,7 @@ tree_attn_simt_kernel(const AttnArgs a) {
     float m_run = -INFINITY, l_run = 0.f;
     const bool score_block = a.chunk_scores != nullptr && a.score_row >= t0 && a.score_row < t0 + a.tpb &&
                              a.score_row < a.T;
+    const int64_t plen = prefix_of(a, g);
 
     // PV ownership
     const int tx = tid & 15, ty = tid >> 4;
@@ -163,7 +164,7 @@ tree_attn_simt_kernel(const AttnArgs a) {
                 bool vis = false;
                 if (srow_valid) {
                     if (tok < a.N) {
-                        vis = true;
+                        vis = tok < plen;
                         raw_sum += s;
                     } else if (tok < L) {
                         vis = mask_bit(a.mask, s_t, (int)(tok - a.N));
@@ -419,11 +420,13 @@ static cudaError_t launch_simt_t(const AttnArgs &a, const SimtPlan &p, cudaStrea
 }
 
 cudaError_t launch_tree_attn_simt(const AttnArgs &a, const SimtPlan &p, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
     if (a.d == 128) return p.rb == 16 ? launch_simt_t<128, 16>(a, p, st) : launch_simt_t<128, 32>(a, p, st);
     return p.rb == 16 ? launch_simt_t<64, 16>(a, p, st) : launch_simt_t<64, 32>(a, p, st);
 }
 
 cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
     const int rows = m.T * m.Hq;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -189,8 +189,9 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
         }
     }
 
-    // ---- visibility: prefix tokens for every row, batch tokens by ancestry
+    // ---- visibility: the head's prefix tokens for every row, batch tokens by ancestry
     const float c = a.scale_log2;
+    const int64_t plen = prefix_of(a, g);
     float m[4], l[4];
 #pragma unroll
     for (int jr = 0; jr < 4; ++jr) {
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             bool vis = in_range[i] && r < R;
-            if (vis && tok[i] >= a.N) vis = mask_bit(a.mask, t, (int)(tok[i] - a.N));
+            if (vis) vis = tok[i] < a.N ? tok[i] < plen : mask_bit(a.mask, t, (int)(tok[i] - a.N));
             s[i][jr] = vis ? s[i][jr] * c : -INFINITY;
             mx = fmaxf(mx, s[i][jr]);
         }
@@ -297,6 +298,7 @@ static cudaError_t launch_small_t(const AttnArgs &a, int splits, cudaStream_t st
 }
 
 cudaError_t launch_tree_attn_small(const AttnArgs &a, int splits, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
     const int r4 = (a.T * a.G + 3) / 4;
     switch (r4) {
         case 1: return launch_small_t<1>(a, splits, st);

@@ -117,16 +117,16 @@ __device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, 
 }
 
 // Softmax helpers on one 32-token chunk of a row of S held in registers.
-// Hide tokens this row may not see: tokens past the prefix are visible only
-// when their batch row is an ancestor-or-self (mask bits), tokens past the
-// batch never.
-__device__ __forceinline__ void mask_chunk(uint32_t (&x)[32], int64_t tok0, int64_t N, int T, uint64_t mk0,
-                                           uint64_t mk1) {
+// Hide tokens this row may not see: prefix tokens at or past the head's
+// prefix length plen (<= N), batch tokens whose row is not an
+// ancestor-or-self (mask bits), tokens past the batch.
+__device__ __forceinline__ void mask_chunk(uint32_t (&x)[32], int64_t tok0, int64_t plen, int64_t N, int T,
+                                           uint64_t mk0, uint64_t mk1) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int64_t tok = tok0 + i;
-        bool vis = tok < N;
-        if (!vis && tok < N + T) {
+        bool vis = tok < plen;
+        if (tok >= N && tok < N + T) {
             const int u = (int)(tok - N);
             vis = ((u < 64 ? (mk0 >> u) : (mk1 >> (u - 64))) & 1ull) != 0;
         }
@@ -438,6 +438,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             const bool is_score_row = score_wm == wm && row_valid && t == a.score_row;
             const bool score_warp = __any_sync(0xffffffffu, is_score_row);
+            const int64_t plen = prefix_of(a, g);
             const uint32_t o_addr = lane_addr + (pair ? 256u + 128u * (uint32_t)wm : 256u);
             const float c = a.scale_log2;
             const float2 c2 = make_float2(c, c);
@@ -487,11 +488,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
 
                 // ---- tiles that reach past the prefix: hide what this row may not see
-                if (tok0 + KV_TILE > a.N) {
-                    mask_chunk(x0, tok0 + 0, a.N, a.T, mk0, mk1);
-                    mask_chunk(x1, tok0 + 32, a.N, a.T, mk0, mk1);
-                    mask_chunk(x2, tok0 + 64, a.N, a.T, mk0, mk1);
-                    mask_chunk(x3, tok0 + 96, a.N, a.T, mk0, mk1);
+                if (tok0 + KV_TILE > plen) {
+                    mask_chunk(x0, tok0 + 0, plen, a.N, a.T, mk0, mk1);
+                    mask_chunk(x1, tok0 + 32, plen, a.N, a.T, mk0, mk1);
+                    mask_chunk(x2, tok0 + 64, plen, a.N, a.T, mk0, mk1);
+                    mask_chunk(x3, tok0 + 96, plen, a.N, a.T, mk0, mk1);
                 }
 
                 // ---- row max (raw units), lazy running-max update
@@ -680,6 +681,7 @@ TcPlan tc_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms) {
 
 cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtensorMap &tq, const CUtensorMap &tk,
                                 const CUtensorMap &tv, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)TC_SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -696,6 +698,29 @@ cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtens
     L.direct = p.splits == 1 ? 1 : 0;
     dim3 grid(p.ctas_per_head * a.Hkv);
     tree_attn_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(tq, tk, tv, a, L);
+    return cudaGetLastError();
+}
+
+// Self-test of the bounded-wait failure path: one warp waits on an mbarrier
+// that no thread arrives at (no copy or MMA is in flight), gives up after
+// budget_ns, records TS_ERR_TIMEOUT in the sticky status word and returns --
+// the same path a stalled pipeline takes in the kernels above.
+__global__ void __launch_bounds__(32) bounded_wait_selftest_kernel(uint64_t budget_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !tc::mbar_wait_for(&bar, 0, &abort_flag, budget_ns))
+        atomicExch(&g_device_error, (int)TS_ERR_TIMEOUT);
+}
+
+cudaError_t launch_bounded_wait_selftest(uint64_t budget_ns, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
+    bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(budget_ns);
     return cudaGetLastError();
 }
 

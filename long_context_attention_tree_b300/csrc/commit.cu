@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(CM_THREADS) commit_path_kernel(__nv_bfloat16 *
 
 cudaError_t launch_commit_path(__nv_bfloat16 *k, __nv_bfloat16 *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d,
                                int32_t *result, const int32_t *path, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
     const size_t smem = (size_t)T * d * 2;  // at most T rows staged
     cudaError_t e = cudaFuncSetAttribute(commit_path_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

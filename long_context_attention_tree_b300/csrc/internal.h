@@ -17,6 +17,11 @@ void note_launches(int n);
 // Records `msg` as this host thread's last error message and returns `st`.
 ts_status report_error(ts_status st, const char *msg);
 
+// Host-side fault injection for tests (ts_selftest_fail_launches): true when
+// the launch about to be made should report cudaErrorInvalidValue instead of
+// launching.  Every launch_* function asks before it launches.
+bool injected_launch_failure();
+
 struct AttnArgs {
     const __nv_bfloat16 *q;
     const __nv_bfloat16 *k;
@@ -26,6 +31,7 @@ struct AttnArgs {
     int T, Hq, Hkv, G, d;
     float scale_log2;  // softmax scale * log2(e)
     const uint64_t *mask;
+    const int32_t *prefix_len;  // nullable: KV head g sees prefix rows [0, min(prefix_len[g], N))
     __nv_bfloat16 *out;
     float *lse;
     float *chunk_scores;  // nullable
@@ -84,14 +90,28 @@ cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtens
                                 const CUtensorMap &tv, cudaStream_t st);
 // sticky device-side error word (TS_ERR_TIMEOUT when a bounded wait gave up)
 cudaError_t read_device_error(int *value, bool clear);
+// one warp whose bounded wait on an mbarrier nobody arrives at gives up
+cudaError_t launch_bounded_wait_selftest(uint64_t budget_ns, cudaStream_t st);
+
+// Visible prefix length of KV head g (ragged partial caches clamp to [0, N]).
+__device__ __forceinline__ int64_t prefix_of(const AttnArgs &a, int g) {
+    if (a.prefix_len == nullptr) return a.N;
+    const int64_t p = a.prefix_len[g];
+    return p < 0 ? 0 : (p > a.N ? a.N : p);
+}
 
 // chunk scoring / selection / gather
+// scores[g * ld_scores + c] for the chunks c in [c_begin, ceil(N / 64))
 cudaError_t launch_score_chunks(const __nv_bfloat16 *q_row, const __nv_bfloat16 *k, int64_t ld_kv, int64_t N,
-                                int Hq, int Hkv, int d, float *scores, cudaStream_t st);
-cudaError_t launch_select_gather(const float *scores, int Hkv, int n_chunks, int k_sel,
+                                int Hq, int Hkv, int d, float *scores, int64_t ld_scores, int c_begin,
+                                cudaStream_t st);
+// scores_new[g][c] = scores_old[g][c] for c < c_keep (row strides nc_new / nc_old)
+cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *scores_new, int nc_new, int c_keep,
+                               int Hkv, cudaStream_t st);
+cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel,
                                  const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
-                                 int32_t *sel, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part, int64_t ld_part,
-                                 int num_sms, cudaStream_t st);
+                                 int32_t *sel, int32_t *part_len, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part,
+                                 int64_t ld_part, int num_sms, cudaStream_t st);
 
 // vocab stage
 struct VocabArgs {

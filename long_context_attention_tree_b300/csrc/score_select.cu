@@ -1,7 +1,8 @@
 // Dynamic partial-KV-cache maintenance: chunk importance, top-k selection up
 // to the retrieval budget, and the gather into the compact partial cache
-// (TokenSwift ICML 2025 summary, "Approach": "a dynamically updated partial KV
-// cache ranked by query-key importance"; model card: retrieval budget 4096).
+// (TokenSwift ICML 2025 summary, "Approach": the drafting pass reads a partial
+// KV cache that is refreshed every step from the chunks whose keys score
+// highest against the current query; model card: retrieval budget 4096).
 #include "internal.h"
 #include "ts_common.cuh"
 
@@ -17,7 +18,8 @@ constexpr int CHUNK = 64;
 template <int D>
 __global__ void __launch_bounds__(128)
 score_chunks_kernel(const __nv_bfloat16 *__restrict__ q_row, const __nv_bfloat16 *__restrict__ k,
-                    int64_t ld_kv, int64_t N, int Hq, int G, int n_chunks, int cpb, float *__restrict__ scores) {
+                    int64_t ld_kv, int64_t N, int Hq, int G, int n_chunks, int c_begin, int cpb,
+                    float *__restrict__ scores, int64_t ld_scores) {
     constexpr int LPR = D / 8;             // 16-byte lanes per row
     constexpr int RIF = 128 / LPR;         // rows in flight
     __shared__ float part[RIF][D];
@@ -28,7 +30,7 @@ score_chunks_kernel(const __nv_bfloat16 *__restrict__ q_row, const __nv_bfloat16
     const int lane16 = tid % LPR, rr = tid / LPR;
     const __nv_bfloat16 *kh = k + (size_t)g * ld_kv * D;
     for (int cc = 0; cc < cpb; ++cc) {
-        const int c = blockIdx.x * cpb + cc;
+        const int c = c_begin + blockIdx.x * cpb + cc;
         if (c >= n_chunks) break;
         const int64_t t0 = (int64_t)c * CHUNK;
         const int64_t t1 = (t0 + CHUNK < N) ? t0 + CHUNK : N;
@@ -61,23 +63,44 @@ score_chunks_kernel(const __nv_bfloat16 *__restrict__ q_row, const __nv_bfloat16
         if (tid == 0) {
             float best = hmax[0];
             for (int j = 1; j < G; ++j) best = fmaxf(best, hmax[j]);
-            scores[(size_t)g * n_chunks + c] = best;
+            scores[(size_t)g * ld_scores + c] = best;
         }
         __syncthreads();
     }
 }
 
 cudaError_t launch_score_chunks(const __nv_bfloat16 *q_row, const __nv_bfloat16 *k, int64_t ld_kv, int64_t N,
-                                int Hq, int Hkv, int d, float *scores, cudaStream_t st) {
+                                int Hq, int Hkv, int d, float *scores, int64_t ld_scores, int c_begin,
+                                cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
     const int nc = (int)((N + CHUNK - 1) / CHUNK);
-    if (nc == 0) return cudaSuccess;
+    if (nc - c_begin <= 0) return cudaSuccess;
     const int cpb = 4;
-    dim3 grid((nc + cpb - 1) / cpb, Hkv);
+    dim3 grid((nc - c_begin + cpb - 1) / cpb, Hkv);
     const int G = Hq / Hkv;
     if (d == 128)
-        score_chunks_kernel<128><<<grid, 128, 0, st>>>(q_row, k, ld_kv, N, Hq, G, nc, cpb, scores);
+        score_chunks_kernel<128><<<grid, 128, 0, st>>>(q_row, k, ld_kv, N, Hq, G, nc, c_begin, cpb, scores,
+                                                       ld_scores);
     else
-        score_chunks_kernel<64><<<grid, 128, 0, st>>>(q_row, k, ld_kv, N, Hq, G, nc, cpb, scores);
+        score_chunks_kernel<64><<<grid, 128, 0, st>>>(q_row, k, ld_kv, N, Hq, G, nc, c_begin, cpb, scores,
+                                                      ld_scores);
+    return cudaGetLastError();
+}
+
+// Scores of the chunks a commit did not touch carry over unchanged.
+__global__ void __launch_bounds__(256) copy_scores_kernel(const float *__restrict__ old_s, int nc_old,
+                                                          float *__restrict__ new_s, int nc_new, int c_keep) {
+    const int g = blockIdx.y;
+    for (int c = blockIdx.x * 256 + threadIdx.x; c < c_keep; c += gridDim.x * 256)
+        new_s[(size_t)g * nc_new + c] = old_s[(size_t)g * nc_old + c];
+}
+
+cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *scores_new, int nc_new, int c_keep,
+                               int Hkv, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
+    if (c_keep <= 0) return cudaSuccess;
+    dim3 grid((c_keep + 255) / 256, Hkv);
+    copy_scores_kernel<<<grid, 256, 0, st>>>(scores_old, nc_old, scores_new, nc_new, c_keep);
     return cudaGetLastError();
 }
 
@@ -126,9 +149,9 @@ __device__ int block_exclusive_scan(int x, int *warp_tot, int *total) {
 
 template <int D>
 __global__ void __launch_bounds__(SG_THREADS)
-select_gather_kernel(const float *__restrict__ scores, int n_chunks, int k_sel,
+select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel,
                      const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v, int64_t ld_kv,
-                     int32_t *__restrict__ sel, __nv_bfloat16 *__restrict__ k_part,
+                     int32_t *__restrict__ sel, int32_t *__restrict__ part_len, __nv_bfloat16 *__restrict__ k_part,
                      __nv_bfloat16 *__restrict__ v_part, int64_t ld_part, int chunks_per_part) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw);          // [n_chunks]
@@ -234,9 +257,16 @@ select_gather_kernel(const float *__restrict__ scores, int n_chunks, int k_sel,
         }
     }
     __syncthreads();
+    // tokens gathered for this head: only the last chunk of the prefix can be
+    // short, and being the largest index it is the last one selected
+    if (p == 0 && tid == 0 && part_len != nullptr) {
+        const int64_t tail = N - (int64_t)(n_chunks - 1) * CHUNK;  // tokens of the last chunk, 1..64
+        part_len[g] = k_sel * CHUNK - (list[k_sel - 1] == n_chunks - 1 ? (int)(CHUNK - tail) : 0);
+    }
 
     // --- gather this part's chunks, K and V: every load of a pair of chunks is
-    // issued before the first store, so each thread keeps 8 x 16 bytes in flight
+    // issued before the first store, so each thread keeps 8 x 16 bytes in flight;
+    // rows of the last chunk at or past N are neither read nor written
     constexpr int U = D / 8;                     // 16-byte units per row
     constexpr int PER = CHUNK * U / SG_THREADS;  // units per thread per chunk (2 for D = 128)
     static_assert(CHUNK * U % SG_THREADS == 0, "chunk must split evenly over the threads");
@@ -248,16 +278,22 @@ select_gather_kernel(const float *__restrict__ scores, int n_chunks, int k_sel,
     for (int i = i0; i < i1; i += 2) {
         const int nb = min(2, i1 - i);
         uint4 wk[2][PER], wv[2][PER];
+        int rows_of[2];
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
+            rows_of[b] = 0;
             if (b < nb) {
                 const int c = min(max(list[i + b], 0), n_chunks - 1);
+                const int64_t left = N - (int64_t)c * CHUNK;
+                rows_of[b] = left < CHUNK ? (int)left : CHUNK;
                 const size_t src_row = (size_t)c * CHUNK;
 #pragma unroll
                 for (int q = 0; q < PER; ++q) {
                     const int e = tid + q * SG_THREADS, r = e / U, u = e % U;
-                    wk[b][q] = *reinterpret_cast<const uint4 *>(kh + (src_row + r) * D + u * 8);
-                    wv[b][q] = *reinterpret_cast<const uint4 *>(vh + (src_row + r) * D + u * 8);
+                    if (r < rows_of[b]) {
+                        wk[b][q] = *reinterpret_cast<const uint4 *>(kh + (src_row + r) * D + u * 8);
+                        wv[b][q] = *reinterpret_cast<const uint4 *>(vh + (src_row + r) * D + u * 8);
+                    }
                 }
             }
         }
@@ -268,18 +304,21 @@ select_gather_kernel(const float *__restrict__ scores, int n_chunks, int k_sel,
 #pragma unroll
                 for (int q = 0; q < PER; ++q) {
                     const int e = tid + q * SG_THREADS, r = e / U, u = e % U;
-                    *reinterpret_cast<uint4 *>(kp + (dst_row + r) * D + u * 8) = wk[b][q];
-                    *reinterpret_cast<uint4 *>(vp + (dst_row + r) * D + u * 8) = wv[b][q];
+                    if (r < rows_of[b]) {
+                        *reinterpret_cast<uint4 *>(kp + (dst_row + r) * D + u * 8) = wk[b][q];
+                        *reinterpret_cast<uint4 *>(vp + (dst_row + r) * D + u * 8) = wv[b][q];
+                    }
                 }
             }
         }
     }
 }
 
-cudaError_t launch_select_gather(const float *scores, int Hkv, int n_chunks, int k_sel,
+cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel,
                                  const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
-                                 int32_t *sel, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part, int64_t ld_part,
-                                 int num_sms, cudaStream_t st) {
+                                 int32_t *sel, int32_t *part_len, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part,
+                                 int64_t ld_part, int num_sms, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
     if (k_sel <= 0 || n_chunks <= 0) return cudaSuccess;
     int parts = (2 * num_sms + Hkv - 1) / Hkv;
     if (parts > k_sel) parts = k_sel;
@@ -292,13 +331,13 @@ cudaError_t launch_select_gather(const float *scores, int Hkv, int n_chunks, int
     if (d == 128) {
         e = cudaFuncSetAttribute(select_gather_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        select_gather_kernel<128><<<grid, SG_THREADS, smem, st>>>(scores, n_chunks, k_sel, k, v, ld_kv, sel,
-                                                                  k_part, v_part, ld_part, cpp);
+        select_gather_kernel<128><<<grid, SG_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, k, v, ld_kv, sel,
+                                                                  part_len, k_part, v_part, ld_part, cpp);
     } else {
         e = cudaFuncSetAttribute(select_gather_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        select_gather_kernel<64><<<grid, SG_THREADS, smem, st>>>(scores, n_chunks, k_sel, k, v, ld_kv, sel,
-                                                                 k_part, v_part, ld_part, cpp);
+        select_gather_kernel<64><<<grid, SG_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, k, v, ld_kv, sel,
+                                                                 part_len, k_part, v_part, ld_part, cpp);
     }
     return cudaGetLastError();
 }

@@ -48,17 +48,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Returns false when
-// the budget ran out or *abort became non-zero (then the caller winds down).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+// `budget_ns` of wall-clock time ran out or *abort became non-zero (then the
+// caller winds down).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                              uint64_t budget_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (abort != nullptr && *abort) return false;
-            if (globaltimer() - t0 > WAIT_BUDGET_NS) return false;
+            if (globaltimer() - t0 > budget_ns) return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return mbar_wait_for(bar, parity, abort, WAIT_BUDGET_NS);
 }
 
 // ---------------------------------------------------------------- TMA

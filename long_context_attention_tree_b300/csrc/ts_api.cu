@@ -21,6 +21,7 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_inject_failures{0};  // launches still to fail (ts_selftest_fail_launches)
 
 ts_status fail(ts_status st, const char *fmt, ...) {
     char buf[512];
@@ -141,6 +142,12 @@ ts_status check_attn_shape(int T, int Hq, int Hkv, int d, int64_t N) {
 
 namespace ts {
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+bool injected_launch_failure() {
+    int n = g_inject_failures.load(std::memory_order_relaxed);
+    while (n > 0)
+        if (g_inject_failures.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) return true;
+    return false;
+}
 ts_status report_error(ts_status st, const char *msg) { return fail(st, "%s", msg ? msg : "error"); }
 }  // namespace ts
 
@@ -187,24 +194,38 @@ ts_status ts_device_error(int clear) {
     return TS_OK;
 }
 
+ts_status ts_selftest_bounded_wait(uint64_t budget_ns, ts_stream_t stream) {
+    if (budget_ns == 0 || budget_ns > 1000000000ull)
+        return fail(TS_ERR_INVALID_ARG, "budget_ns=%llu outside (0, 1e9]", (unsigned long long)budget_ns);
+    cudaError_t e = ts::launch_bounded_wait_selftest(budget_ns, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "bounded_wait_selftest launch");
+    ts::note_launches(1);
+    return TS_OK;
+}
+
+void ts_selftest_fail_launches(int n) { g_inject_failures.store(n > 0 ? n : 0, std::memory_order_relaxed); }
+
 int ts_tree_attn_uses_tensor_cores(int T, int Hq, int Hkv, int d, int64_t N) {
     if (check_attn_shape(T, Hq, Hkv, d, N) != TS_OK || T == 0) return 0;
     return plan_attention(T, Hq, Hkv, d, N).tc ? 1 : 0;
 }
 
-ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_kv,
-                       int64_t N, int T, int Hq, int Hkv, int d, float scale,
-                       const uint64_t *mask, void *out, float *lse,
-                       float *chunk_scores, int score_row,
-                       void *workspace, size_t ws_bytes, ts_stream_t stream) {
+}  // extern "C"
+
+// Shared body of ts_tree_attn and ts_tree_attn_partial.
+static ts_status tree_attn_impl(const void *q, const void *k, const void *v, int64_t ld_kv, int64_t N, int T,
+                                int Hq, int Hkv, int d, float scale, const uint64_t *mask,
+                                const int32_t *prefix_len, void *out, float *lse, float *chunk_scores,
+                                int score_row, void *workspace, size_t ws_bytes, ts_stream_t stream) {
     ts_status st = check_attn_shape(T, Hq, Hkv, d, N);
     if (st != TS_OK) return st;
     if (T == 0) return TS_OK;
     if (!q || !k || !v || !mask || !out) return fail(TS_ERR_INVALID_ARG, "null q/k/v/mask/out");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(TS_ERR_INVALID_ARG, "q/k/v/out must be 16-byte aligned");
-    if (!aligned4(mask) || (lse && !aligned4(lse)) || (chunk_scores && !aligned4(chunk_scores)))
-        return fail(TS_ERR_INVALID_ARG, "mask/lse/chunk_scores misaligned");
+    if (!aligned4(mask) || (lse && !aligned4(lse)) || (chunk_scores && !aligned4(chunk_scores)) ||
+        (prefix_len && !aligned4(prefix_len)))
+        return fail(TS_ERR_INVALID_ARG, "mask/lse/chunk_scores/prefix_len misaligned");
     if (ld_kv < N + T) return fail(TS_ERR_INVALID_ARG, "ld_kv=%lld < N+T=%lld", (long long)ld_kv, (long long)(N + T));
     if (!(scale > 0.f) || !isfinite(scale)) return fail(TS_ERR_INVALID_ARG, "scale must be finite and > 0");
     if (chunk_scores && (score_row < 0 || score_row >= T))
@@ -229,6 +250,7 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
     a.d = d;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.mask = mask;
+    a.prefix_len = prefix_len;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
     a.chunk_scores = chunk_scores;
@@ -279,6 +301,26 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
     return TS_OK;
 }
 
+extern "C" {
+
+ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_kv,
+                       int64_t N, int T, int Hq, int Hkv, int d, float scale,
+                       const uint64_t *mask, void *out, float *lse,
+                       float *chunk_scores, int score_row,
+                       void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    return tree_attn_impl(q, k, v, ld_kv, N, T, Hq, Hkv, d, scale, mask, nullptr, out, lse, chunk_scores, score_row,
+                          workspace, ws_bytes, stream);
+}
+
+ts_status ts_tree_attn_partial(const void *q, const void *k_part, const void *v_part, int64_t ld_part,
+                               int64_t B, int T, int Hq, int Hkv, int d, float scale,
+                               const uint64_t *mask, const int32_t *part_len, void *out, float *lse,
+                               void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    if (T > 0 && part_len == nullptr) return fail(TS_ERR_INVALID_ARG, "null part_len");
+    return tree_attn_impl(q, k_part, v_part, ld_part, B, T, Hq, Hkv, d, scale, mask, part_len, out, lse, nullptr,
+                          0, workspace, ws_bytes, stream);
+}
+
 ts_status ts_score_chunks(const void *q_row, const void *k, int64_t ld_kv, int64_t N,
                           int Hq, int Hkv, int d, int chunk, float *scores, ts_stream_t stream) {
     if (chunk != 64) return fail(TS_ERR_UNSUPPORTED, "chunk=%d (supported: 64)", chunk);
@@ -291,35 +333,73 @@ ts_status ts_score_chunks(const void *q_row, const void *k, int64_t ld_kv, int64
     if (ld_kv < N) return fail(TS_ERR_INVALID_ARG, "ld_kv < N");
     cudaError_t e = ts::launch_score_chunks(static_cast<const __nv_bfloat16 *>(q_row),
                                             static_cast<const __nv_bfloat16 *>(k), ld_kv, N, Hq, Hkv, d, scores,
-                                            reinterpret_cast<cudaStream_t>(stream));
+                                            (N + 63) / 64, 0, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "score_chunks launch");
     ts::note_launches(1);
     return TS_OK;
 }
 
+ts_status ts_rescore_tail(const float *scores_old, int64_t N_old, const void *q_row, const void *k, int64_t ld_kv,
+                          int64_t N_new, int Hq, int Hkv, int d, int chunk, float *scores_new,
+                          ts_stream_t stream) {
+    if (chunk != 64) return fail(TS_ERR_UNSUPPORTED, "chunk=%d (supported: 64)", chunk);
+    ts_status st = check_attn_shape(1, Hq, Hkv, d, N_new);
+    if (st != TS_OK) return st;
+    if (N_old < 0 || N_old > N_new) return fail(TS_ERR_INVALID_ARG, "need 0 <= N_old <= N_new");
+    if (N_new == 0) return TS_OK;
+    if (!q_row || !k || !scores_new || (N_old > 0 && !scores_old))
+        return fail(TS_ERR_INVALID_ARG, "null q_row/k/scores");
+    if (!aligned16(q_row) || !aligned16(k) || !aligned4(scores_new) || (scores_old && !aligned4(scores_old)))
+        return fail(TS_ERR_INVALID_ARG, "q_row/k must be 16-byte aligned, scores 4-byte aligned");
+    if (ld_kv < N_new) return fail(TS_ERR_INVALID_ARG, "ld_kv < N_new");
+    const int nc_old = (int)((N_old + 63) / 64), nc_new = (int)((N_new + 63) / 64);
+    const int c_keep = (int)(N_old / 64);  // chunks that were complete before the new tokens
+    const bool in_place = scores_old == scores_new;
+    if (in_place && nc_old != nc_new)
+        return fail(TS_ERR_INVALID_ARG, "in-place rescoring needs ceil(N_old/64) == ceil(N_new/64)");
+    if (!in_place && N_old > 0) {
+        const uintptr_t a0 = (uintptr_t)scores_old, a1 = a0 + sizeof(float) * (size_t)Hkv * nc_old;
+        const uintptr_t b0 = (uintptr_t)scores_new, b1 = b0 + sizeof(float) * (size_t)Hkv * nc_new;
+        if (a0 < b1 && b0 < a1) return fail(TS_ERR_INVALID_ARG, "scores_old and scores_new overlap");
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (!in_place && c_keep > 0) {
+        e = ts::launch_copy_scores(scores_old, nc_old, scores_new, nc_new, c_keep, Hkv, s);
+        if (e != cudaSuccess) return cuda_fail(e, "copy_scores launch");
+        ts::note_launches(1);
+    }
+    if (c_keep < nc_new) {
+        e = ts::launch_score_chunks(static_cast<const __nv_bfloat16 *>(q_row), static_cast<const __nv_bfloat16 *>(k),
+                                    ld_kv, N_new, Hq, Hkv, d, scores_new, nc_new, c_keep, s);
+        if (e != cudaSuccess) return cuda_fail(e, "score_chunks launch");
+        ts::note_launches(1);
+    }
+    return TS_OK;
+}
+
 ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
                            const void *k, const void *v, int64_t ld_kv, int d,
-                           int32_t *sel, void *k_part, void *v_part, int64_t ld_part,
+                           int32_t *sel, int32_t *part_len, void *k_part, void *v_part, int64_t ld_part,
                            ts_stream_t stream) {
     if (chunk != 64) return fail(TS_ERR_UNSUPPORTED, "chunk=%d (supported: 64)", chunk);
     if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
     if (Hkv <= 0) return fail(TS_ERR_INVALID_ARG, "Hkv=%d", Hkv);
     if (N < 0 || budget_tokens < 0) return fail(TS_ERR_INVALID_ARG, "negative N or budget");
     if (budget_tokens % chunk) return fail(TS_ERR_INVALID_ARG, "budget %d not a multiple of chunk", budget_tokens);
-    if (N % chunk) return fail(TS_ERR_UNSUPPORTED, "N=%lld not a multiple of the chunk", (long long)N);
-    const int64_t nc = N / chunk;
+    const int64_t nc = (N + chunk - 1) / chunk;
     if (nc > 16384) return fail(TS_ERR_UNSUPPORTED, "%lld chunks > 16384", (long long)nc);
     const int k_sel = (int)((int64_t)(budget_tokens / chunk) < nc ? budget_tokens / chunk : nc);
     if (k_sel == 0) return TS_OK;
     if (!scores || !k || !v || !sel || !k_part || !v_part) return fail(TS_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_part) || !aligned16(v_part) || !aligned4(scores) ||
-        !aligned4(sel))
+        !aligned4(sel) || (part_len && !aligned4(part_len)))
         return fail(TS_ERR_INVALID_ARG, "misaligned pointer");
     if (ld_kv < N) return fail(TS_ERR_INVALID_ARG, "ld_kv < N");
     if (ld_part < (int64_t)k_sel * chunk)
         return fail(TS_ERR_INVALID_ARG, "ld_part=%lld < k*chunk=%lld", (long long)ld_part, (long long)k_sel * chunk);
-    cudaError_t e = ts::launch_select_gather(scores, Hkv, (int)nc, k_sel, static_cast<const __nv_bfloat16 *>(k),
-                                             static_cast<const __nv_bfloat16 *>(v), ld_kv, d, sel,
+    cudaError_t e = ts::launch_select_gather(scores, Hkv, N, (int)nc, k_sel, static_cast<const __nv_bfloat16 *>(k),
+                                             static_cast<const __nv_bfloat16 *>(v), ld_kv, d, sel, part_len,
                                              static_cast<__nv_bfloat16 *>(k_part),
                                              static_cast<__nv_bfloat16 *>(v_part), ld_part, num_sms(),
                                              reinterpret_cast<cudaStream_t>(stream));

@@ -24,26 +24,48 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TS_NOALLOC_SCRATCH_BYTES];
 
+constexpr int MAX_DEVICES = 64;
+
 // Device address of g_noalloc_scratch for each device, looked up once with
 // that device current.  In host code the array's name is only a host-side
-// stand-in, so the address must come from cudaGetSymbolAddress.
-void *scratch_for_current_device(ts_status *st, const char **why) {
+// stand-in, so the address must come from cudaGetSymbolAddress.  The lookup
+// may load the module on the device, which must not happen inside a stream
+// capture: a first call whose stream is capturing is refused.
+void *scratch_for_current_device(cudaStream_t stream, ts_status *st, const char **why) {
     static std::mutex mu;
-    static void *addr[64] = {nullptr};
+    static void *addr[MAX_DEVICES] = {nullptr};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    if (e != cudaSuccess) {
         *st = TS_ERR_CUDA;
-        *why = "cudaGetDevice failed";
+        *why = "ts_tree_attn_noalloc: cudaGetDevice failed";
+        return nullptr;
+    }
+    if (dev < 0 || dev >= MAX_DEVICES) {
+        *st = TS_ERR_UNSUPPORTED;
+        *why = "ts_tree_attn_noalloc: device index outside the 64 devices this entry point tracks";
         return nullptr;
     }
     std::lock_guard<std::mutex> lk(mu);
     if (addr[dev] == nullptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            cudaGetLastError();
+            *st = TS_ERR_UNSUPPORTED;
+            *why = "ts_tree_attn_noalloc: the first call on a device sets up its scratch address and must come "
+                   "before any stream capture";
+            return nullptr;
+        }
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
+        if (e != cudaSuccess) {
             *st = TS_ERR_CUDA;
             *why = cudaGetErrorString(e);
+            return nullptr;
+        }
+        if (p == nullptr) {
+            *st = TS_ERR_CUDA;
+            *why = "ts_tree_attn_noalloc: the scratch array has no device address";
             return nullptr;
         }
         addr[dev] = p;
@@ -69,7 +91,7 @@ extern "C" ts_status ts_tree_attn_noalloc(const void *q, const void *k, const vo
     if (need > 0) {
         ts_status st = TS_OK;
         const char *why = nullptr;
-        scratch = scratch_for_current_device(&st, &why);
+        scratch = scratch_for_current_device(reinterpret_cast<cudaStream_t>(stream), &st, &why);
         if (scratch == nullptr) return ts::report_error(st, why);
     }
     return ts_tree_attn(q, k, v, ld_kv, N, T, Hq, Hkv, d, scale, mask, out, lse, chunk_scores, score_row,

@@ -270,6 +270,7 @@ __global__ void __launch_bounds__(1024) accept_kernel(const VocabArgs a) {
 }
 
 cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
     int slice = (a.V + VOCAB_CLUSTER - 1) / VOCAB_CLUSTER;
     slice = (slice + 31) & ~31;
     if (slice > VOCAB_MAX_SLICE) return cudaErrorInvalidValue;

@@ -24,8 +24,8 @@ from typing import List, Optional
 import numpy as np
 import torch
 
-from . import (ts_penalty_minp_verify, ts_select_gather, ts_tree_attn, ts_tree_attn_workspace_bytes,
-               ts_tree_mask_from_parents)
+from . import (ts_penalty_minp_verify, ts_select_gather, ts_tree_attn, ts_tree_attn_partial,
+               ts_tree_attn_workspace_bytes, ts_tree_mask_from_parents)
 from . import workloads as W
 
 
@@ -41,6 +41,7 @@ class LayerBuffers:
     lse: torch.Tensor
     scores: torch.Tensor
     sel: torch.Tensor
+    part_len: torch.Tensor
     out_draft: torch.Tensor
     lse_draft: torch.Tensor
 
@@ -78,6 +79,7 @@ class SpecStep:
                 lse=torch.empty((self.T, cfg.Hq), dtype=torch.float32, device=self.device),
                 scores=torch.empty((cfg.Hkv, nc), dtype=torch.float32, device=self.device),
                 sel=torch.empty((cfg.Hkv, self.k_sel), dtype=torch.int32, device=self.device),
+                part_len=torch.empty((cfg.Hkv,), dtype=torch.int32, device=self.device),
                 out_draft=torch.empty((self.Td, cfg.Hq, cfg.d), dtype=torch.bfloat16, device=self.device),
                 lse_draft=torch.empty((self.Td, cfg.Hq), dtype=torch.float32, device=self.device),
             ))
@@ -100,12 +102,12 @@ class SpecStep:
     def run_refresh(self, i: int, stream=None) -> None:
         cfg, L = self.cfg, self.layers[i]
         ts_select_gather(L.scores, cfg.N, cfg.budget, L.k, L.v, L.sel, L.k_part, L.v_part, chunk=cfg.chunk,
-                         stream=stream)
+                         part_len=L.part_len, stream=stream)
 
     def run_draft(self, i: int, stream=None) -> None:
         cfg, L = self.cfg, self.layers[i]
-        ts_tree_attn(L.q_draft, L.k_part, L.v_part, self.B, self.mask_draft, L.out_draft, lse=L.lse_draft,
-                     workspace=self.workspace, scale=cfg.scale, stream=stream)
+        ts_tree_attn_partial(L.q_draft, L.k_part, L.v_part, self.B, self.mask_draft, L.part_len, L.out_draft,
+                             lse=L.lse_draft, workspace=self.workspace, scale=cfg.scale, stream=stream)
 
     def run_layer(self, i: int, stream=None) -> None:
         self.run_verify(i, stream)

@@ -111,14 +111,42 @@ def test_workspace_size_is_consistent():
 def test_select_gather_rejects():
     L = ts.lib()
     P = 0x10000
-    # N not a multiple of the chunk
-    assert L.ts_select_gather(P, 8, 4100, 4096, 64, P, P, 5000, 128, P, P, P, 4096, None) == ts.TS_ERR_UNSUPPORTED
     # budget not a multiple of the chunk
-    assert L.ts_select_gather(P, 8, 4096, 100, 64, P, P, 5000, 128, P, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_gather(P, 8, 4096, 100, 64, P, P, 5000, 128, P, None, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
     # partial cache too short
-    assert L.ts_select_gather(P, 8, 8192, 4096, 64, P, P, 8192, 128, P, P, P, 4000, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_gather(P, 8, 8192, 4096, 64, P, P, 8192, 128, P, None, P, P, 4000, None) == ts.TS_ERR_INVALID_ARG
     # chunk other than 64
-    assert L.ts_select_gather(P, 8, 8192, 4096, 32, P, P, 8192, 128, P, P, P, 4096, None) == ts.TS_ERR_UNSUPPORTED
+    assert L.ts_select_gather(P, 8, 8192, 4096, 32, P, P, 8192, 128, P, None, P, P, 4096, None) == ts.TS_ERR_UNSUPPORTED
+    # ld_kv below N (a ragged N is accepted: the last chunk is short)
+    assert L.ts_select_gather(P, 8, 4100, 4096, 64, P, P, 4099, 128, P, None, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    # misaligned part_len
+    assert L.ts_select_gather(P, 8, 4100, 4096, 64, P, P, 4100, 128, P, P + 2, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    # more than 16384 chunks
+    assert L.ts_select_gather(P, 8, 16384 * 64 + 1, 4096, 64, P, P, 1 << 21, 128, P, None, P, P, 4096,
+                              None) == ts.TS_ERR_UNSUPPORTED
+
+
+def test_rescore_tail_rejects():
+    L = ts.lib()
+    P = 0x10000
+    # N_old above N_new
+    assert L.ts_rescore_tail(P, 200, P, P, 300, 100, 8, 2, 128, 64, P + 4096, None) == ts.TS_ERR_INVALID_ARG
+    # in place across a change of the chunk count
+    assert L.ts_rescore_tail(P, 100, P, P, 300, 200, 8, 2, 128, 64, P, None) == ts.TS_ERR_INVALID_ARG
+    # overlapping buffers
+    assert L.ts_rescore_tail(P, 100, P, P, 300, 200, 8, 2, 128, 64, P + 4, None) == ts.TS_ERR_INVALID_ARG
+    # chunk other than 64, ld_kv below N_new
+    assert L.ts_rescore_tail(P, 100, P, P, 300, 200, 8, 2, 128, 32, P + 4096, None) == ts.TS_ERR_UNSUPPORTED
+    assert L.ts_rescore_tail(P, 100, P, P, 150, 200, 8, 2, 128, 64, P + 4096, None) == ts.TS_ERR_INVALID_ARG
+    # nothing to do
+    assert L.ts_rescore_tail(None, 0, P, P, 300, 0, 8, 2, 128, 64, P, None) == ts.TS_OK
+
+
+def test_partial_attention_needs_part_len():
+    L = ts.lib()
+    P = 0x10000
+    st = L.ts_tree_attn_partial(P, P, P, 4100, 4096, 4, 40, 8, 128, 0.088, P, None, P, None, P, 1 << 30, None)
+    assert st == ts.TS_ERR_INVALID_ARG and b"part_len" in L.ts_last_error()
 
 
 def test_vocab_rejects():

@@ -40,7 +40,9 @@ def _check_step(step: SpecStep, layers, rows_per_layer=6):
         rsel = oracle.select(rs, cfg.k_sel)
         np.testing.assert_array_equal(Lb.sel.cpu().numpy(), rsel, err_msg=f"layer {i} sel")
         kp, vp = Lb.k_part.cpu(), Lb.v_part.cpu()
-        assert torch.equal(kp, oracle.gather(rsel, k, cfg.N, 64, kp.shape[1], fill=kp)), f"layer {i} k_part"
+        rkp, rlen = oracle.gather(rsel, k, cfg.N, 64, kp.shape[1], fill=kp, return_len=True)
+        assert torch.equal(kp, rkp), f"layer {i} k_part"
+        np.testing.assert_array_equal(Lb.part_len.cpu().numpy(), rlen, err_msg=f"layer {i} part_len")
         assert torch.equal(vp, oracle.gather(rsel, v, cfg.N, 64, vp.shape[1], fill=vp)), f"layer {i} v_part"
         # verify attention on sampled rows: always the scoring row's heads, a tree leaf, a chain end
         rows = np.unique(np.concatenate([
@@ -49,7 +51,7 @@ def _check_step(step: SpecStep, layers, rows_per_layer=6):
         ro, rl = oracle.tree_attn(q, k, v, cfg.N, step.parents, cfg.scale, rows=rows)
         _check_rows(Lb.out, Lb.lse, ro, rl, rows, f"layer {i} verify")
         # draft attention over the partial cache: every row
-        ro, rl = oracle.tree_attn(Lb.q_draft.cpu(), kp, vp, step.B, step.draft_parents, cfg.scale)
+        ro, rl = oracle.tree_attn(Lb.q_draft.cpu(), kp, vp, step.B, step.draft_parents, cfg.scale, prefix_len=rlen)
         _check_rows(Lb.out_draft, Lb.lse_draft, ro.reshape(-1, cfg.d), rl.reshape(-1),
                     np.arange(step.Td * cfg.Hq), f"layer {i} draft")
 
@@ -95,7 +97,7 @@ def test_step_graph_replay_matches_eager():
     assert torch.equal(step.result, res)
 
 
-@pytest.mark.parametrize("N", [20480, 102400])
+@pytest.mark.parametrize("N", [20480, 40960, 61440, 81920, 102400])
 def test_llama8b_sweep_layers(N):
     cfg = W.WORKLOADS["llama8b-sweep"].with_N(N)
     step = SpecStep(cfg, layers=2)

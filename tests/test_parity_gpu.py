@@ -192,26 +192,90 @@ def test_small_batch_fused_scores_and_attention(T, Hq, Hkv, N, score_row):
 
 
 @pytest.mark.parametrize("N,budget,d", [(4096, 1024, 64), (20480, 4096, 128), (64 * 70, 4096, 128),
-                                        (102400, 4096, 128), (640, 4096, 128)])
+                                        (102400, 4096, 128), (640, 4096, 128), (4100, 4096, 128),
+                                        (20483, 4096, 128), (102403, 4096, 128), (1000, 1024, 64), (37, 4096, 128)])
 def test_select_gather_bit_exact(N, budget, d):
+    """Selection, gathered caches and gathered lengths, including a short last
+    chunk (N not a multiple of 64): its rows past N stay untouched."""
     Hq, Hkv = 32, 8
     q, k, v = W.make_qkv(1, Hq, Hkv, d, N, seed=N + budget, device="cuda")
-    nc = N // 64
+    nc = (N + 63) // 64
     sc = torch.empty((Hkv, nc), dtype=torch.float32, device="cuda")
     ts.ts_score_chunks(q[0], k, N, sc)
     kk = min(budget // 64, nc)
     sel = torch.empty((Hkv, kk), dtype=torch.int32, device="cuda")
+    plen = torch.full((Hkv,), -1, dtype=torch.int32, device="cuda")
     ld_part = kk * 64 + 4
-    kp = torch.zeros((Hkv, ld_part, d), dtype=torch.bfloat16, device="cuda")
-    vp = torch.zeros_like(kp)
-    ts.ts_select_gather(sc, N, budget, k, v, sel, kp, vp)
+    fill = torch.full((Hkv, ld_part, d), 3.0, dtype=torch.bfloat16)
+    kp, vp = fill.cuda(), fill.cuda()
+    ts.ts_select_gather(sc, N, budget, k, v, sel, kp, vp, part_len=plen)
     torch.cuda.synchronize()
     scores = sc.cpu().numpy()
     np.testing.assert_array_equal(scores, oracle.score_chunks(q[0].cpu(), k.cpu(), N).astype(np.float32))
     rsel = oracle.select(scores, budget // 64)
     np.testing.assert_array_equal(sel.cpu().numpy(), rsel)
-    assert torch.equal(kp.cpu(), oracle.gather(rsel, k.cpu(), N, 64, ld_part))
-    assert torch.equal(vp.cpu(), oracle.gather(rsel, v.cpu(), N, 64, ld_part))
+    rk, rl = oracle.gather(rsel, k.cpu(), N, 64, ld_part, fill=fill, return_len=True)
+    assert torch.equal(kp.cpu(), rk)
+    assert torch.equal(vp.cpu(), oracle.gather(rsel, v.cpu(), N, 64, ld_part, fill=fill))
+    np.testing.assert_array_equal(plen.cpu().numpy(), rl)
+
+
+@pytest.mark.parametrize("N,Hq,Hkv,d", [(4100, 40, 8, 128), (1000, 32, 32, 128), (130, 8, 2, 64), (4096, 40, 8, 128)])
+def test_partial_cache_drafting_with_a_short_last_chunk(N, Hq, Hkv, d):
+    """Heads that selected the short last chunk hold fewer gathered tokens; the
+    drafting attention over the compact cache sees exactly those."""
+    Td, budget = 4, 1024
+    q, k, v = W.make_qkv(Td, Hq, Hkv, d, N, seed=N + Hkv, device="cuda", value_kind="normal")
+    nc = (N + 63) // 64
+    rng = np.random.default_rng(N)
+    s = rng.integers(-50, 50, size=(Hkv, nc)).astype(np.float32)
+    s[::2, nc - 1] = 1000.0  # every other head keeps the last chunk
+    kk = min(budget // 64, nc)
+    B = kk * 64
+    sel = torch.empty((Hkv, kk), dtype=torch.int32, device="cuda")
+    plen = torch.empty((Hkv,), dtype=torch.int32, device="cuda")
+    kp = torch.full((Hkv, B + Td, d), 7.0, dtype=torch.bfloat16, device="cuda")  # stale rows stand out
+    vp = torch.full_like(kp, -7.0)
+    kp[:, B:] = k[:, N:N + Td]
+    vp[:, B:] = v[:, N:N + Td]
+    ts.ts_select_gather(torch.from_numpy(s).cuda(), N, budget, k, v, sel, kp, vp, part_len=plen)
+    parent = [-1, 0, 1, 2]
+    out = torch.empty((Td, Hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((Td, Hq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(16, ts.ts_tree_attn_workspace_bytes(Td, Hq, Hkv, d, B)), dtype=torch.uint8, device="cuda")
+    ts.ts_tree_attn_partial(q, kp, vp, B, dev_mask(parent), plen, out, lse=lse, workspace=ws, scale=1 / math.sqrt(d))
+    torch.cuda.synchronize()
+    assert ts.ts_device_error(True) == ts.TS_OK
+    rsel = oracle.select(s, budget // 64)
+    np.testing.assert_array_equal(sel.cpu().numpy(), rsel)
+    _, rl = oracle.gather(rsel, k.cpu(), N, 64, B + Td, return_len=True)
+    np.testing.assert_array_equal(plen.cpu().numpy(), rl)
+    if N % 64:
+        assert (rl[::2] < B).all() and (rl[1::2] == B).all()
+    ro, rlse = oracle.tree_attn(q.cpu(), kp.cpu(), vp.cpu(), B, parent, 1 / math.sqrt(d), prefix_len=rl)
+    check_attn(out, lse, ro, rlse, "partial")
+
+
+@pytest.mark.parametrize("N_old,N_new", [(4094, 4098), (4096, 4100), (4100, 4100), (0, 37), (20480, 20483),
+                                         (130, 135), (63, 64), (102400, 102404)])
+def test_rescore_tail_equals_full_scoring(N_old, N_new):
+    """Scores after a commit: the untouched chunks keep their old values, the
+    touched ones are scored again; bit-exact against scoring all of N_new."""
+    Hq, Hkv, d = 40, 8, 128
+    q, k, _ = W.make_qkv(1, Hq, Hkv, d, N_new, seed=N_old + N_new, device="cuda")
+    nc_old, nc_new = (N_old + 63) // 64, (N_new + 63) // 64
+    old = torch.empty((Hkv, max(nc_old, 1)), dtype=torch.float32, device="cuda")
+    if N_old:
+        ts.ts_score_chunks(q[0], k, N_old, old)
+    new = torch.full((Hkv, nc_new), float("nan"), dtype=torch.float32, device="cuda")
+    ts.ts_rescore_tail(old if N_old else None, N_old, q[0], k, N_new, new)
+    torch.cuda.synchronize()
+    want = oracle.score_chunks(q[0].cpu(), k.cpu(), N_new).astype(np.float32)
+    np.testing.assert_array_equal(new.cpu().numpy(), want)
+    if nc_old == nc_new and N_old:
+        ts.ts_rescore_tail(old, N_old, q[0], k, N_new, old)   # in place
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(old.cpu().numpy(), want)
 
 
 def test_select_ties_and_signed_zero():
@@ -245,7 +309,9 @@ def test_draft_attention_over_partial_cache():
     vp = torch.zeros_like(kp)
     kp[:, B:] = x.k_draft_tail
     vp[:, B:] = x.v_draft_tail
-    ts.ts_select_gather(sc, N, cfg.budget, x.k, x.v, sel, kp, vp)
+    plen = torch.empty((cfg.Hkv,), dtype=torch.int32, device="cuda")
+    ts.ts_select_gather(sc, N, cfg.budget, x.k, x.v, sel, kp, vp, part_len=plen)
+    assert (plen.cpu() == B).all()
     parent = [-1, 0, 1, 2]
     out, lse, _ = run_attn(x.q_draft, kp, vp, B, parent, cfg.scale)
     rsel = oracle.select(sc.cpu().numpy(), cfg.k_sel)

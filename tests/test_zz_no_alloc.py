@@ -82,3 +82,20 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         assert (lse2 - lse1).abs().max().item() <= LSE_ABS
         if sc2 is not None:
             assert torch.equal(sc2, sc1)
+
+
+def test_noalloc_rejects_sizes_above_its_scratch():
+    """Sizes whose split partials need more than the fixed array are refused
+    before any pointer is read or any kernel is launched, and the message names
+    the maximum.  A 4-row drafting batch over 200000 tokens splits into 1563
+    ranges of 128 tokens: 1563 x 4 x 40 x 130 x 4 bytes, above 64 MiB."""
+    from long_context_attention_tree_b300 import build
+    build.build()
+    T, Hq, Hkv, d, N = 4, 40, 8, 128, 200000
+    need = ts.ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N)
+    assert need > ts.TS_NOALLOC_SCRATCH_BYTES
+    L = ts.lib()
+    P = ctypes.c_void_p(0x10000)
+    st = L.ts_tree_attn_noalloc(P, P, P, N + T, N, T, Hq, Hkv, d, 0.088, P, P, None, None, 0, None)
+    assert st == ts.TS_ERR_UNSUPPORTED
+    assert str(ts.TS_NOALLOC_SCRATCH_BYTES).encode() in L.ts_last_error()
