@@ -57,6 +57,7 @@ def _load():
         lib.oracle_gather.argtypes = [P, i32, i32, i32, i64, P, i64, i32, P, i64, P]
         lib.oracle_penalty_minp.argtypes = [P, i32, i32, P, i32, flt, flt, dbl, P, P, P]
         lib.oracle_accept.argtypes = [P, P, P, i32, i32, P, P]
+        lib.oracle_accept_ex.argtypes = [P, P, P, i32, i32, i32, ctypes.c_uint64, ctypes.c_uint64, P, P]
         lib.oracle_commit.argtypes = [P, i64, i64, i32, i32, i32, P, P, P]
         lib.oracle_philox4x64.argtypes = [P, P, P]
         lib.oracle_ln_f32.argtypes = [flt]
@@ -189,15 +190,19 @@ def penalty_minp(logits, history, theta: float, min_p: float, temperature: float
     return (target, kept, pen) if return_logits else (target, kept)
 
 
-def accept(draft, parent, target, anchor: int):
-    """(result int32[4] = {L, best, bonus, status}, path int32[T])."""
+def accept(draft, parent, target, anchor: int, seed=None, offset: int = 0):
+    """(result int32[4] = {L, best, bonus, status}, path int32[T]).
+    seed None keeps the lowest of the longest accepted rows; a seed draws it
+    uniformly (Philox4x64-10 at counter (0, 0, offset, 1), key (seed, 0))."""
     dr = np.ascontiguousarray(np.asarray(draft, dtype=np.int32))
     p = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
     tg = np.ascontiguousarray(np.asarray(target, dtype=np.int32))
     T = dr.size
     res = np.zeros(4, dtype=np.int32)
     path = np.zeros(max(T, 1), dtype=np.int32)
-    _load().oracle_accept(_ptr(dr), _ptr(p), _ptr(tg), T, int(anchor), _ptr(res), _ptr(path))
+    _load().oracle_accept_ex(_ptr(dr), _ptr(p), _ptr(tg), T, int(anchor), 0 if seed is None else 1,
+                             0 if seed is None else int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                             _ptr(res), _ptr(path))
     return res, path[:T]
 
 

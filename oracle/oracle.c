@@ -326,8 +326,18 @@ int oracle_penalty_minp(const float *logits, int T, int V, const int32_t *histor
 /*   bonus = L > 0 ? target[best] : anchor; path = root..best.              */
 /*   result = {L, best, bonus, status}; path int32[T], unused entries -1.   */
 /* ---------------------------------------------------------------------- */
-int oracle_accept(const int32_t *draft, const int32_t *parent, const int32_t *target, int T,
-                  int32_t anchor, int32_t *result, int32_t *path)
+/* The pages keep one of the longest valid drafts at random ("How it works"). */
+/* With choose != 0 the kept row is drawn uniformly from the m accepted rows  */
+/* of depth L, listed in ascending row order S[0..m): index                   */
+/*   j = floor(x * m / 2^64)   (the high word of the 128-bit product)         */
+/* with x = word 0 of Philox4x64-10 (below) at counter (0, 0, offset, 1) under */
+/* key (seed, 0) -- the last counter word keeps this draw apart from the       */
+/* token draws of oracle_sample, which use 0 there.  choose == 0 keeps S[0].   */
+void oracle_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
+
+int oracle_accept_ex(const int32_t *draft, const int32_t *parent, const int32_t *target, int T,
+                     int32_t anchor, int choose, uint64_t seed, uint64_t offset,
+                     int32_t *result, int32_t *path)
 {
     for (int i = 0; i < T; ++i) path[i] = -1;
     for (int i = 0; i < T; ++i)
@@ -345,6 +355,20 @@ int oracle_accept(const int32_t *draft, const int32_t *parent, const int32_t *ta
         depth[i] = p >= 0 ? depth[p] + 1 : 1;
         if (acc[i] && depth[i] > L) { L = depth[i]; best = i; }
     }
+    if (choose && L > 0) {
+        uint64_t m = 0;
+        for (int i = 0; i < T; ++i) m += (acc[i] && depth[i] == L);
+        const uint64_t ctr[4] = {0, 0, offset, 1}, key[2] = {seed, 0};
+        uint64_t x[4];
+        oracle_philox4x64(ctr, key, x);
+        const uint64_t j = (uint64_t)(((unsigned __int128)x[0] * m) >> 64);
+        uint64_t seen = 0;
+        for (int i = 0; i < T; ++i)
+            if (acc[i] && depth[i] == L) {
+                if (seen == j) { best = i; break; }
+                ++seen;
+            }
+    }
     result[0] = L;
     result[1] = best;
     result[2] = L > 0 ? target[best] : anchor;
@@ -353,6 +377,12 @@ int oracle_accept(const int32_t *draft, const int32_t *parent, const int32_t *ta
     free(acc);
     free(depth);
     return 0;
+}
+
+int oracle_accept(const int32_t *draft, const int32_t *parent, const int32_t *target, int T,
+                  int32_t anchor, int32_t *result, int32_t *path)
+{
+    return oracle_accept_ex(draft, parent, target, T, anchor, 0, 0, 0, result, path);
 }
 
 /* ---------------------------------------------------------------------- */

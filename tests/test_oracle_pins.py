@@ -450,6 +450,73 @@ def test_accept_matches_path_enumeration(seed):
         assert path[L - 1] == best
 
 
+def _longest_rows(draft, parent, target, anchor):
+    """Rows of the longest accepted paths, ascending, by networkx path enumeration."""
+    g = nx.DiGraph()
+    g.add_node("r")
+    for i, p in enumerate(parent):
+        g.add_edge("r" if p < 0 else p, i)
+    ok = {}
+    for i in range(len(parent)):
+        path = nx.shortest_path(g, "r", i)[1:]
+        if all(draft[n] == (anchor if parent[n] < 0 else target[parent[n]]) for n in path):
+            ok[i] = len(path)
+    L = max(ok.values(), default=0)
+    return L, sorted(i for i, n in ok.items() if n == L and L > 0)
+
+
+def test_random_longest_choice_follows_numpy_philox():
+    """The kept row is S[floor(x m / 2^64)], S the longest accepted rows in
+    ascending order (networkx), x word 0 of numpy's Philox4x64 at counter
+    (0, 0, offset, 1) under key (seed, 0)."""
+    parent = [-1, 0, 0, 0, 1, 2, 3, -1, 7, 8]
+    target = [5, 6, 6, 6, 9, 9, 9, 1, 2, 3]
+    draft = [4, 5, 5, 5, 6, 6, 6, 4, 1, 2]     # rows 4, 5, 6 and 9 end paths of depth 3
+    L, S = _longest_rows(draft, parent, target, 4)
+    assert L == 3 and S == [4, 5, 6, 9]
+    picks = []
+    for seed, offset in [(1, 0), (1, 1), (99, 7), (2**63 + 5, 2**40)]:
+        c = (offset << 128) + (1 << 192) - 1   # numpy adds 1 to the 256-bit counter before each block
+        ctr = np.array([(c >> (64 * i)) & (2**64 - 1) for i in range(4)], dtype=np.uint64)
+        bg = np.random.Philox(counter=ctr, key=np.array([seed, 0], dtype=np.uint64))
+        x = int(bg.random_raw(1)[0])
+        want = S[(x * len(S)) >> 64]
+        r, path = oracle.accept(draft, parent, target, 4, seed=seed, offset=offset)
+        assert (r[0], r[1], r[2]) == (3, want, target[want])
+        assert path[:3].tolist() == nx.shortest_path(
+            nx.DiGraph([("r" if p < 0 else p, i) for i, p in enumerate(parent)]), "r", want)[1:]
+        picks.append(want)
+    assert len(set(picks)) > 1
+
+
+def test_random_longest_choice_is_uniform_and_valid():
+    parent = W.verify_parents()
+    vi = W.make_vocab_inputs(parent, V=300, W=20, seed=12)
+    target = vi.designed_target.numpy()
+    # every chain repeats the tree's path so that several rows tie for the longest
+    draft = vi.draft.numpy().copy()
+    L0, S0 = _longest_rows(draft.tolist(), parent, target.tolist(), vi.anchor)
+    for c in range(20):
+        rows = [40 + 4 * c + j for j in range(4)]
+        draft[rows[0]] = vi.anchor
+        for j in range(1, 4):
+            draft[rows[j]] = target[rows[j - 1]]
+    L, S = _longest_rows(draft.tolist(), parent, target.tolist(), vi.anchor)
+    assert L == 4 and len(S) >= 20
+    R = 6000
+    counts = np.zeros(len(S))
+    for o in range(R):
+        r, _ = oracle.accept(draft, parent, target, vi.anchor, seed=2024, offset=o)
+        assert r[0] == L and r[1] in S
+        counts[S.index(r[1])] += 1
+    chi2 = (((counts - R / len(S)) ** 2) / (R / len(S))).sum()
+    assert scipy.stats.chi2.sf(chi2, len(S) - 1) > 1e-4
+    # one longest row: the draw has nothing to choose
+    if len(S0) == 1:
+        r, _ = oracle.accept(vi.draft.numpy(), parent, target, vi.anchor, seed=5)
+        assert r[1] == S0[0]
+
+
 def test_planted_targets_are_the_oracle_targets():
     """The input generator's designed tokens are what the greedy step picks."""
     parent = W.verify_parents()
