@@ -22,7 +22,9 @@
  *                            greedy target and exact-match acceptance.
  *   ts_penalty_minp_sample_verify  the same with min-p sampled targets;
  *   ts_commit_path           the accepted path's K/V rows become the
- *                            continuation of the full cache.
+ *                            continuation of the full cache;
+ *   ts_ngram_update/_topk    the n-gram table of the generated text and its
+ *                            top-k 4-grams for the next anchor.
  *
  * Conventions shared by every call:
  *   - Pointers without a _host suffix are device memory owned by the caller.
@@ -314,7 +316,11 @@ ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_
  * under key (seed, 0); ln is evaluated in fp32 as ln x = e ln 2 + 2 atanh(s),
  * s = (m - 1)/(m + 1), x = 2^e m, m in [sqrt(1/2), sqrt(2)), with the series
  * s (1 + s^2/3 + ... + s^10/11), every operation an IEEE fp32 one.
- * Acceptance then uses these sampled targets.  kept, result and path as for
+ * Acceptance then uses these sampled targets, and the kept row among the m
+ * longest accepted rows S (ascending row order) is drawn uniformly ("How it
+ * works": one of the longest valid drafts is selected at random):
+ * best = S[floor(x m / 2^64)], x = word 0 of Philox4x64-10 at counter
+ * (0, 0, offset, 1) under key (seed, 0).  kept, result and path as for
  * ts_penalty_minp_verify.
  */
 ts_status ts_penalty_minp_sample_verify(const float *logits, int T, int V, const int32_t *history, int W,
@@ -342,6 +348,50 @@ ts_status ts_penalty_minp_sample_verify(const float *logits, int T, int V, const
  */
 ts_status ts_commit_path(void *k, void *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d, int32_t *result,
                          const int32_t *path, ts_stream_t stream);
+
+/*
+ * n-gram table of the generated text and top-k 4-gram retrieval (TokenSwift
+ * tool listing, "How it works": the top-k candidate 4-grams become draft
+ * tokens and the n-gram table is updated after every step; model card:
+ * --ngram_topk 20 --gamma 4).
+ *
+ * The table counts every 4-gram w = seq[p-3..p] of the sequence added to it.
+ * The candidates for an anchor a (the token every draft root must equal) are
+ * the 4-grams with w0 = a, by count descending, then (w1, w2, w3) ascending.
+ *
+ * Layout (caller-owned device memory, ts_ngram_table_bytes(capacity) bytes,
+ * 16-byte aligned): int32 keys [capacity][4] (all ones = empty slot), int32
+ * counts [capacity], int32 first [capacity] (start position of the 4-gram's
+ * first occurrence).  capacity is a power of two in [64, 2^30]; keep it at
+ * least twice the number of distinct 4-grams (a sequence of n tokens has at
+ * most n - 3).  Open addressing with linear probing from a hash of all four
+ * tokens.
+ *
+ * ts_ngram_reset   empties the table.
+ * ts_ngram_update  adds the windows that end at positions [max(3, n_old),
+ *                  n_new) of seq (device int32 [n_new], ids >= 0,
+ *                  n_new < 2^31): call it with the old and new lengths after
+ *                  each commit.  A full table or a negative id sets *status
+ *                  (device int32) to TS_ERR_DATA; otherwise *status is left
+ *                  as it was.
+ * ts_ngram_topk    the top k 4-grams of seq[0, n) that start with the anchor;
+ *                  the table must hold exactly the windows of seq[0, n).  It
+ *                  reads the anchor from device memory (e.g. the bonus token
+ *                  result + 2 of ts_penalty_minp_verify: no host round trip),
+ *                  scans seq for it and takes each distinct 4-gram once (at
+ *                  its first occurrence) with its count from the table.  It
+ *                  writes chains int32 [k][4] (w0..w3 of the i-th candidate;
+ *                  -1 past the last one), counts int32 [k] (0 past the last
+ *                  one) and found (device int32: how many, <= k).  chains can
+ *                  point straight at the draft tokens of the verify batch's
+ *                  chain rows.  1 <= k <= 1024.
+ */
+size_t ts_ngram_table_bytes(int64_t capacity);
+ts_status ts_ngram_reset(void *table, int64_t capacity, ts_stream_t stream);
+ts_status ts_ngram_update(void *table, int64_t capacity, const int32_t *seq, int64_t n_old, int64_t n_new,
+                          int32_t *status, ts_stream_t stream);
+ts_status ts_ngram_topk(const void *table, int64_t capacity, const int32_t *seq, int64_t n, const int32_t *anchor,
+                        int k, int32_t *chains, int32_t *counts, int32_t *found, ts_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,8 @@ __all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree
            "ts_launch_count", "ts_tree_attn_uses_tensor_cores", "ts_device_error", "ts_selftest_bounded_wait",
            "ts_selftest_fail_launches", "ts_tree_attn",
            "ts_tree_attn_partial", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_rescore_tail",
-           "ts_select_gather", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path"]
+           "ts_select_gather", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path",
+           "ts_ngram_table_bytes", "ts_ngram_reset", "ts_ngram_update", "ts_ngram_topk"]
 
 
 class TSError(RuntimeError):
@@ -72,12 +73,18 @@ def lib() -> ctypes.CDLL:
         L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
                                              P, P, P, P, P, sz, P]
         L.ts_commit_path.argtypes = [P, P, i64, i64, i32, i32, i32, P, P, P]
+        L.ts_ngram_table_bytes.argtypes = [i64]
+        L.ts_ngram_table_bytes.restype = sz
+        L.ts_ngram_reset.argtypes = [P, i64, P]
+        L.ts_ngram_update.argtypes = [P, i64, P, i64, i64, P, P]
+        L.ts_ngram_topk.argtypes = [P, i64, P, i64, P, i32, P, P, P, P]
         u64 = ctypes.c_uint64
         L.ts_penalty_minp_sample_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, u64, u64, P, P,
                                                     ctypes.c_int32, P, P, P, P, P]
         for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_partial", "ts_tree_attn_noalloc",
                      "ts_score_chunks", "ts_rescore_tail", "ts_select_gather", "ts_penalty_minp_verify",
-                     "ts_commit_path", "ts_penalty_minp_sample_verify"):
+                     "ts_commit_path", "ts_penalty_minp_sample_verify", "ts_ngram_reset", "ts_ngram_update",
+                     "ts_ngram_topk"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -241,3 +248,25 @@ def ts_penalty_minp_sample_verify(logits, history, theta: float, min_p: float, t
                                                temperature, int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
                                                _ptr(draft), _ptr(parent), int(anchor), _ptr(target), _ptr(kept),
                                                _ptr(result), _ptr(path), _stream(stream)))
+
+
+def ts_ngram_table_bytes(capacity: int) -> int:
+    """Bytes of an n-gram table of `capacity` slots (0 if capacity is invalid)."""
+    return int(lib().ts_ngram_table_bytes(int(capacity)))
+
+
+def ts_ngram_reset(table, capacity: int, stream=None) -> None:
+    _check(lib().ts_ngram_reset(_ptr(table), int(capacity), _stream(stream)))
+
+
+def ts_ngram_update(table, capacity: int, seq, n_old: int, n_new: int, status, stream=None) -> None:
+    """Add the 4-grams ending at positions [max(3, n_old), n_new) of seq (int32, CUDA)."""
+    _check(lib().ts_ngram_update(_ptr(table), int(capacity), _ptr(seq), int(n_old), int(n_new), _ptr(status),
+                                 _stream(stream)))
+
+
+def ts_ngram_topk(table, capacity: int, seq, n: int, anchor, k: int, chains, counts, found, stream=None) -> None:
+    """Top-k 4-grams of seq[0, n) starting with the device int32 anchor:
+    chains [k][4], counts [k], found [1] (the table holds the windows of seq[0, n))."""
+    _check(lib().ts_ngram_topk(_ptr(table), int(capacity), _ptr(seq), int(n), _ptr(anchor), int(k), _ptr(chains),
+                               _ptr(counts), _ptr(found), _stream(stream)))

@@ -130,6 +130,14 @@ struct VocabArgs {
 };
 cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st);
 
+// n-gram table: int4 keys [C], int32 counts [C], int32 first positions [C]
+// (C a power of two >= 64)
+cudaError_t launch_ngram_reset(void *table, uint32_t C, cudaStream_t st);
+cudaError_t launch_ngram_update(void *table, uint32_t C, const int32_t *seq, int64_t n_old, int64_t n_new,
+                                int32_t *status, cudaStream_t st);
+cudaError_t launch_ngram_topk(const void *table, uint32_t C, const int32_t *seq, int64_t n, const int32_t *anchor,
+                              int k, int32_t *chains, int32_t *counts, int32_t *found, cudaStream_t st);
+
 // commit of the accepted path into the full cache (T <= 128)
 cudaError_t launch_commit_path(__nv_bfloat16 *k, __nv_bfloat16 *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d,
                                int32_t *result, const int32_t *path, cudaStream_t st);

@@ -472,6 +472,61 @@ ts_status ts_penalty_minp_sample_verify(const float *logits, int T, int V, const
                        target, kept, result, path, stream);
 }
 
+static ts_status check_ngram_table(const void *table, int64_t capacity) {
+    if (capacity < 64 || capacity > ((int64_t)1 << 30) || (capacity & (capacity - 1)))
+        return fail(TS_ERR_INVALID_ARG, "capacity=%lld must be a power of two in [64, 2^30]", (long long)capacity);
+    if (!table) return fail(TS_ERR_INVALID_ARG, "null table");
+    if (!aligned16(table)) return fail(TS_ERR_INVALID_ARG, "table must be 16-byte aligned");
+    return TS_OK;
+}
+
+size_t ts_ngram_table_bytes(int64_t capacity) {
+    if (capacity < 64 || capacity > ((int64_t)1 << 30) || (capacity & (capacity - 1))) return 0;
+    return (size_t)capacity * 24;
+}
+
+ts_status ts_ngram_reset(void *table, int64_t capacity, ts_stream_t stream) {
+    ts_status st = check_ngram_table(table, capacity);
+    if (st != TS_OK) return st;
+    cudaError_t e = ts::launch_ngram_reset(table, (uint32_t)capacity, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ngram_reset launch");
+    ts::note_launches(1);
+    return TS_OK;
+}
+
+ts_status ts_ngram_update(void *table, int64_t capacity, const int32_t *seq, int64_t n_old, int64_t n_new,
+                          int32_t *status, ts_stream_t stream) {
+    ts_status st = check_ngram_table(table, capacity);
+    if (st != TS_OK) return st;
+    if (n_old < 0 || n_new < n_old) return fail(TS_ERR_INVALID_ARG, "need 0 <= n_old <= n_new");
+    if (n_new > INT32_MAX) return fail(TS_ERR_UNSUPPORTED, "n_new=%lld above 2^31 - 1", (long long)n_new);
+    if (n_new <= 3 || n_new <= n_old) return TS_OK;  // no new window
+    if (!seq || !status) return fail(TS_ERR_INVALID_ARG, "null seq/status");
+    if (!aligned4(seq) || !aligned4(status)) return fail(TS_ERR_INVALID_ARG, "misaligned seq/status");
+    cudaError_t e = ts::launch_ngram_update(table, (uint32_t)capacity, seq, n_old, n_new, status,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ngram_update launch");
+    ts::note_launches(1);
+    return TS_OK;
+}
+
+ts_status ts_ngram_topk(const void *table, int64_t capacity, const int32_t *seq, int64_t n, const int32_t *anchor,
+                        int k, int32_t *chains, int32_t *counts, int32_t *found, ts_stream_t stream) {
+    ts_status st = check_ngram_table(table, capacity);
+    if (st != TS_OK) return st;
+    if (k < 1 || k > 1024) return fail(TS_ERR_UNSUPPORTED, "k=%d outside [1, 1024]", k);
+    if (n < 0 || n > INT32_MAX) return fail(TS_ERR_INVALID_ARG, "n=%lld outside [0, 2^31 - 1]", (long long)n);
+    if (!anchor || !chains || !counts || !found || (n > 0 && !seq))
+        return fail(TS_ERR_INVALID_ARG, "null seq/anchor/chains/counts/found");
+    if (!aligned4(anchor) || !aligned4(chains) || !aligned4(counts) || !aligned4(found) || (seq && !aligned4(seq)))
+        return fail(TS_ERR_INVALID_ARG, "misaligned pointer");
+    cudaError_t e = ts::launch_ngram_topk(table, (uint32_t)capacity, seq, n, anchor, k, chains, counts, found,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ngram_topk launch");
+    ts::note_launches(1);
+    return TS_OK;
+}
+
 ts_status ts_commit_path(void *k, void *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d, int32_t *result,
                          const int32_t *path, ts_stream_t stream) {
     if (T < 1 || T > 128) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [1, 128]", T);

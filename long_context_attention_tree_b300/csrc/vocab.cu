@@ -211,13 +211,20 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
 }
 
 // Acceptance: one CTA, one thread per batch row walking its (short) ancestor
-// chain; the longest accepted depth wins, ties to the lowest row.
+// chain; the longest accepted depth wins.  Greedy targets keep the lowest of
+// the longest rows; sampled targets draw one of them uniformly ("How it
+// works": one of the longest valid drafts is selected at random): with S the
+// m longest accepted rows in ascending order, the kept row is
+// S[floor(x m / 2^64)], x = word 0 of Philox4x64-10 at counter
+// (0, 0, offset, 1) under key (seed, 0).
 __global__ void __launch_bounds__(1024) accept_kernel(const VocabArgs a) {
     __shared__ int s_parent[1024];
     __shared__ int s_target[1024];
     __shared__ int s_draft[1024];
+    __shared__ int s_depth[1024];  // depth of an accepted row, 0 otherwise
     __shared__ int s_bad;
     __shared__ int s_key;
+    __shared__ int s_pick;
     const int tid = threadIdx.x;
     if (tid == 0) {
         s_bad = 0;
@@ -253,13 +260,38 @@ __global__ void __launch_bounds__(1024) accept_kernel(const VocabArgs a) {
             ok = ok && (s_draft[n] == expected);
             ++depth;
         }
+        s_depth[i] = ok ? depth : 0;
         if (ok) atomicMax(&s_key, (depth << 16) | (0xffff - i));
+    }
+    __syncthreads();
+    const int L_all = s_key < 0 ? 0 : (s_key >> 16);
+    if (a.sample && L_all > 0 && tid < 32) {
+        // warp 0: m = #longest rows, then the j-th of them in row order
+        int m = 0;
+        for (int b = 0; b < a.T; b += 32) {
+            const int i = b + tid;
+            m += __popc(__ballot_sync(0xffffffffu, i < a.T && s_depth[i] == L_all));
+        }
+        const uint64_t x = philox_word(0ull, 0ull, a.offset, 1ull, a.seed, 0ull, 0);
+        int j = (int)__umul64hi(x, (uint64_t)m);
+        for (int b = 0; b < a.T; b += 32) {
+            const int i = b + tid;
+            const unsigned bal = __ballot_sync(0xffffffffu, i < a.T && s_depth[i] == L_all);
+            const int c = __popc(bal);
+            if (j < c) {
+                unsigned rest = bal;
+                for (int q = 0; q < j; ++q) rest &= rest - 1;  // drop the j lowest set bits
+                if (tid == 0) s_pick = b + __ffs(rest) - 1;
+                break;
+            }
+            j -= c;
+        }
     }
     __syncthreads();
     if (tid == 0) {
         const int key = s_key;
         const int L = key < 0 ? 0 : (key >> 16);
-        const int best = key < 0 ? -1 : 0xffff - (key & 0xffff);
+        const int best = key < 0 ? -1 : (a.sample ? s_pick : 0xffff - (key & 0xffff));
         a.result[0] = L;
         a.result[1] = best;
         a.result[2] = L > 0 ? s_target[best] : a.anchor;

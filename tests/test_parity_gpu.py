@@ -555,6 +555,38 @@ def test_sampled_vocab_stage_bit_exact(V, W_, flip, seed, min_p, temp):
     rs = oracle.sample(pen, min_p, 77 + seed, 5)
     np.testing.assert_array_equal(target.cpu().numpy(), rs)
     np.testing.assert_array_equal(kept.cpu().numpy(), rk)
-    rr, rp = oracle.accept(vi.draft.cpu().numpy(), parent, rs, vi.anchor)
+    rr, rp = oracle.accept(vi.draft.cpu().numpy(), parent, rs, vi.anchor, seed=77 + seed, offset=5)
     np.testing.assert_array_equal(result.cpu().numpy(), rr)
     np.testing.assert_array_equal(path.cpu().numpy(), rp)
+
+
+def test_sampled_stage_draws_among_the_longest_paths():
+    """Rows tie for the longest accepted path (every chain repeats a path of the
+    sampled targets); the kept row is the oracle's seeded uniform draw, offset
+    by offset, and over many offsets every tied row is drawn."""
+    parent = W.verify_parents()
+    T = len(parent)
+    V = 64
+    vi = W.make_vocab_inputs(parent, V, 8, seed=21, device="cuda")
+    logits = torch.full((T, V), -20.0, dtype=torch.float32)
+    logits[:, 7] = 5.0   # every sampled target is token 7 (min-p keeps only it)
+    draft = torch.full((T,), 7, dtype=torch.int32)
+    draft[40::4] = 3     # chain heads match the anchor 3, the rest match target 7
+    for c in range(0, 20, 3):
+        draft[40 + 4 * c + 2] = 1   # some chains break at depth 3
+    target = torch.empty((T,), dtype=torch.int32, device="cuda")
+    kept = torch.empty_like(target)
+    result = torch.empty((4,), dtype=torch.int32, device="cuda")
+    path = torch.empty_like(target)
+    seen = set()
+    hist = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for off in range(40):
+        ts.ts_penalty_minp_sample_verify(logits.cuda(), hist, 1.2, 0.1, 1.0, 9, off, draft.cuda(), vi.parent, 3,
+                                         target, kept, result, path)
+        torch.cuda.synchronize()
+        rr, rp = oracle.accept(draft.numpy(), parent, np.full(T, 7, np.int32), 3, seed=9, offset=off)
+        np.testing.assert_array_equal(result.cpu().numpy(), rr)
+        np.testing.assert_array_equal(path.cpu().numpy(), rp)
+        assert rr[0] == 4
+        seen.add(int(rr[1]))
+    assert len(seen) >= 8
