@@ -79,12 +79,15 @@ uint64_t ts_launch_count(void);
  * attention over the candidate tokens; the n-gram candidates are chains).
  *   parent_host: int32[T], parent_host[i] = parent row of i, or -1 for a root;
  *                requires -1 <= parent_host[i] < i (topological order).
- *   mask_host:   uint64[T][2]; bit u of row i (word u/64, bit u%64) is set
- *                iff u == i or u is an ancestor of i.
- *   T in [0, 128].  Host memory only; no CUDA call.
+ *   mask_host:   uint64[T][mw], mw = ts_tree_mask_words(T) = max(2, ceil(T/64));
+ *                bit u of row i (word u/64, bit u%64) is set iff u == i or u
+ *                is an ancestor of i.
+ *   T in [0, 1024] (a [1,9,9,9] tree is 820 rows).  Host memory only; no
+ *   CUDA call.
  * Errors: TS_ERR_INVALID_ARG for a null pointer, T out of range or a parent
  * index out of order.
  */
+int ts_tree_mask_words(int T);
 ts_status ts_tree_mask_from_parents(const int32_t *parent_host, int T, uint64_t *mask_host);
 
 /*
@@ -107,8 +110,8 @@ size_t ts_tree_attn_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t N);
  *
  *   q        bf16 [T][Hq][d]
  *   k, v     bf16 [Hkv][ld_kv][d], ld_kv >= N + T
- *   mask     device uint64 [T][2] from ts_tree_mask_from_parents; every row
- *            must see itself
+ *   mask     device uint64 [T][ts_tree_mask_words(T)] from
+ *            ts_tree_mask_from_parents; every row must see itself
  *   out      bf16 [T][Hq][d]
  *   lse      fp32 [T][Hq] or NULL
  *   chunk_scores  fp32 [Hkv][ceil(N/64)] or NULL: when given, the chunk
@@ -119,7 +122,7 @@ size_t ts_tree_attn_workspace_bytes(int T, int Hq, int Hkv, int d, int64_t N);
  *            up to fp32 summation order).
  *   workspace at least ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N) bytes,
  *            or NULL when that is 0.
- * Supported: d in {64, 128}; Hq % Hkv == 0; Hq/Hkv <= 32; 0 <= T <= 128;
+ * Supported: d in {64, 128}; Hq % Hkv == 0; Hq/Hkv <= 32; 0 <= T <= 1024;
  * N >= 0; N + T >= 1 when T >= 1.  T >= 64 with d == 128 runs on the tensor
  * cores (tcgen05, TMEM accumulators); other shapes run on the CUDA cores
  * (batches of at most 24 (row, head) pairs per KV head with d == 128, such as
@@ -344,7 +347,7 @@ ts_status ts_penalty_minp_sample_verify(const float *logits, int T, int V, const
  *   k, v    bf16 [Hkv][ld_kv][d], ld_kv >= N + T (updated in place)
  *   result  int32[4] device (result[0] read, result[3] written on a data error)
  *   path    int32[T] device
- * Supported: 1 <= T <= 128, d in {64, 128}.
+ * Supported: 1 <= T <= 1024, d in {64, 128}.
  */
 ts_status ts_commit_path(void *k, void *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d, int32_t *result,
                          const int32_t *path, ts_stream_t stream);

@@ -54,6 +54,8 @@ def lib() -> ctypes.CDLL:
         L.ts_version.restype = ctypes.c_char_p
         L.ts_launch_count.restype = ctypes.c_uint64
         L.ts_tree_mask_from_parents.argtypes = [P, i32, P]
+        L.ts_tree_mask_words.argtypes = [i32]
+        L.ts_tree_mask_words.restype = i32
         L.ts_tree_attn_workspace_bytes.argtypes = [i32, i32, i32, i32, i64]
         L.ts_tree_attn_workspace_bytes.restype = sz
         L.ts_tree_attn_uses_tensor_cores.argtypes = [i32, i32, i32, i32, i64]
@@ -118,10 +120,10 @@ def ts_launch_count() -> int:
 
 
 def ts_tree_mask_from_parents(parent) -> np.ndarray:
-    """uint64 [T][2] ancestor-or-self mask (host)."""
+    """uint64 [T][max(2, ceil(T/64))] ancestor-or-self mask (host)."""
     p = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
     T = p.size
-    mask = np.zeros((max(T, 1), 2), dtype=np.uint64)
+    mask = np.zeros((max(T, 1), int(lib().ts_tree_mask_words(T))), dtype=np.uint64)
     _check(lib().ts_tree_mask_from_parents(p.ctypes.data_as(ctypes.c_void_p), T,
                                            mask.ctypes.data_as(ctypes.c_void_p)))
     return mask[:T]

@@ -167,7 +167,7 @@ tree_attn_simt_kernel(const AttnArgs a) {
                         vis = tok < plen;
                         raw_sum += s;
                     } else if (tok < L) {
-                        vis = mask_bit(a.mask, s_t, (int)(tok - a.N));
+                        vis = mask_bit(a.mask, a.mw, s_t, (int)(tok - a.N));
                     }
                 }
                 x[i] = vis ? s * a.scale_log2 : -INFINITY;

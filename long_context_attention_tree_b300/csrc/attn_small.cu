@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             bool vis = in_range[i] && r < R;
-            if (vis) vis = tok[i] < a.N ? tok[i] < plen : mask_bit(a.mask, t, (int)(tok[i] - a.N));
+            if (vis) vis = tok[i] < a.N ? tok[i] < plen : mask_bit(a.mask, a.mw, t, (int)(tok[i] - a.N));
             s[i][jr] = vis ? s[i][jr] * c : -INFINITY;
             mx = fmaxf(mx, s[i][jr]);
         }

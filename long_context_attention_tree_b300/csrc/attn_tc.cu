@@ -120,15 +120,27 @@ __device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, 
 // Hide tokens this row may not see: prefix tokens at or past the head's
 // prefix length plen (<= N), batch tokens whose row is not an
 // ancestor-or-self (mask bits), tokens past the batch.
+// mrow is the row's mask (uint64 words), or null for a padding row, which
+// sees no batch token; a 32-token chunk touches at most two of its words.
 __device__ __forceinline__ void mask_chunk(uint32_t (&x)[32], int64_t tok0, int64_t plen, int64_t N, int T,
-                                           uint64_t mk0, uint64_t mk1) {
+                                           const uint64_t *mrow) {
+    const int64_t u0 = tok0 - N;  // batch index of the chunk's first token (may be negative)
+    uint64_t wa = 0, wb = 0;
+    int wbase = 0;
+    if (mrow != nullptr && u0 + 32 > 0 && u0 < T) {
+        const int ufirst = u0 > 0 ? (int)u0 : 0;
+        const int ulast = u0 + 31 < T - 1 ? (int)(u0 + 31) : T - 1;
+        wbase = ufirst >> 6;
+        wa = mrow[wbase];
+        if ((ulast >> 6) != wbase) wb = mrow[wbase + 1];
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int64_t tok = tok0 + i;
         bool vis = tok < plen;
         if (tok >= N && tok < N + T) {
             const int u = (int)(tok - N);
-            vis = ((u < 64 ? (mk0 >> u) : (mk1 >> (u - 64))) & 1ull) != 0;
+            vis = ((((u >> 6) == wbase ? wa : wb) >> (u & 63)) & 1ull) != 0;
         }
         if (!vis) x[i] = __float_as_uint(-INFINITY);
     }
@@ -431,11 +443,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const int t = mt * tpb + r / G;
             const int j = r % G;
             const bool row_valid = r < rows_loaded && t < a.T;
-            uint64_t mk0 = 0, mk1 = 0;
-            if (row_valid) {
-                mk0 = a.mask[2 * t];
-                mk1 = a.mask[2 * t + 1];
-            }
+            const uint64_t *mrow = row_valid ? a.mask + (size_t)a.mw * t : nullptr;
             const bool is_score_row = score_wm == wm && row_valid && t == a.score_row;
             const bool score_warp = __any_sync(0xffffffffu, is_score_row);
             const int64_t plen = prefix_of(a, g);
@@ -489,10 +497,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
                 // ---- tiles that reach past the prefix: hide what this row may not see
                 if (tok0 + KV_TILE > plen) {
-                    mask_chunk(x0, tok0 + 0, plen, a.N, a.T, mk0, mk1);
-                    mask_chunk(x1, tok0 + 32, plen, a.N, a.T, mk0, mk1);
-                    mask_chunk(x2, tok0 + 64, plen, a.N, a.T, mk0, mk1);
-                    mask_chunk(x3, tok0 + 96, plen, a.N, a.T, mk0, mk1);
+                    mask_chunk(x0, tok0 + 0, plen, a.N, a.T, mrow);
+                    mask_chunk(x1, tok0 + 32, plen, a.N, a.T, mrow);
+                    mask_chunk(x2, tok0 + 64, plen, a.N, a.T, mrow);
+                    mask_chunk(x3, tok0 + 96, plen, a.N, a.T, mrow);
                 }
 
                 // ---- row max (raw units), lazy running-max update
@@ -634,7 +642,7 @@ static int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 TcPlan tc_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms) {
     TcPlan p{};
     const int G = Hq / Hkv;
-    p.ok = d == 128 && T >= 64 && T <= 128 && G >= 1 && G <= 32;
+    p.ok = d == 128 && T >= 64 && T <= TS_MAX_T && G >= 1 && G <= 32;
     if (!p.ok) return p;
     p.tpb = 128 / G;
     p.n_mtiles = ceil_div(T, p.tpb);

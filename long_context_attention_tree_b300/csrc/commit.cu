@@ -17,14 +17,18 @@ namespace ts {
 
 namespace {
 constexpr int CM_THREADS = 256;
-constexpr int CM_MAX_T = 128;
+constexpr int CM_ROUND = 128;  // path rows staged in shared memory at a time
 }  // namespace
 
+// Rows are moved in rounds of CM_ROUND path entries, each round read in full
+// before it is written.  A round never overwrites a later round's source: the
+// path is strictly increasing from >= 0, so entry j reads row path[j] >= j,
+// while the rounds before it write rows i < j.
 __global__ void __launch_bounds__(CM_THREADS) commit_path_kernel(__nv_bfloat16 *k, __nv_bfloat16 *v, int64_t ld_kv,
                                                                  int64_t N, int T, int d, int32_t *result,
                                                                  const int32_t *path) {
-    extern __shared__ __align__(16) uint4 rows[];  // [L][d / 8]
-    __shared__ int32_t s_path[CM_MAX_T];
+    extern __shared__ __align__(16) uint4 rows[];  // [CM_ROUND][d / 8]
+    __shared__ int32_t s_path[TS_MAX_T];
     __shared__ int s_L, s_ok;
     const int g = blockIdx.x, tid = threadIdx.x;
     __nv_bfloat16 *base = (blockIdx.y == 0 ? k : v) + ((size_t)g * ld_kv + (size_t)N) * d;
@@ -48,21 +52,25 @@ __global__ void __launch_bounds__(CM_THREADS) commit_path_kernel(__nv_bfloat16 *
         return;
     }
     const int U = d / 8;  // 16-byte units per row
-    for (int e = tid; e < L * U; e += CM_THREADS) {
-        const int i = e / U, u = e % U;
-        rows[e] = reinterpret_cast<const uint4 *>(base + (size_t)s_path[i] * d)[u];
-    }
-    __syncthreads();
-    for (int e = tid; e < L * U; e += CM_THREADS) {
-        const int i = e / U, u = e % U;
-        reinterpret_cast<uint4 *>(base + (size_t)i * d)[u] = rows[e];
+    for (int r0 = 0; r0 < L; r0 += CM_ROUND) {
+        const int nr = L - r0 < CM_ROUND ? L - r0 : CM_ROUND;
+        for (int e = tid; e < nr * U; e += CM_THREADS) {
+            const int i = e / U, u = e % U;
+            rows[e] = reinterpret_cast<const uint4 *>(base + (size_t)s_path[r0 + i] * d)[u];
+        }
+        __syncthreads();
+        for (int e = tid; e < nr * U; e += CM_THREADS) {
+            const int i = e / U, u = e % U;
+            reinterpret_cast<uint4 *>(base + (size_t)(r0 + i) * d)[u] = rows[e];
+        }
+        __syncthreads();
     }
 }
 
 cudaError_t launch_commit_path(__nv_bfloat16 *k, __nv_bfloat16 *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d,
                                int32_t *result, const int32_t *path, cudaStream_t st) {
     if (injected_launch_failure()) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)T * d * 2;  // at most T rows staged
+    const size_t smem = (size_t)(T < CM_ROUND ? T : CM_ROUND) * d * 2;  // rows staged per round
     cudaError_t e = cudaFuncSetAttribute(commit_path_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     commit_path_kernel<<<dim3(Hkv, 2), CM_THREADS, smem, st>>>(k, v, ld_kv, N, T, d, result, path);

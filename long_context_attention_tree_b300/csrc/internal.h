@@ -11,6 +11,8 @@
 
 namespace ts {
 
+constexpr int TS_MAX_T = 1024;  // largest speculative batch (rows) any call takes
+
 // Counts every kernel launch the library enqueues (diagnostic).
 void note_launches(int n);
 
@@ -30,7 +32,8 @@ struct AttnArgs {
     int64_t N;
     int T, Hq, Hkv, G, d;
     float scale_log2;  // softmax scale * log2(e)
-    const uint64_t *mask;
+    const uint64_t *mask;       // uint64 [T][mw]
+    int mw;                     // mask words per row: max(2, ceil(T / 64))
     const int32_t *prefix_len;  // nullable: KV head g sees prefix rows [0, min(prefix_len[g], N))
     __nv_bfloat16 *out;
     float *lse;

@@ -16,6 +16,7 @@
 
 #include "../../include/ts.h"
 #include "internal.h"
+#include "ts_common.cuh"
 
 namespace {
 
@@ -132,7 +133,7 @@ ts_status check_attn_shape(int T, int Hq, int Hkv, int d, int64_t N) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
         return fail(TS_ERR_INVALID_ARG, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
     if (Hq / Hkv > 32) return fail(TS_ERR_UNSUPPORTED, "group size Hq/Hkv=%d > 32", Hq / Hkv);
-    if (T < 0 || T > 128) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [0, 128]", T);
+    if (T < 0 || T > ts::TS_MAX_T) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [0, %d]", T, ts::TS_MAX_T);
     if (N < 0) return fail(TS_ERR_INVALID_ARG, "N=%lld < 0", (long long)N);
     if (N > (int64_t)1 << 30) return fail(TS_ERR_UNSUPPORTED, "N=%lld too large", (long long)N);
     return TS_OK;
@@ -159,24 +160,22 @@ const char *ts_last_error(void) { return g_last_error.c_str(); }
 
 const char *ts_version(void) { return "ts 0.1 (sm_103a)"; }
 
+int ts_tree_mask_words(int T) { return T < 0 ? 0 : ts::mask_words(T); }
+
 ts_status ts_tree_mask_from_parents(const int32_t *parent_host, int T, uint64_t *mask_host) {
-    if (T < 0 || T > 128) return fail(TS_ERR_INVALID_ARG, "T=%d outside [0, 128]", T);
+    if (T < 0 || T > ts::TS_MAX_T) return fail(TS_ERR_INVALID_ARG, "T=%d outside [0, %d]", T, ts::TS_MAX_T);
     if (T > 0 && (parent_host == nullptr || mask_host == nullptr))
         return fail(TS_ERR_INVALID_ARG, "null parent or mask pointer");
     for (int i = 0; i < T; ++i)
         if (parent_host[i] < -1 || parent_host[i] >= i)
             return fail(TS_ERR_INVALID_ARG, "parent[%d]=%d must satisfy -1 <= parent[i] < i", i, parent_host[i]);
+    const int mw = ts::mask_words(T);
     for (int i = 0; i < T; ++i) {
         // a row's ancestors are its parent's ancestors plus the parent itself
-        uint64_t w0 = 0, w1 = 0;
+        uint64_t *row = mask_host + (size_t)mw * i;
         const int p = parent_host[i];
-        if (p >= 0) {
-            w0 = mask_host[2 * p];
-            w1 = mask_host[2 * p + 1];
-        }
-        if (i < 64) w0 |= 1ull << i; else w1 |= 1ull << (i - 64);
-        mask_host[2 * i] = w0;
-        mask_host[2 * i + 1] = w1;
+        for (int w = 0; w < mw; ++w) row[w] = p >= 0 ? mask_host[(size_t)mw * p + w] : 0;
+        row[i >> 6] |= 1ull << (i & 63);
     }
     return TS_OK;
 }
@@ -250,6 +249,7 @@ static ts_status tree_attn_impl(const void *q, const void *k, const void *v, int
     a.d = d;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.mask = mask;
+    a.mw = ts::mask_words(T);
     a.prefix_len = prefix_len;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
@@ -529,7 +529,7 @@ ts_status ts_ngram_topk(const void *table, int64_t capacity, const int32_t *seq,
 
 ts_status ts_commit_path(void *k, void *v, int64_t ld_kv, int64_t N, int T, int Hkv, int d, int32_t *result,
                          const int32_t *path, ts_stream_t stream) {
-    if (T < 1 || T > 128) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [1, 128]", T);
+    if (T < 1 || T > ts::TS_MAX_T) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [1, %d]", T, ts::TS_MAX_T);
     if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
     if (Hkv <= 0) return fail(TS_ERR_INVALID_ARG, "Hkv=%d", Hkv);
     if (N < 0) return fail(TS_ERR_INVALID_ARG, "N=%lld < 0", (long long)N);

@@ -39,9 +39,12 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Row visibility of batch token u for batch row t (mask is uint64 [T][2]).
-__device__ __forceinline__ bool mask_bit(const uint64_t *mask, int t, int u) {
-    return (mask[2 * t + (u >> 6)] >> (u & 63)) & 1ull;
+// 64-bit words per row of a batch mask: uint64 [T][mask_words(T)], at least 2.
+__host__ __device__ __forceinline__ int mask_words(int T) { return T > 128 ? (T + 63) / 64 : 2; }
+
+// Row visibility of batch token u for batch row t (mask is uint64 [T][mw]).
+__device__ __forceinline__ bool mask_bit(const uint64_t *mask, int mw, int t, int u) {
+    return (mask[(size_t)mw * t + (u >> 6)] >> (u & 63)) & 1ull;
 }
 
 }  // namespace ts

@@ -39,17 +39,20 @@ def test_library_exports_every_declared_symbol():
 @pytest.mark.parametrize("parent", [
     W.verify_parents(), W.tree_parents([1, 3, 3, 3]), W.tree_parents([3, 3, 3, 3]),
     W.chain_parents(32, 4), [-1] * 128, [-1] + list(range(127)), [],
+    W.verify_parents((1, 9, 9, 9)), W.verify_parents((3, 3, 3, 3)), [-1] + list(range(1023)), [-1] * 129,
 ])
 def test_mask_matches_oracle_visibility(parent):
     mask = ts.ts_tree_mask_from_parents(parent)
     T = len(parent)
     if T == 0:
         return
+    mw = max(2, (T + 63) // 64)
+    assert mask.shape == (T, mw)
     vis = oracle.visible(parent)
-    for i in range(T):
+    for i in range(0, T, max(1, T // 97)):
         bits = [(int(mask[i, u // 64]) >> (u % 64)) & 1 for u in range(T)]
         assert bits == vis[i].astype(int).tolist()
-        assert all(((int(mask[i, u // 64]) >> (u % 64)) & 1) == 0 for u in range(T, 128))
+        assert all(((int(mask[i, u // 64]) >> (u % 64)) & 1) == 0 for u in range(T, 64 * mw))
 
 
 @pytest.mark.parametrize("parent", [[-1, 1], [0], [-1, -2], [-1, 0, 5]])
@@ -61,7 +64,9 @@ def test_mask_rejects_bad_parents(parent):
 
 def test_mask_rejects_too_many_rows():
     with pytest.raises(ts.TSError):
-        ts.ts_tree_mask_from_parents([-1] * 129)
+        ts.ts_tree_mask_from_parents([-1] * 1025)
+    assert ts.lib().ts_tree_mask_words(128) == 2 and ts.lib().ts_tree_mask_words(129) == 3
+    assert ts.lib().ts_tree_mask_words(820) == 13 and ts.lib().ts_tree_mask_words(1) == 2
 
 
 def _attn(**kw):
@@ -80,7 +85,7 @@ def _attn(**kw):
     (dict(d=96), ts.TS_ERR_UNSUPPORTED),
     (dict(Hq=6, Hkv=4), ts.TS_ERR_INVALID_ARG),
     (dict(Hq=66, Hkv=1), ts.TS_ERR_UNSUPPORTED),
-    (dict(T=129), ts.TS_ERR_UNSUPPORTED),
+    (dict(T=1025, ld=6000), ts.TS_ERR_UNSUPPORTED),
     (dict(N=-1), ts.TS_ERR_INVALID_ARG),
     (dict(q=None), ts.TS_ERR_INVALID_ARG),
     (dict(mask=None), ts.TS_ERR_INVALID_ARG),
@@ -205,7 +210,7 @@ def test_product_does_not_import_oracle():
 
 @pytest.mark.parametrize("kw,status", [
     (dict(T=0), ts.TS_ERR_UNSUPPORTED),
-    (dict(T=129), ts.TS_ERR_UNSUPPORTED),
+    (dict(T=1025, ld=6000), ts.TS_ERR_UNSUPPORTED),
     (dict(d=96), ts.TS_ERR_UNSUPPORTED),
     (dict(Hkv=0), ts.TS_ERR_INVALID_ARG),
     (dict(N=-1), ts.TS_ERR_INVALID_ARG),

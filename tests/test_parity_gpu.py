@@ -100,6 +100,39 @@ def test_tree_attn_matches_oracle(case):
     check_attn(out, lse, ro, rl, str(case))
 
 
+@pytest.mark.parametrize("branching,chains,Hq,Hkv,d,N", [
+    ((3, 3, 3, 3), 20, 40, 8, 128, 3000),   # 200 rows, GQA group 5
+    ((1, 9, 9, 9), 0, 8, 2, 128, 1500),     # 820 rows, group 4
+    ((1, 9, 9, 9), 20, 10, 2, 128, 701),    # 900 rows, group 5
+    ((3, 3, 3, 3), 20, 8, 8, 128, 2000),    # 200 rows, MHA
+    ((1, 9, 9, 9), 20, 4, 1, 64, 500),      # 900 rows, head dim 64 (CUDA cores)
+])
+def test_wide_trees_beyond_128_rows(branching, chains, Hq, Hkv, d, N):
+    """The tree ablations of the pages ([3,3,3,3], [1,9,9,9]) with and without
+    the n-gram chains: multi-word masks, many M-tiles per KV head."""
+    parent = W.verify_parents(branching, chains)
+    T = len(parent)
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=T + N, device="cuda", value_kind="normal", ld_extra=2)
+    scale = 1 / math.sqrt(d)
+    out, lse, sc = run_attn(q, k, v, N, parent, scale, scores=True, score_row=T - 1)
+    assert ts.ts_tree_attn_uses_tensor_cores(T, Hq, Hkv, d, N) == (d == 128)
+    ro, rl = oracle.tree_attn(q.cpu(), k.cpu(), v.cpu(), N, parent, scale)
+    check_attn(out, lse, ro, rl, f"T{T}")
+    rs = oracle.score_chunks(q[T - 1].cpu(), k.cpu(), N)
+    np.testing.assert_allclose(sc.cpu().numpy(), rs, rtol=1e-4, atol=1e-2)
+
+
+def test_wide_tree_cuda_core_path_matches(monkeypatch):
+    monkeypatch.setenv("TS_FORCE_SIMT", "1")
+    parent = W.verify_parents((1, 9, 9, 9), 20)
+    T, Hq, Hkv, d, N = len(parent), 10, 2, 128, 333
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=4, device="cuda")
+    out, lse, sc = run_attn(q, k, v, N, parent, 1 / math.sqrt(d), scores=True, score_row=5)
+    ro, rl = oracle.tree_attn(q.cpu(), k.cpu(), v.cpu(), N, parent, 1 / math.sqrt(d))
+    check_attn(out, lse, ro, rl)
+    np.testing.assert_array_equal(sc.cpu().numpy(), oracle.score_chunks(q[5].cpu(), k.cpu(), N).astype(np.float32))
+
+
 def test_tensor_core_path_is_selected_and_status_clean():
     assert ts.ts_tree_attn_uses_tensor_cores(120, 32, 8, 128, 20480)
     assert ts.ts_tree_attn_uses_tensor_cores(64, 40, 8, 128, 1)
@@ -471,9 +504,12 @@ def _ancestors(parent, row):
 
 
 @pytest.mark.parametrize("Hkv,d,N,T,seed", [(8, 128, 20480, 120, 0), (2, 64, 4096, 40, 1), (32, 128, 1000, 64, 2),
-                                            (1, 128, 0, 1, 3)])
+                                            (1, 128, 0, 1, 3), (8, 128, 2048, 900, 4), (2, 64, 100, 300, 5)])
 def test_commit_path_bit_exact(Hkv, d, N, T, seed):
-    parent = verify_parent(T)
+    """Includes a 900-row batch of the [1,9,9,9] tree and a 300-row chain whose
+    accepted path (300 rows) is moved in several shared-memory rounds."""
+    parent = verify_parent(T) if T <= 120 else (W.verify_parents((1, 9, 9, 9), 20) if T == 900
+                                                else [-1] + list(range(T - 1)))
     _, k, v = W.make_qkv(T, Hkv, Hkv, d, N, seed=500 + seed, device="cuda", value_kind="normal", ld_extra=3)
     rng = np.random.default_rng(seed)
     for best in list(rng.choice(T, size=min(T, 4), replace=False)) + [T - 1]:
