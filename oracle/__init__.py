@@ -56,6 +56,8 @@ def _load():
         lib.oracle_select.argtypes = [P, i32, i32, i32, P]
         lib.oracle_gather.argtypes = [P, i32, i32, i32, i64, P, i64, i32, P, i64, P]
         lib.oracle_penalty_minp.argtypes = [P, i32, i32, P, i32, flt, flt, dbl, P, P, P]
+        lib.oracle_penalty_minp_path.argtypes = [P, i32, i32, P, i32, P, P, flt, flt, dbl, P, P, P]
+        lib.oracle_select_kept.argtypes = [P, i32, i32, i32, i32, i32, P]
         lib.oracle_accept.argtypes = [P, P, P, i32, i32, P, P]
         lib.oracle_accept_ex.argtypes = [P, P, P, i32, i32, i32, ctypes.c_uint64, ctypes.c_uint64, P, P]
         lib.oracle_commit.argtypes = [P, i64, i64, i32, i32, i32, P, P, P]
@@ -137,14 +139,15 @@ def score_chunks(q_row, k, N: int, chunk: int = 64) -> np.ndarray:
     return out
 
 
-def select(scores_f32, k: int) -> np.ndarray:
+def select(scores_f32, k: int, sink: int = 0, recent: int = 0) -> np.ndarray:
     """int32 [Hkv][min(k, nc)]: top-k by (score desc, index asc), returned ascending.
-    The decision is taken on fp32 scores (the kernel's precision)."""
+    The decision is taken on fp32 scores (the kernel's precision).  The first
+    `sink` and last `recent` chunks are always kept (sink + recent <= k)."""
     s = np.ascontiguousarray(np.asarray(scores_f32, dtype=np.float32))
     Hkv, nc = s.shape
     kk = min(k, nc)
     sel = np.zeros((Hkv, kk), dtype=np.int32)
-    rc = _load().oracle_select(_ptr(s), Hkv, nc, k, _ptr(sel))
+    rc = _load().oracle_select_kept(_ptr(s), Hkv, nc, k, int(sink), int(recent), _ptr(sel))
     if rc:
         raise ValueError(f"oracle_select failed ({rc})")
     return sel
@@ -174,17 +177,23 @@ def log_min_p(min_p: float) -> float:
     return -math.inf if mp <= 0.0 else math.log(mp)
 
 
-def penalty_minp(logits, history, theta: float, min_p: float, temperature: float, return_logits=False):
-    """(target int32 [T], kept int32 [T][, final fp32 logits]) for fp32 logits [T][V]."""
+def penalty_minp(logits, history, theta: float, min_p: float, temperature: float, return_logits=False,
+                 path_parent=None, path_draft=None):
+    """(target int32 [T], kept int32 [T][, final fp32 logits]) for fp32 logits [T][V].
+    With path_parent / path_draft, each row's window is the last W tokens of
+    history followed by the drafts on its path (root .. the row)."""
     lg = np.ascontiguousarray(np.asarray(logits, dtype=np.float32))
     T, V = lg.shape
     h = np.ascontiguousarray(np.asarray(history, dtype=np.int32))
     target = np.zeros(T, dtype=np.int32)
     kept = np.zeros(T, dtype=np.int32)
     pen = np.zeros((T, V), dtype=np.float32) if return_logits else None
-    rc = _load().oracle_penalty_minp(_ptr(lg), T, V, _ptr(h), h.size, float(theta), float(temperature),
-                                     log_min_p(min_p), _ptr(target), _ptr(kept),
-                                     _ptr(pen) if pen is not None else None)
+    pp = None if path_parent is None else np.ascontiguousarray(np.asarray(path_parent, dtype=np.int32))
+    pd = None if path_draft is None else np.ascontiguousarray(np.asarray(path_draft, dtype=np.int32))
+    rc = _load().oracle_penalty_minp_path(_ptr(lg), T, V, _ptr(h), h.size, _ptr(pp) if pp is not None else None,
+                                          _ptr(pd) if pd is not None else None, float(theta), float(temperature),
+                                          log_min_p(min_p), _ptr(target), _ptr(kept),
+                                          _ptr(pen) if pen is not None else None)
     if rc:
         raise ValueError(f"oracle_penalty_minp failed ({rc})")
     return (target, kept, pen) if return_logits else (target, kept)

@@ -215,24 +215,45 @@ static int ascending(const void *a, const void *b)
     return (ia > ib) - (ia < ib);
 }
 
-int oracle_select(const float *scores, int Hkv, int nc, int k, int32_t *sel)
+/* Always-kept chunks (the SnapKV / TriForce lineage the summary's related   */
+/* work names: attention sinks at the start, a recent window at the end):    */
+/* with n_sink, n_recent > 0 the chunks [0, n_sink) and [nc - n_recent, nc)  */
+/* are selected first, and the rest of the k by score among the others.      */
+/* Requires n_sink + n_recent <= k.                                          */
+static int g_nc_forced, g_n_sink, g_n_recent;
+static int forced(int c) { return c < g_n_sink || c >= g_nc_forced - g_n_recent; }
+static int forced_then_score_then_index(const void *a, const void *b)
 {
-    if (Hkv <= 0 || nc < 0 || k < 0) return 2;
+    int ia = *(const int *)a, ib = *(const int *)b;
+    int fa = forced(ia), fb = forced(ib);
+    if (fa != fb) return fa ? -1 : 1;
+    return by_score_then_index(a, b);
+}
+
+int oracle_select_kept(const float *scores, int Hkv, int nc, int k, int n_sink, int n_recent, int32_t *sel)
+{
+    if (Hkv <= 0 || nc < 0 || k < 0 || n_sink < 0 || n_recent < 0 || n_sink + n_recent > k) return 2;
     if (k > nc) k = nc;
     int *idx = (int *)malloc(sizeof(int) * (size_t)(nc > 0 ? nc : 1));
     if (!idx) return 2;
+    g_nc_forced = nc; g_n_sink = n_sink; g_n_recent = n_recent;
     for (int g = 0; g < Hkv; ++g) {
         for (int c = 0; c < nc; ++c) {
             if (scores[(size_t)g * nc + c] != scores[(size_t)g * nc + c]) { free(idx); return 3; }
             idx[c] = c;
         }
         g_sort_keys = scores + (size_t)g * nc;
-        qsort(idx, (size_t)nc, sizeof(int), by_score_then_index);
+        qsort(idx, (size_t)nc, sizeof(int), forced_then_score_then_index);
         qsort(idx, (size_t)k, sizeof(int), ascending);
         for (int i = 0; i < k; ++i) sel[(size_t)g * k + i] = idx[i];
     }
     free(idx);
     return 0;
+}
+
+int oracle_select(const float *scores, int Hkv, int nc, int k, int32_t *sel)
+{
+    return oracle_select_kept(scores, Hkv, nc, k, 0, 0, sel);
 }
 
 /* Gather the selected chunks into a compact cache (byte copy).            */
@@ -277,9 +298,17 @@ int oracle_gather(const int32_t *sel, int Hkv, int k, int chunk, int64_t N,
 /*   pen_out (nullable): the final fp32 logits.                             */
 /* Returns 0, or 4 for a history id outside [0, V).                        */
 /* ---------------------------------------------------------------------- */
-int oracle_penalty_minp(const float *logits, int T, int V, const int32_t *history, int W,
-                        float theta, float temperature, double log_min_p,
-                        int32_t *target, int32_t *kept, float *pen_out)
+/* Path-aware window (path_parent and path_draft given): the logits of row i */
+/* follow the drafts on its path root..i (depth d_i tokens), so its window is */
+/* the last W tokens of history ++ (draft of the root, ..., draft[i]):        */
+/* history[min(d_i, W) .. W) and the last min(d_i, W) drafts of the path     */
+/* (a draft outside [0, V), such as an unused n-gram row's -1, is no token   */
+/* and adds nothing).                                                        */
+/* Returns 0, 4 for a history id outside [0, V), 1 for a bad parent array.   */
+int oracle_penalty_minp_path(const float *logits, int T, int V, const int32_t *history, int W,
+                             const int32_t *path_parent, const int32_t *path_draft,
+                             float theta, float temperature, double log_min_p,
+                             int32_t *target, int32_t *kept, float *pen_out)
 {
     uint8_t *inwin = (uint8_t *)calloc((size_t)(V > 0 ? V : 1), 1);
     if (!inwin) return 2;
@@ -287,14 +316,38 @@ int oracle_penalty_minp(const float *logits, int T, int V, const int32_t *histor
         if (history[w] < 0 || history[w] >= V) { free(inwin); return 4; }
         inwin[history[w]] = 1;
     }
+    if (path_parent) {
+        for (int i = 0; i < T; ++i)
+            if (path_parent[i] < -1 || path_parent[i] >= i) { free(inwin); return 1; }
+    }
+    int err = 0;
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < T; ++i) {
         float *row = (float *)malloc(sizeof(float) * (size_t)(V > 0 ? V : 1));
+        uint8_t *mine = NULL;  /* this row's window, when it differs by path */
+        if (path_parent) {
+            mine = (uint8_t *)calloc((size_t)(V > 0 ? V : 1), 1);
+            int depth = 0;
+            for (int j = i; j >= 0; j = path_parent[j]) ++depth;
+            int take = depth < W ? depth : W;   /* path drafts in the window */
+            for (int w = take; w < W; ++w) mine[history[w]] = 1;
+            int pos = depth;                     /* 1-based position of j on the path */
+            for (int j = i; j >= 0; j = path_parent[j], --pos)
+                if (pos > depth - take && path_draft[j] >= 0 && path_draft[j] < V) mine[path_draft[j]] = 1;
+        }
+        const uint8_t *win = mine ? mine : inwin;
+        if (!row || (path_parent && !mine)) {
+#pragma omp atomic write
+            err = 2;
+            free(row);
+            free(mine);
+            continue;
+        }
         float m = -INFINITY;
         int arg = -1;
         for (int vv = 0; vv < V; ++vv) {
             float l = logits[(size_t)i * V + vv];
-            if (inwin[vv]) {
+            if (win[vv]) {
                 if (l > 0.0f) l = (float)((double)l / (double)theta);
                 else          l = (float)((double)l * (double)theta);
             }
@@ -310,9 +363,18 @@ int oracle_penalty_minp(const float *logits, int T, int V, const int32_t *histor
         kept[i] = cnt;
         if (pen_out) memcpy(pen_out + (size_t)i * V, row, sizeof(float) * (size_t)V);
         free(row);
+        free(mine);
     }
     free(inwin);
-    return 0;
+    return err;
+}
+
+int oracle_penalty_minp(const float *logits, int T, int V, const int32_t *history, int W,
+                        float theta, float temperature, double log_min_p,
+                        int32_t *target, int32_t *kept, float *pen_out)
+{
+    return oracle_penalty_minp_path(logits, T, V, history, W, NULL, NULL, theta, temperature, log_min_p, target,
+                                    kept, pen_out);
 }
 
 /* ---------------------------------------------------------------------- */

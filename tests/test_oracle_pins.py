@@ -310,6 +310,27 @@ def test_select_hand_cases():
     np.testing.assert_array_equal(oracle.select(z2, 2)[0], [0, 2])
 
 
+def test_select_keeps_sink_and_recent_chunks():
+    """Always-kept first / last chunks: equal to a lexsort in which those
+    chunks score +inf; and a hand case."""
+    rng = np.random.default_rng(7)
+    s = rng.integers(-5, 6, size=(3, 200)).astype(np.float32)
+    for sink, recent, k in ((1, 1, 16), (2, 3, 16), (0, 4, 4), (3, 0, 10), (5, 5, 10)):
+        sel = oracle.select(s, k, sink=sink, recent=recent)
+        for g in range(3):
+            f = s[g].astype(np.float64).copy()
+            f[:sink] = np.inf
+            if recent:
+                f[200 - recent:] = np.inf
+            order = np.lexsort((np.arange(200), -f))[:k]
+            np.testing.assert_array_equal(sel[g], np.sort(order))
+    h = np.array([[5, 5, 3, 5, 1]], dtype=np.float32)
+    np.testing.assert_array_equal(oracle.select(h, 3, sink=1, recent=1)[0], [0, 1, 4])
+    np.testing.assert_array_equal(oracle.select(h, 2, sink=0, recent=2)[0], [3, 4])
+    with pytest.raises(ValueError):
+        oracle.select(h, 2, sink=2, recent=1)
+
+
 # ---------------------------------------------------------------- gather
 def test_gather_identity_when_budget_covers_cache():
     Hkv, d, N = 2, 64, 192
@@ -397,6 +418,57 @@ def test_minp_count_matches_softmax_definition():
         assert not np.any(np.abs(ratio - np.float32(0.1)) < 1e-9)   # no boundary case
         assert kp[i] == int((ratio >= np.float64(np.float32(0.1))).sum())
         assert t[i] == int(np.argmax(pen[i]))
+
+
+def _path_window_brute(logits, history, parent, draft, theta, min_p, temp):
+    """Each row's window built as an explicit token list, the penalty in numpy fp32."""
+    T, V = logits.shape
+    W_ = len(history)
+    out = logits.astype(np.float32).copy()
+    for i in range(T):
+        path = []
+        j = i
+        while j >= 0:
+            path.append(int(draft[j]))
+            j = parent[j]
+        ctx = list(history) + path[::-1]
+        win = {t for t in (ctx[-W_:] if W_ else []) if 0 <= t < V}
+        for t in win:
+            x = out[i, t]
+            out[i, t] = x / np.float32(theta) if x > 0 else x * np.float32(theta)
+        out[i] = out[i] / np.float32(temp)
+    m = out.max(axis=1)
+    thr = m.astype(np.float64) + math.log(float(np.float32(min_p)))
+    kept = (out.astype(np.float64) >= thr[:, None]).sum(axis=1)
+    return out.argmax(axis=1), kept, out
+
+
+def test_path_window_hand_example():
+    """history [0 1 2], W = 3; tree 0 <- {1, 2} with drafts 3, 4, 5: row 0's
+    window is {1, 2, 3}, row 1's {2, 3, 4}, row 2's {2, 3, 5}."""
+    logits = np.full((3, 6), 1.0, dtype=np.float32)
+    t, _, pen = oracle.penalty_minp(logits, np.array([0, 1, 2], np.int32), 2.0, 0.1, 1.0, return_logits=True,
+                                    path_parent=[-1, 0, 0], path_draft=[3, 4, 5])
+    np.testing.assert_array_equal(pen, np.array([[1, .5, .5, .5, 1, 1], [1, 1, .5, .5, .5, 1],
+                                                 [1, 1, .5, .5, 1, .5]], dtype=np.float32))
+    np.testing.assert_array_equal(t, [0, 0, 0])
+
+
+@pytest.mark.parametrize("seed,W_", [(0, 16), (1, 3), (2, 0), (3, 64)])
+def test_path_window_matches_explicit_windows(seed, W_):
+    rng = np.random.default_rng(seed)
+    parent = W.verify_parents((1, 3, 3, 3), 5)
+    T, V = len(parent), 40
+    logits = (rng.standard_normal((T, V)) * 3).astype(np.float32)
+    history = rng.integers(0, V, W_).astype(np.int32)
+    draft = rng.integers(0, V, T).astype(np.int32)
+    draft[-3] = -1   # an unused n-gram row adds no token
+    t, kp, pen = oracle.penalty_minp(logits, history, 1.2, 0.1, 1.0, return_logits=True, path_parent=parent,
+                                     path_draft=draft)
+    bt, bk, bpen = _path_window_brute(logits, history.tolist(), parent, draft, 1.2, 0.1, 1.0)
+    np.testing.assert_array_equal(pen, bpen)
+    np.testing.assert_array_equal(t, bt)
+    np.testing.assert_array_equal(kp, bk)
 
 
 def test_penalty_empty_window_is_plain_argmax():
