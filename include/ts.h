@@ -262,6 +262,11 @@ ts_status ts_rescore_tail(const float *scores_old, int64_t N_old, const void *q_
  *   of head g are the rows [0, part_len[g]).
  *   The call takes N rather than the chunk count because the length of the
  *   last chunk matters.
+ *   sink_chunks, recent_chunks: the first sink_chunks and the last
+ *   recent_chunks chunks are always kept (attention sinks and the recent
+ *   window of the SnapKV / TriForce line of work the ICML 2025 summary builds
+ *   on); the rest of the k go by score.  0, 0 is pure top-k; their sum must
+ *   not exceed budget_tokens / chunk.
  *   scores  fp32 [Hkv][ceil(N/chunk)], finite
  *   k, v    bf16 [Hkv][ld_kv][d], ld_kv >= N
  *   sel     int32 [Hkv][k]
@@ -273,7 +278,7 @@ ts_status ts_rescore_tail(const float *scores_old, int64_t N_old, const void *q_
  * ceil(N/chunk) <= 16384.
  */
 ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
-                           const void *k, const void *v, int64_t ld_kv, int d,
+                           int sink_chunks, int recent_chunks, const void *k, const void *v, int64_t ld_kv, int d,
                            int32_t *sel, int32_t *part_len, void *k_part, void *v_part, int64_t ld_part,
                            ts_stream_t stream);
 
@@ -305,6 +310,26 @@ ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_
                                  const int32_t *draft, const int32_t *parent, int32_t anchor,
                                  int32_t *target, int32_t *kept, int32_t *result, int32_t *path,
                                  void *workspace, size_t ws_bytes, ts_stream_t stream);
+
+/*
+ * The vocabulary step with options; ts_penalty_minp_verify is flags = 0 and
+ * ts_penalty_minp_sample_verify is flags = TS_VOCAB_SAMPLE.
+ *   TS_VOCAB_SAMPLE       min-p sampled targets and a uniformly drawn longest
+ *                         path, from (seed, offset), as described below.
+ *   TS_VOCAB_PATH_WINDOW  row i's logits follow the drafts on its path, so its
+ *                         penalty window is the last W tokens of
+ *                         history ++ (draft of the root, ..., draft[i]):
+ *                         history[min(d_i, W)..W) plus the path's last
+ *                         min(d_i, W) drafts, d_i = depth of row i (roots 1);
+ *                         draft ids outside [0, V) (e.g. -1 of an unused
+ *                         n-gram row) add nothing.
+ */
+#define TS_VOCAB_SAMPLE 1u
+#define TS_VOCAB_PATH_WINDOW 2u
+ts_status ts_vocab_verify(const float *logits, int T, int V, const int32_t *history, int W, float theta, float min_p,
+                          float temperature, unsigned flags, uint64_t seed, uint64_t offset, const int32_t *draft,
+                          const int32_t *parent, int32_t anchor, int32_t *target, int32_t *kept, int32_t *result,
+                          int32_t *path, ts_stream_t stream);
 
 /*
  * The same step with sampled targets (model card: --min_p 0.1 with

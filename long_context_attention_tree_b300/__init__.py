@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libts.so")
 
 TS_NOALLOC_SCRATCH_BYTES = 64 << 20
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT, TS_ERR_DATA = range(6)
+TS_VOCAB_SAMPLE, TS_VOCAB_PATH_WINDOW = 1, 2
 _STATUS = {0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_UNSUPPORTED", 3: "TS_ERR_CUDA",
            4: "TS_ERR_TIMEOUT", 5: "TS_ERR_DATA"}
 
@@ -29,7 +30,7 @@ __all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree
            "ts_selftest_fail_launches", "ts_tree_attn",
            "ts_tree_attn_partial", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_rescore_tail",
            "ts_select_gather", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path",
-           "ts_ngram_table_bytes", "ts_ngram_reset", "ts_ngram_update", "ts_ngram_topk"]
+           "ts_ngram_table_bytes", "ts_ngram_reset", "ts_ngram_update", "ts_ngram_topk", "ts_vocab_verify"]
 
 
 class TSError(RuntimeError):
@@ -71,7 +72,9 @@ def lib() -> ctypes.CDLL:
         L.ts_tree_attn_noalloc.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P]
         L.ts_score_chunks.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P, P]
         L.ts_rescore_tail.argtypes = [P, i64, P, P, i64, i64, i32, i32, i32, i32, P, P]
-        L.ts_select_gather.argtypes = [P, i32, i64, i32, i32, P, P, i64, i32, P, P, P, P, i64, P]
+        L.ts_select_gather.argtypes = [P, i32, i64, i32, i32, i32, i32, P, P, i64, i32, P, P, P, P, i64, P]
+        L.ts_vocab_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, ctypes.c_uint, ctypes.c_uint64,
+                                      ctypes.c_uint64, P, P, ctypes.c_int32, P, P, P, P, P]
         L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
                                              P, P, P, P, P, sz, P]
         L.ts_commit_path.argtypes = [P, P, i64, i64, i32, i32, i32, P, P, P]
@@ -86,7 +89,7 @@ def lib() -> ctypes.CDLL:
         for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_partial", "ts_tree_attn_noalloc",
                      "ts_score_chunks", "ts_rescore_tail", "ts_select_gather", "ts_penalty_minp_verify",
                      "ts_commit_path", "ts_penalty_minp_sample_verify", "ts_ngram_reset", "ts_ngram_update",
-                     "ts_ngram_topk"):
+                     "ts_ngram_topk", "ts_vocab_verify"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -216,12 +219,12 @@ def ts_rescore_tail(scores_old, N_old: int, q_row, k, N_new: int, scores_new, ch
 
 
 def ts_select_gather(scores, N: int, budget_tokens: int, k, v, sel, k_part, v_part, chunk: int = 64,
-                     part_len=None, stream=None) -> None:
+                     part_len=None, sink_chunks: int = 0, recent_chunks: int = 0, stream=None) -> None:
     Hkv, ld, d = k.shape
     ld_part = k_part.shape[1]
-    _check(lib().ts_select_gather(_ptr(scores), Hkv, N, budget_tokens, chunk, _ptr(k), _ptr(v), ld, d,
-                                  _ptr(sel), _ptr(part_len), _ptr(k_part), _ptr(v_part), ld_part,
-                                  _stream(stream)))
+    _check(lib().ts_select_gather(_ptr(scores), Hkv, N, budget_tokens, chunk, int(sink_chunks), int(recent_chunks),
+                                  _ptr(k), _ptr(v), ld, d, _ptr(sel), _ptr(part_len), _ptr(k_part), _ptr(v_part),
+                                  ld_part, _stream(stream)))
 
 
 def ts_penalty_minp_verify(logits, history, theta: float, min_p: float, temperature: float, draft, parent,
@@ -272,3 +275,14 @@ def ts_ngram_topk(table, capacity: int, seq, n: int, anchor, k: int, chains, cou
     chains [k][4], counts [k], found [1] (the table holds the windows of seq[0, n))."""
     _check(lib().ts_ngram_topk(_ptr(table), int(capacity), _ptr(seq), int(n), _ptr(anchor), int(k), _ptr(chains),
                                _ptr(counts), _ptr(found), _stream(stream)))
+
+
+def ts_vocab_verify(logits, history, theta: float, min_p: float, temperature: float, flags: int, seed: int,
+                    offset: int, draft, parent, anchor: int, target, kept, result, path, stream=None) -> None:
+    """The vocab stage with options: TS_VOCAB_SAMPLE, TS_VOCAB_PATH_WINDOW."""
+    T, V = logits.shape
+    W = 0 if history is None else history.numel()
+    _check(lib().ts_vocab_verify(_ptr(logits), T, V, _ptr(history) if W else None, W, theta, min_p, temperature,
+                                 int(flags), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(draft),
+                                 _ptr(parent), int(anchor), _ptr(target), _ptr(kept), _ptr(result), _ptr(path),
+                                 _stream(stream)))

@@ -111,7 +111,8 @@ cudaError_t launch_score_chunks(const __nv_bfloat16 *q_row, const __nv_bfloat16 
 // scores_new[g][c] = scores_old[g][c] for c < c_keep (row strides nc_new / nc_old)
 cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *scores_new, int nc_new, int c_keep,
                                int Hkv, cudaStream_t st);
-cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel,
+cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel, int n_sink,
+                                 int n_recent,
                                  const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
                                  int32_t *sel, int32_t *part_len, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part,
                                  int64_t ld_part, int num_sms, cudaStream_t st);
@@ -129,6 +130,7 @@ struct VocabArgs {
     int32_t anchor;
     int32_t *target, *kept, *result, *path;
     int sample;                      // 1: target = min-p sample (Gumbel-max), 0: greedy
+    int path_window;                 // 1: each row's window ends with the drafts on its path
     unsigned long long seed, offset; // Philox4x64-10 key word 0 and counter word 2
 };
 cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st);

@@ -149,7 +149,7 @@ __device__ int block_exclusive_scan(int x, int *warp_tot, int *total) {
 
 template <int D>
 __global__ void __launch_bounds__(SG_THREADS)
-select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel,
+select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
                      const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v, int64_t ld_kv,
                      int32_t *__restrict__ sel, int32_t *__restrict__ part_len, __nv_bfloat16 *__restrict__ k_part,
                      __nv_bfloat16 *__restrict__ v_part, int64_t ld_part, int chunks_per_part) {
@@ -164,7 +164,10 @@ select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, 
 
     const int g = blockIdx.y, p = blockIdx.x, tid = threadIdx.x;
     const float *sc = scores + (size_t)g * n_chunks;
-    for (int c = tid; c < n_chunks; c += SG_THREADS) keys[c] = order_key(sc[c]);
+    // always-kept chunks (the first n_sink, the last n_recent) take the largest
+    // key, above every finite score's
+    for (int c = tid; c < n_chunks; c += SG_THREADS)
+        keys[c] = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
     for (int i = tid; i < k_sel; i += SG_THREADS) list[i] = 0;
     if (tid == 0) {
         s_prefix = 0u;
@@ -314,7 +317,8 @@ select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, 
     }
 }
 
-cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel,
+cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel, int n_sink,
+                                 int n_recent,
                                  const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
                                  int32_t *sel, int32_t *part_len, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part,
                                  int64_t ld_part, int num_sms, cudaStream_t st) {
@@ -331,13 +335,13 @@ cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_
     if (d == 128) {
         e = cudaFuncSetAttribute(select_gather_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        select_gather_kernel<128><<<grid, SG_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, k, v, ld_kv, sel,
-                                                                  part_len, k_part, v_part, ld_part, cpp);
+        select_gather_kernel<128><<<grid, SG_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, n_sink, n_recent, k, v,
+                                                                  ld_kv, sel, part_len, k_part, v_part, ld_part, cpp);
     } else {
         e = cudaFuncSetAttribute(select_gather_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        select_gather_kernel<64><<<grid, SG_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, k, v, ld_kv, sel,
-                                                                 part_len, k_part, v_part, ld_part, cpp);
+        select_gather_kernel<64><<<grid, SG_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, n_sink, n_recent, k, v,
+                                                                 ld_kv, sel, part_len, k_part, v_part, ld_part, cpp);
     }
     return cudaGetLastError();
 }

@@ -379,7 +379,7 @@ ts_status ts_rescore_tail(const float *scores_old, int64_t N_old, const void *q_
 }
 
 ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
-                           const void *k, const void *v, int64_t ld_kv, int d,
+                           int sink_chunks, int recent_chunks, const void *k, const void *v, int64_t ld_kv, int d,
                            int32_t *sel, int32_t *part_len, void *k_part, void *v_part, int64_t ld_part,
                            ts_stream_t stream) {
     if (chunk != 64) return fail(TS_ERR_UNSUPPORTED, "chunk=%d (supported: 64)", chunk);
@@ -387,6 +387,8 @@ ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_t
     if (Hkv <= 0) return fail(TS_ERR_INVALID_ARG, "Hkv=%d", Hkv);
     if (N < 0 || budget_tokens < 0) return fail(TS_ERR_INVALID_ARG, "negative N or budget");
     if (budget_tokens % chunk) return fail(TS_ERR_INVALID_ARG, "budget %d not a multiple of chunk", budget_tokens);
+    if (sink_chunks < 0 || recent_chunks < 0 || (int64_t)sink_chunks + recent_chunks > budget_tokens / chunk)
+        return fail(TS_ERR_INVALID_ARG, "need sink_chunks, recent_chunks >= 0 and their sum <= budget/chunk");
     const int64_t nc = (N + chunk - 1) / chunk;
     if (nc > 16384) return fail(TS_ERR_UNSUPPORTED, "%lld chunks > 16384", (long long)nc);
     const int k_sel = (int)((int64_t)(budget_tokens / chunk) < nc ? budget_tokens / chunk : nc);
@@ -398,7 +400,8 @@ ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_t
     if (ld_kv < N) return fail(TS_ERR_INVALID_ARG, "ld_kv < N");
     if (ld_part < (int64_t)k_sel * chunk)
         return fail(TS_ERR_INVALID_ARG, "ld_part=%lld < k*chunk=%lld", (long long)ld_part, (long long)k_sel * chunk);
-    cudaError_t e = ts::launch_select_gather(scores, Hkv, N, (int)nc, k_sel, static_cast<const __nv_bfloat16 *>(k),
+    cudaError_t e = ts::launch_select_gather(scores, Hkv, N, (int)nc, k_sel, sink_chunks, recent_chunks,
+                                             static_cast<const __nv_bfloat16 *>(k),
                                              static_cast<const __nv_bfloat16 *>(v), ld_kv, d, sel, part_len,
                                              static_cast<__nv_bfloat16 *>(k_part),
                                              static_cast<__nv_bfloat16 *>(v_part), ld_part, num_sms(),
@@ -409,10 +412,12 @@ ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_t
 }
 
 static ts_status vocab_stage(const float *logits, int T, int V, const int32_t *history, int W, float theta,
-                             float min_p, float temperature, int sample, uint64_t seed, uint64_t offset,
+                             float min_p, float temperature, unsigned flags, uint64_t seed, uint64_t offset,
                              const int32_t *draft, const int32_t *parent, int32_t anchor, int32_t *target,
                              int32_t *kept, int32_t *result, int32_t *path, ts_stream_t stream) {
     if (T < 1 || T > 1024) return fail(TS_ERR_UNSUPPORTED, "T=%d outside [1, 1024]", T);
+    if (flags & ~(unsigned)(TS_VOCAB_SAMPLE | TS_VOCAB_PATH_WINDOW))
+        return fail(TS_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     if (V < 1 || V > 163840) return fail(TS_ERR_UNSUPPORTED, "V=%d outside [1, 163840]", V);
     if (W < 0) return fail(TS_ERR_INVALID_ARG, "W=%d < 0", W);
     if (!(theta > 0.f) || !isfinite(theta)) return fail(TS_ERR_INVALID_ARG, "theta must be finite and > 0");
@@ -441,7 +446,8 @@ static ts_status vocab_stage(const float *logits, int T, int V, const int32_t *h
     a.kept = kept;
     a.result = result;
     a.path = path;
-    a.sample = sample;
+    a.sample = (flags & TS_VOCAB_SAMPLE) ? 1 : 0;
+    a.path_window = (flags & TS_VOCAB_PATH_WINDOW) ? 1 : 0;
     a.seed = seed;
     a.offset = offset;
     cudaError_t e = ts::launch_vocab(a, reinterpret_cast<cudaStream_t>(stream));
@@ -459,8 +465,16 @@ ts_status ts_penalty_minp_verify(const float *logits, int T, int V, const int32_
                                  void *workspace, size_t ws_bytes, ts_stream_t stream) {
     (void)workspace;
     (void)ws_bytes;
-    return vocab_stage(logits, T, V, history, W, theta, min_p, temperature, 0, 0, 0, draft, parent, anchor, target,
+    return vocab_stage(logits, T, V, history, W, theta, min_p, temperature, 0u, 0, 0, draft, parent, anchor, target,
                        kept, result, path, stream);
+}
+
+ts_status ts_vocab_verify(const float *logits, int T, int V, const int32_t *history, int W, float theta, float min_p,
+                          float temperature, unsigned flags, uint64_t seed, uint64_t offset, const int32_t *draft,
+                          const int32_t *parent, int32_t anchor, int32_t *target, int32_t *kept, int32_t *result,
+                          int32_t *path, ts_stream_t stream) {
+    return vocab_stage(logits, T, V, history, W, theta, min_p, temperature, flags, seed, offset, draft, parent, anchor,
+                       target, kept, result, path, stream);
 }
 
 ts_status ts_penalty_minp_sample_verify(const float *logits, int T, int V, const int32_t *history, int W,
@@ -468,8 +482,8 @@ ts_status ts_penalty_minp_sample_verify(const float *logits, int T, int V, const
                                         uint64_t offset, const int32_t *draft, const int32_t *parent,
                                         int32_t anchor, int32_t *target, int32_t *kept, int32_t *result,
                                         int32_t *path, ts_stream_t stream) {
-    return vocab_stage(logits, T, V, history, W, theta, min_p, temperature, 1, seed, offset, draft, parent, anchor,
-                       target, kept, result, path, stream);
+    return vocab_stage(logits, T, V, history, W, theta, min_p, temperature, TS_VOCAB_SAMPLE, seed, offset, draft,
+                       parent, anchor, target, kept, result, path, stream);
 }
 
 static ts_status check_ngram_table(const void *table, int64_t capacity) {

@@ -112,12 +112,34 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     // window bitmap restricted to this slice (ids outside [0, V) are ignored
-    // here; the acceptance kernel reports them)
+    // here; the acceptance kernel reports them).  With the path-aware window,
+    // row i's window is the last W tokens of history ++ the drafts on its
+    // path root..i: history[min(d, W)..W) and the path's last min(d, W) drafts.
     for (int w = tid; w < VOCAB_BITMAP_WORDS; w += VOCAB_THREADS) bitmap[w] = 0u;
+    int depth = 0;
+    if (a.path_window) {
+        // the walk stops at a parent that is not below its child (a bad parent
+        // array, which the acceptance kernel reports)
+        for (int j = row; j >= 0;) {
+            ++depth;
+            const int p = a.parent[j];
+            j = (p < j && p >= -1) ? p : -1;
+        }
+    }
+    const int take = depth < a.W ? depth : a.W;  // path drafts inside the window
     __syncthreads();
-    for (int w = tid; w < a.W; w += VOCAB_THREADS) {
+    for (int w = take + tid; w < a.W; w += VOCAB_THREADS) {
         const int id = a.history[w];
         if (id >= v0 && id < v1) atomicOr(&bitmap[(id - v0) >> 5], 1u << ((id - v0) & 31));
+    }
+    if (a.path_window && tid == 0) {
+        int pos = depth;  // 1-based position of j on the path
+        for (int j = row; j >= 0 && pos > depth - take; --pos) {
+            const int id = a.draft[j];
+            if (id >= v0 && id < v1) atomicOr(&bitmap[(id - v0) >> 5], 1u << ((id - v0) & 31));
+            const int p = a.parent[j];
+            j = (p < j && p >= -1) ? p : -1;
+        }
     }
     __syncthreads();
 

@@ -117,17 +117,20 @@ def test_select_gather_rejects():
     L = ts.lib()
     P = 0x10000
     # budget not a multiple of the chunk
-    assert L.ts_select_gather(P, 8, 4096, 100, 64, P, P, 5000, 128, P, None, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_gather(P, 8, 4096, 100, 64, 0, 0, P, P, 5000, 128, P, None, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
     # partial cache too short
-    assert L.ts_select_gather(P, 8, 8192, 4096, 64, P, P, 8192, 128, P, None, P, P, 4000, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_gather(P, 8, 8192, 4096, 64, 0, 0, P, P, 8192, 128, P, None, P, P, 4000, None) == ts.TS_ERR_INVALID_ARG
     # chunk other than 64
-    assert L.ts_select_gather(P, 8, 8192, 4096, 32, P, P, 8192, 128, P, None, P, P, 4096, None) == ts.TS_ERR_UNSUPPORTED
+    assert L.ts_select_gather(P, 8, 8192, 4096, 32, 0, 0, P, P, 8192, 128, P, None, P, P, 4096, None) == ts.TS_ERR_UNSUPPORTED
     # ld_kv below N (a ragged N is accepted: the last chunk is short)
-    assert L.ts_select_gather(P, 8, 4100, 4096, 64, P, P, 4099, 128, P, None, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_gather(P, 8, 4100, 4096, 64, 0, 0, P, P, 4099, 128, P, None, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
     # misaligned part_len
-    assert L.ts_select_gather(P, 8, 4100, 4096, 64, P, P, 4100, 128, P, P + 2, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_gather(P, 8, 4100, 4096, 64, 0, 0, P, P, 4100, 128, P, P + 2, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    # always-kept chunks beyond the budget, negative counts
+    assert L.ts_select_gather(P, 8, 8192, 4096, 64, 40, 30, P, P, 8192, 128, P, None, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_gather(P, 8, 8192, 4096, 64, -1, 0, P, P, 8192, 128, P, None, P, P, 4096, None) == ts.TS_ERR_INVALID_ARG
     # more than 16384 chunks
-    assert L.ts_select_gather(P, 8, 16384 * 64 + 1, 4096, 64, P, P, 1 << 21, 128, P, None, P, P, 4096,
+    assert L.ts_select_gather(P, 8, 16384 * 64 + 1, 4096, 64, 0, 0, P, P, 1 << 21, 128, P, None, P, P, 4096,
                               None) == ts.TS_ERR_UNSUPPORTED
 
 

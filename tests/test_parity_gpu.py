@@ -311,6 +311,30 @@ def test_rescore_tail_equals_full_scoring(N_old, N_new):
         np.testing.assert_array_equal(old.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("N,sink,recent", [(102400, 1, 4), (4100, 2, 2), (20480, 0, 3), (640, 5, 5)])
+def test_select_gather_keeps_sink_and_recent_chunks(N, sink, recent):
+    Hq, Hkv, d, budget = 32, 8, 128, 4096
+    q, k, v = W.make_qkv(1, Hq, Hkv, d, N, seed=N + sink, device="cuda")
+    nc = (N + 63) // 64
+    sc = torch.empty((Hkv, nc), dtype=torch.float32, device="cuda")
+    ts.ts_score_chunks(q[0], k, N, sc)
+    kk = min(budget // 64, nc)
+    sel = torch.empty((Hkv, kk), dtype=torch.int32, device="cuda")
+    plen = torch.empty((Hkv,), dtype=torch.int32, device="cuda")
+    kp = torch.zeros((Hkv, kk * 64, d), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    ts.ts_select_gather(sc, N, budget, k, v, sel, kp, vp, part_len=plen, sink_chunks=sink, recent_chunks=recent)
+    torch.cuda.synchronize()
+    rsel = oracle.select(sc.cpu().numpy(), budget // 64, sink=sink, recent=recent)
+    np.testing.assert_array_equal(sel.cpu().numpy(), rsel)
+    rk, rl = oracle.gather(rsel, k.cpu(), N, 64, kk * 64, return_len=True)
+    assert torch.equal(kp.cpu(), rk)
+    np.testing.assert_array_equal(plen.cpu().numpy(), rl)
+    if nc > kk:
+        assert (sel[:, :sink].cpu() == torch.arange(sink, dtype=torch.int32)).all()
+        assert (sel[:, kk - recent:].cpu() == torch.arange(nc - recent, nc, dtype=torch.int32)).all()
+
+
 def test_select_ties_and_signed_zero():
     Hkv, nc = 3, 300
     rng = np.random.default_rng(1)
@@ -626,3 +650,41 @@ def test_sampled_stage_draws_among_the_longest_paths():
         assert rr[0] == 4
         seen.add(int(rr[1]))
     assert len(seen) >= 8
+
+
+# --------------------------------------------------------------------------
+# path-aware penalty window (each row's window ends with the drafts on its path)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("V,W_,sample,branching", [(152064, 1024, False, (1, 3, 3, 3)), (5000, 40, False, (1, 3, 3, 3)),
+                                                   (4096, 8, True, (3, 3, 3, 3)), (1000, 3, False, (1, 9, 9, 9))])
+def test_path_window_vocab_stage_bit_exact(V, W_, sample, branching):
+    parent = W.verify_parents(branching)
+    T = len(parent)
+    vi = W.make_vocab_inputs(parent, V, W_, seed=V + W_, device="cuda", flip_rows=0.3)
+    # drafts that sit inside the windows of their descendants: raise their logits
+    lg = vi.logits.clone()
+    dr = vi.draft.cpu().numpy()
+    for i, p in enumerate(parent):
+        if p >= 0:
+            lg[i, int(dr[p])] = lg[i].max() + 0.7
+    target = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    kept = torch.full_like(target, -7)
+    result = torch.full((4,), -7, dtype=torch.int32, device="cuda")
+    path = torch.full_like(target, -7)
+    flags = ts.TS_VOCAB_PATH_WINDOW | (ts.TS_VOCAB_SAMPLE if sample else 0)
+    ts.ts_vocab_verify(lg, vi.history, 1.2, 0.1, 1.0, flags, 31, 2, vi.draft, vi.parent, vi.anchor, target, kept,
+                       result, path)
+    torch.cuda.synchronize()
+    rt, rk, pen = oracle.penalty_minp(lg.cpu().numpy(), vi.history.cpu().numpy(), 1.2, 0.1, 1.0, return_logits=True,
+                                      path_parent=parent, path_draft=dr)
+    if sample:
+        rt = oracle.sample(pen, 0.1, 31, 2)
+    np.testing.assert_array_equal(target.cpu().numpy(), rt)
+    np.testing.assert_array_equal(kept.cpu().numpy(), rk)
+    rr, rp = oracle.accept(dr, parent, rt, vi.anchor, seed=31 if sample else None, offset=2)
+    np.testing.assert_array_equal(result.cpu().numpy(), rr)
+    np.testing.assert_array_equal(path.cpu().numpy(), rp)
+    # the path-aware window changes some targets against the shared window
+    if not sample:
+        t0, _ = oracle.penalty_minp(lg.cpu().numpy(), vi.history.cpu().numpy(), 1.2, 0.1, 1.0)
+        assert (t0 != rt).any()
