@@ -262,7 +262,8 @@ def test_partial_cache_drafting_with_a_short_last_chunk(N, Hq, Hkv, d):
     nc = (N + 63) // 64
     rng = np.random.default_rng(N)
     s = rng.integers(-50, 50, size=(Hkv, nc)).astype(np.float32)
-    s[::2, nc - 1] = 1000.0  # every other head keeps the last chunk
+    s[::2, nc - 1] = 1000.0   # every other head keeps the last chunk,
+    s[1::2, nc - 1] = -1000.0  # the others drop it
     kk = min(budget // 64, nc)
     B = kk * 64
     sel = torch.empty((Hkv, kk), dtype=torch.int32, device="cuda")
