@@ -8,18 +8,20 @@
 // in groups of four.  The range's K and V (32 KB each) are copied into
 // shared memory with 16-byte cp.async at the start, so every byte of the
 // range is in flight at once (K rows XOR-swizzled by 16-byte chunk so that
-// lanes reading different rows hit different banks).  Warp w owns rows
-// 4w..4w+3 for the whole range, so the softmax of its rows never leaves the
-// warp:
-//   S:  lane l takes tokens l, l+32, l+64, l+96 (16 scores in registers),
-//       8 dims at a time; Q sits in shared memory as [d][row][2] fp32 (each
-//       value twice), so one broadcast 16-byte read gives two rows as pairs
-//       and the products are packed fp32x2 FMAs over token pairs.
-//   softmax over the range: max and sum per row with warp shuffles; P goes
-//       to the warp's own shared-memory slab as [token][row][2].
+// lanes reading different rows hit different banks).  Two warps own each
+// group of four rows, one per 64-token half of the range, so a CTA runs
+// 2 x ceil(R/4) warps and the latencies of one warp's chain hide behind the
+// others':
+//   S:  lane l of half h takes tokens 64h + l and 64h + l + 32, 8 dims at a
+//       time; Q sits in shared memory as [d][row][2] fp32 (each value twice),
+//       so one broadcast 16-byte read gives two rows as pairs and the products
+//       are packed fp32x2 FMAs over the token pair.
+//   softmax over the range: row max per half by warp shuffles, the two halves
+//       combined through shared memory; P goes to the warp's own slab as
+//       [token][row][2]; row sums per half, added at the end.
 //   O:  lane l owns dims 4l..4l+3; per token one 8-byte V read (the warp
 //       reads the whole 256-byte row) and two broadcast reads of P feed 16
-//       FMAs.
+//       FMAs; half 1 hands its partial O to half 0 through shared memory.
 // The partial (O, m, l) of each range goes to the split workspace and the
 // log-sum-exp merge kernel combines the ranges (a single range writes the
 // normalised output directly).  The chunk importance of the scoring row can
@@ -37,16 +39,20 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return _
 }  // namespace
 
 template <int R4>
-__global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs a, int n_splits) {
+__global__ void __launch_bounds__(R4 * 64) tree_attn_small_kernel(const AttnArgs a, int n_splits) {
     constexpr int RP = 4 * R4;
+    constexpr int NT = R4 * 64;                        // threads: two warps per row group
     extern __shared__ __align__(16) unsigned char smem_raw[];
     unsigned char *sk = smem_raw;                      // [SM_TOKENS][D] bf16, 16-byte chunks swizzled
     unsigned char *sv = sk + SM_TOKENS * D * 2;        // [SM_TOKENS][D] bf16
     float *qs = reinterpret_cast<float *>(sv + SM_TOKENS * D * 2);  // [D][RP][2]
-    float *ps = qs + D * RP * 2;                       // [R4][SM_TOKENS][4][2]
+    float *ps = qs + D * RP * 2;                       // [2 R4 warps][64 tokens][4][2]
+    float *oc = reinterpret_cast<float *>(sk);         // [R4][4 rows][D]: half 1's P.V partial (K is dead by then)
     __shared__ float scs[2][32];                       // chunk sums of the scoring rows, [chunk][head]
+    __shared__ float red_m[2][RP], red_l[2][RP];       // per half: row max and row sum
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int half = warp / R4, rg = warp % R4;        // tokens [64 half, 64 half + 64), rows 4 rg .. 4 rg + 3
     const int split = blockIdx.x, g = blockIdx.y;
     const int G = a.G, R = a.T * G;
     const int64_t L = a.N + a.T;
@@ -56,11 +62,11 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
     // ---- Q of the group: global loads first (they must not queue behind the
     // range's K/V copies); rows vary fastest across the threads so that the
     // transposed shared-memory stores do not collide in one bank
-    constexpr int QITER = (RP * (D / 8) + R4 * 32 - 1) / (R4 * 32);
+    constexpr int QITER = (RP * (D / 8) + NT - 1) / NT;
     uint4 qw[QITER];
 #pragma unroll
     for (int u = 0; u < QITER; ++u) {
-        const int e = threadIdx.x + u * R4 * 32;
+        const int e = threadIdx.x + u * NT;
         const int r = e % RP, c8 = (e / RP) * 8;
         qw[u] = make_uint4(0u, 0u, 0u, 0u);
         if (e < RP * (D / 8) && r < R) {
@@ -74,13 +80,13 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
     {
         const __nv_bfloat16 *kg = a.k + ((size_t)g * a.ld_kv + (size_t)t0) * D;
         const __nv_bfloat16 *vg = a.v + ((size_t)g * a.ld_kv + (size_t)t0) * D;
-        for (int e = threadIdx.x; e < SM_TOKENS * (D / 8); e += R4 * 32) {
+        for (int e = threadIdx.x; e < SM_TOKENS * (D / 8); e += NT) {
             const int row = e / (D / 8), c = e % (D / 8);
             const bool ok = row < n_tok;
             cp_async16_zfill(sk + row * (D * 2) + ((c ^ (row & 7)) * 16), kg + (ok ? (size_t)row * D + c * 8 : 0), ok);
         }
         cp_async_commit();
-        for (int e = threadIdx.x; e < SM_TOKENS * (D / 8); e += R4 * 32) {
+        for (int e = threadIdx.x; e < SM_TOKENS * (D / 8); e += NT) {
             const int row = e / (D / 8), c = e % (D / 8);
             const bool ok = row < n_tok;
             cp_async16_zfill(sv + row * (D * 2) + c * 16, vg + (ok ? (size_t)row * D + c * 8 : 0), ok);
@@ -91,7 +97,7 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
     // ---- Q -> shared memory as [d][row][2] (padding rows zero)
 #pragma unroll
     for (int u = 0; u < QITER; ++u) {
-        const int e = threadIdx.x + u * R4 * 32;
+        const int e = threadIdx.x + u * NT;
         if (e < RP * (D / 8)) {
             const int r = e % RP, c8 = (e / RP) * 8;
             const uint4 w = qw[u];
@@ -105,86 +111,57 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
     cp_async_wait<1>();  // K has landed
     __syncthreads();
 
-    // ---- S for tokens tok[i] = t0 + lane + 32 i and rows 4 warp + jr:
-    // acc[jr][0] = (tokens 0, 1), acc[jr][1] = (tokens 2, 3)
-    int64_t tok[4];
-    bool in_range[4];
+    // ---- S for tokens tok[i] = t0 + 64 half + lane + 32 i (i = 0, 1) and rows
+    // 4 rg + jr: acc[jr] = (token 0, token 1)
+    int64_t tok[2];
+    bool in_range[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        tok[i] = t0 + lane + 32 * i;
+    for (int i = 0; i < 2; ++i) {
+        tok[i] = t0 + 64 * half + lane + 32 * i;
         in_range[i] = tok[i] < L;
     }
-    float2 acc[4][2];
+    float2 acc[4];
 #pragma unroll
-    for (int jr = 0; jr < 4; ++jr) acc[jr][0] = acc[jr][1] = make_float2(0.f, 0.f);
+    for (int jr = 0; jr < 4; ++jr) acc[jr] = make_float2(0.f, 0.f);
     {
-        const float4 *q4 = reinterpret_cast<const float4 *>(qs) + warp * 2;  // rows 4w..4w+3 of dim 0
-        const unsigned char *krow = sk + lane * (D * 2);                     // token lane; + 32 i rows
-        const int sw = lane & 7;                                             // (lane + 32 i) & 7
-#pragma unroll 2
+        const float4 *q4 = reinterpret_cast<const float4 *>(qs) + rg * 2;             // rows 4rg..4rg+3 of dim 0
+        const unsigned char *krow = sk + (64 * half + lane) * (D * 2);               // token 64 half + lane; + 32 i
+        const int sw = lane & 7;                                                     // (64 half + lane + 32 i) & 7
+#pragma unroll 4
         for (int c = 0; c < D / 8; ++c) {
-            uint4 kw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                kw[i] = *reinterpret_cast<const uint4 *>(krow + i * 32 * (D * 2) + ((c ^ sw) * 16));
-            const uint32_t w[4][4] = {{kw[0].x, kw[0].y, kw[0].z, kw[0].w},
-                                      {kw[1].x, kw[1].y, kw[1].z, kw[1].w},
-                                      {kw[2].x, kw[2].y, kw[2].z, kw[2].w},
-                                      {kw[3].x, kw[3].y, kw[3].z, kw[3].w}};
+            const uint4 k0 = *reinterpret_cast<const uint4 *>(krow + ((c ^ sw) * 16));
+            const uint4 k1 = *reinterpret_cast<const uint4 *>(krow + 32 * (D * 2) + ((c ^ sw) * 16));
+            const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w}, w1[4] = {k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float4 qa = q4[(c * 8 + e) * (RP / 2)];      // (q0, q0, q1, q1)
                 const float4 qb = q4[(c * 8 + e) * (RP / 2) + 1];  // (q2, q2, q3, q3)
-                float kv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) kv[i] = (e & 1) ? bf16_hi(w[i][e >> 1]) : bf16_lo(w[i][e >> 1]);
-                const float2 k01 = make_float2(kv[0], kv[1]), k23 = make_float2(kv[2], kv[3]);
-                acc[0][0] = ffma2(k01, make_float2(qa.x, qa.y), acc[0][0]);
-                acc[0][1] = ffma2(k23, make_float2(qa.x, qa.y), acc[0][1]);
-                acc[1][0] = ffma2(k01, make_float2(qa.z, qa.w), acc[1][0]);
-                acc[1][1] = ffma2(k23, make_float2(qa.z, qa.w), acc[1][1]);
-                acc[2][0] = ffma2(k01, make_float2(qb.x, qb.y), acc[2][0]);
-                acc[2][1] = ffma2(k23, make_float2(qb.x, qb.y), acc[2][1]);
-                acc[3][0] = ffma2(k01, make_float2(qb.z, qb.w), acc[3][0]);
-                acc[3][1] = ffma2(k23, make_float2(qb.z, qb.w), acc[3][1]);
+                const float2 kk = (e & 1) ? make_float2(bf16_hi(w0[e >> 1]), bf16_hi(w1[e >> 1]))
+                                          : make_float2(bf16_lo(w0[e >> 1]), bf16_lo(w1[e >> 1]));
+                acc[0] = ffma2(kk, make_float2(qa.x, qa.y), acc[0]);
+                acc[1] = ffma2(kk, make_float2(qa.z, qa.w), acc[1]);
+                acc[2] = ffma2(kk, make_float2(qb.x, qb.y), acc[2]);
+                acc[3] = ffma2(kk, make_float2(qb.z, qb.w), acc[3]);
             }
         }
     }
-    float s[4][4];  // [token i][row jr], raw q.k
+    float s[2][4];  // [token i][row jr], raw q.k
 #pragma unroll
     for (int jr = 0; jr < 4; ++jr) {
-        s[0][jr] = acc[jr][0].x; s[1][jr] = acc[jr][0].y;
-        s[2][jr] = acc[jr][1].x; s[3][jr] = acc[jr][1].y;
+        s[0][jr] = acc[jr].x;
+        s[1][jr] = acc[jr].y;
     }
 
     // ---- fused chunk importance of the scoring row (raw q.k over tokens < N):
-    // chunk 2*split takes tokens i = 0, 1, chunk 2*split+1 tokens i = 2, 3
+    // half h covers chunk 2 split + h
     if (a.chunk_scores != nullptr) {
 #pragma unroll
         for (int jr = 0; jr < 4; ++jr) {
-            const int r = 4 * warp + jr;
+            const int r = 4 * rg + jr;
             if (r < R && r / G == a.score_row) {  // warp-uniform
-                float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float v = tok[i] < a.N ? s[i][jr] : 0.f;
-                    if (i < 2) x0 += v; else x1 += v;
-                }
-                x0 = warp_sum(x0);
-                x1 = warp_sum(x1);
-                if (lane == 0) {
-                    scs[0][r % G] = x0;
-                    scs[1][r % G] = x1;
-                }
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x < 2) {
-            const int64_t ch0 = t0 + 64 * threadIdx.x;
-            if (ch0 < a.N) {
-                float best = -INFINITY;
-                for (int j = 0; j < G; ++j) best = fmaxf(best, scs[threadIdx.x][j]);
-                a.chunk_scores[(size_t)g * a.n_chunks + (size_t)(ch0 / 64)] = best;
+                float x = (tok[0] < a.N ? s[0][jr] : 0.f) + (tok[1] < a.N ? s[1][jr] : 0.f);
+                x = warp_sum(x);
+                if (lane == 0) scs[half][r % G] = x;
             }
         }
     }
@@ -192,45 +169,65 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
     // ---- visibility: the head's prefix tokens for every row, batch tokens by ancestry
     const float c = a.scale_log2;
     const int64_t plen = prefix_of(a, g);
-    float m[4], l[4];
+    float mh[4];
 #pragma unroll
     for (int jr = 0; jr < 4; ++jr) {
-        const int r = 4 * warp + jr;
+        const int r = 4 * rg + jr;
         const int t = r < R ? r / G : 0;
         float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             bool vis = in_range[i] && r < R;
             if (vis) vis = tok[i] < a.N ? tok[i] < plen : mask_bit(a.mask, a.mw, t, (int)(tok[i] - a.N));
             s[i][jr] = vis ? s[i][jr] * c : -INFINITY;
             mx = fmaxf(mx, s[i][jr]);
         }
-        m[jr] = warp_max(mx);
+        mh[jr] = warp_max(mx);
+        if (lane == 0) red_m[half][4 * rg + jr] = mh[jr];
     }
-    // ---- P = 2^(s*c - m) into this warp's slab [token][row][2], row sums
-    float *pw = ps + (size_t)warp * SM_TOKENS * 8;
+    __syncthreads();
+    if (a.chunk_scores != nullptr && threadIdx.x < 2) {
+        const int64_t ch0 = t0 + 64 * threadIdx.x;
+        if (ch0 < a.N) {
+            float best = -INFINITY;
+            for (int j = 0; j < G; ++j) best = fmaxf(best, scs[threadIdx.x][j]);
+            a.chunk_scores[(size_t)g * a.n_chunks + (size_t)(ch0 / 64)] = best;
+        }
+    }
+    // ---- P = 2^(s*c - m) with the range's row max into this warp's slab
+    // [token][row][2]; row sums per half
+    float m[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int jr = 0; jr < 4; ++jr) m[jr] = fmaxf(red_m[0][4 * rg + jr], red_m[1][4 * rg + jr]);
+    float *pw = ps + (size_t)warp * 64 * 8;
+    float lh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
         float p[4];
 #pragma unroll
-        for (int jr = 0; jr < 4; ++jr) p[jr] = (m[jr] == -INFINITY) ? 0.f : exp2f(s[i][jr] - m[jr]);
+        for (int jr = 0; jr < 4; ++jr) {
+            p[jr] = (m[jr] == -INFINITY) ? 0.f : exp2f(s[i][jr] - m[jr]);
+            lh[jr] += p[jr];
+        }
         float4 *dst = reinterpret_cast<float4 *>(pw + (lane + 32 * i) * 8);
         dst[0] = make_float4(p[0], p[0], p[1], p[1]);
         dst[1] = make_float4(p[2], p[2], p[3], p[3]);
-#pragma unroll
-        for (int jr = 0; jr < 4; ++jr) s[i][jr] = p[jr];
     }
 #pragma unroll
-    for (int jr = 0; jr < 4; ++jr) l[jr] = warp_sum((s[0][jr] + s[1][jr]) + (s[2][jr] + s[3][jr]));
+    for (int jr = 0; jr < 4; ++jr) {
+        lh[jr] = warp_sum(lh[jr]);
+        if (lane == 0) red_l[half][4 * rg + jr] = lh[jr];
+    }
     cp_async_wait<0>();  // V has landed (this thread's copies) ...
     __syncthreads();     // ... and every thread's; P of this warp is visible too
 
-    // ---- O: lane = dims [4 lane, 4 lane + 4), every token of the range
+    // ---- O: lane = dims [4 lane, 4 lane + 4), the 64 tokens of this half
     float2 o[4][2];
 #pragma unroll
     for (int jr = 0; jr < 4; ++jr) o[jr][0] = o[jr][1] = make_float2(0.f, 0.f);
-    const uint2 *vcol = reinterpret_cast<const uint2 *>(sv) + lane;
-    for (int i0 = 0; i0 < n_tok; i0 += 16) {
+    const uint2 *vcol = reinterpret_cast<const uint2 *>(sv) + (size_t)64 * half * (D / 4) + lane;
+    const int n_half = max(0, min(64, n_tok - 64 * half));
+    for (int i0 = 0; i0 < n_half; i0 += 16) {
         uint2 vw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) vw[i] = vcol[(i0 + i) * (D / 4)];  // zero past the range
@@ -250,25 +247,37 @@ __global__ void __launch_bounds__(R4 * 32) tree_attn_small_kernel(const AttnArgs
             o[3][1] = ffma2(make_float2(pb.z, pb.w), v23, o[3][1]);
         }
     }
+    // ---- half 1 hands its partial to half 0 (through the dead K buffer)
+    if (half == 1) {
+#pragma unroll
+        for (int jr = 0; jr < 4; ++jr)
+            *reinterpret_cast<float4 *>(oc + ((size_t)rg * 4 + jr) * D + 4 * lane) =
+                make_float4(o[jr][0].x, o[jr][0].y, o[jr][1].x, o[jr][1].y);
+    }
+    __syncthreads();
+    if (half == 1) return;
 
     // ---- this range's result for the warp's rows
 #pragma unroll
     for (int jr = 0; jr < 4; ++jr) {
-        const int r = 4 * warp + jr;
+        const int r = 4 * rg + jr;
         if (r >= R) break;
+        const float4 q1 = *reinterpret_cast<const float4 *>(oc + ((size_t)rg * 4 + jr) * D + 4 * lane);
+        o[jr][0].x += q1.x; o[jr][0].y += q1.y; o[jr][1].x += q1.z; o[jr][1].y += q1.w;
+        const float l = red_l[0][r] + red_l[1][r];
         const int t = r / G, j = r % G;
         const size_t row = (size_t)t * a.Hq + g * G + j;
         if (n_splits == 1) {
-            const float inv = l[jr] > 0.f ? 1.f / l[jr] : 0.f;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(a.out + row * D) + 2 * lane;
             dst[0] = __floats2bfloat162_rn(o[jr][0].x * inv, o[jr][0].y * inv);
             dst[1] = __floats2bfloat162_rn(o[jr][1].x * inv, o[jr][1].y * inv);
-            if (a.lse != nullptr && lane == 0) a.lse[row] = (m[jr] + log2f(l[jr])) * TS_LN2;
+            if (a.lse != nullptr && lane == 0) a.lse[row] = (m[jr] + log2f(l)) * TS_LN2;
         } else {
             float4 *dst = reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * D) + lane;
             *dst = make_float4(o[jr][0].x, o[jr][0].y, o[jr][1].x, o[jr][1].y);
             if (lane == 0)
-                reinterpret_cast<float2 *>(a.ws_ml)[(size_t)split * a.T * a.Hq + row] = make_float2(m[jr], l[jr]);
+                reinterpret_cast<float2 *>(a.ws_ml)[(size_t)split * a.T * a.Hq + row] = make_float2(m[jr], l);
         }
     }
 }
@@ -283,7 +292,8 @@ int small_splits(int T, int64_t N) { return (int)((N + T + SM_TOKENS - 1) / SM_T
 template <int R4>
 static size_t small_smem() {
     constexpr int RP = 4 * R4;
-    return 2 * (size_t)SM_TOKENS * D * 2 + sizeof(float) * ((size_t)D * RP * 2 + (size_t)R4 * SM_TOKENS * 8);
+    // K, V; Q as fp32 pairs; a 64-token P slab per warp (2 R4 warps)
+    return 2 * (size_t)SM_TOKENS * D * 2 + sizeof(float) * ((size_t)D * RP * 2 + (size_t)2 * R4 * 64 * 8);
 }
 
 template <int R4>
@@ -293,7 +303,7 @@ static cudaError_t launch_small_t(const AttnArgs &a, int splits, cudaStream_t st
                                          (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(splits, a.Hkv);
-    tree_attn_small_kernel<R4><<<grid, R4 * 32, smem, st>>>(a, splits);
+    tree_attn_small_kernel<R4><<<grid, R4 * 64, smem, st>>>(a, splits);
     return cudaGetLastError();
 }
 

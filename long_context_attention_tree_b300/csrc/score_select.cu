@@ -181,9 +181,15 @@ select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, 
         for (int b = tid; b < 256; b += SG_THREADS) hist[b] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix;
-        for (int c = tid; c < n_chunks; c += SG_THREADS) {
-            const uint32_t key = keys[c];
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+        // lanes of a warp that hit the same bin add once (the top digits of
+        // close scores coincide, and single-address atomics would serialise)
+        for (int c0 = 0; c0 < n_chunks; c0 += SG_THREADS) {
+            const int c = c0 + tid;
+            const uint32_t key = c < n_chunks ? keys[c] : 0u;
+            const bool live = c < n_chunks && (key & pmask) == prefix;
+            const uint32_t bin = live ? (key >> shift) & 255u : 256u;
+            const unsigned same = __match_any_sync(0xffffffffu, bin);
+            if (live && (tid & 31) == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
         }
         __syncthreads();
         if (tid < 32) {

@@ -7,9 +7,13 @@
 //     the target tokens, and one of the longest valid drafts is kept.
 //
 // Row pass: one thread-block cluster of VOCAB_CLUSTER CTAs per batch row; each
-// CTA owns a contiguous slice of the vocabulary, holds it in registers, and
-// the CTAs exchange (max, argmax) and then the min-p counts through
-// distributed shared memory.  The logits are read from HBM exactly once.
+// CTA owns a contiguous slice of the vocabulary.  Pass 1 streams the slice
+// from HBM (kept in L2) for its penalised (max, argmax); the CTAs exchange
+// those through distributed shared memory; pass 2 re-reads the slice from L2
+// for the min-p count (and the Gumbel-max draw when sampling).  The logits of
+// a step (73 MB for 120 x 152064) fit the 126 MB L2 but not the register
+// file, so two passes with small CTAs keep every SM streaming in about one
+// wave instead of holding a slice in registers.
 #include <cooperative_groups.h>
 
 #include "internal.h"
@@ -20,9 +24,9 @@ namespace cg = cooperative_groups;
 namespace ts {
 
 constexpr int VOCAB_CLUSTER = 8;
-constexpr int VOCAB_THREADS = 512;
-constexpr int VOCAB_CACHE = 40;                     // register-resident logits per thread
-constexpr int VOCAB_MAX_SLICE = VOCAB_THREADS * VOCAB_CACHE;  // 20480
+constexpr int VOCAB_THREADS = 256;
+constexpr int VOCAB_BATCH = 8;                      // loads in flight per thread
+constexpr int VOCAB_MAX_SLICE = 20480;              // V <= 8 * 20480 = 163840
 constexpr int VOCAB_BITMAP_WORDS = VOCAB_MAX_SLICE / 32;
 
 struct ArgMax {
@@ -93,16 +97,30 @@ __device__ __forceinline__ float gumbel(int v, int row, const VocabArgs &a) {
     return -ln_f32(-ln_f32(u));
 }
 
+// Reductions of (value, index) pairs and counts over one CTA; every thread
+// receives the result.  `red` holds one slot per warp.
+__device__ __forceinline__ ArgMax block_best(ArgMax b, ArgMax *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ArgMax other{__shfl_xor_sync(0xffffffffu, b.v, o), __shfl_xor_sync(0xffffffffu, b.i, o)};
+        b = better(b, other);
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = b;
+    __syncthreads();
+    ArgMax r = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = better(r, red[w]);
+    return r;
+}
+
 template <bool SAMPLE>
-__global__ void __cluster_dims__(VOCAB_CLUSTER, 1, 1) __launch_bounds__(VOCAB_THREADS)
+__global__ void __cluster_dims__(VOCAB_CLUSTER, 1, 1) __launch_bounds__(VOCAB_THREADS, SAMPLE ? 4 : 7)
 penalty_minp_kernel(const VocabArgs a, int slice) {
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ uint32_t bitmap[VOCAB_BITMAP_WORDS];
-    __shared__ ArgMax warp_best[VOCAB_THREADS / 32];
+    __shared__ ArgMax red[VOCAB_THREADS / 32];
     __shared__ ArgMax cta_best;
     __shared__ int warp_cnt[VOCAB_THREADS / 32];
     __shared__ int cta_cnt;
-    __shared__ ArgMax warp_samp[SAMPLE ? VOCAB_THREADS / 32 : 1];
     __shared__ ArgMax cta_samp;
 
     const int row = blockIdx.y;
@@ -143,80 +161,79 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
     }
     __syncthreads();
 
+    // penalised, tempered logit of token vv (dividing by a temperature of 1 is
+    // exact, so that division is skipped)
+    const bool tempered = a.temperature != 1.0f;
+    auto final_logit = [&](float l, int vv) {
+        const int o = vv - v0;
+        if ((bitmap[o >> 5] >> (o & 31)) & 1u) l = l > 0.f ? __fdiv_rn(l, a.theta) : __fmul_rn(l, a.theta);
+        return tempered ? __fdiv_rn(l, a.temperature) : l;
+    };
     const float *lrow = a.logits + (size_t)row * a.V;
-    float x[VOCAB_CACHE];
+
+    // ---- pass 1 (HBM): max and lowest argmax of this slice.  A thread's
+    // tokens increase with the loop, so a strict > keeps the lowest index.
     ArgMax best{-INFINITY, -1};
+    for (int base = v0 + tid; base < v1; base += VOCAB_BATCH * VOCAB_THREADS) {
+        float x[VOCAB_BATCH];
 #pragma unroll
-    for (int i = 0; i < VOCAB_CACHE; ++i) {
-        const int vv = v0 + i * VOCAB_THREADS + tid;
-        float l = -INFINITY;
-        if (vv < v1) {
-            l = __ldcs(lrow + vv);
-            const int o = vv - v0;
-            if ((bitmap[o >> 5] >> (o & 31)) & 1u) l = l > 0.f ? __fdiv_rn(l, a.theta) : __fmul_rn(l, a.theta);
-            l = __fdiv_rn(l, a.temperature);
-            best = better(best, ArgMax{l, vv});
+        for (int j = 0; j < VOCAB_BATCH; ++j) {
+            const int vv = base + j * VOCAB_THREADS;
+            x[j] = vv < v1 ? __ldcg(lrow + vv) : 0.f;  // keep the row in L2 for pass 2
         }
-        x[i] = l;
-    }
-    // block (max, argmax)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        ArgMax other{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.i, o)};
-        best = better(best, other);
+        for (int j = 0; j < VOCAB_BATCH; ++j) {
+            const int vv = base + j * VOCAB_THREADS;
+            if (vv < v1) {
+                const float l = final_logit(x[j], vv);
+                if (best.i < 0 || l > best.v) best = ArgMax{l, vv};
+            }
+        }
     }
-    if (lane == 0) warp_best[warp] = best;
-    __syncthreads();
-    if (tid == 0) {
-        ArgMax b = warp_best[0];
-        for (int w = 1; w < VOCAB_THREADS / 32; ++w) b = better(b, warp_best[w]);
-        cta_best = b;
-    }
+    best = block_best(best, red);
+    if (tid == 0) cta_best = best;
     cluster.sync();
     // every CTA reduces the cluster's candidates in rank order
     ArgMax gbest{-INFINITY, -1};
-    for (int r = 0; r < VOCAB_CLUSTER; ++r) {
-        const ArgMax *rb = cluster.map_shared_rank(&cta_best, r);
-        gbest = better(gbest, *rb);
-    }
+    for (int r = 0; r < VOCAB_CLUSTER; ++r) gbest = better(gbest, *cluster.map_shared_rank(&cta_best, r));
     // min-p threshold: smallest fp32 >= m + ln(min_p) (exact comparison)
-    const double thr = (double)gbest.v + a.log_min_p;
-    const float f = __double2float_ru(thr);
+    const float f = __double2float_ru((double)gbest.v + a.log_min_p);
+
+    // ---- pass 2 (L2): min-p count, and the Gumbel-max draw over the kept ids
     int cnt = 0;
+    ArgMax sb{-INFINITY, -1};
+    for (int base = v0 + tid; base < v1; base += VOCAB_BATCH * VOCAB_THREADS) {
+        float x[VOCAB_BATCH];
 #pragma unroll
-    for (int i = 0; i < VOCAB_CACHE; ++i) {
-        const int vv = v0 + i * VOCAB_THREADS + tid;
-        if (vv < v1 && x[i] >= f) ++cnt;
+        for (int j = 0; j < VOCAB_BATCH; ++j) {
+            const int vv = base + j * VOCAB_THREADS;
+            x[j] = vv < v1 ? __ldcs(lrow + vv) : 0.f;  // last use: evict first
+        }
+#pragma unroll
+        for (int j = 0; j < VOCAB_BATCH; ++j) {
+            const int vv = base + j * VOCAB_THREADS;
+            if (vv < v1) {
+                const float l = final_logit(x[j], vv);
+                if (l >= f) {
+                    ++cnt;
+                    if constexpr (SAMPLE) sb = better(sb, ArgMax{__fadd_rn(l, gumbel(vv, row, a)), vv});
+                }
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     if (lane == 0) warp_cnt[warp] = cnt;
+    if constexpr (SAMPLE) {
+        __syncthreads();  // red[] is reused
+        sb = block_best(sb, red);
+        if (tid == 0) cta_samp = sb;
+    }
     __syncthreads();
     if (tid == 0) {
         int c = 0;
         for (int w = 0; w < VOCAB_THREADS / 32; ++w) c += warp_cnt[w];
         cta_cnt = c;
-    }
-    if constexpr (SAMPLE) {
-        // Gumbel-max draw over this slice's kept ids
-        ArgMax sb{-INFINITY, -1};
-#pragma unroll
-        for (int i = 0; i < VOCAB_CACHE; ++i) {
-            const int vv = v0 + i * VOCAB_THREADS + tid;
-            if (vv < v1 && x[i] >= f) sb = better(sb, ArgMax{__fadd_rn(x[i], gumbel(vv, row, a)), vv});
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            ArgMax other{__shfl_xor_sync(0xffffffffu, sb.v, o), __shfl_xor_sync(0xffffffffu, sb.i, o)};
-            sb = better(sb, other);
-        }
-        if (lane == 0) warp_samp[warp] = sb;
-        __syncthreads();
-        if (tid == 0) {
-            ArgMax b = warp_samp[0];
-            for (int w = 1; w < VOCAB_THREADS / 32; ++w) b = better(b, warp_samp[w]);
-            cta_samp = b;
-        }
     }
     cluster.sync();
     if (rank == 0 && tid == 0) {

@@ -284,7 +284,7 @@ def test_partial_cache_drafting_with_a_short_last_chunk(N, Hq, Hkv, d):
     np.testing.assert_array_equal(sel.cpu().numpy(), rsel)
     _, rl = oracle.gather(rsel, k.cpu(), N, 64, B + Td, return_len=True)
     np.testing.assert_array_equal(plen.cpu().numpy(), rl)
-    if N % 64:
+    if N % 64 and nc > kk:  # (when every chunk fits the budget, every head holds all N tokens)
         assert (rl[::2] < B).all() and (rl[1::2] == B).all()
     ro, rlse = oracle.tree_attn(q.cpu(), kp.cpu(), vp.cpu(), B, parent, 1 / math.sqrt(d), prefix_len=rl)
     check_attn(out, lse, ro, rlse, "partial")
