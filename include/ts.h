@@ -346,7 +346,7 @@ ts_status ts_vocab_verify(const float *logits, int T, int V, const int32_t *hist
  * s (1 + s^2/3 + ... + s^10/11), every operation an IEEE fp32 one.
  * Acceptance then uses these sampled targets, and the kept row among the m
  * longest accepted rows S (ascending row order) is drawn uniformly ("How it
- * works": one of the longest valid drafts is selected at random):
+ * works": a random longest accepted draft is kept):
  * best = S[floor(x m / 2^64)], x = word 0 of Philox4x64-10 at counter
  * (0, 0, offset, 1) under key (seed, 0).  kept, result and path as for
  * ts_penalty_minp_verify.

@@ -1,8 +1,8 @@
 // Split-KV tree-masked GQA attention on the 5th-generation tensor cores
 // (tcgen05, TMEM accumulators, TMA), for the TokenSwift verify pass: a batch
 // of T >= 64 speculative rows (draft tree + n-gram chains) against the full
-// bf16 KV cache ("fed into the LLM with a full KV cache", "How it works" on
-// the TokenSwift tool listing).
+// bf16 KV cache (the drafts are checked by the target model over its whole KV
+// cache, "How it works" on the TokenSwift tool listing).
 //
 // Rows of one KV head g are the T x G pairs (t, j), t-major; an M-tile is
 // tpb = floor(128/G) whole batch rows times the G query heads of the group,

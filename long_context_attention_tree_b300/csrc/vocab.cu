@@ -4,7 +4,7 @@
 //   model card, "Example using TokenSwift command line": --penalty 1.2
 //     --penalty_length 1024 --min_p 0.1 --temperature 1.0;
 //   tool listing, "How it works": drafts are accepted when they exactly match
-//     the target tokens, and one of the longest valid drafts is kept.
+//     the target tokens, and a longest accepted draft is kept.
 //
 // Row pass: one thread-block cluster of VOCAB_CLUSTER CTAs per batch row; each
 // CTA owns a contiguous slice of the vocabulary.  Pass 1 streams the slice
@@ -252,7 +252,7 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
 // Acceptance: one CTA, one thread per batch row walking its (short) ancestor
 // chain; the longest accepted depth wins.  Greedy targets keep the lowest of
 // the longest rows; sampled targets draw one of them uniformly ("How it
-// works": one of the longest valid drafts is selected at random): with S the
+// works": a random longest accepted draft is kept): with S the
 // m longest accepted rows in ascending order, the kept row is
 // S[floor(x m / 2^64)], x = word 0 of Philox4x64-10 at counter
 // (0, 0, offset, 1) under key (seed, 0).

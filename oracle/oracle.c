@@ -12,7 +12,7 @@
  *     tree-based attention over candidates, verification with the full KV
  *     cache, exact match of draft and target tokens, one longest valid draft
  *     kept;
- *   - ICML 2025 summary, "Approach": partial KV cache ranked by query-key
+ *   - ICML 2025 summary, "Approach": the partial KV cache keeps the chunks whose
  *     importance, windowed contextual penalty; ablation table: tree
  *     [1,3,3,3], theta 1.2, W 1024.
  * Where the pages are silent the plainest reading is used; every reading is
@@ -159,7 +159,8 @@ int oracle_tree_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
 }
 
 /* ---------------------------------------------------------------------- */
-/* Chunk importance ("partial KV cache ranked by query-key importance").   */
+/* Chunk importance (ICML 2025 summary, "Approach": the partial cache is   */
+/* chosen by how strongly the query attends to each part of the keys).     */
 /*   score[g][c] = max_{h in group g} q_h . sum_{t in chunk c} k_t          */
 /* over prefix tokens only; the last chunk may be partial.  Unscaled.      */
 /*   q_row: bf16 [Hq][d];  scores: double [Hkv][ceil(N/chunk)].             */
@@ -379,7 +380,7 @@ int oracle_penalty_minp(const float *logits, int T, int V, const int32_t *histor
 
 /* ---------------------------------------------------------------------- */
 /* Exact-match acceptance along every tree / n-gram path ("How it works":  */
-/* drafts must exactly match the target tokens; one of the longest valid   */
+/* a draft counts only when it equals the target token; a longest        */
 /* drafts is kept -- here the lowest row among them).                      */
 /*   expected(i) = parent[i] >= 0 ? target[parent[i]] : anchor              */
 /*   acc(i) = draft[i] == expected(i) && (parent[i] < 0 || acc(parent[i]))  */
@@ -388,7 +389,7 @@ int oracle_penalty_minp(const float *logits, int T, int V, const int32_t *histor
 /*   bonus = L > 0 ? target[best] : anchor; path = root..best.              */
 /*   result = {L, best, bonus, status}; path int32[T], unused entries -1.   */
 /* ---------------------------------------------------------------------- */
-/* The pages keep one of the longest valid drafts at random ("How it works"). */
+/* The pages keep a random longest accepted draft ("How it works").       */
 /* With choose != 0 the kept row is drawn uniformly from the m accepted rows  */
 /* of depth L, listed in ascending row order S[0..m): index                   */
 /*   j = floor(x * m / 2^64)   (the high word of the 128-bit product)         */
