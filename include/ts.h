@@ -297,8 +297,10 @@ ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_t
  *     is accepted; L = the largest depth (roots have depth 1) of an accepted
  *     row, best = the lowest such row, bonus = L > 0 ? target[best] : anchor.
  *   result int32[4] = {L, best (-1 if L == 0), bonus, status}; status is
- *     TS_OK, or TS_ERR_DATA if a history id is outside [0, V) or a parent
- *     index is out of order.
+ *     TS_OK, TS_ERR_DATA if a history id is outside [0, V) or a parent
+ *     index is out of order, or TS_ERR_TIMEOUT if a row's copy of its logits
+ *     into shared memory never completed (a bounded wait gave up; that row's
+ *     kept count reads -1).
  *   path   int32[T]: rows root..best in path[0..L), -1 after.
  *   draft, parent: int32 [T] device.  history: int32 [W] device (W >= 0).
  *   workspace: unused, pass NULL / 0.

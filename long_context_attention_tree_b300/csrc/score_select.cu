@@ -105,12 +105,14 @@ cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *score
 }
 
 // ---------------------------------------------------------------------------
-// Top-k selection (radix select on order-preserving keys) + gather.
-// CTA = (part p, KV head g).  Every CTA of a head computes the same selection
-// from the head's scores (a few KB, L2-resident), then copies its share of the
-// selected chunks.  Part 0 also writes sel[g][.].
+// Top-k selection (radix select on order-preserving keys), then the gather.
+// select_kernel: one CTA per KV head computes sel[g][.] and part_len[g];
+// gather_kernel: CTA = (selected chunk, KV head) copies the chunk's K and V
+// rows.  The gather is launched as a programmatic dependent of the selection
+// so its CTAs are resident and waiting when the selection finishes.
 // ---------------------------------------------------------------------------
-constexpr int SG_THREADS = 512;
+constexpr int SEL_THREADS = 1024;
+constexpr int GA_THREADS = 256;
 
 __device__ __forceinline__ uint32_t order_key(float x) {
     x = x + 0.0f;  // -0 -> +0 (round-to-nearest), so equal values get equal keys
@@ -147,49 +149,40 @@ __device__ int block_exclusive_scan(int x, int *warp_tot, int *total) {
     return r;
 }
 
-template <int D>
-__global__ void __launch_bounds__(SG_THREADS)
-select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
-                     const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v, int64_t ld_kv,
-                     int32_t *__restrict__ sel, int32_t *__restrict__ part_len, __nv_bfloat16 *__restrict__ k_part,
-                     __nv_bfloat16 *__restrict__ v_part, int64_t ld_part, int chunks_per_part) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint32_t *keys = reinterpret_cast<uint32_t *>(smem_raw);          // [n_chunks]
-    int32_t *list = reinterpret_cast<int32_t *>(keys + n_chunks);     // [k_sel]
+__global__ void __launch_bounds__(SEL_THREADS)
+select_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
+              int32_t *__restrict__ sel, int32_t *__restrict__ part_len) {
+    extern __shared__ __align__(16) uint32_t keys[];  // [n_chunks]
     __shared__ int hist[256];
     __shared__ int warp_tot[32];
-    __shared__ int s_total;
+    __shared__ int s_total, s_last;
     __shared__ uint32_t s_prefix;
     __shared__ int s_remaining;
+    // the gather grid may launch now; it waits for this grid's results
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    const int g = blockIdx.y, p = blockIdx.x, tid = threadIdx.x;
+    const int g = blockIdx.x, tid = threadIdx.x;
     const float *sc = scores + (size_t)g * n_chunks;
     // always-kept chunks (the first n_sink, the last n_recent) take the largest
     // key, above every finite score's
-    for (int c = tid; c < n_chunks; c += SG_THREADS)
+    for (int c = tid; c < n_chunks; c += SEL_THREADS)
         keys[c] = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
-    for (int i = tid; i < k_sel; i += SG_THREADS) list[i] = 0;
     if (tid == 0) {
         s_prefix = 0u;
         s_remaining = k_sel;
+        s_last = 0;
     }
     __syncthreads();
 
     // --- radix select of the k-th largest key, 8 bits at a time from the top
     uint32_t pmask = 0u;
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int b = tid; b < 256; b += SG_THREADS) hist[b] = 0;
+        for (int b = tid; b < 256; b += SEL_THREADS) hist[b] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix;
-        // lanes of a warp that hit the same bin add once (the top digits of
-        // close scores coincide, and single-address atomics would serialise)
-        for (int c0 = 0; c0 < n_chunks; c0 += SG_THREADS) {
-            const int c = c0 + tid;
-            const uint32_t key = c < n_chunks ? keys[c] : 0u;
-            const bool live = c < n_chunks && (key & pmask) == prefix;
-            const uint32_t bin = live ? (key >> shift) & 255u : 256u;
-            const unsigned same = __match_any_sync(0xffffffffu, bin);
-            if (live && (tid & 31) == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
+        for (int c = tid; c < n_chunks; c += SEL_THREADS) {
+            const uint32_t key = keys[c];
+            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
         }
         __syncthreads();
         if (tid < 32) {
@@ -209,9 +202,7 @@ select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, 
             }
             const int excl = incl - lsum;
             const int rem = s_remaining;
-            const bool here = excl < rem && incl >= rem;
-            const unsigned who = __ballot_sync(0xffffffffu, here);
-            if (here) {
+            if (excl < rem && incl >= rem) {
                 int cum = excl;
                 int digit = 255 - 8 * tid;
 #pragma unroll
@@ -225,7 +216,6 @@ select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, 
                 s_prefix = prefix | ((uint32_t)digit << shift);
                 s_remaining = rem - cum;
             }
-            (void)who;
         }
         __syncthreads();
         pmask |= 255u << shift;
@@ -234,11 +224,11 @@ select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, 
     const int need_eq = s_remaining; // how many keys equal to kth are taken (lowest indices)
 
     // --- flags in index order: key > kth, or key == kth among the first need_eq equals
-    const int per = (n_chunks + SG_THREADS - 1) / SG_THREADS;
+    const int per = (n_chunks + SEL_THREADS - 1) / SEL_THREADS;
     const int c_begin = min(n_chunks, tid * per), c_end = min(n_chunks, c_begin + per);
     int eq_local = 0;
     for (int c = c_begin; c < c_end; ++c) eq_local += keys[c] == kth;
-    int eq_before = block_exclusive_scan(eq_local, warp_tot, &s_total);
+    const int eq_before = block_exclusive_scan(eq_local, warp_tot, &s_total);
     int sel_local = 0;
     {
         int e = eq_before;
@@ -258,8 +248,8 @@ select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, 
             else if (key == kth) { take = e < need_eq; ++e; }
             if (take) {
                 if (pos < k_sel) {  // exactly k_sel are taken; the guard only bounds the writes
-                    list[pos] = c;
-                    if (p == 0) sel[(size_t)g * k_sel + pos] = c;
+                    sel[(size_t)g * k_sel + pos] = c;
+                    if (c == n_chunks - 1) s_last = 1;
                 }
                 ++pos;
             }
@@ -268,57 +258,48 @@ select_gather_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, 
     __syncthreads();
     // tokens gathered for this head: only the last chunk of the prefix can be
     // short, and being the largest index it is the last one selected
-    if (p == 0 && tid == 0 && part_len != nullptr) {
+    if (tid == 0 && part_len != nullptr) {
         const int64_t tail = N - (int64_t)(n_chunks - 1) * CHUNK;  // tokens of the last chunk, 1..64
-        part_len[g] = k_sel * CHUNK - (list[k_sel - 1] == n_chunks - 1 ? (int)(CHUNK - tail) : 0);
+        part_len[g] = k_sel * CHUNK - (s_last ? (int)(CHUNK - tail) : 0);
     }
+}
 
-    // --- gather this part's chunks, K and V: every load of a pair of chunks is
-    // issued before the first store, so each thread keeps 8 x 16 bytes in flight;
-    // rows of the last chunk at or past N are neither read nor written
+// One selected chunk of one KV head: its K and V rows (rows of the last chunk
+// at or past N are neither read nor written), every load issued before the
+// first store.
+template <int D>
+__global__ void __launch_bounds__(GA_THREADS)
+gather_kernel(const int32_t *__restrict__ sel, int64_t N, int n_chunks, int k_sel,
+              const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v, int64_t ld_kv,
+              __nv_bfloat16 *__restrict__ k_part, __nv_bfloat16 *__restrict__ v_part, int64_t ld_part) {
     constexpr int U = D / 8;                     // 16-byte units per row
-    constexpr int PER = CHUNK * U / SG_THREADS;  // units per thread per chunk (2 for D = 128)
-    static_assert(CHUNK * U % SG_THREADS == 0, "chunk must split evenly over the threads");
-    const int i0 = p * chunks_per_part, i1 = min(k_sel, i0 + chunks_per_part);
-    const __nv_bfloat16 *kh = k + (size_t)g * ld_kv * D;
-    const __nv_bfloat16 *vh = v + (size_t)g * ld_kv * D;
-    __nv_bfloat16 *kp = k_part + (size_t)g * ld_part * D;
-    __nv_bfloat16 *vp = v_part + (size_t)g * ld_part * D;
-    for (int i = i0; i < i1; i += 2) {
-        const int nb = min(2, i1 - i);
-        uint4 wk[2][PER], wv[2][PER];
-        int rows_of[2];
+    constexpr int PER = CHUNK * U / GA_THREADS;  // units per thread per chunk (4 for D = 128)
+    static_assert(CHUNK * U % GA_THREADS == 0, "chunk must split evenly over the threads");
+    // wait until the selection grid has finished and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int i = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+    const int c = min(max(sel[(size_t)g * k_sel + i], 0), n_chunks - 1);
+    const int64_t left = N - (int64_t)c * CHUNK;
+    const int rows = left < CHUNK ? (int)left : CHUNK;
+    const __nv_bfloat16 *kh = k + ((size_t)g * ld_kv + (size_t)c * CHUNK) * D;
+    const __nv_bfloat16 *vh = v + ((size_t)g * ld_kv + (size_t)c * CHUNK) * D;
+    __nv_bfloat16 *kp = k_part + ((size_t)g * ld_part + (size_t)i * CHUNK) * D;
+    __nv_bfloat16 *vp = v_part + ((size_t)g * ld_part + (size_t)i * CHUNK) * D;
+    uint4 wk[PER], wv[PER];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            rows_of[b] = 0;
-            if (b < nb) {
-                const int c = min(max(list[i + b], 0), n_chunks - 1);
-                const int64_t left = N - (int64_t)c * CHUNK;
-                rows_of[b] = left < CHUNK ? (int)left : CHUNK;
-                const size_t src_row = (size_t)c * CHUNK;
-#pragma unroll
-                for (int q = 0; q < PER; ++q) {
-                    const int e = tid + q * SG_THREADS, r = e / U, u = e % U;
-                    if (r < rows_of[b]) {
-                        wk[b][q] = *reinterpret_cast<const uint4 *>(kh + (src_row + r) * D + u * 8);
-                        wv[b][q] = *reinterpret_cast<const uint4 *>(vh + (src_row + r) * D + u * 8);
-                    }
-                }
-            }
+    for (int q = 0; q < PER; ++q) {
+        const int e = tid + q * GA_THREADS, r = e / U, u = e % U;
+        if (r < rows) {
+            wk[q] = *reinterpret_cast<const uint4 *>(kh + (size_t)r * D + u * 8);
+            wv[q] = *reinterpret_cast<const uint4 *>(vh + (size_t)r * D + u * 8);
         }
+    }
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            if (b < nb) {
-                const size_t dst_row = (size_t)(i + b) * CHUNK;
-#pragma unroll
-                for (int q = 0; q < PER; ++q) {
-                    const int e = tid + q * SG_THREADS, r = e / U, u = e % U;
-                    if (r < rows_of[b]) {
-                        *reinterpret_cast<uint4 *>(kp + (dst_row + r) * D + u * 8) = wk[b][q];
-                        *reinterpret_cast<uint4 *>(vp + (dst_row + r) * D + u * 8) = wv[b][q];
-                    }
-                }
-            }
+    for (int q = 0; q < PER; ++q) {
+        const int e = tid + q * GA_THREADS, r = e / U, u = e % U;
+        if (r < rows) {
+            *reinterpret_cast<uint4 *>(kp + (size_t)r * D + u * 8) = wk[q];
+            *reinterpret_cast<uint4 *>(vp + (size_t)r * D + u * 8) = wv[q];
         }
     }
 }
@@ -328,28 +309,33 @@ cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_
                                  const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
                                  int32_t *sel, int32_t *part_len, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part,
                                  int64_t ld_part, int num_sms, cudaStream_t st) {
+    (void)num_sms;
     if (injected_launch_failure()) return cudaErrorInvalidValue;
     if (k_sel <= 0 || n_chunks <= 0) return cudaSuccess;
-    int parts = (2 * num_sms + Hkv - 1) / Hkv;
-    if (parts > k_sel) parts = k_sel;
-    if (parts < 1) parts = 1;
-    const int cpp = (k_sel + parts - 1) / parts;
-    parts = (k_sel + cpp - 1) / cpp;
-    const size_t smem = sizeof(uint32_t) * (size_t)n_chunks + sizeof(int32_t) * (size_t)k_sel;
-    dim3 grid(parts, Hkv);
-    cudaError_t e;
-    if (d == 128) {
-        e = cudaFuncSetAttribute(select_gather_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        select_gather_kernel<128><<<grid, SG_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, n_sink, n_recent, k, v,
-                                                                  ld_kv, sel, part_len, k_part, v_part, ld_part, cpp);
-    } else {
-        e = cudaFuncSetAttribute(select_gather_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        select_gather_kernel<64><<<grid, SG_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, n_sink, n_recent, k, v,
-                                                                 ld_kv, sel, part_len, k_part, v_part, ld_part, cpp);
-    }
-    return cudaGetLastError();
+    const size_t smem = sizeof(uint32_t) * (size_t)n_chunks;
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    select_kernel<<<Hkv, SEL_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, n_sink, n_recent, sel, part_len);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the gather as a programmatic dependent of the selection
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(k_sel, Hkv);
+    cfg.blockDim = dim3(GA_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (d == 128)
+        e = cudaLaunchKernelEx(&cfg, gather_kernel<128>, (const int32_t *)sel, N, n_chunks, k_sel, k, v, ld_kv, k_part,
+                               v_part, ld_part);
+    else
+        e = cudaLaunchKernelEx(&cfg, gather_kernel<64>, (const int32_t *)sel, N, n_chunks, k_sel, k, v, ld_kv, k_part,
+                               v_part, ld_part);
+    return e;
 }
 
 }  // namespace ts

@@ -407,7 +407,7 @@ ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_t
                                              static_cast<__nv_bfloat16 *>(v_part), ld_part, num_sms(),
                                              reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "select_gather launch");
-    ts::note_launches(1);
+    ts::note_launches(2);
     return TS_OK;
 }
 

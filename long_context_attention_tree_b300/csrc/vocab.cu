@@ -7,16 +7,17 @@
 //     the target tokens, and a longest accepted draft is kept.
 //
 // Row pass: one thread-block cluster of VOCAB_CLUSTER CTAs per batch row; each
-// CTA owns a contiguous slice of the vocabulary.  Pass 1 streams the slice
-// from HBM (kept in L2) for its penalised (max, argmax); the CTAs exchange
-// those through distributed shared memory; pass 2 re-reads the slice from L2
-// for the min-p count (and the Gumbel-max draw when sampling).  The logits of
-// a step (73 MB for 120 x 152064) fit the 126 MB L2 but not the register
-// file, so two passes with small CTAs keep every SM streaming in about one
-// wave instead of holding a slice in registers.
+// CTA owns a contiguous slice of the vocabulary (76 KB for 152064 ids), which
+// one bulk copy (TMA) moves into shared memory while the CTA builds its
+// window bitmap.  Pass 1 over shared memory gives the slice's penalised
+// (max, argmax); the CTAs exchange those through distributed shared memory;
+// pass 2 over shared memory counts the min-p kept ids (and draws the Gumbel
+// maximum when sampling).  The logits are read from HBM once, by the copy
+// engine, with no chain of dependent loads per thread.
 #include <cooperative_groups.h>
 
 #include "internal.h"
+#include "tc_ptx.cuh"
 #include "ts_common.cuh"
 
 namespace cg = cooperative_groups;
@@ -24,9 +25,8 @@ namespace cg = cooperative_groups;
 namespace ts {
 
 constexpr int VOCAB_CLUSTER = 8;
-constexpr int VOCAB_THREADS = 256;
-constexpr int VOCAB_BATCH = 8;                      // loads in flight per thread
-constexpr int VOCAB_MAX_SLICE = 20480;              // V <= 8 * 20480 = 163840
+constexpr int VOCAB_THREADS = 512;
+constexpr int VOCAB_MAX_SLICE = 20480;              // V <= 8 * 20480 = 163840 (80 KB of shared memory)
 constexpr int VOCAB_BITMAP_WORDS = VOCAB_MAX_SLICE / 32;
 
 struct ArgMax {
@@ -112,22 +112,52 @@ __device__ __forceinline__ ArgMax block_best(ArgMax b, ArgMax *red) {
     return r;
 }
 
+// Bulk copy (TMA, no tensor map) of `bytes` from global to this CTA's shared
+// memory, completing on `bar` (address and size multiples of 16 bytes).
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            tc::smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+
 template <bool SAMPLE>
-__global__ void __cluster_dims__(VOCAB_CLUSTER, 1, 1) __launch_bounds__(VOCAB_THREADS, SAMPLE ? 4 : 7)
+__global__ void __cluster_dims__(VOCAB_CLUSTER, 1, 1) __launch_bounds__(VOCAB_THREADS)
 penalty_minp_kernel(const VocabArgs a, int slice) {
     cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ __align__(16) float xs[];  // this CTA's slice of the row's logits
     __shared__ uint32_t bitmap[VOCAB_BITMAP_WORDS];
     __shared__ ArgMax red[VOCAB_THREADS / 32];
     __shared__ ArgMax cta_best;
     __shared__ int warp_cnt[VOCAB_THREADS / 32];
     __shared__ int cta_cnt;
     __shared__ ArgMax cta_samp;
+    __shared__ __align__(8) uint64_t bar;
 
     const int row = blockIdx.y;
     const unsigned rank = cluster.block_rank();
     const int v0 = (int)rank * slice;
     const int v1 = min(a.V, v0 + slice);
+    const int n = max(0, v1 - v0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *lrow = a.logits + (size_t)row * a.V;
+    // the slice's whole 16-byte units go by one bulk copy; a ragged end (rows
+    // whose start is not 16-byte aligned, or a length not a multiple of 4)
+    // by plain loads
+    const bool aligned = (((uintptr_t)(lrow + v0)) & 15u) == 0;
+    const int n_bulk = aligned ? (n & ~3) : 0;
+    if (tid == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+        if (n_bulk > 0) {
+            tc::mbar_arrive_expect_tx(&bar, (uint32_t)n_bulk * 4u);
+            bulk_g2s(xs, lrow + v0, (uint32_t)n_bulk * 4u, &bar);
+        } else {
+            tc::mbar_arrive(&bar);
+        }
+    }
+    for (int i = n_bulk + tid; i < n; i += VOCAB_THREADS) xs[i] = lrow[v0 + i];
 
     // window bitmap restricted to this slice (ids outside [0, V) are ignored
     // here; the acceptance kernel reports them).  With the path-aware window,
@@ -159,36 +189,27 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
             j = (p < j && p >= -1) ? p : -1;
         }
     }
+    // the slice has landed (bounded wait; a copy that never lands leaves the
+    // row's target undefined, kept = -1, and the acceptance kernel reports
+    // TS_ERR_TIMEOUT in result[3])
+    const bool landed = tc::mbar_wait(&bar, 0, nullptr);
     __syncthreads();
 
-    // penalised, tempered logit of token vv (dividing by a temperature of 1 is
-    // exact, so that division is skipped)
+    // penalised, tempered logit of slice element i (dividing by a temperature
+    // of 1 is exact, so that division is skipped)
     const bool tempered = a.temperature != 1.0f;
-    auto final_logit = [&](float l, int vv) {
-        const int o = vv - v0;
-        if ((bitmap[o >> 5] >> (o & 31)) & 1u) l = l > 0.f ? __fdiv_rn(l, a.theta) : __fmul_rn(l, a.theta);
+    auto final_logit = [&](int i) {
+        float l = xs[i];
+        if ((bitmap[i >> 5] >> (i & 31)) & 1u) l = l > 0.f ? __fdiv_rn(l, a.theta) : __fmul_rn(l, a.theta);
         return tempered ? __fdiv_rn(l, a.temperature) : l;
     };
-    const float *lrow = a.logits + (size_t)row * a.V;
 
-    // ---- pass 1 (HBM): max and lowest argmax of this slice.  A thread's
-    // tokens increase with the loop, so a strict > keeps the lowest index.
+    // ---- pass 1: max and lowest argmax of this slice.  A thread's indices
+    // increase with the loop, so a strict > keeps the lowest one.
     ArgMax best{-INFINITY, -1};
-    for (int base = v0 + tid; base < v1; base += VOCAB_BATCH * VOCAB_THREADS) {
-        float x[VOCAB_BATCH];
-#pragma unroll
-        for (int j = 0; j < VOCAB_BATCH; ++j) {
-            const int vv = base + j * VOCAB_THREADS;
-            x[j] = vv < v1 ? __ldcg(lrow + vv) : 0.f;  // keep the row in L2 for pass 2
-        }
-#pragma unroll
-        for (int j = 0; j < VOCAB_BATCH; ++j) {
-            const int vv = base + j * VOCAB_THREADS;
-            if (vv < v1) {
-                const float l = final_logit(x[j], vv);
-                if (best.i < 0 || l > best.v) best = ArgMax{l, vv};
-            }
-        }
+    for (int i = tid; i < n; i += VOCAB_THREADS) {
+        const float l = final_logit(i);
+        if (best.i < 0 || l > best.v) best = ArgMax{l, v0 + i};
     }
     best = block_best(best, red);
     if (tid == 0) cta_best = best;
@@ -199,26 +220,14 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
     // min-p threshold: smallest fp32 >= m + ln(min_p) (exact comparison)
     const float f = __double2float_ru((double)gbest.v + a.log_min_p);
 
-    // ---- pass 2 (L2): min-p count, and the Gumbel-max draw over the kept ids
+    // ---- pass 2: min-p count, and the Gumbel-max draw over the kept ids
     int cnt = 0;
     ArgMax sb{-INFINITY, -1};
-    for (int base = v0 + tid; base < v1; base += VOCAB_BATCH * VOCAB_THREADS) {
-        float x[VOCAB_BATCH];
-#pragma unroll
-        for (int j = 0; j < VOCAB_BATCH; ++j) {
-            const int vv = base + j * VOCAB_THREADS;
-            x[j] = vv < v1 ? __ldcs(lrow + vv) : 0.f;  // last use: evict first
-        }
-#pragma unroll
-        for (int j = 0; j < VOCAB_BATCH; ++j) {
-            const int vv = base + j * VOCAB_THREADS;
-            if (vv < v1) {
-                const float l = final_logit(x[j], vv);
-                if (l >= f) {
-                    ++cnt;
-                    if constexpr (SAMPLE) sb = better(sb, ArgMax{__fadd_rn(l, gumbel(vv, row, a)), vv});
-                }
-            }
+    for (int i = tid; i < n; i += VOCAB_THREADS) {
+        const float l = final_logit(i);
+        if (l >= f) {
+            ++cnt;
+            if constexpr (SAMPLE) sb = better(sb, ArgMax{__fadd_rn(l, gumbel(v0 + i, row, a)), v0 + i});
         }
     }
 #pragma unroll
@@ -233,18 +242,21 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
     if (tid == 0) {
         int c = 0;
         for (int w = 0; w < VOCAB_THREADS / 32; ++w) c += warp_cnt[w];
-        cta_cnt = c;
+        cta_cnt = landed ? c : -1;  // -1: this CTA's slice never landed
     }
     cluster.sync();
     if (rank == 0 && tid == 0) {
         int total = 0;
+        bool lost = false;
         ArgMax sbest{-INFINITY, -1};
         for (int r = 0; r < VOCAB_CLUSTER; ++r) {
-            total += *cluster.map_shared_rank(&cta_cnt, r);
+            const int c = *cluster.map_shared_rank(&cta_cnt, r);
+            lost = lost || c < 0;
+            total += c;
             if constexpr (SAMPLE) sbest = better(sbest, *cluster.map_shared_rank(&cta_samp, r));
         }
         a.target[row] = SAMPLE ? sbest.i : gbest.i;
-        a.kept[row] = total;
+        a.kept[row] = lost ? -1 : total;
     }
     cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
@@ -276,6 +288,7 @@ __global__ void __launch_bounds__(1024) accept_kernel(const VocabArgs a) {
         s_target[i] = a.target[i];
         s_draft[i] = a.draft[i];
         if (p < -1 || p >= i) atomicOr(&s_bad, 1);
+        if (a.kept[i] < 0) atomicOr(&s_bad, 4);  // the row pass's copy never landed
         a.path[i] = -1;
     }
     for (int w = tid; w < a.W; w += blockDim.x) {
@@ -334,7 +347,7 @@ __global__ void __launch_bounds__(1024) accept_kernel(const VocabArgs a) {
         a.result[0] = L;
         a.result[1] = best;
         a.result[2] = L > 0 ? s_target[best] : a.anchor;
-        a.result[3] = (s_bad & 2) ? 5 : 0;
+        a.result[3] = (s_bad & 4) ? (int)TS_ERR_TIMEOUT : ((s_bad & 2) ? (int)TS_ERR_DATA : 0);
         int pos = L - 1;
         for (int n = best; n >= 0 && pos >= 0; n = s_parent[n], --pos) a.path[pos] = n;
     }
@@ -346,10 +359,17 @@ cudaError_t launch_vocab(const VocabArgs &a, cudaStream_t st) {
     slice = (slice + 31) & ~31;
     if (slice > VOCAB_MAX_SLICE) return cudaErrorInvalidValue;
     dim3 grid(VOCAB_CLUSTER, a.T);
-    if (a.sample)
-        penalty_minp_kernel<true><<<grid, VOCAB_THREADS, 0, st>>>(a, slice);
-    else
-        penalty_minp_kernel<false><<<grid, VOCAB_THREADS, 0, st>>>(a, slice);
+    const size_t smem = (size_t)slice * sizeof(float);
+    cudaError_t e0;
+    if (a.sample) {
+        e0 = cudaFuncSetAttribute(penalty_minp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e0 != cudaSuccess) return e0;
+        penalty_minp_kernel<true><<<grid, VOCAB_THREADS, smem, st>>>(a, slice);
+    } else {
+        e0 = cudaFuncSetAttribute(penalty_minp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e0 != cudaSuccess) return e0;
+        penalty_minp_kernel<false><<<grid, VOCAB_THREADS, smem, st>>>(a, slice);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     accept_kernel<<<1, 1024, 0, st>>>(a);
