@@ -7,40 +7,38 @@
 // Rows of one KV head g are the T x G pairs (t, j), t-major; an M-tile is
 // tpb = floor(128/G) whole batch rows times the G query heads of the group,
 // so every K/V byte staged in shared memory serves all G heads.  A CTA owns
-// one or two M-tiles of one KV head (a pair stream or a single stream) and a
-// contiguous range of 64-token KV tiles.
-//
-// KV tiles are 64 tokens (one scoring chunk), so TMEM holds two S buffers per
-// M-tile: S(m, 0) S(m, 1) (64 columns each) and O(m) (128 columns); for a
-// pair stream that is 4 x 64 + 2 x 128 = all 512 columns.  With S double
-// buffered the MMAs of tile i+1's S run while the softmax of tile i works,
-// so an M-tile's chain is no longer softmax -> P.V -> next S -> softmax: the
-// issuer computes S(i+1) of both M-tiles, then P.V(i) of each as its P lands.
+// one or two M-tiles of one KV head and a contiguous range of 128-token KV
+// tiles:
+//   pair stream   two M-tiles sharing every K/V load; the MMAs of one tile
+//                 run while the softmax of the other works (ping-pong).
+//                 TMEM: S_0 S_1 O_0 O_1 (128 columns each), P_m over S_m.
+//   single stream one M-tile; S is double-buffered so the MMA of the next
+//                 KV tile runs while the softmax works.  TMEM: S_a S_b O.
 // The split counts are chosen on the host so that every CTA carries about
 // the same tensor-core work; the partials are combined by the log-sum-exp
 // merge kernel.
 //
-// Per KV tile and M-tile: S = Q K^T (8 MMAs, M=128 N=64 K=16, operands
-// K-major in shared memory), softmax, O += P V (4 MMAs, M=128 N=128 K=16, P
-// read from TMEM, V MN-major in shared memory).  Every MMA descriptor is
-// precomputed, so the issuing thread only adds constants.
+// Per KV tile and M-tile: S = Q K^T (8 MMAs, M=128 N=128 K=16, operands
+// K-major in shared memory), softmax, O += P V (8 MMAs, P read from TMEM,
+// V MN-major in shared memory).  Every MMA descriptor is precomputed, so the
+// issuing thread only adds constants: issue keeps up with the 64-cycle MMAs.
 //
 // Warp roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: Q once, then K and V tiles into 4-stage rings;
+//   warp 0      TMA producer: Q once, then K and V tiles into 2-stage rings;
 //   warp 1      owns TMEM (512 columns); one thread issues every tcgen05.mma;
 //   warp 2      chunk-score reducer: takes the scoring rows' chunk sums from a
 //               shared-memory ring and writes the max over the group's heads;
 //   warp 3      idle;
 //   warps 4-7   softmax warpgroup 0 (thread = row of M-tile 0);
 //   warps 8-11  softmax warpgroup 1 (M-tile 1 of a pair stream).
-// A softmax thread loads its row of S (64 fp32) into registers and writes
-// P = 2^(s*c - m) as bf16 over the first 32 columns of that S buffer.  The
-// running max is lazy: O and l are rescaled only when a row's max grows by
-// more than 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so the
-// TMEM round trip of a rescale is rare.  The normaliser l sums the
-// bf16-rounded weights that the P.V product uses.  The chunk importance of
-// the scoring row is summed from the same S values and handed to warp 2, so
-// the softmax warps never wait for the reduction.
+// A softmax thread loads its row of S (128 fp32) into registers and writes
+// P = 2^(s*c - m) as bf16 over the first 64 columns of S.  The running max
+// is lazy: O and l are rescaled only when a row's max grows by more than
+// 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so the TMEM
+// round trip of a rescale is rare.  The normaliser l sums the bf16-rounded
+// weights that the P.V product uses.  The chunk importance of the scoring
+// row is summed from the same S values (packed adds) and handed to warp 2,
+// so the softmax warps never wait for the reduction.
 // Every wait is bounded (see tc_ptx.cuh): a wait that gives up raises the
 // CTA's abort flag and the sticky device status word, and the CTA winds down.
 #include "internal.h"
@@ -54,29 +52,28 @@ __device__ int g_device_error = 0;
 namespace {
 
 constexpr int TC_THREADS = 384;  // 168 registers per thread (3 warps per SM sub-partition)
-constexpr int KV_TILE = TC_KV_TILE;           // 64 tokens: one scoring chunk
-constexpr int Q_TILE_BYTES = 128 * 128 * 2;   // 128 rows x 128 dims, two 64-column swizzled halves
-constexpr int Q_HALF_BYTES = Q_TILE_BYTES / 2;
-constexpr int KV_TILE_BYTES = KV_TILE * 128 * 2;  // 64 tokens x 128 dims
-constexpr int KV_HALF_BYTES = KV_TILE_BYTES / 2;
-constexpr int NSTAGE = 4;                     // K and V ring depth
-constexpr int SMEM_DATA_BYTES = 2 * Q_TILE_BYTES + 2 * NSTAGE * KV_TILE_BYTES;  // 192 KB
-constexpr float RESCALE_THRESHOLD = 20.0f;    // log2 units
-constexpr int SCORE_RING = 4;                 // chunk-score slots between the scoring rows and warp 2
+constexpr int KV_TILE = TC_KV_TILE;         // 128 tokens
+constexpr int TILE_BYTES = 128 * 128 * 2;   // 128 rows x 128 dims, two 64-column swizzled halves
+constexpr int HALF_BYTES = TILE_BYTES / 2;
+constexpr int NSTAGE = 2;                   // K and V ring depth (pair: 2 Q + 2 K + 2 V = 192 KB)
+constexpr int SMEM_DATA_BYTES = 6 * TILE_BYTES;
+constexpr float RESCALE_THRESHOLD = 20.0f;  // log2 units
+constexpr int SCORE_RING = 4;               // chunk-score slots between the scoring rows and warp 2
 
 struct __align__(8) TcSmemTail {
     uint64_t q_full;
     uint64_t k_full[NSTAGE], k_empty[NSTAGE];
     uint64_t v_full[NSTAGE], v_empty[NSTAGE];
-    // [M-tile][S buffer]: completion n of a buffer is tile 2n + b, parity n & 1
-    uint64_t s_full[2][2], p_full[2][2];
-    uint64_t o_done[2];   // one commit per tile: the P.V of tile i completes phase i
-    uint64_t o_final[2];  // one commit after the last P.V of the M-tile (epilogue)
+    // [slot]: the M-tile (pair stream, phase = tile) or the S buffer tile & 1
+    // (single stream, phase = tile >> 1).  A single stream's warps may run a
+    // tile ahead of one another, so its barriers are per buffer: a parity
+    // wait must never be two phases behind.
+    uint64_t s_full[2], p_half[2], p_full[2], o_done[2];  // p_half: P of tokens 0-63 written
     uint64_t mma_done;
-    // Chunk scores: the G scoring rows put their chunk sum of a KV tile into a
-    // ring slot (tile & 3); warp 2 takes the max over the group's heads.
+    // Chunk scores: the G scoring rows put their two chunk sums of a KV tile
+    // into a ring slot (tile & 3); warp 2 takes the max over the group's heads.
     uint64_t score_full[SCORE_RING], score_empty[SCORE_RING];
-    float score_sum[SCORE_RING][32];  // [slot][head j]
+    float score_sum[SCORE_RING][2][32];          // [slot][chunk half][head j]
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -95,26 +92,27 @@ __device__ __forceinline__ void raise_abort(TcSmemTail *tl) {
     atomicExch(&g_device_error, (int)TS_ERR_TIMEOUT);
 }
 
-// Descriptors of swizzled tile halves, as 64-bit values to which a byte
-// offset >> 4 is added directly (the 14-bit start field cannot overflow
+// Descriptors of 128-row swizzled tile halves, as 64-bit values to which a
+// byte offset >> 4 is added directly (the 14-bit start field cannot overflow
 // inside the 227 KB shared-memory window).
 __device__ __forceinline__ uint64_t desc_k(uint32_t addr) { return tc::smem_desc_sw128(addr, 16, 1024); }
-__device__ __forceinline__ uint64_t desc_mn(uint32_t addr) { return tc::smem_desc_sw128(addr, KV_HALF_BYTES, 1024); }
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr) { return tc::smem_desc_sw128(addr, HALF_BYTES, 1024); }
 __device__ __forceinline__ uint64_t dplus(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
-// S[128 x 64] = Q[128 x 128] K^T: 8 MMAs with K = 16 over the head dim.
+// S[128 x 128] = Q[128 x 128] K^T: 8 MMAs with K = 16 over the head dim.
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t dq, uint64_t dk, uint32_t idesc) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint32_t col = (uint32_t)((k & 3) * 32);
-        tc::mma_ss(d_tmem, dplus(dq, (uint32_t)(k >> 2) * Q_HALF_BYTES + col),
-                   dplus(dk, (uint32_t)(k >> 2) * KV_HALF_BYTES + col), idesc, k > 0);
+        const uint32_t off = (uint32_t)((k >> 2) * HALF_BYTES + (k & 3) * 32);
+        tc::mma_ss(d_tmem, dplus(dq, off), dplus(dk, off), idesc, k > 0);
     }
 }
-// O[128 x 128] += P[128 x 64 tokens] V[64 tokens x 128]: 4 MMAs with K = 16 tokens.
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t dv, uint32_t idesc, bool accumulate) {
+// O[128 x 128] += P[128 x 64 tokens] V[64 tokens x 128] for one half of the
+// tile (tokens 64h..64h+63): 4 MMAs with K = 16 tokens.
+__device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, uint64_t dv, uint32_t idesc, int h,
+                                              bool accumulate) {
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
+    for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
         tc::mma_ts(o_tmem, p_tmem + kk * 8, dplus(dv, (uint32_t)kk * 2048), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
@@ -177,7 +175,7 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], float2 c2, f
     }
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
-// Chunk sum of the scoring row.  A whole 64-token chunk (a[] and b[]) is a
+// Chunk sums of the scoring row.  A whole 64-token chunk (a[] and b[]) is a
 // tree of packed adds (32 instructions); the chunk at the end of the prefix
 // sums x[0..lim) (lim clamped to [0, 32]) with eight partial sums.
 __device__ __forceinline__ float sum64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
@@ -198,10 +196,6 @@ __device__ __forceinline__ float sum_chunk(const uint32_t (&x)[32], int lim) {
     for (int i = 0; i < 32; ++i) p[i & 7] += (i < lim) ? __uint_as_float(x[i]) : 0.f;
     return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
-
-// TMEM columns: S(m, b) at 64 (2m + b); O(m) at 256 + 128 m.
-__device__ __forceinline__ uint32_t s_col(int m, int b) { return (uint32_t)(64 * (2 * m + b)); }
-__device__ __forceinline__ uint32_t o_col(int m) { return (uint32_t)(256 + 128 * m); }
 
 }  // namespace
 
@@ -233,9 +227,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int nm = pair ? 2 : 1;
     const int tile_begin = split * tiles_per;
     const int n_my = max(0, min(L.n_tiles, tile_begin + tiles_per) - tile_begin);
-    unsigned char *sQ = base;                            // [2][Q_TILE_BYTES]
-    unsigned char *sK = sQ + (size_t)2 * Q_TILE_BYTES;   // [NSTAGE][KV_TILE_BYTES]
-    unsigned char *sV = sK + (size_t)NSTAGE * KV_TILE_BYTES;
+    unsigned char *sQ = base;                          // [nm][TILE_BYTES]
+    unsigned char *sK = sQ + (size_t)nm * TILE_BYTES;  // [NSTAGE][TILE_BYTES]
+    unsigned char *sV = sK + (size_t)NSTAGE * TILE_BYTES;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.G, tpb = L.tpb;
@@ -253,12 +247,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tc::mbar_init(&tl->v_empty[s], 1);
         }
         for (int m = 0; m < 2; ++m) {
-            for (int b = 0; b < 2; ++b) {
-                tc::mbar_init(&tl->s_full[m][b], 1);
-                tc::mbar_init(&tl->p_full[m][b], 128);
-            }
+            tc::mbar_init(&tl->s_full[m], 1);
+            tc::mbar_init(&tl->p_half[m], 128);
+            tc::mbar_init(&tl->p_full[m], 128);
             tc::mbar_init(&tl->o_done[m], 1);
-            tc::mbar_init(&tl->o_final[m], 1);
         }
         tc::mbar_init(&tl->mma_done, 1);
         for (int sl = 0; sl < SCORE_RING; ++sl) {
@@ -274,7 +266,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int per_half = (128 - rows_loaded) * 8;  // 16-byte units
         for (int e = threadIdx.x; e < nm * 2 * per_half; e += TC_THREADS) {
             const int mh = e / per_half, u = e % per_half;
-            uint4 *dst = reinterpret_cast<uint4 *>(sQ + (size_t)mh * Q_HALF_BYTES + (size_t)rows_loaded * 128) + u;
+            uint4 *dst = reinterpret_cast<uint4 *>(sQ + (size_t)mh * HALF_BYTES + (size_t)rows_loaded * 128) + u;
             *dst = make_uint4(0u, 0u, 0u, 0u);
         }
         tc::fence_proxy_async();
@@ -299,7 +291,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tc::mbar_arrive_expect_tx(&tl->q_full, qbytes * nm);
             for (int m = 0; m < nm; ++m)
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sQ + m * Q_TILE_BYTES + h * Q_HALF_BYTES, &tm_q, &tl->q_full, h * 64, g * G,
+                    tc::tma_load_3d(sQ + m * TILE_BYTES + h * HALF_BYTES, &tm_q, &tl->q_full, h * 64, g * G,
                                     (mt0 + m) * tpb);
             int nk = 0, nv = 0;  // K and V tiles issued
             int st = 0;
@@ -307,14 +299,14 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             for (int it = 0; it < n_my; ++it) {
                 const int tok0 = (tile_begin + it) * KV_TILE;
                 if (it >= NSTAGE && !tc::mbar_wait(&tl->k_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
-                tc::mbar_arrive_expect_tx(&tl->k_full[st], KV_TILE_BYTES);
+                tc::mbar_arrive_expect_tx(&tl->k_full[st], TILE_BYTES);
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sK + st * KV_TILE_BYTES + h * KV_HALF_BYTES, &tm_k, &tl->k_full[st], h * 64, tok0, g);
+                    tc::tma_load_3d(sK + st * TILE_BYTES + h * HALF_BYTES, &tm_k, &tl->k_full[st], h * 64, tok0, g);
                 nk = it + 1;
                 if (it >= NSTAGE && !tc::mbar_wait(&tl->v_empty[st], ph ^ 1u, abort_flag)) { raise_abort(tl); break; }
-                tc::mbar_arrive_expect_tx(&tl->v_full[st], KV_TILE_BYTES);
+                tc::mbar_arrive_expect_tx(&tl->v_full[st], TILE_BYTES);
                 for (int h = 0; h < 2; ++h)
-                    tc::tma_load_3d(sV + st * KV_TILE_BYTES + h * KV_HALF_BYTES, &tm_v, &tl->v_full[st], h * 64, tok0, g);
+                    tc::tma_load_3d(sV + st * TILE_BYTES + h * HALF_BYTES, &tm_v, &tl->v_full[st], h * 64, tok0, g);
                 nv = it + 1;
                 if (++st == NSTAGE) { st = 0; ph ^= 1u; }
             }
@@ -327,8 +319,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
       } else if (warp == 2) {
         // ------------------------------------------------------------ chunk-score reducer
-        // Off the softmax's critical path: per KV tile (one chunk), the max over
-        // the group's heads of the scoring rows' chunk sums.
+        // Off the softmax's critical path: per KV tile, the max over the group's
+        // heads of the scoring rows' two chunk sums.
         if (lane == 0 && score_wm >= 0) {
             for (int it = 0; it < n_my; ++it) {
                 const int sl = it & (SCORE_RING - 1);
@@ -336,60 +328,104 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     raise_abort(tl);
                     break;
                 }
-                float b0 = -INFINITY;
-                for (int j = 0; j < G; ++j) b0 = fmaxf(b0, tl->score_sum[sl][j]);
+                float b0 = -INFINITY, b1 = -INFINITY;
+                for (int j = 0; j < G; ++j) {
+                    b0 = fmaxf(b0, tl->score_sum[sl][0][j]);
+                    b1 = fmaxf(b1, tl->score_sum[sl][1][j]);
+                }
                 tc::mbar_arrive(&tl->score_empty[sl]);
                 const int tile = tile_begin + it;
-                if ((int64_t)tile * KV_TILE < a.N) a.chunk_scores[(size_t)g * a.n_chunks + tile] = b0;
+                const int64_t tok0 = (int64_t)tile * KV_TILE;
+                if (tok0 < a.N) a.chunk_scores[(size_t)g * a.n_chunks + 2 * tile] = b0;
+                if (tok0 + 64 < a.N) a.chunk_scores[(size_t)g * a.n_chunks + 2 * tile + 1] = b1;
             }
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // S(i+1) of every M-tile is issued before P.V(i): the S buffers alternate,
-        // so S(i+1) overwrites the buffer of tile i-1, whose P.V was issued (and,
-        // the pipe being in order, executed) before.
         if (lane == 0 && n_my > 0) {
-            const uint32_t id_s = tc::idesc_bf16_f32(128, KV_TILE, false);
+            const uint32_t id_s = tc::idesc_bf16_f32(128, 128, false);
             const uint32_t id_o = tc::idesc_bf16_f32(128, 128, true);
-            const uint64_t dq[2] = {desc_k(tc::smem_u32(sQ)), desc_k(tc::smem_u32(sQ + Q_TILE_BYTES))};
+            const uint64_t dq0 = desc_k(tc::smem_u32(sQ)), dq1 = desc_k(tc::smem_u32(sQ + TILE_BYTES));
             const uint64_t dk0 = desc_k(tc::smem_u32(sK)), dv0 = desc_mn(tc::smem_u32(sV));
+            int kst = 0, vst = 0;
+            uint32_t kph = 0, vph = 0;
             bool ok = tc::mbar_wait(&tl->q_full, 0, abort_flag);
-            if (ok) ok = tc::mbar_wait(&tl->k_full[0], 0, abort_flag);
+            if (ok) ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag);
             if (ok) {
                 tc::fence_after_sync();
-                for (int m = 0; m < nm; ++m) {
-                    issue_s(tbase + s_col(m, 0), dq[m], dk0, id_s);
-                    tc::mma_commit(&tl->s_full[m][0]);
+                const uint64_t dk = dplus(dk0, (uint32_t)kst * TILE_BYTES);
+                issue_s(tbase + 0, dq0, dk, id_s);
+                tc::mma_commit(&tl->s_full[0]);
+                if (pair) {
+                    issue_s(tbase + 128, dq1, dk, id_s);
+                    tc::mma_commit(&tl->s_full[1]);
                 }
-                tc::mma_commit(&tl->k_empty[0]);
+                tc::mma_commit(&tl->k_empty[kst]);
+                if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
             }
             for (int it = 0; ok && it < n_my; ++it) {
-                if (it + 1 < n_my) {
-                    const int kst = (it + 1) % NSTAGE;
-                    if (!(ok = tc::mbar_wait(&tl->k_full[kst], (uint32_t)((it + 1) / NSTAGE) & 1u, abort_flag))) break;
+                const bool more = it + 1 < n_my;
+                if (pair) {
+                    // PV_0(it), S_0(it+1), PV_1(it), S_1(it+1): while one M-tile's
+                    // softmax works, the tensor pipe runs the other tile's MMAs.
+                    const uint32_t par = (uint32_t)it & 1u;
+                    if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
+                    const uint64_t dv = dplus(dv0, (uint32_t)vst * TILE_BYTES);
+                    // each half of P goes to the tensor pipe as soon as it is written
+                    if (!(ok = tc::mbar_wait(&tl->p_half[0], par, abort_flag))) break;
                     tc::fence_after_sync();
-                    const uint64_t dk = dplus(dk0, (uint32_t)kst * KV_TILE_BYTES);
-                    const int b = (it + 1) & 1;
-                    for (int m = 0; m < nm; ++m) {
-                        issue_s(tbase + s_col(m, b), dq[m], dk, id_s);
-                        tc::mma_commit(&tl->s_full[m][b]);
+                    issue_pv_half(tbase + 256, tbase + 0, dv, id_o, 0, it > 0);
+                    if (!(ok = tc::mbar_wait(&tl->p_full[0], par, abort_flag))) break;
+                    tc::fence_after_sync();
+                    issue_pv_half(tbase + 256, tbase + 0, dv, id_o, 1, true);
+                    tc::mma_commit(&tl->o_done[0]);
+                    uint64_t dk = 0;
+                    if (more) {
+                        if (!(ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag))) break;
+                        tc::fence_after_sync();
+                        dk = dplus(dk0, (uint32_t)kst * TILE_BYTES);
+                        issue_s(tbase + 0, dq0, dk, id_s);
+                        tc::mma_commit(&tl->s_full[0]);
                     }
-                    tc::mma_commit(&tl->k_empty[kst]);
-                }
-                const int vst = it % NSTAGE;
-                if (!(ok = tc::mbar_wait(&tl->v_full[vst], (uint32_t)(it / NSTAGE) & 1u, abort_flag))) break;
-                const uint64_t dv = dplus(dv0, (uint32_t)vst * KV_TILE_BYTES);
-                const int b = it & 1;
-                for (int m = 0; m < nm && ok; ++m) {
-                    if (!(ok = tc::mbar_wait(&tl->p_full[m][b], (uint32_t)(it >> 1) & 1u, abort_flag))) break;
+                    if (!(ok = tc::mbar_wait(&tl->p_half[1], par, abort_flag))) break;
                     tc::fence_after_sync();
-                    issue_pv(tbase + o_col(m), tbase + s_col(m, b), dv, id_o, it > 0);
-                    tc::mma_commit(&tl->o_done[m]);
+                    issue_pv_half(tbase + 384, tbase + 128, dv, id_o, 0, it > 0);
+                    if (!(ok = tc::mbar_wait(&tl->p_full[1], par, abort_flag))) break;
+                    tc::fence_after_sync();
+                    issue_pv_half(tbase + 384, tbase + 128, dv, id_o, 1, true);
+                    tc::mma_commit(&tl->o_done[1]);
+                    tc::mma_commit(&tl->v_empty[vst]);
+                    if (++vst == NSTAGE) { vst = 0; vph ^= 1u; }
+                    if (more) {
+                        issue_s(tbase + 128, dq1, dk, id_s);
+                        tc::mma_commit(&tl->s_full[1]);
+                        tc::mma_commit(&tl->k_empty[kst]);
+                        if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
+                    }
+                } else {
+                    // S(it+1) into the other S buffer, then PV(it).
+                    if (more) {
+                        if (!(ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag))) break;
+                        tc::fence_after_sync();
+                        const int b = (it + 1) & 1;
+                        issue_s(tbase + 128 * b, dq0, dplus(dk0, (uint32_t)kst * TILE_BYTES), id_s);
+                        tc::mma_commit(&tl->s_full[b]);
+                        tc::mma_commit(&tl->k_empty[kst]);
+                        if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
+                    }
+                    if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
+                    const int b = it & 1;
+                    // (a single stream's next S is already in flight: P.V goes as one piece)
+                    const uint64_t dv = dplus(dv0, (uint32_t)vst * TILE_BYTES);
+                    if (!(ok = tc::mbar_wait(&tl->p_full[b], (uint32_t)(it >> 1) & 1u, abort_flag))) break;
+                    tc::fence_after_sync();
+                    issue_pv_half(tbase + 256, tbase + 128 * b, dv, id_o, 0, it > 0);
+                    issue_pv_half(tbase + 256, tbase + 128 * b, dv, id_o, 1, true);
+                    tc::mma_commit(&tl->o_done[b]);
+                    tc::mma_commit(&tl->v_empty[vst]);
+                    if (++vst == NSTAGE) { vst = 0; vph ^= 1u; }
                 }
-                if (ok) tc::mma_commit(&tl->v_empty[vst]);
             }
-            if (ok)
-                for (int m = 0; m < nm; ++m) tc::mma_commit(&tl->o_final[m]);
             if (!ok) raise_abort(tl);
             // drain: every issued MMA completes before TMEM is released
             tc::mma_commit(&tl->mma_done);
@@ -411,56 +447,51 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const bool is_score_row = score_wm == wm && row_valid && t == a.score_row;
             const bool score_warp = __any_sync(0xffffffffu, is_score_row);
             const int64_t plen = prefix_of(a, g);
-            const uint32_t o_addr = lane_addr + o_col(wm);
+            const uint32_t o_addr = lane_addr + (pair ? 256u + 128u * (uint32_t)wm : 256u);
             const float c = a.scale_log2;
             const float2 c2 = make_float2(c, c);
             float m_run = -INFINITY, l_run = 0.f;
             bool ok = true;
             for (int it = 0; it < n_my; ++it) {
-                const int b = it & 1;
+                const int slot = pair ? wm : (it & 1);
+                const uint32_t spar = pair ? ((uint32_t)it & 1u) : ((uint32_t)(it >> 1) & 1u);
                 const int tile = tile_begin + it;
                 const int64_t tok0 = (int64_t)tile * KV_TILE;
-                ok = tc::mbar_wait(&tl->s_full[wm][b], (uint32_t)(it >> 1) & 1u, abort_flag);
+                ok = tc::mbar_wait(&tl->s_full[slot], spar, abort_flag);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc::fence_after_sync();
-                const uint32_t s_addr = lane_addr + s_col(wm, b);
-                uint32_t x0[32], x1[32];
+                const uint32_t s_addr = lane_addr + 128u * (uint32_t)slot;
+                uint32_t x0[32], x1[32], x2[32], x3[32];
+                // the second half of S loads while the first half's max is taken
                 tc::tmem_ld32(s_addr + 0, x0);
                 tc::tmem_ld32(s_addr + 32, x1);
                 tc::tmem_wait_ld();
-
-                // ---- fused chunk importance of the scoring row: chunk `tile`
-                // (raw q.k summed over its tokens < N) into the ring for warp 2
-                if (score_warp) {
-                    if (is_score_row) {
-                        float s0;
-                        if (tok0 + KV_TILE <= a.N) {
-                            s0 = sum64(x0, x1);
-                        } else {
-                            const int64_t lim64 = a.N - tok0;
-                            const int lim = lim64 < 0 ? 0 : (int)lim64;
-                            s0 = sum_chunk(x0, lim) + sum_chunk(x1, lim - 32);
-                        }
-                        const int sl = it & (SCORE_RING - 1);
-                        if (it < SCORE_RING ||
-                            tc::mbar_wait(&tl->score_empty[sl], (uint32_t)(it / SCORE_RING - 1) & 1u, abort_flag)) {
-                            tl->score_sum[sl][j] = s0;
-                            tc::mbar_arrive(&tl->score_full[sl]);
-                        } else {
-                            raise_abort(tl);
-                        }
-                    }
-                    __syncwarp();
-                }
-
-                // ---- tiles that reach past the head's prefix: hide what this row may not see
-                if (tok0 + KV_TILE > plen) {
+                tc::tmem_ld32(s_addr + 64, x2);
+                tc::tmem_ld32(s_addr + 96, x3);
+                const bool tail = tok0 + KV_TILE > plen;
+                // the scoring row's chunk sums read raw S; the masking below only
+                // hides tokens past the prefix, which the sums leave out anyway
+                float mx01;
+                if (tail) {
                     mask_chunk(x0, tok0 + 0, plen, a.N, a.T, mrow);
                     mask_chunk(x1, tok0 + 32, plen, a.N, a.T, mrow);
                 }
+                mx01 = fmaxf(max_chunk(x0), max_chunk(x1));
+                // the scoring row's chunk sums (tokens < N of chunks 2*tile, 2*tile+1);
+                // they go to warp 2 after P is handed over
+                float cs0 = 0.f, cs1 = 0.f;
+                const bool whole = tok0 + KV_TILE <= a.N;
+                const int lim = whole ? KV_TILE : (a.N - tok0 < 0 ? 0 : (int)(a.N - tok0));
+                if (is_score_row) cs0 = whole ? sum64(x0, x1) : sum_chunk(x0, lim) + sum_chunk(x1, lim - 32);
+                tc::tmem_wait_ld();
+                if (is_score_row) cs1 = whole ? sum64(x2, x3) : sum_chunk(x2, lim - 64) + sum_chunk(x3, lim - 96);
+                if (tail) {
+                    mask_chunk(x2, tok0 + 64, plen, a.N, a.T, mrow);
+                    mask_chunk(x3, tok0 + 96, plen, a.N, a.T, mrow);
+                }
 
                 // ---- row max (raw units), lazy running-max update
-                const float mx = fmaxf(max_chunk(x0), max_chunk(x1));
+                const float mx = fmaxf(mx01, fmaxf(max_chunk(x2), max_chunk(x3)));
                 const float m_new = fmaxf(m_run, mx * c);
                 const bool resc = m_new > m_run + RESCALE_THRESHOLD;
                 const float alpha = resc ? tc::ex2(m_run - m_new) : 1.f;
@@ -469,25 +500,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     m_run = m_new;
                 }
 
-                // ---- rescale O by alpha before this tile's P.V: the previous
-                // tile's P.V into O must have completed
-                if (it > 0 && __any_sync(0xffffffffu, resc)) {
-                    ok = tc::mbar_wait(&tl->o_done[wm], (uint32_t)(it - 1) & 1u, abort_flag);
-                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t ov[32];
-                        tc::tmem_ld32(o_addr + cc * 32, ov);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tc::tmem_st32(o_addr + cc * 32, ov);
-                    }
-                }
-
-                // ---- P = 2^(s*c - m) in bf16 over the first 32 columns of this S
-                // buffer (token k -> column k/2, even k in the lower half)
+                // ---- P = 2^(s*c - m) in bf16 over the first 64 columns of S
+                // (token k -> column k/2, even k in the lower half; S is in registers).
+                // Tokens 0-63 first: their P.V is issued while tokens 64-127 are
+                // exponentiated.
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 const float2 nm2 = make_float2(neg_m, neg_m);
                 float lsum;
@@ -501,16 +517,71 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     lsum += exp_chunk(x1, c2, nm2, pk);
                     tc::tmem_st16(s_addr + 16, pk);
                 }
+
+                // ---- rescale O by alpha (before this tile's first P.V)
+                if (it > 0 && __any_sync(0xffffffffu, resc)) {
+                    if (!pair) {
+                        // a single stream computes S ahead: wait for the previous P.V into O
+                        ok = tc::mbar_wait(&tl->o_done[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1u, abort_flag);
+                        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                    }
+                    // (a pair stream's S_m(it) was issued after P_m(it-1).V, so O_m is final here)
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t ov[32];
+                        tc::tmem_ld32(o_addr + cc * 32, ov);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tc::tmem_st32(o_addr + cc * 32, ov);
+                    }
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                tc::mbar_arrive(&tl->p_half[slot]);
+                {
+                    uint32_t pk[16];
+                    lsum += exp_chunk(x2, c2, nm2, pk);
+                    tc::tmem_st16(s_addr + 32, pk);
+                }
+                {
+                    uint32_t pk[16];
+                    lsum += exp_chunk(x3, c2, nm2, pk);
+                    tc::tmem_st16(s_addr + 48, pk);
+                }
                 l_run += lsum;
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
-                tc::mbar_arrive(&tl->p_full[wm][b]);
+                tc::mbar_arrive(&tl->p_full[slot]);
+
+                // ---- fused chunk importance of the scoring row into the ring for
+                // warp 2, after P is handed over so that the ring handshake stays off
+                // the M-tile's critical path
+                if (score_warp) {
+                    if (is_score_row) {
+                        const int sl = it & (SCORE_RING - 1);
+                        if (it < SCORE_RING ||
+                            tc::mbar_wait(&tl->score_empty[sl], (uint32_t)(it / SCORE_RING - 1) & 1u, abort_flag)) {
+                            tl->score_sum[sl][0][j] = cs0;
+                            tl->score_sum[sl][1][j] = cs1;
+                            tc::mbar_arrive(&tl->score_full[sl]);
+                        } else {
+                            raise_abort(tl);
+                        }
+                    }
+                    __syncwarp();
+                }
             }
 
-            // ---- epilogue: O of this range.  S(i+1) is issued before P.V(i), so the
-            // last softmax does not imply that the P.V before the last one has
-            // completed: wait on the commit that follows every P.V of this M-tile.
-            if (ok) ok = tc::mbar_wait(&tl->o_final[wm], 0u, abort_flag);
+            // ---- epilogue: O of this range
+            // (completion of the last P.V implies every earlier one: MMAs complete in order)
+            if (ok) {
+                if (pair)
+                    ok = tc::mbar_wait(&tl->o_done[wm], (uint32_t)(n_my - 1) & 1u, abort_flag);
+                else
+                    ok = tc::mbar_wait(&tl->o_done[(n_my - 1) & 1], (uint32_t)((n_my - 1) >> 1) & 1u, abort_flag);
+            }
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 raise_abort(tl);

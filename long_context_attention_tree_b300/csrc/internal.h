@@ -72,7 +72,7 @@ int small_splits(int T, int64_t N);
 cudaError_t launch_tree_attn_small(const AttnArgs &a, int splits, cudaStream_t st);
 
 // tensor-core (tcgen05) path, head_dim 128, 64 <= T <= 128.
-constexpr int TC_KV_TILE = 64;   // KV tokens per pipeline step (one scoring chunk)
+constexpr int TC_KV_TILE = 128;  // KV tokens per pipeline step (two 64-token scoring chunks)
 // Per KV head the M-tiles are grouped into n_pair two-tile streams (ping-pong
 // between the two tiles) and n_single one-tile streams (double-buffered S);
 // each stream's KV tiles are split into s_pair / s_single contiguous ranges.

@@ -105,7 +105,7 @@ cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *score
 }
 
 // ---------------------------------------------------------------------------
-// Top-k selection (radix select on order-preserving keys), then the gather.
+// Top-k selection (bitonic sort of order-preserving keys), then the gather.
 // select_kernel: one CTA per KV head computes sel[g][.] and part_len[g];
 // gather_kernel: CTA = (selected chunk, KV head) copies the chunk's K and V
 // rows.  The gather is launched as a programmatic dependent of the selection
@@ -120,142 +120,71 @@ __device__ __forceinline__ uint32_t order_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block scan of one int per thread; returns the prefix, writes the total.
-__device__ int block_exclusive_scan(int x, int *warp_tot, int *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        int w = lane < nw ? warp_tot[lane] : 0;
-        int wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += y;
+// Bitonic sort of v[0, P) (P a power of two, at least 64) into descending
+// (DESC) or ascending order by every thread of the CTA.  Stages whose stride
+// is below 64 pair elements inside one warp's 64-element window, so only the
+// wider stages need a block barrier.
+template <typename K, bool DESC>
+__device__ void bitonic_sort_block(K *v, int P) {
+    const int nthr = blockDim.x;
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < (P >> 1); i += nthr) {
+                const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+                const bool first = (lo & size) == 0;  // this run ends in the requested order
+                const K a = v[lo], b = v[hi];
+                if ((first == DESC) ? (a < b) : (a > b)) {
+                    v[lo] = b;
+                    v[hi] = a;
+                }
+            }
+            if (stride > 32) __syncthreads(); else __syncwarp();
         }
-        if (lane < nw) warp_tot[lane] = wi - w;  // exclusive warp offsets
-        if (lane == nw - 1) *total = wi;
+        __syncthreads();
     }
-    __syncthreads();
-    const int r = warp_tot[warp] + incl - x;
-    __syncthreads();
-    return r;
 }
 
+// Per KV head: composite keys (order key << 32 | ~index) sorted descending put
+// the k largest scores first, equal scores by lower index; their indices are
+// then sorted ascending.
 __global__ void __launch_bounds__(SEL_THREADS)
 select_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
               int32_t *__restrict__ sel, int32_t *__restrict__ part_len) {
-    extern __shared__ __align__(16) uint32_t keys[];  // [n_chunks]
-    __shared__ int hist[256];
-    __shared__ int warp_tot[32];
-    __shared__ int s_total, s_last;
-    __shared__ uint32_t s_prefix;
-    __shared__ int s_remaining;
+    extern __shared__ __align__(16) uint64_t keys[];  // [P] then uint32 idx[PK]
+    __shared__ int s_last;
     // the gather grid may launch now; it waits for this grid's results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
     const int g = blockIdx.x, tid = threadIdx.x;
+    int P = 64;
+    while (P < n_chunks) P <<= 1;
+    int PK = 64;
+    while (PK < k_sel) PK <<= 1;
+    uint32_t *idx = reinterpret_cast<uint32_t *>(keys + P);
     const float *sc = scores + (size_t)g * n_chunks;
     // always-kept chunks (the first n_sink, the last n_recent) take the largest
-    // key, above every finite score's
-    for (int c = tid; c < n_chunks; c += SEL_THREADS)
-        keys[c] = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
-    if (tid == 0) {
-        s_prefix = 0u;
-        s_remaining = k_sel;
-        s_last = 0;
+    // key, above every finite score's; padding sorts last (0 is below every key)
+    for (int c = tid; c < P; c += SEL_THREADS) {
+        uint64_t kv = 0;
+        if (c < n_chunks) {
+            const uint32_t key = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
+            kv = ((uint64_t)key << 32) | (uint32_t)~(uint32_t)c;
+        }
+        keys[c] = kv;
+    }
+    if (tid == 0) s_last = 0;
+    __syncthreads();
+    bitonic_sort_block<uint64_t, true>(keys, P);
+    for (int i = tid; i < PK; i += SEL_THREADS) {
+        uint32_t c = 0xffffffffu;  // padding sorts last
+        if (i < k_sel) {
+            c = ~(uint32_t)keys[i];
+            if ((int)c == n_chunks - 1) s_last = 1;
+        }
+        idx[i] = c;
     }
     __syncthreads();
-
-    // --- radix select of the k-th largest key, 8 bits at a time from the top
-    uint32_t pmask = 0u;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int b = tid; b < 256; b += SEL_THREADS) hist[b] = 0;
-        __syncthreads();
-        const uint32_t prefix = s_prefix;
-        for (int c = tid; c < n_chunks; c += SEL_THREADS) {
-            const uint32_t key = keys[c];
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
-        }
-        __syncthreads();
-        if (tid < 32) {
-            // lane L owns digits 255-8L .. 248-8L (descending)
-            int cnt[8];
-            int lsum = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                cnt[i] = hist[255 - 8 * tid - i];
-                lsum += cnt[i];
-            }
-            int incl = lsum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl += y;
-            }
-            const int excl = incl - lsum;
-            const int rem = s_remaining;
-            if (excl < rem && incl >= rem) {
-                int cum = excl;
-                int digit = 255 - 8 * tid;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (cum + cnt[i] >= rem) {
-                        digit = 255 - 8 * tid - i;
-                        break;
-                    }
-                    cum += cnt[i];
-                }
-                s_prefix = prefix | ((uint32_t)digit << shift);
-                s_remaining = rem - cum;
-            }
-        }
-        __syncthreads();
-        pmask |= 255u << shift;
-    }
-    const uint32_t kth = s_prefix;   // k-th largest key
-    const int need_eq = s_remaining; // how many keys equal to kth are taken (lowest indices)
-
-    // --- flags in index order: key > kth, or key == kth among the first need_eq equals
-    const int per = (n_chunks + SEL_THREADS - 1) / SEL_THREADS;
-    const int c_begin = min(n_chunks, tid * per), c_end = min(n_chunks, c_begin + per);
-    int eq_local = 0;
-    for (int c = c_begin; c < c_end; ++c) eq_local += keys[c] == kth;
-    const int eq_before = block_exclusive_scan(eq_local, warp_tot, &s_total);
-    int sel_local = 0;
-    {
-        int e = eq_before;
-        for (int c = c_begin; c < c_end; ++c) {
-            const uint32_t key = keys[c];
-            if (key > kth) ++sel_local;
-            else if (key == kth) { if (e < need_eq) ++sel_local; ++e; }
-        }
-    }
-    int pos = block_exclusive_scan(sel_local, warp_tot, &s_total);
-    {
-        int e = eq_before;
-        for (int c = c_begin; c < c_end; ++c) {
-            const uint32_t key = keys[c];
-            bool take = false;
-            if (key > kth) take = true;
-            else if (key == kth) { take = e < need_eq; ++e; }
-            if (take) {
-                if (pos < k_sel) {  // exactly k_sel are taken; the guard only bounds the writes
-                    sel[(size_t)g * k_sel + pos] = c;
-                    if (c == n_chunks - 1) s_last = 1;
-                }
-                ++pos;
-            }
-        }
-    }
-    __syncthreads();
+    bitonic_sort_block<uint32_t, false>(idx, PK);
+    for (int i = tid; i < k_sel; i += SEL_THREADS) sel[(size_t)g * k_sel + i] = (int32_t)idx[i];
     // tokens gathered for this head: only the last chunk of the prefix can be
     // short, and being the largest index it is the last one selected
     if (tid == 0 && part_len != nullptr) {
@@ -312,7 +241,10 @@ cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_
     (void)num_sms;
     if (injected_launch_failure()) return cudaErrorInvalidValue;
     if (k_sel <= 0 || n_chunks <= 0) return cudaSuccess;
-    const size_t smem = sizeof(uint32_t) * (size_t)n_chunks;
+    int P = 64, PK = 64;
+    while (P < n_chunks) P <<= 1;
+    while (PK < k_sel) PK <<= 1;
+    const size_t smem = sizeof(uint64_t) * (size_t)P + sizeof(uint32_t) * (size_t)PK;
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     select_kernel<<<Hkv, SEL_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, n_sink, n_recent, sel, part_len);

@@ -9,10 +9,11 @@
 // Row pass: one thread-block cluster of VOCAB_CLUSTER CTAs per batch row; each
 // CTA owns a contiguous slice of the vocabulary (76 KB for 152064 ids), which
 // one bulk copy (TMA) moves into shared memory while the CTA builds its
-// window bitmap.  Pass 1 over shared memory gives the slice's penalised
-// (max, argmax); the CTAs exchange those through distributed shared memory;
-// pass 2 over shared memory counts the min-p kept ids (and draws the Gumbel
-// maximum when sampling).  The logits are read from HBM once, by the copy
+// window bitmap.  Pass 1 over shared memory (four logits per 16-byte read)
+// gives the slice's penalised maximum; the CTAs exchange those through
+// distributed shared memory; pass 2 counts the min-p kept ids, finds the
+// lowest id attaining the row maximum (the greedy target) and draws the
+// Gumbel maximum when sampling.  The logits are read from HBM once, by the copy
 // engine, with no chain of dependent loads per thread.
 #include <cooperative_groups.h>
 
@@ -129,9 +130,10 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
     extern __shared__ __align__(16) float xs[];  // this CTA's slice of the row's logits
     __shared__ uint32_t bitmap[VOCAB_BITMAP_WORDS];
     __shared__ ArgMax red[VOCAB_THREADS / 32];
-    __shared__ ArgMax cta_best;
-    __shared__ int warp_cnt[VOCAB_THREADS / 32];
-    __shared__ int cta_cnt;
+    __shared__ float red_max[VOCAB_THREADS / 32];
+    __shared__ float cta_max;
+    __shared__ int warp_cnt[VOCAB_THREADS / 32], warp_arg[VOCAB_THREADS / 32];
+    __shared__ int cta_cnt, cta_arg;
     __shared__ ArgMax cta_samp;
     __shared__ __align__(8) uint64_t bar;
 
@@ -195,67 +197,108 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
     const bool landed = tc::mbar_wait(&bar, 0, nullptr);
     __syncthreads();
 
-    // penalised, tempered logit of slice element i (dividing by a temperature
-    // of 1 is exact, so that division is skipped)
+    // penalised, tempered logits of slice elements 4q..4q+3 (dividing by a
+    // temperature of 1 is exact, so that division is skipped)
     const bool tempered = a.temperature != 1.0f;
-    auto final_logit = [&](int i) {
+    const int n4 = n >> 2;
+    const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
+    auto final4 = [&](int q, float (&l)[4]) {
+        const float4 x = xs4[q];
+        l[0] = x.x; l[1] = x.y; l[2] = x.z; l[3] = x.w;
+        const uint32_t bits = (bitmap[q >> 3] >> ((q & 7) * 4)) & 0xfu;
+        if (bits) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if ((bits >> e) & 1u) l[e] = l[e] > 0.f ? __fdiv_rn(l[e], a.theta) : __fmul_rn(l[e], a.theta);
+        }
+        if (tempered) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) l[e] = __fdiv_rn(l[e], a.temperature);
+        }
+    };
+    auto final1 = [&](int i) {
         float l = xs[i];
         if ((bitmap[i >> 5] >> (i & 31)) & 1u) l = l > 0.f ? __fdiv_rn(l, a.theta) : __fmul_rn(l, a.theta);
         return tempered ? __fdiv_rn(l, a.temperature) : l;
     };
 
-    // ---- pass 1: max and lowest argmax of this slice.  A thread's indices
-    // increase with the loop, so a strict > keeps the lowest one.
-    ArgMax best{-INFINITY, -1};
-    for (int i = tid; i < n; i += VOCAB_THREADS) {
-        const float l = final_logit(i);
-        if (best.i < 0 || l > best.v) best = ArgMax{l, v0 + i};
+    // ---- pass 1: the slice's maximum
+    float mx = -INFINITY;
+    for (int q = tid; q < n4; q += VOCAB_THREADS) {
+        float l[4];
+        final4(q, l);
+        mx = fmaxf(mx, fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3])));
     }
-    best = block_best(best, red);
-    if (tid == 0) cta_best = best;
+    for (int i = 4 * n4 + tid; i < n; i += VOCAB_THREADS) mx = fmaxf(mx, final1(i));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red_max[warp] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float b = red_max[0];
+        for (int w = 1; w < VOCAB_THREADS / 32; ++w) b = fmaxf(b, red_max[w]);
+        cta_max = b;
+    }
     cluster.sync();
-    // every CTA reduces the cluster's candidates in rank order
-    ArgMax gbest{-INFINITY, -1};
-    for (int r = 0; r < VOCAB_CLUSTER; ++r) gbest = better(gbest, *cluster.map_shared_rank(&cta_best, r));
+    float m = -INFINITY;
+    for (int r = 0; r < VOCAB_CLUSTER; ++r) m = fmaxf(m, *cluster.map_shared_rank(&cta_max, r));
     // min-p threshold: smallest fp32 >= m + ln(min_p) (exact comparison)
-    const float f = __double2float_ru((double)gbest.v + a.log_min_p);
+    const float f = __double2float_ru((double)m + a.log_min_p);
 
-    // ---- pass 2: min-p count, and the Gumbel-max draw over the kept ids
-    int cnt = 0;
+    // ---- pass 2: min-p count, the lowest id attaining the maximum, and the
+    // Gumbel-max draw over the kept ids
+    int cnt = 0, arg = 0x7fffffff;
     ArgMax sb{-INFINITY, -1};
-    for (int i = tid; i < n; i += VOCAB_THREADS) {
-        const float l = final_logit(i);
+    auto visit = [&](float l, int v) {
         if (l >= f) {
             ++cnt;
-            if constexpr (SAMPLE) sb = better(sb, ArgMax{__fadd_rn(l, gumbel(v0 + i, row, a)), v0 + i});
+            if (l == m && v < arg) arg = v;
+            if constexpr (SAMPLE) sb = better(sb, ArgMax{__fadd_rn(l, gumbel(v, row, a)), v});
         }
-    }
+    };
+    for (int q = tid; q < n4; q += VOCAB_THREADS) {
+        float l[4];
+        final4(q, l);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (lane == 0) warp_cnt[warp] = cnt;
+        for (int e = 0; e < 4; ++e) visit(l[e], v0 + 4 * q + e);
+    }
+    for (int i = 4 * n4 + tid; i < n; i += VOCAB_THREADS) visit(final1(i), v0 + i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, o));
+    }
+    if (lane == 0) {
+        warp_cnt[warp] = cnt;
+        warp_arg[warp] = arg;
+    }
     if constexpr (SAMPLE) {
-        __syncthreads();  // red[] is reused
         sb = block_best(sb, red);
         if (tid == 0) cta_samp = sb;
     }
     __syncthreads();
     if (tid == 0) {
-        int c = 0;
-        for (int w = 0; w < VOCAB_THREADS / 32; ++w) c += warp_cnt[w];
+        int c = 0, ar = 0x7fffffff;
+        for (int w = 0; w < VOCAB_THREADS / 32; ++w) {
+            c += warp_cnt[w];
+            ar = min(ar, warp_arg[w]);
+        }
         cta_cnt = landed ? c : -1;  // -1: this CTA's slice never landed
+        cta_arg = ar;
     }
     cluster.sync();
     if (rank == 0 && tid == 0) {
-        int total = 0;
+        int total = 0, ar = 0x7fffffff;
         bool lost = false;
         ArgMax sbest{-INFINITY, -1};
         for (int r = 0; r < VOCAB_CLUSTER; ++r) {
             const int c = *cluster.map_shared_rank(&cta_cnt, r);
             lost = lost || c < 0;
             total += c;
+            ar = min(ar, *cluster.map_shared_rank(&cta_arg, r));
             if constexpr (SAMPLE) sbest = better(sbest, *cluster.map_shared_rank(&cta_samp, r));
         }
-        a.target[row] = SAMPLE ? sbest.i : gbest.i;
+        a.target[row] = SAMPLE ? sbest.i : ar;
         a.kept[row] = lost ? -1 : total;
     }
     cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
