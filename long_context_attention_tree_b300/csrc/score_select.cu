@@ -105,19 +105,132 @@ cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *score
 }
 
 // ---------------------------------------------------------------------------
-// Top-k selection (bitonic sort of order-preserving keys), then the gather.
-// select_kernel: one CTA per KV head computes sel[g][.] and part_len[g];
+// Top-k selection, then the gather.
+// select_kernel: one CTA per KV head computes sel[g][.] and part_len[g] from
+// composite keys (order key << 32 | ~chunk index), which are unique and order
+// equal scores by lower index.  For k <= 256 every warp keeps a sorted list of
+// its best L = 32R keys in registers (R per lane), merging in one batch of L
+// keys at a time, and the 32 lists are merged pairwise through shared memory;
+// larger k sort all keys in shared memory.
 // gather_kernel: CTA = (selected chunk, KV head) copies the chunk's K and V
 // rows.  The gather is launched as a programmatic dependent of the selection
 // so its CTAs are resident and waiting when the selection finishes.
 // ---------------------------------------------------------------------------
 constexpr int SEL_THREADS = 1024;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int GA_THREADS = 256;
 
 __device__ __forceinline__ uint32_t order_key(float x) {
     x = x + 0.0f;  // -0 -> +0 (round-to-nearest), so equal values get equal keys
     const uint32_t u = __float_as_uint(x);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The composite key of chunk c: always-kept chunks (the first n_sink, the
+// last n_recent) take the largest order key, above every finite score's;
+// padding (c >= n_chunks) is 0, below every key.
+__device__ __forceinline__ uint64_t chunk_key(const float *sc, int c, int n_chunks, int n_sink, int n_recent) {
+    if (c >= n_chunks) return 0ull;
+    const uint32_t key = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
+    return ((uint64_t)key << 32) | (uint32_t)~(uint32_t)c;
+}
+
+// One compare-exchange step of a bitonic network at distance j over a list of
+// 32R keys held by one warp, element e = s*32 + lane in v[s].  Runs of length
+// k end in descending order where (e & k) == 0 for DESC (ascending otherwise).
+template <int R, typename K, bool DESC>
+__device__ __forceinline__ void warp_cx(K (&v)[R], int k, int j, int lane) {
+    if (j >= 32) {
+        const int js = j >> 5;
+#pragma unroll
+        for (int s = 0; s < R; ++s) {
+            if ((s & js) == 0) {
+                const int e = s * 32 + lane;
+                const bool desc = ((e & k) == 0) == DESC;
+                const K a = v[s], b = v[s + js];
+                const bool sw = desc ? (a < b) : (a > b);
+                v[s] = sw ? b : a;
+                v[s + js] = sw ? a : b;
+            }
+        }
+    } else {
+        const bool lower = (lane & j) == 0;
+#pragma unroll
+        for (int s = 0; s < R; ++s) {
+            const int e = s * 32 + lane;
+            const bool desc = ((e & k) == 0) == DESC;
+            const K o = __shfl_xor_sync(0xffffffffu, v[s], j);
+            v[s] = (lower == desc) ? (v[s] > o ? v[s] : o) : (v[s] < o ? v[s] : o);
+        }
+    }
+}
+template <int R, typename K, bool DESC>
+__device__ __forceinline__ void warp_sort(K (&v)[R], int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32 * R; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) warp_cx<R, K, DESC>(v, k, j, lane);
+}
+// v (descending) and b (ascending): v <- the 32R largest of both, descending.
+// The element-wise maximum of a descending and an ascending list holds the
+// largest half of their union as a bitonic sequence, which the half-cleaner
+// stages then sort.
+template <int R>
+__device__ __forceinline__ void warp_merge_top(uint64_t (&v)[R], const uint64_t (&b)[R], int lane) {
+#pragma unroll
+    for (int s = 0; s < R; ++s) v[s] = v[s] > b[s] ? v[s] : b[s];
+#pragma unroll
+    for (int j = 16 * R; j > 0; j >>= 1) warp_cx<R, uint64_t, true>(v, 64 * R, j, lane);
+}
+
+template <int R>
+__device__ void select_topk_warps(const float *sc, int n_chunks, int k_sel, int n_sink, int n_recent,
+                                  uint64_t *lists, int32_t *sel_g, int *last_selected) {
+    constexpr int L = 32 * R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_batches = (n_chunks + L - 1) / L;
+    uint64_t v[R];
+#pragma unroll
+    for (int s = 0; s < R; ++s) v[s] = 0ull;
+    for (int bt = warp; bt < n_batches; bt += SEL_WARPS) {
+        uint64_t b[R];
+#pragma unroll
+        for (int s = 0; s < R; ++s) b[s] = chunk_key(sc, bt * L + s * 32 + lane, n_chunks, n_sink, n_recent);
+        warp_sort<R, uint64_t, false>(b, lane);
+        warp_merge_top<R>(v, b, lane);
+    }
+    // pairwise merge of the warps' lists: list w takes list w + act, reversed
+    int act = 1;
+    while (act < n_batches && act < SEL_WARPS) act <<= 1;
+    for (act >>= 1; act >= 1; act >>= 1) {
+        if (warp >= act && warp < 2 * act) {
+#pragma unroll
+            for (int s = 0; s < R; ++s) lists[(warp - act) * L + s * 32 + lane] = v[s];
+        }
+        __syncthreads();
+        if (warp < act) {
+            uint64_t b[R];
+#pragma unroll
+            for (int s = 0; s < R; ++s) b[s] = lists[warp * L + (L - 1 - (s * 32 + lane))];
+            warp_merge_top<R>(v, b, lane);
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        // the chosen chunk indices, ascending; padding sorts last
+        uint32_t c[R];
+#pragma unroll
+        for (int s = 0; s < R; ++s) c[s] = (s * 32 + lane < k_sel) ? ~(uint32_t)v[s] : 0xffffffffu;
+        bool last = false;
+#pragma unroll
+        for (int s = 0; s < R; ++s) last |= (int)c[s] == n_chunks - 1;
+        warp_sort<R, uint32_t, false>(c, lane);
+#pragma unroll
+        for (int s = 0; s < R; ++s)
+            if (s * 32 + lane < k_sel) sel_g[s * 32 + lane] = (int32_t)c[s];
+        const bool any_last = __any_sync(0xffffffffu, last);
+        if (lane == 0) *last_selected = any_last ? 1 : 0;
+    }
 }
 
 // Bitonic sort of v[0, P) (P a power of two, at least 64) into descending
@@ -129,8 +242,9 @@ __device__ void bitonic_sort_block(K *v, int P) {
     const int nthr = blockDim.x;
     for (int size = 2; size <= P; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const int ls = __ffs(stride) - 1;
             for (int i = threadIdx.x; i < (P >> 1); i += nthr) {
-                const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+                const int lo = ((i >> ls) << (ls + 1)) + (i & (stride - 1)), hi = lo + stride;
                 const bool first = (lo & size) == 0;  // this run ends in the requested order
                 const K a = v[lo], b = v[hi];
                 if ((first == DESC) ? (a < b) : (a > b)) {
@@ -138,53 +252,52 @@ __device__ void bitonic_sort_block(K *v, int P) {
                     v[hi] = a;
                 }
             }
-            if (stride > 32) __syncthreads(); else __syncwarp();
+            if (stride > 32 || (P >> 1) > nthr) __syncthreads(); else __syncwarp();
         }
         __syncthreads();
     }
 }
 
-// Per KV head: composite keys (order key << 32 | ~index) sorted descending put
-// the k largest scores first, equal scores by lower index; their indices are
-// then sorted ascending.
 __global__ void __launch_bounds__(SEL_THREADS)
 select_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
               int32_t *__restrict__ sel, int32_t *__restrict__ part_len) {
-    extern __shared__ __align__(16) uint64_t keys[];  // [P] then uint32 idx[PK]
+    extern __shared__ __align__(16) uint64_t keys[];
     __shared__ int s_last;
     // the gather grid may launch now; it waits for this grid's results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int g = blockIdx.x, tid = threadIdx.x;
-    int P = 64;
-    while (P < n_chunks) P <<= 1;
-    int PK = 64;
-    while (PK < k_sel) PK <<= 1;
-    uint32_t *idx = reinterpret_cast<uint32_t *>(keys + P);
     const float *sc = scores + (size_t)g * n_chunks;
-    // always-kept chunks (the first n_sink, the last n_recent) take the largest
-    // key, above every finite score's; padding sorts last (0 is below every key)
-    for (int c = tid; c < P; c += SEL_THREADS) {
-        uint64_t kv = 0;
-        if (c < n_chunks) {
-            const uint32_t key = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
-            kv = ((uint64_t)key << 32) | (uint32_t)~(uint32_t)c;
+    int32_t *sel_g = sel + (size_t)g * k_sel;
+    if (k_sel <= 64) {
+        select_topk_warps<2>(sc, n_chunks, k_sel, n_sink, n_recent, keys, sel_g, &s_last);
+    } else if (k_sel <= 128) {
+        select_topk_warps<4>(sc, n_chunks, k_sel, n_sink, n_recent, keys, sel_g, &s_last);
+    } else if (k_sel <= 256) {
+        select_topk_warps<8>(sc, n_chunks, k_sel, n_sink, n_recent, keys, sel_g, &s_last);
+    } else {
+        // all keys sorted descending, then the first k_sel indices ascending
+        int P = 64;
+        while (P < n_chunks) P <<= 1;
+        int PK = 64;
+        while (PK < k_sel) PK <<= 1;
+        uint32_t *idx = reinterpret_cast<uint32_t *>(keys + P);
+        for (int c = tid; c < P; c += SEL_THREADS) keys[c] = chunk_key(sc, c, n_chunks, n_sink, n_recent);
+        if (tid == 0) s_last = 0;
+        __syncthreads();
+        bitonic_sort_block<uint64_t, true>(keys, P);
+        for (int i = tid; i < PK; i += SEL_THREADS) {
+            uint32_t c = 0xffffffffu;  // padding sorts last
+            if (i < k_sel) {
+                c = ~(uint32_t)keys[i];
+                if ((int)c == n_chunks - 1) s_last = 1;
+            }
+            idx[i] = c;
         }
-        keys[c] = kv;
-    }
-    if (tid == 0) s_last = 0;
-    __syncthreads();
-    bitonic_sort_block<uint64_t, true>(keys, P);
-    for (int i = tid; i < PK; i += SEL_THREADS) {
-        uint32_t c = 0xffffffffu;  // padding sorts last
-        if (i < k_sel) {
-            c = ~(uint32_t)keys[i];
-            if ((int)c == n_chunks - 1) s_last = 1;
-        }
-        idx[i] = c;
+        __syncthreads();
+        bitonic_sort_block<uint32_t, false>(idx, PK);
+        for (int i = tid; i < k_sel; i += SEL_THREADS) sel_g[i] = (int32_t)idx[i];
     }
     __syncthreads();
-    bitonic_sort_block<uint32_t, false>(idx, PK);
-    for (int i = tid; i < k_sel; i += SEL_THREADS) sel[(size_t)g * k_sel + i] = (int32_t)idx[i];
     // tokens gathered for this head: only the last chunk of the prefix can be
     // short, and being the largest index it is the last one selected
     if (tid == 0 && part_len != nullptr) {
@@ -241,10 +354,17 @@ cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_
     (void)num_sms;
     if (injected_launch_failure()) return cudaErrorInvalidValue;
     if (k_sel <= 0 || n_chunks <= 0) return cudaSuccess;
-    int P = 64, PK = 64;
-    while (P < n_chunks) P <<= 1;
-    while (PK < k_sel) PK <<= 1;
-    const size_t smem = sizeof(uint64_t) * (size_t)P + sizeof(uint32_t) * (size_t)PK;
+    size_t smem;
+    if (k_sel <= 256) {
+        int R = 2;
+        while (32 * R < k_sel) R <<= 1;
+        smem = sizeof(uint64_t) * (size_t)(SEL_WARPS / 2) * 32 * R;  // the lists merged in the first round
+    } else {
+        int P = 64, PK = 64;
+        while (P < n_chunks) P <<= 1;
+        while (PK < k_sel) PK <<= 1;
+        smem = sizeof(uint64_t) * (size_t)P + sizeof(uint32_t) * (size_t)PK;
+    }
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     select_kernel<<<Hkv, SEL_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, n_sink, n_recent, sel, part_len);
