@@ -235,6 +235,8 @@ tree_attn_simt_kernel(const AttnArgs a) {
     }
 
     // --- epilogue: publish m, l; write final output or split partials
+    // (the split merge, a programmatic dependent, may start launching now)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (spart == 0) {
         sM[srow] = m_run;
         sL[srow] = l_run;
@@ -292,6 +294,8 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeArgs a) {
     const int n_split = !live ? 0 : ((row / a.Hq) < a.t_split ? a.splits : a.splits_hi);
     const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml) + row;
     const float *src0 = a.ws_o + (size_t)row * D + lane * DPL;
+    // the partials are the attention kernel's output (this grid may start early)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     float v[BATCH][DPL];
     auto load_batch = [&](int s0) {
@@ -433,14 +437,20 @@ cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st) {
     // few rows: four warps share a row's splits; many rows: a warp per row
     const bool few = (int64_t)rows * 4 <= (int64_t)sms * 32;
     const int blocks = few ? rows : (rows + 3) / 4;
-    if (d == 128) {
-        if (few) lse_merge_kernel<128, 4><<<blocks, 128, 0, st>>>(m);
-        else lse_merge_kernel<128, 1><<<blocks, 128, 0, st>>>(m);
-    } else {
-        if (few) lse_merge_kernel<64, 4><<<blocks, 128, 0, st>>>(m);
-        else lse_merge_kernel<64, 1><<<blocks, 128, 0, st>>>(m);
-    }
-    return cudaGetLastError();
+    // a programmatic dependent of the attention kernel: its CTAs launch while
+    // the attention kernel's last CTAs finish, then wait for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(128);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (d == 128)
+        return few ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 4>, m) : cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 1>, m);
+    return few ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<64, 4>, m) : cudaLaunchKernelEx(&cfg, lse_merge_kernel<64, 1>, m);
 }
 
 }  // namespace ts

@@ -247,6 +247,8 @@ __global__ void __launch_bounds__(R4 * 64) tree_attn_small_kernel(const AttnArgs
             o[3][1] = ffma2(make_float2(pb.z, pb.w), v23, o[3][1]);
         }
     }
+    // the split merge, a programmatic dependent, may start launching now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // ---- half 1 hands its partial to half 0 (through the dead K buffer)
     if (half == 1) {
 #pragma unroll

@@ -23,22 +23,28 @@
 // V MN-major in shared memory).  Every MMA descriptor is precomputed, so the
 // issuing thread only adds constants: issue keeps up with the 64-cycle MMAs.
 //
-// Warp roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: Q once, then K and V tiles into 2-stage rings;
-//   warp 1      owns TMEM (512 columns); one thread issues every tcgen05.mma;
-//   warp 2      chunk-score reducer: takes the scoring rows' chunk sums from a
-//               shared-memory ring and writes the max over the group's heads;
-//   warp 3      idle;
-//   warps 4-7   softmax warpgroup 0 (thread = row of M-tile 0);
-//   warps 8-11  softmax warpgroup 1 (M-tile 1 of a pair stream).
-// A softmax thread loads its row of S (128 fp32) into registers and writes
-// P = 2^(s*c - m) as bf16 over the first 64 columns of S.  The running max
-// is lazy: O and l are rescaled only when a row's max grows by more than
-// 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so the TMEM
-// round trip of a rescale is rare.  The normaliser l sums the bf16-rounded
-// weights that the P.V product uses.  The chunk importance of the scoring
-// row is summed from the same S values (packed adds) and handed to warp 2,
-// so the softmax warps never wait for the reduction.
+// Warp roles (608 threads, 19 warps):
+//   warp 0       TMA producer: Q once, then K and V tiles into 2-stage rings;
+//   warp 1       owns TMEM (512 columns); one thread issues every tcgen05.mma;
+//   warp 2       chunk-score reducer: takes the scoring rows' chunk sums from a
+//                shared-memory ring and writes the max over the group's heads;
+//   warps 3-10   softmax of M-tile slot 0, warps 11-18 of slot 1 (pair stream).
+// Two threads own each row of S: of the eight warps of a slot, the first four
+// take tokens 0-63 of every KV tile and the next four tokens 64-127 (warp w
+// reaches TMEM lanes 32 (w % 4) .. +31, so warps w and w + 4 share a lane
+// quadrant).  A softmax thread loads its 64 values of S into registers; the
+// two threads of a row swap their maxima through one tagged 64-bit shared-
+// memory word each and write P = 2^(s*c - m) as bf16 over the first 64
+// columns of S (tokens 0-63 in columns 0-31).  Half of each thread's chain of
+// a 128-token tile is then in flight, so the two halves' latencies overlap.
+// The running max is lazy: O and l are rescaled only when a row's max grows by
+// more than 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so the
+// TMEM round trip of a rescale is rare; each thread rescales its 64 columns of
+// O.  The output's normaliser sums the bf16-rounded weights that the P.V
+// product uses; a second sum of the unrounded weights gives the log-sum-exp
+// (and the split merge's weights).  The chunk importance of the scoring row is summed from the same S
+// values (one 64-token chunk per thread) and handed to warp 2, so the softmax
+// warps never wait for the reduction.
 // Every wait is bounded (see tc_ptx.cuh): a wait that gives up raises the
 // CTA's abort flag and the sticky device status word, and the CTA winds down.
 #include "internal.h"
@@ -51,7 +57,7 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int TC_THREADS = 384;  // 168 registers per thread (3 warps per SM sub-partition)
+constexpr int TC_THREADS = 608;  // 19 warps, at most 104 registers per thread
 constexpr int KV_TILE = TC_KV_TILE;         // 128 tokens
 constexpr int TILE_BYTES = 128 * 128 * 2;   // 128 rows x 128 dims, two 64-column swizzled halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
@@ -74,6 +80,9 @@ struct __align__(8) TcSmemTail {
     // into a ring slot (tile & 3); warp 2 takes the max over the group's heads.
     uint64_t score_full[SCORE_RING], score_empty[SCORE_RING];
     float score_sum[SCORE_RING][2][32];          // [slot][chunk half][head j]
+    // Row-max (and final normaliser) swap between the two threads of a row:
+    // [tile parity][M-tile slot][token half][row] = (tile + 1) << 32 | value bits.
+    uint64_t xch[2][2][2][128];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -157,38 +166,45 @@ __device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
     return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 // P = 2^(x*c - m) for 32 tokens -> 16 packed bf16x2 words (even token in the
-// lower half); returns the fp32 sum of the 32 bf16-rounded values, so that the
-// normaliser sums exactly the weights the P.V product uses (a row dominated
-// by one key then reproduces that key's value without the weight's rounding).
-__device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], float2 c2, float2 nm2, uint32_t (&pk)[16]) {
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+// lower half).  Adds the fp32 sum of the 32 bf16-rounded values to lr, so that
+// the output's normaliser sums exactly the weights the P.V product uses (a row
+// dominated by one key then reproduces that key's value without the weight's
+// rounding), and (EXACT) the sum of the unrounded weights to le, for the
+// log-sum-exp.
+template <bool EXACT>
+__device__ __forceinline__ void exp_chunk(const uint32_t (&x)[32], float2 c2, float2 nm2, uint32_t (&pk)[16],
+                                          float &lr, float &le) {
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f), ex = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
         const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), c2, nm2);
         const float2 y1 =
             __ffma2_rn(make_float2(__uint_as_float(x[2 * i + 2]), __uint_as_float(x[2 * i + 3])), c2, nm2);
-        pk[i] = tc::pack_bf16x2(tc::ex2(y0.x), tc::ex2(y0.y));
-        pk[i + 1] = tc::pack_bf16x2(tc::ex2(y1.x), tc::ex2(y1.y));
+        const float2 e0 = make_float2(tc::ex2(y0.x), tc::ex2(y0.y));
+        const float2 e1 = make_float2(tc::ex2(y1.x), tc::ex2(y1.y));
+        pk[i] = tc::pack_bf16x2(e0.x, e0.y);
+        pk[i + 1] = tc::pack_bf16x2(e1.x, e1.y);
         acc0 = __fadd2_rn(acc0, make_float2(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u)));
         acc1 = __fadd2_rn(acc1,
                           make_float2(__uint_as_float(pk[i + 1] << 16), __uint_as_float(pk[i + 1] & 0xffff0000u)));
+        if constexpr (EXACT) ex = __fadd2_rn(ex, __fadd2_rn(e0, e1));
     }
-    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    lr += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    if constexpr (EXACT) le += ex.x + ex.y;
 }
-// Chunk sums of the scoring row.  A whole 64-token chunk (a[] and b[]) is a
-// tree of packed adds (32 instructions); the chunk at the end of the prefix
-// sums x[0..lim) (lim clamped to [0, 32]) with eight partial sums.
+// Chunk sums of the scoring row.  A whole 64-token chunk (a[] and b[]) is
+// summed with packed adds into four running pairs (few live registers); the
+// chunk at the end of the prefix sums x[0..lim) (lim clamped to [0, 32]) with
+// eight partial sums.
 __device__ __forceinline__ float sum64(const uint32_t (&a)[32], const uint32_t (&b)[32]) {
-    float2 p[16];
+    float2 p[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        p[i] = __fadd2_rn(make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1])),
-                          make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1])));
-#pragma unroll
-    for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i) p[i] = __fadd2_rn(p[i], p[i + w]);
-    return p[0].x + p[0].y;
+    for (int i = 0; i < 16; ++i) {
+        p[i & 3] = __fadd2_rn(p[i & 3], make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1])));
+        p[(i + 2) & 3] = __fadd2_rn(p[(i + 2) & 3], make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1])));
+    }
+    const float2 q = __fadd2_rn(__fadd2_rn(p[0], p[1]), __fadd2_rn(p[2], p[3]));
+    return q.x + q.y;
 }
 __device__ __forceinline__ float sum_chunk(const uint32_t (&x)[32], int lim) {
     float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -197,8 +213,29 @@ __device__ __forceinline__ float sum_chunk(const uint32_t (&x)[32], int lim) {
     return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
+// Publish this thread's value for tile `tag - 1` and wait (bounded) for the
+// partner thread's word with the same tag; false if the wait gave up.
+__device__ __forceinline__ bool swap_with_partner(uint64_t *mine, const uint64_t *theirs, uint32_t tag, float val,
+                                                  float &other, volatile int *abort) {
+    *reinterpret_cast<volatile uint64_t *>(mine) = ((uint64_t)tag << 32) | __float_as_uint(val);
+    const volatile uint64_t *p = reinterpret_cast<const volatile uint64_t *>(theirs);
+    uint64_t v = *p;
+    if ((uint32_t)(v >> 32) != tag) {
+        const uint64_t t0 = tc::globaltimer();
+        for (uint32_t i = 1;; ++i) {
+            v = *p;
+            if ((uint32_t)(v >> 32) == tag) break;
+            if ((i & 63u) == 0 && (*abort || tc::globaltimer() - t0 > tc::WAIT_BUDGET_NS)) return false;
+        }
+    }
+    other = __uint_as_float((uint32_t)v);
+    return true;
+}
+
 }  // namespace
 
+// EXACT_LSE: the call wants the log-sum-exp, which takes the second sum.
+template <bool EXACT_LSE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const TcLaunch L) {
@@ -248,13 +285,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         for (int m = 0; m < 2; ++m) {
             tc::mbar_init(&tl->s_full[m], 1);
-            tc::mbar_init(&tl->p_half[m], 128);
-            tc::mbar_init(&tl->p_full[m], 128);
+            tc::mbar_init(&tl->p_half[m], 256);  // P of tokens 0-63 written, O rescaled by both halves
+            tc::mbar_init(&tl->p_full[m], 128);  // P of tokens 64-127 written
             tc::mbar_init(&tl->o_done[m], 1);
         }
         tc::mbar_init(&tl->mma_done, 1);
         for (int sl = 0; sl < SCORE_RING; ++sl) {
-            tc::mbar_init(&tl->score_full[sl], (uint32_t)G);
+            tc::mbar_init(&tl->score_full[sl], (uint32_t)(2 * G));
             tc::mbar_init(&tl->score_empty[sl], 1);
         }
         tl->abort_flag = 0;
@@ -271,6 +308,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         tc::fence_proxy_async();
     }
+    // swap words start untagged (shared memory holds an earlier CTA's values)
+    for (int e = threadIdx.x; e < (int)(sizeof(tl->xch) / sizeof(uint64_t)); e += TC_THREADS)
+        (&tl->xch[0][0][0][0])[e] = 0ull;
     if (warp == 1) {
         tc::tmem_alloc(&tl->tmem_base, 512);
         tc::tmem_relinquish();
@@ -280,7 +320,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc::fence_after_sync();
     const uint32_t tbase = tl->tmem_base;
 
-    if (warp < 4) {
+    if (warp < 3) {
       if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n_my > 0) {
@@ -415,11 +455,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     }
                     if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
                     const int b = it & 1;
-                    // (a single stream's next S is already in flight: P.V goes as one piece)
+                    const uint32_t bpar = (uint32_t)(it >> 1) & 1u;
                     const uint64_t dv = dplus(dv0, (uint32_t)vst * TILE_BYTES);
-                    if (!(ok = tc::mbar_wait(&tl->p_full[b], (uint32_t)(it >> 1) & 1u, abort_flag))) break;
+                    // P of tokens 0-63 (and both halves' O rescale), then P of tokens 64-127:
+                    // the two halves are written by different threads
+                    if (!(ok = tc::mbar_wait(&tl->p_half[b], bpar, abort_flag))) break;
                     tc::fence_after_sync();
                     issue_pv_half(tbase + 256, tbase + 128 * b, dv, id_o, 0, it > 0);
+                    if (!(ok = tc::mbar_wait(&tl->p_full[b], bpar, abort_flag))) break;
+                    tc::fence_after_sync();
                     issue_pv_half(tbase + 256, tbase + 128 * b, dv, id_o, 1, true);
                     tc::mma_commit(&tl->o_done[b]);
                     tc::mma_commit(&tl->v_empty[vst]);
@@ -433,8 +477,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
       }
     } else {
-        // ------------------------------------------------------------ softmax warpgroups
-        const int wm = (warp - 4) >> 2;  // M-tile slot 0 or 1
+        // ------------------------------------------------------------ softmax warps
+        const int sw = warp - 3;
+        const int wm = sw >> 3;          // M-tile slot 0 or 1
+        const int hh = (sw >> 2) & 1;    // token half of every KV tile: 64 hh .. 64 hh + 63
         const int quad = warp & 3;       // TMEM lane quadrant this warp may access
         const int r = quad * 32 + lane;  // row inside the M-tile
         const uint32_t lane_addr = tbase + ((uint32_t)(quad * 32) << 16);
@@ -447,79 +493,79 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const bool is_score_row = score_wm == wm && row_valid && t == a.score_row;
             const bool score_warp = __any_sync(0xffffffffu, is_score_row);
             const int64_t plen = prefix_of(a, g);
-            const uint32_t o_addr = lane_addr + (pair ? 256u + 128u * (uint32_t)wm : 256u);
+            // this thread's 64 columns of O
+            const uint32_t o_addr = lane_addr + (pair ? 256u + 128u * (uint32_t)wm : 256u) + 64u * (uint32_t)hh;
             const float c = a.scale_log2;
             const float2 c2 = make_float2(c, c);
-            float m_run = -INFINITY, l_run = 0.f;
+            // l_run: sum of the bf16-rounded weights (the output's normaliser);
+            // e_run: sum of the unrounded weights (the log-sum-exp)
+            float m_run = -INFINITY, l_run = 0.f, e_run = 0.f;
             bool ok = true;
             for (int it = 0; it < n_my; ++it) {
                 const int slot = pair ? wm : (it & 1);
                 const uint32_t spar = pair ? ((uint32_t)it & 1u) : ((uint32_t)(it >> 1) & 1u);
-                const int tile = tile_begin + it;
-                const int64_t tok0 = (int64_t)tile * KV_TILE;
+                const int64_t tok0 = (int64_t)(tile_begin + it) * KV_TILE + 64 * hh;  // this thread's first token
                 ok = tc::mbar_wait(&tl->s_full[slot], spar, abort_flag);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
                 tc::fence_after_sync();
-                const uint32_t s_addr = lane_addr + 128u * (uint32_t)slot;
-                uint32_t x0[32], x1[32], x2[32], x3[32];
-                // the second half of S loads while the first half's max is taken
+                const uint32_t s_addr = lane_addr + 128u * (uint32_t)slot + 64u * (uint32_t)hh;
+                uint32_t x0[32], x1[32];
                 tc::tmem_ld32(s_addr + 0, x0);
                 tc::tmem_ld32(s_addr + 32, x1);
                 tc::tmem_wait_ld();
-                tc::tmem_ld32(s_addr + 64, x2);
-                tc::tmem_ld32(s_addr + 96, x3);
-                const bool tail = tok0 + KV_TILE > plen;
-                // the scoring row's chunk sums read raw S; the masking below only
-                // hides tokens past the prefix, which the sums leave out anyway
-                float mx01;
-                if (tail) {
+                // the scoring row's chunk sum (chunk 2 tile + hh, its tokens < N) from
+                // raw S; the masking below only hides tokens the sum leaves out anyway
+                float cs = 0.f;
+                if (is_score_row) {
+                    const int64_t lim = a.N - tok0;
+                    cs = lim >= 64 ? sum64(x0, x1)
+                                   : (lim <= 0 ? 0.f : sum_chunk(x0, (int)lim) + sum_chunk(x1, (int)lim - 32));
+                }
+                if (tok0 + 64 > plen) {
                     mask_chunk(x0, tok0 + 0, plen, a.N, a.T, mrow);
                     mask_chunk(x1, tok0 + 32, plen, a.N, a.T, mrow);
                 }
-                mx01 = fmaxf(max_chunk(x0), max_chunk(x1));
-                // the scoring row's chunk sums (tokens < N of chunks 2*tile, 2*tile+1);
-                // they go to warp 2 after P is handed over
-                float cs0 = 0.f, cs1 = 0.f;
-                const bool whole = tok0 + KV_TILE <= a.N;
-                const int lim = whole ? KV_TILE : (a.N - tok0 < 0 ? 0 : (int)(a.N - tok0));
-                if (is_score_row) cs0 = whole ? sum64(x0, x1) : sum_chunk(x0, lim) + sum_chunk(x1, lim - 32);
-                tc::tmem_wait_ld();
-                if (is_score_row) cs1 = whole ? sum64(x2, x3) : sum_chunk(x2, lim - 64) + sum_chunk(x3, lim - 96);
-                if (tail) {
-                    mask_chunk(x2, tok0 + 64, plen, a.N, a.T, mrow);
-                    mask_chunk(x3, tok0 + 96, plen, a.N, a.T, mrow);
+                float mx = fmaxf(max_chunk(x0), max_chunk(x1));
+                // ---- the row max over both halves, lazy running-max update
+                {
+                    float other;
+                    ok = swap_with_partner(&tl->xch[it & 1][wm][hh][r], &tl->xch[it & 1][wm][hh ^ 1][r],
+                                           (uint32_t)it + 1u, mx, other, abort_flag);
+                    if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                    mx = fmaxf(mx, other);
                 }
-
-                // ---- row max (raw units), lazy running-max update
-                const float mx = fmaxf(mx01, fmaxf(max_chunk(x2), max_chunk(x3)));
                 const float m_new = fmaxf(m_run, mx * c);
                 const bool resc = m_new > m_run + RESCALE_THRESHOLD;
                 const float alpha = resc ? tc::ex2(m_run - m_new) : 1.f;
                 if (resc) {
                     l_run *= alpha;
+                    e_run *= alpha;
                     m_run = m_new;
                 }
-
-                // ---- P = 2^(s*c - m) in bf16 over the first 64 columns of S
-                // (token k -> column k/2, even k in the lower half; S is in registers).
-                // Tokens 0-63 first: their P.V is issued while tokens 64-127 are
-                // exponentiated.
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 const float2 nm2 = make_float2(neg_m, neg_m);
-                float lsum;
+
+                // A warp whose rows need no rescale lets the tile's first P.V start now
+                // (for tokens 64-127: the P of tokens 0-63 is the other half's).
+                const bool warp_resc = it > 0 && __any_sync(0xffffffffu, resc);
+                if (hh == 1 && !warp_resc) tc::mbar_arrive(&tl->p_half[slot]);
+
+                // ---- P = 2^(s*c - m) in bf16: token 64 hh + k -> column 32 hh + k/2
+                const uint32_t p_addr = lane_addr + 128u * (uint32_t)slot + 32u * (uint32_t)hh;
                 {
                     uint32_t pk[16];
-                    lsum = exp_chunk(x0, c2, nm2, pk);
-                    tc::tmem_st16(s_addr + 0, pk);
+                    exp_chunk<EXACT_LSE>(x0, c2, nm2, pk, l_run, e_run);
+                    tc::tmem_st16(p_addr + 0, pk);
                 }
                 {
                     uint32_t pk[16];
-                    lsum += exp_chunk(x1, c2, nm2, pk);
-                    tc::tmem_st16(s_addr + 16, pk);
+                    exp_chunk<EXACT_LSE>(x1, c2, nm2, pk, l_run, e_run);
+                    tc::tmem_st16(p_addr + 16, pk);
                 }
 
-                // ---- rescale O by alpha (before this tile's first P.V)
-                if (it > 0 && __any_sync(0xffffffffu, resc)) {
+                // ---- rescale this thread's 64 columns of O by alpha before this tile's
+                // first P.V (which waits for both halves' arrivals on p_half)
+                if (warp_resc) {
                     if (!pair) {
                         // a single stream computes S ahead: wait for the previous P.V into O
                         ok = tc::mbar_wait(&tl->o_done[(it - 1) & 1], (uint32_t)((it - 1) >> 1) & 1u, abort_flag);
@@ -528,7 +574,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     // (a pair stream's S_m(it) was issued after P_m(it-1).V, so O_m is final here)
                     tc::fence_after_sync();
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
+                    for (int cc = 0; cc < 2; ++cc) {
                         uint32_t ov[32];
                         tc::tmem_ld32(o_addr + cc * 32, ov);
                         tc::tmem_wait_ld();
@@ -539,32 +585,17 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
-                tc::mbar_arrive(&tl->p_half[slot]);
-                {
-                    uint32_t pk[16];
-                    lsum += exp_chunk(x2, c2, nm2, pk);
-                    tc::tmem_st16(s_addr + 32, pk);
-                }
-                {
-                    uint32_t pk[16];
-                    lsum += exp_chunk(x3, c2, nm2, pk);
-                    tc::tmem_st16(s_addr + 48, pk);
-                }
-                l_run += lsum;
-                tc::tmem_wait_st();
-                tc::fence_before_sync();
-                tc::mbar_arrive(&tl->p_full[slot]);
+                if (hh == 0 || warp_resc) tc::mbar_arrive(&tl->p_half[slot]);
+                if (hh == 1) tc::mbar_arrive(&tl->p_full[slot]);
 
                 // ---- fused chunk importance of the scoring row into the ring for
-                // warp 2, after P is handed over so that the ring handshake stays off
-                // the M-tile's critical path
+                // warp 2, after P is handed over
                 if (score_warp) {
                     if (is_score_row) {
                         const int sl = it & (SCORE_RING - 1);
                         if (it < SCORE_RING ||
                             tc::mbar_wait(&tl->score_empty[sl], (uint32_t)(it / SCORE_RING - 1) & 1u, abort_flag)) {
-                            tl->score_sum[sl][0][j] = cs0;
-                            tl->score_sum[sl][1][j] = cs1;
+                            tl->score_sum[sl][hh][j] = cs;
                             tc::mbar_arrive(&tl->score_full[sl]);
                         } else {
                             raise_abort(tl);
@@ -575,6 +606,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
 
             // ---- epilogue: O of this range
+            // (the split merge, a programmatic dependent, may start launching now)
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             // (completion of the last P.V implies every earlier one: MMAs complete in order)
             if (ok) {
                 if (pair)
@@ -583,18 +616,37 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     ok = tc::mbar_wait(&tl->o_done[(n_my - 1) & 1], (uint32_t)((n_my - 1) >> 1) & 1u, abort_flag);
             }
             ok = __all_sync(0xffffffffu, ok);
+            float l_tot = 0.f, e_tot = 0.f;
+            if (ok) {
+                // the row's two sums over both halves (swapped as tiles n_my, n_my + 1)
+                float other;
+                ok = swap_with_partner(&tl->xch[n_my & 1][wm][hh][r], &tl->xch[n_my & 1][wm][hh ^ 1][r],
+                                       (uint32_t)n_my + 1u, l_run, other, abort_flag);
+                l_tot = l_run + other;
+                e_tot = l_tot;
+                if (EXACT_LSE && ok)
+                    ok = swap_with_partner(&tl->xch[(n_my + 1) & 1][wm][hh][r],
+                                           &tl->xch[(n_my + 1) & 1][wm][hh ^ 1][r], (uint32_t)n_my + 2u, e_run,
+                                           other, abort_flag);
+                if (EXACT_LSE) e_tot = e_run + other;
+                ok = __all_sync(0xffffffffu, ok);
+            }
             if (!ok) {
                 raise_abort(tl);
             } else {
                 tc::fence_after_sync();
                 const int h = g * G + j;
                 const size_t row = (size_t)t * a.Hq + h;
-                const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+                const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+                // a split partial is scaled so that its ratio to the unrounded sum
+                // (the merge's normaliser) is this range's O / l_tot
+                const float to_e = (l_tot > 0.f) ? e_tot / l_tot : 0.f;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < 2; ++cc) {
                     uint32_t ov[32];
                     tc::tmem_ld32(o_addr + cc * 32, ov);
                     tc::tmem_wait_ld();
+                    const int d0 = 64 * hh + 32 * cc;  // first head dim of this piece
                     if (row_valid) {
                         if (L.direct) {
                             uint32_t pk[16];
@@ -602,27 +654,28 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                             for (int i = 0; i < 16; ++i)
                                 pk[i] = tc::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv,
                                                         __uint_as_float(ov[2 * i + 1]) * inv);
-                            uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * 128 + cc * 32);
+                            uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * 128 + d0);
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
                                 dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                         } else {
                             float4 *dst =
-                                reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * 128 + cc * 32);
+                                reinterpret_cast<float4 *>(a.ws_o + ((size_t)split * a.T * a.Hq + row) * 128 + d0);
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
-                                dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
-                                                     __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+                                dst[i] = make_float4(__uint_as_float(ov[4 * i]) * to_e, __uint_as_float(ov[4 * i + 1]) * to_e,
+                                                     __uint_as_float(ov[4 * i + 2]) * to_e,
+                                                     __uint_as_float(ov[4 * i + 3]) * to_e);
                         }
                     }
                     __syncwarp();
                 }
-                if (row_valid) {
+                if (row_valid && hh == 0) {
                     if (L.direct) {
-                        if (a.lse != nullptr) a.lse[row] = (m_run + log2f(l_run)) * TS_LN2;
+                        if (a.lse != nullptr) a.lse[row] = (m_run + log2f(e_tot)) * TS_LN2;
                     } else {
                         reinterpret_cast<float2 *>(a.ws_ml)[(size_t)split * a.T * a.Hq + row] =
-                            make_float2(m_run, l_run);
+                            make_float2(m_run, e_tot);
                     }
                 }
             }
@@ -695,8 +748,11 @@ TcPlan tc_plan(int T, int Hq, int Hkv, int d, int64_t N, int num_sms) {
 cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtensorMap &tq, const CUtensorMap &tk,
                                 const CUtensorMap &tv, cudaStream_t st) {
     if (injected_launch_failure()) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)TC_SMEM_BYTES);
+    const bool exact = a.lse != nullptr;
+    cudaError_t e = exact ? cudaFuncSetAttribute(tree_attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)TC_SMEM_BYTES)
+                          : cudaFuncSetAttribute(tree_attn_tc_kernel<false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     TcLaunch L{};
     L.tpb = p.tpb;
@@ -710,7 +766,10 @@ cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtens
     L.ctas_per_head = p.ctas_per_head;
     L.direct = p.splits == 1 ? 1 : 0;
     dim3 grid(p.ctas_per_head * a.Hkv);
-    tree_attn_tc_kernel<<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(tq, tk, tv, a, L);
+    if (exact)
+        tree_attn_tc_kernel<true><<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(tq, tk, tv, a, L);
+    else
+        tree_attn_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(tq, tk, tv, a, L);
     return cudaGetLastError();
 }
 

@@ -48,8 +48,11 @@ class LayerBuffers:
 
 class SpecStep:
     def __init__(self, cfg: W.Config, device="cuda", layers: Optional[int] = None, vocab: Optional[bool] = None,
-                 value_kind: str = "int", fill_draft_tail: bool = True):
+                 value_kind: str = "int", fill_draft_tail: bool = True, want_lse: bool = True):
         self.cfg = cfg
+        # the log-sum-exp outputs (the method itself consumes only O; the
+        # kernels skip the exact normaliser sum when it is not asked for)
+        self.want_lse = want_lse
         self.device = torch.device(device)
         self.n_layers = cfg.layers if layers is None else layers
         self.T = cfg.T
@@ -96,7 +99,8 @@ class SpecStep:
     # ------------------------------------------------------------------
     def run_verify(self, i: int, stream=None) -> None:
         cfg, L = self.cfg, self.layers[i]
-        ts_tree_attn(L.q, L.k, L.v, cfg.N, self.mask, L.out, lse=L.lse, chunk_scores=L.scores, score_row=0,
+        ts_tree_attn(L.q, L.k, L.v, cfg.N, self.mask, L.out, lse=L.lse if self.want_lse else None,
+                     chunk_scores=L.scores, score_row=0,
                      workspace=self.workspace, scale=cfg.scale, stream=stream)
 
     def run_refresh(self, i: int, stream=None) -> None:
@@ -107,7 +111,8 @@ class SpecStep:
     def run_draft(self, i: int, stream=None) -> None:
         cfg, L = self.cfg, self.layers[i]
         ts_tree_attn_partial(L.q_draft, L.k_part, L.v_part, self.B, self.mask_draft, L.part_len, L.out_draft,
-                             lse=L.lse_draft, workspace=self.workspace, scale=cfg.scale, stream=stream)
+                             lse=L.lse_draft if self.want_lse else None, workspace=self.workspace, scale=cfg.scale,
+                             stream=stream)
 
     def run_layer(self, i: int, stream=None) -> None:
         self.run_verify(i, stream)
