@@ -10,10 +10,12 @@
 // CTA owns a contiguous slice of the vocabulary (76 KB for 152064 ids), which
 // one bulk copy (TMA) moves into shared memory while the CTA builds its
 // window bitmap.  Pass 1 over shared memory (four logits per 16-byte read)
-// gives the slice's penalised maximum; the CTAs exchange those through
-// distributed shared memory; pass 2 counts the min-p kept ids, finds the
-// lowest id attaining the row maximum (the greedy target) and draws the
-// Gumbel maximum when sampling.  The logits are read from HBM once, by the copy
+// writes the penalised logits back, keeps each thread's per-slot maxima in
+// registers and gives the slice's maximum; eight remote reads per CTA give
+// the row maximum; pass 2 visits only the slots whose maximum reaches the
+// min-p threshold (a few per row), counts the kept ids, finds the lowest id
+// attaining the row maximum (the greedy target) and draws the Gumbel maximum
+// when sampling.  The logits are read from HBM once, by the copy
 // engine, with no chain of dependent loads per thread.
 #include <cooperative_groups.h>
 
@@ -92,7 +94,8 @@ __device__ __forceinline__ float ln_f32(float x) {
     const float lm = __fmul_rn(__fmul_rn(2.0f, s), p);
     return __fmaf_rn(__int2float_rn(e), 0x1.62e430p-1f, lm);
 }
-__device__ __forceinline__ float gumbel(int v, int row, const VocabArgs &a) {
+// (not inlined: the row pass calls it from several unrolled sites)
+__device__ __noinline__ float gumbel(int v, int row, const VocabArgs &a) {
     const uint64_t x = philox_word((uint64_t)(v >> 2), (uint64_t)row, a.offset, 0ull, a.seed, 0ull, v & 3);
     const float u = __fmul_rn(__uint2float_rn(2u * (uint32_t)(x >> 41) + 1u), 0x1p-24f);
     return -ln_f32(-ln_f32(u));
@@ -135,6 +138,7 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
     __shared__ int warp_cnt[VOCAB_THREADS / 32], warp_arg[VOCAB_THREADS / 32];
     __shared__ int cta_cnt, cta_arg;
     __shared__ ArgMax cta_samp;
+    __shared__ float row_max;
     __shared__ __align__(8) uint64_t bar;
 
     const int row = blockIdx.y;
@@ -222,14 +226,27 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
         return tempered ? __fdiv_rn(l, a.temperature) : l;
     };
 
-    // ---- pass 1: the slice's maximum
+    // ---- pass 1: the penalised logits written back in place, each 16-byte
+    // slot's maximum kept in a register, and the slice's maximum
+    constexpr int SLOTS = VOCAB_MAX_SLICE / 4 / VOCAB_THREADS;  // 10
+    float m4[SLOTS];
     float mx = -INFINITY;
-    for (int q = tid; q < n4; q += VOCAB_THREADS) {
-        float l[4];
-        final4(q, l);
-        mx = fmaxf(mx, fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3])));
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) {
+        const int q = i * VOCAB_THREADS + tid;
+        m4[i] = -INFINITY;
+        if (q < n4) {
+            float l[4];
+            final4(q, l);
+            reinterpret_cast<float4 *>(xs)[q] = make_float4(l[0], l[1], l[2], l[3]);
+            m4[i] = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+            mx = fmaxf(mx, m4[i]);
+        }
     }
-    for (int i = 4 * n4 + tid; i < n; i += VOCAB_THREADS) mx = fmaxf(mx, final1(i));
+    for (int i = 4 * n4 + tid; i < n; i += VOCAB_THREADS) {
+        xs[i] = final1(i);
+        mx = fmaxf(mx, xs[i]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) red_max[warp] = mx;
@@ -240,8 +257,16 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
         cta_max = b;
     }
     cluster.sync();
-    float m = -INFINITY;
-    for (int r = 0; r < VOCAB_CLUSTER; ++r) m = fmaxf(m, *cluster.map_shared_rank(&cta_max, r));
+    // the row maximum: lanes 0..7 of warp 0 read one CTA's slice maximum each
+    // (eight remote reads per CTA, not eight per thread)
+    if (warp == 0) {
+        float v = lane < VOCAB_CLUSTER ? *cluster.map_shared_rank(&cta_max, lane) : -INFINITY;
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) row_max = v;
+    }
+    __syncthreads();
+    const float m = row_max;
     // min-p threshold: smallest fp32 >= m + ln(min_p) (exact comparison)
     const float f = __double2float_ru((double)m + a.log_min_p);
 
@@ -256,13 +281,20 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
             if constexpr (SAMPLE) sb = better(sb, ArgMax{__fadd_rn(l, gumbel(v, row, a)), v});
         }
     };
-    for (int q = tid; q < n4; q += VOCAB_THREADS) {
-        float l[4];
-        final4(q, l);
+    // only slots whose maximum reaches the threshold are visited element by
+    // element (a few per row at min-p 0.1)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) visit(l[e], v0 + 4 * q + e);
+    for (int i = 0; i < SLOTS; ++i) {
+        const int q = i * VOCAB_THREADS + tid;
+        if (q < n4 && m4[i] >= f) {
+            const float4 l = reinterpret_cast<const float4 *>(xs)[q];
+            visit(l.x, v0 + 4 * q + 0);
+            visit(l.y, v0 + 4 * q + 1);
+            visit(l.z, v0 + 4 * q + 2);
+            visit(l.w, v0 + 4 * q + 3);
+        }
     }
-    for (int i = 4 * n4 + tid; i < n; i += VOCAB_THREADS) visit(final1(i), v0 + i);
+    for (int i = 4 * n4 + tid; i < n; i += VOCAB_THREADS) visit(xs[i], v0 + i);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
@@ -287,19 +319,29 @@ penalty_minp_kernel(const VocabArgs a, int slice) {
         cta_arg = ar;
     }
     cluster.sync();
-    if (rank == 0 && tid == 0) {
-        int total = 0, ar = 0x7fffffff;
-        bool lost = false;
+    if (rank == 0 && warp == 0) {
+        // lane r < 8 reads CTA r's results (remote reads in parallel)
+        int c = 0, ar = 0x7fffffff;
         ArgMax sbest{-INFINITY, -1};
-        for (int r = 0; r < VOCAB_CLUSTER; ++r) {
-            const int c = *cluster.map_shared_rank(&cta_cnt, r);
-            lost = lost || c < 0;
-            total += c;
-            ar = min(ar, *cluster.map_shared_rank(&cta_arg, r));
-            if constexpr (SAMPLE) sbest = better(sbest, *cluster.map_shared_rank(&cta_samp, r));
+        if (lane < VOCAB_CLUSTER) {
+            c = *cluster.map_shared_rank(&cta_cnt, lane);
+            ar = *cluster.map_shared_rank(&cta_arg, lane);
+            if constexpr (SAMPLE) sbest = *cluster.map_shared_rank(&cta_samp, lane);
         }
-        a.target[row] = SAMPLE ? sbest.i : ar;
-        a.kept[row] = lost ? -1 : total;
+        const bool lost = __any_sync(0xffffffffu, c < 0);
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) {
+            c += __shfl_xor_sync(0xffffffffu, c, o);
+            ar = min(ar, __shfl_xor_sync(0xffffffffu, ar, o));
+            if constexpr (SAMPLE) {
+                const ArgMax other{__shfl_xor_sync(0xffffffffu, sbest.v, o), __shfl_xor_sync(0xffffffffu, sbest.i, o)};
+                sbest = better(sbest, other);
+            }
+        }
+        if (lane == 0) {
+            a.target[row] = SAMPLE ? sbest.i : ar;
+            a.kept[row] = lost ? -1 : c;
+        }
     }
     cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
