@@ -285,8 +285,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         for (int m = 0; m < 2; ++m) {
             tc::mbar_init(&tl->s_full[m], 1);
-            tc::mbar_init(&tl->p_half[m], 256);  // P of tokens 0-63 written, O rescaled by both halves
-            tc::mbar_init(&tl->p_full[m], 128);  // P of tokens 64-127 written
+            // one arrival per softmax warp (an arrival by each of 128-256 threads
+            // serialises on the barrier word and lengthens every hand-over)
+            tc::mbar_init(&tl->p_half[m], 8);  // P of tokens 0-63 written, O rescaled by both halves
+            tc::mbar_init(&tl->p_full[m], 4);  // P of tokens 64-127 written
             tc::mbar_init(&tl->o_done[m], 1);
         }
         tc::mbar_init(&tl->mma_done, 1);
@@ -548,7 +550,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // A warp whose rows need no rescale lets the tile's first P.V start now
                 // (for tokens 64-127: the P of tokens 0-63 is the other half's).
                 const bool warp_resc = it > 0 && __any_sync(0xffffffffu, resc);
-                if (hh == 1 && !warp_resc) tc::mbar_arrive(&tl->p_half[slot]);
+                if (hh == 1 && !warp_resc) {
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&tl->p_half[slot]);
+                }
 
                 // ---- P = 2^(s*c - m) in bf16: token 64 hh + k -> column 32 hh + k/2
                 const uint32_t p_addr = lane_addr + 128u * (uint32_t)slot + 32u * (uint32_t)hh;
@@ -583,10 +588,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         tc::tmem_st32(o_addr + cc * 32, ov);
                     }
                 }
+                // every lane's P (and O) stores have completed; one lane hands the
+                // warp's rows over
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
-                if (hh == 0 || warp_resc) tc::mbar_arrive(&tl->p_half[slot]);
-                if (hh == 1) tc::mbar_arrive(&tl->p_full[slot]);
+                __syncwarp();
+                if (lane == 0) {
+                    if (hh == 0 || warp_resc) tc::mbar_arrive(&tl->p_half[slot]);
+                    if (hh == 1) tc::mbar_arrive(&tl->p_full[slot]);
+                }
 
                 // ---- fused chunk importance of the scoring row into the ring for
                 // warp 2, after P is handed over
