@@ -39,14 +39,14 @@ METRIC = "tree-verify attn KV GB/s (% of HBM peak) at 100K ctx; µs/layer/spec s
 UNIT = "GB/s"
 
 
-# DRAM traffic of the tcgen05 verify kernel, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum of one launch, Qwen2.5-14B
-# shape at 40960 tokens: 247.38 + 3.65 MB for 167.77 MB of prefix K/V), scaled
-# to a launch by its prefix K/V bytes.  It holds only for the kernel code it
-# was taken on: the fingerprint below is of that code with comments and
+# DRAM traffic of the tcgen05 verify kernel, from one ncu capture of a
+# full-size launch (dram__bytes_read.sum + dram__bytes_write.sum, one pass,
+# Qwen2.5-14B shape at 102400 tokens: 751.77 + 4.56 MB for 419.43 MB of
+# prefix K/V), expressed per prefix K/V byte.  It holds only for the kernel
+# code it was taken on: the fingerprint below is of that code with comments and
 # whitespace removed; for any other code the traffic is unknown (null).
-VERIFY_TRAFFIC_PER_KV_BYTE = (247.375104 + 3.650304) / 167.772160
-VERIFY_TRAFFIC_CODE_SHA1 = "8ca1a49f8b8f972d773faf4abffc4b6cedf060e7"
+VERIFY_TRAFFIC_PER_KV_BYTE = (751.773696 + 4.562432) / 419.430400
+VERIFY_TRAFFIC_CODE_SHA1 = "412735b82a2bbb4a2b028b5b698b6fcc6ed5a46f"
 
 
 def _code_fingerprint(paths) -> str:

@@ -285,8 +285,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         for (int m = 0; m < 2; ++m) {
             tc::mbar_init(&tl->s_full[m], 1);
-            // one arrival per softmax warp (an arrival by each of 128-256 threads
-            // serialises on the barrier word and lengthens every hand-over)
+            // one arrival per softmax warp, by lane 0 after the warp's lanes have
+            // finished their TMEM stores (__syncwarp orders them before it)
             tc::mbar_init(&tl->p_half[m], 8);  // P of tokens 0-63 written, O rescaled by both halves
             tc::mbar_init(&tl->p_full[m], 4);  // P of tokens 64-127 written
             tc::mbar_init(&tl->o_done[m], 1);
