@@ -192,7 +192,13 @@ __device__ void select_topk_warps(const float *sc, int n_chunks, int k_sel, int 
     uint64_t v[R];
 #pragma unroll
     for (int s = 0; s < R; ++s) v[s] = 0ull;
-    for (int bt = warp; bt < n_batches; bt += SEL_WARPS) {
+    if (warp < n_batches) {
+        // the warp's first batch, sorted descending, is its list
+#pragma unroll
+        for (int s = 0; s < R; ++s) v[s] = chunk_key(sc, warp * L + s * 32 + lane, n_chunks, n_sink, n_recent);
+        warp_sort<R, uint64_t, true>(v, lane);
+    }
+    for (int bt = warp + SEL_WARPS; bt < n_batches; bt += SEL_WARPS) {
         uint64_t b[R];
 #pragma unroll
         for (int s = 0; s < R; ++s) b[s] = chunk_key(sc, bt * L + s * 32 + lane, n_chunks, n_sink, n_recent);
@@ -217,17 +223,30 @@ __device__ void select_topk_warps(const float *sc, int n_chunks, int k_sel, int 
         __syncthreads();
     }
     if (warp == 0) {
-        // the chosen chunk indices, ascending; padding sorts last
+        // the chosen chunk indices (padding: all ones)
         uint32_t c[R];
 #pragma unroll
         for (int s = 0; s < R; ++s) c[s] = (s * 32 + lane < k_sel) ? ~(uint32_t)v[s] : 0xffffffffu;
         bool last = false;
 #pragma unroll
         for (int s = 0; s < R; ++s) last |= (int)c[s] == n_chunks - 1;
-        warp_sort<R, uint32_t, false>(c, lane);
+        // ascending order by rank: the indices are distinct, and the padding
+        // (all ones) is above every index, so a chosen index's rank is the
+        // number of chosen indices below it
+        int rank[R];
+#pragma unroll
+        for (int s = 0; s < R; ++s) rank[s] = 0;
+#pragma unroll
+        for (int t = 0; t < R; ++t)
+#pragma unroll 8
+            for (int src = 0; src < 32; ++src) {
+                const uint32_t o = __shfl_sync(0xffffffffu, c[t], src);
+#pragma unroll
+                for (int s = 0; s < R; ++s) rank[s] += o < c[s] ? 1 : 0;
+            }
 #pragma unroll
         for (int s = 0; s < R; ++s)
-            if (s * 32 + lane < k_sel) sel_g[s * 32 + lane] = (int32_t)c[s];
+            if (s * 32 + lane < k_sel) sel_g[rank[s]] = (int32_t)c[s];
         const bool any_last = __any_sync(0xffffffffu, last);
         if (lane == 0) *last_selected = any_last ? 1 : 0;
     }
