@@ -21,7 +21,7 @@
 // Per KV tile and M-tile: S = Q K^T (8 MMAs, M=128 N=128 K=16, operands
 // K-major in shared memory), softmax, O += P V (8 MMAs, P read from TMEM,
 // V MN-major in shared memory).  Every MMA descriptor is precomputed, so the
-// issuing thread only adds constants: issue keeps up with the 64-cycle MMAs.
+// issuing thread only adds constants between MMAs.
 //
 // Warp roles (608 threads, 19 warps):
 //   warp 0       TMA producer: Q once, then K and V tiles into 2-stage rings;
@@ -35,16 +35,18 @@
 // quadrant).  A softmax thread loads its 64 values of S into registers; the
 // two threads of a row swap their maxima through one tagged 64-bit shared-
 // memory word each and write P = 2^(s*c - m) as bf16 over the first 64
-// columns of S (tokens 0-63 in columns 0-31).  Half of each thread's chain of
-// a 128-token tile is then in flight, so the two halves' latencies overlap.
+// columns of S (tokens 0-63 in columns 0-31).  The second half's P lands on
+// columns 32-63, which hold the first half's S values for tokens 32-63: it is
+// written only after the swap, which the first half enters after its loads.
 // The running max is lazy: O and l are rescaled only when a row's max grows by
 // more than 2^20 (P stays below 2^20, far inside bf16 and fp32 range), so the
 // TMEM round trip of a rescale is rare; each thread rescales its 64 columns of
 // O.  The output's normaliser sums the bf16-rounded weights that the P.V
-// product uses; a second sum of the unrounded weights gives the log-sum-exp
-// (and the split merge's weights).  The chunk importance of the scoring row is summed from the same S
-// values (one 64-token chunk per thread) and handed to warp 2, so the softmax
-// warps never wait for the reduction.
+// product uses; when the call asks for the log-sum-exp, a second sum of the
+// unrounded weights gives it (and the split merge's weights).  The chunk
+// importance of the scoring row is summed from the same S values (one 64-token
+// chunk per thread) and handed to warp 2, so the softmax warps never wait for
+// the reduction.
 // Every wait is bounded (see tc_ptx.cuh): a wait that gives up raises the
 // CTA's abort flag and the sticky device status word, and the CTA winds down.
 #include "internal.h"
