@@ -64,6 +64,7 @@ constexpr int KV_TILE = TC_KV_TILE;         // 128 tokens
 constexpr int TILE_BYTES = 128 * 128 * 2;   // 128 rows x 128 dims, two 64-column swizzled halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int NSTAGE = 2;                   // K and V ring depth (pair: 2 Q + 2 K + 2 V = 192 KB)
+static_assert(NSTAGE == 2, "the MMA issuer derives ring stages from the tile's parity");
 constexpr int SMEM_DATA_BYTES = 6 * TILE_BYTES;
 constexpr float RESCALE_THRESHOLD = 20.0f;  // log2 units
 constexpr int SCORE_RING = 4;               // chunk-score slots between the scoring rows and warp 2
@@ -214,6 +215,12 @@ __device__ __forceinline__ float sum_chunk(const uint32_t (&x)[32], int lim) {
     for (int i = 0; i < 32; ++i) p[i & 7] += (i < lim) ? __uint_as_float(x[i]) : 0.f;
     return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
+
+// A compile-time ring stage (the issuer's tile step is instantiated per parity).
+template <int V>
+struct StageC {
+    static constexpr int value = V;
+};
 
 // Publish this thread's value for tile `tag - 1` and wait (bounded) for the
 // partner thread's word with the same tag; false if the wait gave up.
@@ -391,89 +398,89 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const uint32_t id_o = tc::idesc_bf16_f32(128, 128, true);
             const uint64_t dq0 = desc_k(tc::smem_u32(sQ)), dq1 = desc_k(tc::smem_u32(sQ + TILE_BYTES));
             const uint64_t dk0 = desc_k(tc::smem_u32(sK)), dv0 = desc_mn(tc::smem_u32(sV));
-            int kst = 0, vst = 0;
-            uint32_t kph = 0, vph = 0;
+            // S of tile 0 (K stage 0, phase 0)
             bool ok = tc::mbar_wait(&tl->q_full, 0, abort_flag);
-            if (ok) ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag);
+            if (ok) ok = tc::mbar_wait(&tl->k_full[0], 0, abort_flag);
             if (ok) {
                 tc::fence_after_sync();
-                const uint64_t dk = dplus(dk0, (uint32_t)kst * TILE_BYTES);
-                issue_s(tbase + 0, dq0, dk, id_s);
+                issue_s(tbase + 0, dq0, dk0, id_s);
                 tc::mma_commit(&tl->s_full[0]);
                 if (pair) {
-                    issue_s(tbase + 128, dq1, dk, id_s);
+                    issue_s(tbase + 128, dq1, dk0, id_s);
                     tc::mma_commit(&tl->s_full[1]);
                 }
-                tc::mma_commit(&tl->k_empty[kst]);
-                if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
+                tc::mma_commit(&tl->k_empty[0]);
             }
-            for (int it = 0; ok && it < n_my; ++it) {
+            // One tile: V of tile it sits in ring stage it % 2 and K of tile it+1 in
+            // stage (it + 1) % 2, so the stages (and every descriptor and barrier
+            // address derived from them) are compile-time constants of the
+            // tile's parity P; the two parities alternate.
+            auto tile_step = [&](auto Pc, int it) -> bool {
+                constexpr int VS = decltype(Pc)::value;  // V stage of tile it
+                constexpr int KS = VS ^ 1;               // K stage of tile it + 1
+                const uint32_t vph = (uint32_t)(it >> 1) & 1u;
+                const uint32_t kph = (uint32_t)((it + 1) >> 1) & 1u;
                 const bool more = it + 1 < n_my;
+                const uint64_t dv = dplus(dv0, (uint32_t)VS * TILE_BYTES);
+                const uint64_t dk = dplus(dk0, (uint32_t)KS * TILE_BYTES);
                 if (pair) {
                     // PV_0(it), S_0(it+1), PV_1(it), S_1(it+1): while one M-tile's
                     // softmax works, the tensor pipe runs the other tile's MMAs.
                     const uint32_t par = (uint32_t)it & 1u;
-                    if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
-                    const uint64_t dv = dplus(dv0, (uint32_t)vst * TILE_BYTES);
+                    if (!tc::mbar_wait(&tl->v_full[VS], vph, abort_flag)) return false;
                     // each half of P goes to the tensor pipe as soon as it is written
-                    if (!(ok = tc::mbar_wait(&tl->p_half[0], par, abort_flag))) break;
+                    if (!tc::mbar_wait(&tl->p_half[0], par, abort_flag)) return false;
                     tc::fence_after_sync();
                     issue_pv_half(tbase + 256, tbase + 0, dv, id_o, 0, it > 0);
-                    if (!(ok = tc::mbar_wait(&tl->p_full[0], par, abort_flag))) break;
+                    if (!tc::mbar_wait(&tl->p_full[0], par, abort_flag)) return false;
                     tc::fence_after_sync();
                     issue_pv_half(tbase + 256, tbase + 0, dv, id_o, 1, true);
                     tc::mma_commit(&tl->o_done[0]);
-                    uint64_t dk = 0;
                     if (more) {
-                        if (!(ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag))) break;
+                        if (!tc::mbar_wait(&tl->k_full[KS], kph, abort_flag)) return false;
                         tc::fence_after_sync();
-                        dk = dplus(dk0, (uint32_t)kst * TILE_BYTES);
                         issue_s(tbase + 0, dq0, dk, id_s);
                         tc::mma_commit(&tl->s_full[0]);
                     }
-                    if (!(ok = tc::mbar_wait(&tl->p_half[1], par, abort_flag))) break;
+                    if (!tc::mbar_wait(&tl->p_half[1], par, abort_flag)) return false;
                     tc::fence_after_sync();
                     issue_pv_half(tbase + 384, tbase + 128, dv, id_o, 0, it > 0);
-                    if (!(ok = tc::mbar_wait(&tl->p_full[1], par, abort_flag))) break;
+                    if (!tc::mbar_wait(&tl->p_full[1], par, abort_flag)) return false;
                     tc::fence_after_sync();
                     issue_pv_half(tbase + 384, tbase + 128, dv, id_o, 1, true);
                     tc::mma_commit(&tl->o_done[1]);
-                    tc::mma_commit(&tl->v_empty[vst]);
-                    if (++vst == NSTAGE) { vst = 0; vph ^= 1u; }
+                    tc::mma_commit(&tl->v_empty[VS]);
                     if (more) {
                         issue_s(tbase + 128, dq1, dk, id_s);
                         tc::mma_commit(&tl->s_full[1]);
-                        tc::mma_commit(&tl->k_empty[kst]);
-                        if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
+                        tc::mma_commit(&tl->k_empty[KS]);
                     }
                 } else {
-                    // S(it+1) into the other S buffer, then PV(it).
+                    // S(it+1) into the other S buffer (buffer KS), then PV(it) from
+                    // buffer VS.
                     if (more) {
-                        if (!(ok = tc::mbar_wait(&tl->k_full[kst], kph, abort_flag))) break;
+                        if (!tc::mbar_wait(&tl->k_full[KS], kph, abort_flag)) return false;
                         tc::fence_after_sync();
-                        const int b = (it + 1) & 1;
-                        issue_s(tbase + 128 * b, dq0, dplus(dk0, (uint32_t)kst * TILE_BYTES), id_s);
-                        tc::mma_commit(&tl->s_full[b]);
-                        tc::mma_commit(&tl->k_empty[kst]);
-                        if (++kst == NSTAGE) { kst = 0; kph ^= 1u; }
+                        issue_s(tbase + 128 * KS, dq0, dk, id_s);
+                        tc::mma_commit(&tl->s_full[KS]);
+                        tc::mma_commit(&tl->k_empty[KS]);
                     }
-                    if (!(ok = tc::mbar_wait(&tl->v_full[vst], vph, abort_flag))) break;
-                    const int b = it & 1;
-                    const uint32_t bpar = (uint32_t)(it >> 1) & 1u;
-                    const uint64_t dv = dplus(dv0, (uint32_t)vst * TILE_BYTES);
+                    if (!tc::mbar_wait(&tl->v_full[VS], vph, abort_flag)) return false;
                     // P of tokens 0-63 (and both halves' O rescale), then P of tokens 64-127:
                     // the two halves are written by different threads
-                    if (!(ok = tc::mbar_wait(&tl->p_half[b], bpar, abort_flag))) break;
+                    if (!tc::mbar_wait(&tl->p_half[VS], vph, abort_flag)) return false;
                     tc::fence_after_sync();
-                    issue_pv_half(tbase + 256, tbase + 128 * b, dv, id_o, 0, it > 0);
-                    if (!(ok = tc::mbar_wait(&tl->p_full[b], bpar, abort_flag))) break;
+                    issue_pv_half(tbase + 256, tbase + 128 * VS, dv, id_o, 0, it > 0);
+                    if (!tc::mbar_wait(&tl->p_full[VS], vph, abort_flag)) return false;
                     tc::fence_after_sync();
-                    issue_pv_half(tbase + 256, tbase + 128 * b, dv, id_o, 1, true);
-                    tc::mma_commit(&tl->o_done[b]);
-                    tc::mma_commit(&tl->v_empty[vst]);
-                    if (++vst == NSTAGE) { vst = 0; vph ^= 1u; }
+                    issue_pv_half(tbase + 256, tbase + 128 * VS, dv, id_o, 1, true);
+                    tc::mma_commit(&tl->o_done[VS]);
+                    tc::mma_commit(&tl->v_empty[VS]);
                 }
-            }
+                return true;
+            };
+            for (int it = 0; ok && it < n_my; ++it)
+                ok = (it & 1) ? tile_step(StageC<1>{}, it) : tile_step(StageC<0>{}, it);
             if (!ok) raise_abort(tl);
             // drain: every issued MMA completes before TMEM is released
             tc::mma_commit(&tl->mma_done);
