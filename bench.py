@@ -41,12 +41,12 @@ UNIT = "GB/s"
 
 # DRAM traffic of the tcgen05 verify kernel, from one ncu capture of a
 # full-size launch (dram__bytes_read.sum + dram__bytes_write.sum, one pass,
-# Qwen2.5-14B shape at 102400 tokens: 751.77 + 4.56 MB for 419.43 MB of
+# Qwen2.5-14B shape at 102400 tokens: 751.82 + 3.73 MB for 419.43 MB of
 # prefix K/V), expressed per prefix K/V byte.  It holds only for the kernel
 # code it was taken on: the fingerprint below is of that code with comments and
 # whitespace removed; for any other code the traffic is unknown (null).
-VERIFY_TRAFFIC_PER_KV_BYTE = (751.773696 + 4.562432) / 419.430400
-VERIFY_TRAFFIC_CODE_SHA1 = "412735b82a2bbb4a2b028b5b698b6fcc6ed5a46f"
+VERIFY_TRAFFIC_PER_KV_BYTE = (751.821824 + 3.734272) / 419.430400
+VERIFY_TRAFFIC_CODE_SHA1 = "3ddb4335b947345b6c9040a9fb9fbb9d8c1332aa"
 
 
 def _code_fingerprint(paths) -> str:
