@@ -296,6 +296,8 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeArgs a) {
     const float *src0 = a.ws_o + (size_t)row * D + lane * DPL;
     // the partials are the attention kernel's output (this grid may start early)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next kernel (a programmatic dependent, e.g. the chunk selection) may launch
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     float v[BATCH][DPL];
     auto load_batch = [&](int s0) {

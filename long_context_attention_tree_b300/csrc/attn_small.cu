@@ -51,6 +51,9 @@ __global__ void __launch_bounds__(R4 * 64) tree_attn_small_kernel(const AttnArgs
     __shared__ float scs[2][32];                       // chunk sums of the scoring rows, [chunk][head]
     __shared__ float red_m[2][RP], red_l[2][RP];       // per half: row max and row sum
 
+    // a programmatic dependent: the previous kernel (e.g. the gather of the
+    // partial cache) has completed and its writes are visible past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int half = warp / R4, rg = warp % R4;        // tokens [64 half, 64 half + 64), rows 4 rg .. 4 rg + 3
     const int split = blockIdx.x, g = blockIdx.y;
@@ -304,9 +307,17 @@ static cudaError_t launch_small_t(const AttnArgs &a, int splits, cudaStream_t st
     cudaError_t e = cudaFuncSetAttribute(tree_attn_small_kernel<R4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(splits, a.Hkv);
-    tree_attn_small_kernel<R4><<<grid, R4 * 64, smem, st>>>(a, splits);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, a.Hkv);
+    cfg.blockDim = dim3(R4 * 64);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tree_attn_small_kernel<R4>, a, splits);
 }
 
 cudaError_t launch_tree_attn_small(const AttnArgs &a, int splits, cudaStream_t st) {

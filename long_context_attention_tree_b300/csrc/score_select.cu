@@ -284,6 +284,9 @@ select_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_s
     __shared__ int s_last;
     // the gather grid may launch now; it waits for this grid's results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this grid is itself a programmatic dependent: the scores are the previous
+    // kernel's output
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g = blockIdx.x, tid = threadIdx.x;
     const float *sc = scores + (size_t)g * n_chunks;
     int32_t *sel_g = sel + (size_t)g * k_sel;
@@ -338,6 +341,8 @@ gather_kernel(const int32_t *__restrict__ sel, int64_t N, int n_chunks, int k_se
     static_assert(CHUNK * U % GA_THREADS == 0, "chunk must split evenly over the threads");
     // wait until the selection grid has finished and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next kernel (a programmatic dependent, e.g. the drafting attention) may launch
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int i = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
     const int c = min(max(sel[(size_t)g * k_sel + i], 0), n_chunks - 1);
     const int64_t left = N - (int64_t)c * CHUNK;
@@ -386,9 +391,22 @@ cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_
     }
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    select_kernel<<<Hkv, SEL_THREADS, smem, st>>>(scores, N, n_chunks, k_sel, n_sink, n_recent, sel, part_len);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    {
+        // the selection as a programmatic dependent of the kernel that wrote the
+        // scores (it waits for that grid before reading them)
+        cudaLaunchConfig_t scfg = {};
+        scfg.gridDim = dim3(Hkv);
+        scfg.blockDim = dim3(SEL_THREADS);
+        scfg.dynamicSmemBytes = smem;
+        scfg.stream = st;
+        cudaLaunchAttribute sattr[1];
+        sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        sattr[0].val.programmaticStreamSerializationAllowed = 1;
+        scfg.attrs = sattr;
+        scfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&scfg, select_kernel, scores, N, n_chunks, k_sel, n_sink, n_recent, sel, part_len);
+        if (e != cudaSuccess) return e;
+    }
     // the gather as a programmatic dependent of the selection
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(k_sel, Hkv);
