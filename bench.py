@@ -5,8 +5,8 @@ Default workload: one full speculative step of a Qwen2.5-14B-shaped model at
 102400 tokens of context (48 layers, 40 query heads, 8 KV heads, head dim 128,
 bf16 KV cache of 20.1 GB), every layer running the 120-row tree + n-gram
 verify attention over the full cache (chunk importance fused), top-64 chunk
-selection + gather into a 4096-token partial cache and 4-row draft attention
-over it; then the vocabulary stage on 120 x 152064 fp32 logits (penalty 1.2
+selection, then the gather into a 4096-token partial cache fused with the
+4-row draft attention over it; then the vocabulary stage on 120 x 152064 fp32 logits (penalty 1.2
 over a 1024-token window, min-p 0.1, greedy target, acceptance).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
@@ -366,7 +366,7 @@ def run_native(args, ws, rank, local):
     cfg = workload_config(args.workload)
     peaks = read_peaks()
     # the step computes what the method consumes: O (and the chunk scores), no log-sum-exp
-    step = SpecStep(cfg, layers=args.layers, want_lse=False)
+    step = SpecStep(cfg, layers=args.layers, want_lse=False, fuse_gather=not args.separate_gather)
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -472,13 +472,23 @@ def run_native(args, ws, rank, local):
     draft_s = statistics.mean(draft_ms) / 1e3
     gather_bytes = 4 * cfg.Hkv * B * d * 2           # selected K and V chunks read, then written
     draft_bytes = 2 * cfg.Hkv * (B + Td) * d * 2     # partial-cache K and V
+    draft_flops = 4.0 * Td * Hq * (B + Td) * d
     kernels = {
         "verify": {"us": verify_avg_s * 1e6, "kv_gbs": kv_layer / verify_avg_s / 1e9,
                    "tflops": flops / verify_avg_s / 1e12},
-        "select_gather": {"us": refresh_s * 1e6, "gbs": gather_bytes / refresh_s / 1e9, "bytes": gather_bytes},
-        "draft_attention": {"us": draft_s * 1e6, "gbs": draft_bytes / draft_s / 1e9, "bytes": draft_bytes,
-                            "tflops": 4.0 * Td * Hq * (B + Td) * d / draft_s / 1e12},
     }
+    if step.fuse_gather:
+        # selection alone, then the gather fused with the drafting pass (the
+        # selected K/V read once, written once into the compact cache)
+        fused_bytes = gather_bytes + 2 * cfg.Hkv * Td * d * 2
+        kernels["select"] = {"us": refresh_s * 1e6}
+        kernels["gather_draft_attention"] = {"us": draft_s * 1e6, "gbs": fused_bytes / draft_s / 1e9,
+                                             "bytes": fused_bytes, "tflops": draft_flops / draft_s / 1e12}
+    else:
+        kernels["select_gather"] = {"us": refresh_s * 1e6, "gbs": gather_bytes / refresh_s / 1e9,
+                                    "bytes": gather_bytes}
+        kernels["draft_attention"] = {"us": draft_s * 1e6, "gbs": draft_bytes / draft_s / 1e9, "bytes": draft_bytes,
+                                      "tflops": draft_flops / draft_s / 1e12}
     if vocab_ms:
         vocab_s = statistics.mean(vocab_ms) / 1e3
         vbytes = T * cfg.vocab * 4
@@ -536,11 +546,12 @@ def run_native(args, ws, rank, local):
 
 def run_e2e(step, s, args, ws):
     """Same metric through the public API with host buffers: every step copies
-    that step's inputs (per-layer Q, the batch's own K/V rows, draft Q; logits,
-    history, drafts, parents) from pinned host memory and reads the result back,
-    all inside the timed region (the copies overlap earlier layers' compute)."""
+    that step's inputs (per-layer Q, the batch's own K/V rows, draft Q and the
+    draft rows' own K/V; logits, history, drafts, parents) from pinned host
+    memory and reads the result back, all inside the timed region (the copies
+    overlap earlier layers' compute)."""
     cfg = step.cfg
-    N, T = cfg.N, cfg.T
+    N, T, B = cfg.N, cfg.T, step.B
     host = []
     h2d = 0
     for L in step.layers:
@@ -548,8 +559,10 @@ def run_e2e(step, s, args, ws):
         hkt = L.k[:, N:N + T].contiguous().cpu().pin_memory()
         hvt = L.v[:, N:N + T].contiguous().cpu().pin_memory()
         hqd = L.q_draft.cpu().pin_memory()
-        host.append((hq, hkt, hvt, hqd))
-        h2d += sum(t.numel() * t.element_size() for t in (hq, hkt, hvt, hqd))
+        hkd = L.k_part[:, B:].contiguous().cpu().pin_memory()
+        hvd = L.v_part[:, B:].contiguous().cpu().pin_memory()
+        host.append((hq, hkt, hvt, hqd, hkd, hvd))
+        h2d += sum(t.numel() * t.element_size() for t in (hq, hkt, hvt, hqd, hkd, hvd))
     hv = None
     if step.vocab:
         vi = step.vocab_inputs
@@ -574,12 +587,14 @@ def run_e2e(step, s, args, ws):
             if start is not None:
                 cs.wait_event(start)  # nothing of the timed region starts before its first event
             for i, L in enumerate(step.layers):
-                hq, hkt, hvt, hqd = host[i]
+                hq, hkt, hvt, hqd, hkd, hvd = host[i]
                 cs.wait_event(done[i])
                 L.q.copy_(hq, non_blocking=True)
                 L.k[:, N:N + T].copy_(hkt, non_blocking=True)
                 L.v[:, N:N + T].copy_(hvt, non_blocking=True)
                 L.q_draft.copy_(hqd, non_blocking=True)
+                L.k_part[:, B:].copy_(hkd, non_blocking=True)
+                L.v_part[:, B:].copy_(hvd, non_blocking=True)
                 ready[i].record(cs)
             if step.vocab:
                 vi = step.vocab_inputs
@@ -632,6 +647,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip timing the verify call on the other workloads")
     ap.add_argument("--layers", type=int, default=None, help="run only this many layers (profiling)")
+    ap.add_argument("--separate-gather", action="store_true",
+                    help="gather with the selection call, then the drafting attention over the compact cache")
     ap.add_argument("--cpu-row-fraction", type=float, default=1.0,
                     help="fraction of verify rows the CPU oracle baseline computes")
     ap.add_argument("--ref-row-fraction", type=float, default=1.0 / 32,

@@ -18,6 +18,9 @@
  *   ts_rescore_tail          the same for the chunks a commit touched only;
  *   ts_select_gather         top-k chunks up to the retrieval budget, gathered
  *                            into a compact partial cache;
+ *   ts_select_chunks         the selection alone;
+ *   ts_gather_tree_attn      the gather fused with the drafting pass over the
+ *                            gathered cache (the chosen K/V read once);
  *   ts_penalty_minp_verify   windowed contextual penalty, temperature, min-p,
  *                            greedy target and exact-match acceptance.
  *   ts_penalty_minp_sample_verify  the same with min-p sampled targets;
@@ -281,6 +284,43 @@ ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_t
                            int sink_chunks, int recent_chunks, const void *k, const void *v, int64_t ld_kv, int d,
                            int32_t *sel, int32_t *part_len, void *k_part, void *v_part, int64_t ld_part,
                            ts_stream_t stream);
+
+/*
+ * The selection of ts_select_gather without the gather: sel and part_len as
+ * there, same arguments, sizes and errors (no cache is read or written).
+ */
+ts_status ts_select_chunks(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
+                           int sink_chunks, int recent_chunks, int32_t *sel, int32_t *part_len,
+                           ts_stream_t stream);
+
+/*
+ * The gather of ts_select_gather fused with the drafting pass over its result
+ * (tool listing, "How it works": the partial KV cache is refreshed from the
+ * full cache and the target model drafts over it).  In one pass over the
+ * selected chunks it
+ *   - writes k_part[g][i*64 + t] = k[g][sel[g][i]*64 + t] (and v) for i < k_sel,
+ *     t < 64 and sel[g][i]*64 + t < N, exactly as ts_select_gather's gather
+ *     (other rows of k_part / v_part are not written), and
+ *   - computes ts_tree_attn_partial(q, k_part, v_part, ld_part, B = 64*k_sel,
+ *     T, ..., part_len) over the gathered rows, where part_len[g] = B less the
+ *     rows a selected short last chunk lacks; the batch's own K/V rows must
+ *     already be in rows [B, B+T) of k_part / v_part.
+ * The output equals ts_select_gather followed by ts_tree_attn_partial bit for
+ * bit.
+ *   q        bf16 [T][Hq][d]; k, v: the full cache, bf16 [Hkv][ld_kv][d],
+ *            ld_kv >= N
+ *   sel      device int32 [Hkv][k_sel] from ts_select_chunks (ascending
+ *            chunk indices below ceil(N/64); values outside are clamped)
+ *   k_part, v_part  bf16 [Hkv][ld_part][d], ld_part >= 64*k_sel + T
+ *   mask, out, lse, scale: as ts_tree_attn
+ *   workspace  ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, 64*k_sel) bytes
+ * Supported: d == 128 and T*Hq/Hkv <= 24 (the drafting pass's shapes),
+ * 1 <= k_sel <= ceil(N/64).  Chunk size 64.
+ */
+ts_status ts_gather_tree_attn(const void *q, const void *k, const void *v, int64_t ld_kv, int64_t N,
+                              const int32_t *sel, int k_sel, void *k_part, void *v_part, int64_t ld_part,
+                              int T, int Hq, int Hkv, int d, float scale, const uint64_t *mask,
+                              void *out, float *lse, void *workspace, size_t ws_bytes, ts_stream_t stream);
 
 /*
  * Vocabulary side of one verification step (model card flags --penalty,

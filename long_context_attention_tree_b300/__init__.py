@@ -29,7 +29,7 @@ __all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree
            "ts_launch_count", "ts_tree_attn_uses_tensor_cores", "ts_device_error", "ts_selftest_bounded_wait",
            "ts_selftest_fail_launches", "ts_tree_attn",
            "ts_tree_attn_partial", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_rescore_tail",
-           "ts_select_gather", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path",
+           "ts_select_gather", "ts_select_chunks", "ts_gather_tree_attn", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path",
            "ts_ngram_table_bytes", "ts_ngram_reset", "ts_ngram_update", "ts_ngram_topk", "ts_vocab_verify"]
 
 
@@ -73,6 +73,9 @@ def lib() -> ctypes.CDLL:
         L.ts_score_chunks.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P, P]
         L.ts_rescore_tail.argtypes = [P, i64, P, P, i64, i64, i32, i32, i32, i32, P, P]
         L.ts_select_gather.argtypes = [P, i32, i64, i32, i32, i32, i32, P, P, i64, i32, P, P, P, P, i64, P]
+        L.ts_select_chunks.argtypes = [P, i32, i64, i32, i32, i32, i32, P, P, P]
+        L.ts_gather_tree_attn.argtypes = [P, P, P, i64, i64, P, i32, P, P, i64, i32, i32, i32, i32, f32, P, P, P,
+                                          P, sz, P]
         L.ts_vocab_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, ctypes.c_uint, ctypes.c_uint64,
                                       ctypes.c_uint64, P, P, ctypes.c_int32, P, P, P, P, P]
         L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
@@ -87,7 +90,8 @@ def lib() -> ctypes.CDLL:
         L.ts_penalty_minp_sample_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, u64, u64, P, P,
                                                     ctypes.c_int32, P, P, P, P, P]
         for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_partial", "ts_tree_attn_noalloc",
-                     "ts_score_chunks", "ts_rescore_tail", "ts_select_gather", "ts_penalty_minp_verify",
+                     "ts_score_chunks", "ts_rescore_tail", "ts_select_gather", "ts_select_chunks",
+                     "ts_gather_tree_attn", "ts_penalty_minp_verify",
                      "ts_commit_path", "ts_penalty_minp_sample_verify", "ts_ngram_reset", "ts_ngram_update",
                      "ts_ngram_topk", "ts_vocab_verify"):
             getattr(L, name).restype = i32
@@ -225,6 +229,30 @@ def ts_select_gather(scores, N: int, budget_tokens: int, k, v, sel, k_part, v_pa
     _check(lib().ts_select_gather(_ptr(scores), Hkv, N, budget_tokens, chunk, int(sink_chunks), int(recent_chunks),
                                   _ptr(k), _ptr(v), ld, d, _ptr(sel), _ptr(part_len), _ptr(k_part), _ptr(v_part),
                                   ld_part, _stream(stream)))
+
+
+def ts_select_chunks(scores, N: int, budget_tokens: int, sel, chunk: int = 64, part_len=None, sink_chunks: int = 0,
+                     recent_chunks: int = 0, stream=None) -> None:
+    """The selection of ts_select_gather alone (sel, part_len)."""
+    Hkv = scores.shape[0]
+    _check(lib().ts_select_chunks(_ptr(scores), Hkv, N, budget_tokens, chunk, int(sink_chunks), int(recent_chunks),
+                                  _ptr(sel), _ptr(part_len), _stream(stream)))
+
+
+def ts_gather_tree_attn(q, k, v, N: int, sel, k_part, v_part, mask, out, lse=None, workspace=None,
+                        scale: Optional[float] = None, stream=None) -> None:
+    """The gather of the selected chunks (sel [Hkv][k_sel]) into k_part/v_part
+    fused with the drafting attention over them (batch rows at [64 k_sel, +T))."""
+    T, Hq, d = q.shape
+    Hkv, ld, _ = k.shape
+    k_sel = sel.shape[1]
+    ld_part = k_part.shape[1]
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ts_gather_tree_attn(_ptr(q), _ptr(k), _ptr(v), ld, N, _ptr(sel), k_sel, _ptr(k_part), _ptr(v_part),
+                                     ld_part, T, Hq, Hkv, d, scale, _ptr(mask), _ptr(out), _ptr(lse),
+                                     _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def ts_penalty_minp_verify(logits, history, theta: float, min_p: float, temperature: float, draft, parent,

@@ -69,7 +69,20 @@ cudaError_t launch_lse_merge(const MergeArgs &m, int d, cudaStream_t st);
 // KV range per CTA, splits = ceil((N + T) / 128)
 bool small_ok(int T, int Hq, int Hkv, int d);
 int small_splits(int T, int64_t N);
-cudaError_t launch_tree_attn_small(const AttnArgs &a, int splits, cudaStream_t st);
+// The gather variant: the prefix rows [0, N) of the attention (N = 64 k_sel)
+// come from the chosen 64-token chunks of a full cache and are written into
+// k_dst / v_dst (the compact cache the attention's k / v point at) as they
+// are read; rows of a short last chunk at or past the full cache's N are
+// neither read, seen nor written.
+struct SmallGather {
+    const int32_t *sel = nullptr;  // [Hkv][k_sel], ascending chunk indices
+    int k_sel = 0;
+    int n_chunks = 0;              // chunks of the full cache, ceil(N / 64)
+    const __nv_bfloat16 *k = nullptr, *v = nullptr;  // full cache [Hkv][ld][d]
+    int64_t ld = 0, N = 0;
+    __nv_bfloat16 *k_dst = nullptr, *v_dst = nullptr;
+};
+cudaError_t launch_tree_attn_small(const AttnArgs &a, const SmallGather *gs, int splits, cudaStream_t st);
 
 // tensor-core (tcgen05) path, head_dim 128, 64 <= T <= 128.
 constexpr int TC_KV_TILE = 128;  // KV tokens per pipeline step (two 64-token scoring chunks)
@@ -111,11 +124,13 @@ cudaError_t launch_score_chunks(const __nv_bfloat16 *q_row, const __nv_bfloat16 
 // scores_new[g][c] = scores_old[g][c] for c < c_keep (row strides nc_new / nc_old)
 cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *scores_new, int nc_new, int c_keep,
                                int Hkv, cudaStream_t st);
-cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel, int n_sink,
-                                 int n_recent,
-                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
-                                 int32_t *sel, int32_t *part_len, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part,
-                                 int64_t ld_part, int num_sms, cudaStream_t st);
+// top-k chunk selection (a programmatic dependent of the kernel before it)
+cudaError_t launch_select(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
+                          int32_t *sel, int32_t *part_len, cudaStream_t st);
+// gather of the selected chunks (a programmatic dependent of the selection)
+cudaError_t launch_gather(const int32_t *sel, int Hkv, int64_t N, int n_chunks, int k_sel,
+                          const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
+                          __nv_bfloat16 *k_part, __nv_bfloat16 *v_part, int64_t ld_part, cudaStream_t st);
 
 // vocab stage
 struct VocabArgs {

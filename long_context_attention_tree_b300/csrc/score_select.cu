@@ -370,12 +370,8 @@ gather_kernel(const int32_t *__restrict__ sel, int64_t N, int n_chunks, int k_se
     }
 }
 
-cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel, int n_sink,
-                                 int n_recent,
-                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
-                                 int32_t *sel, int32_t *part_len, __nv_bfloat16 *k_part, __nv_bfloat16 *v_part,
-                                 int64_t ld_part, int num_sms, cudaStream_t st) {
-    (void)num_sms;
+cudaError_t launch_select(const float *scores, int Hkv, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
+                          int32_t *sel, int32_t *part_len, cudaStream_t st) {
     if (injected_launch_failure()) return cudaErrorInvalidValue;
     if (k_sel <= 0 || n_chunks <= 0) return cudaSuccess;
     size_t smem;
@@ -391,22 +387,26 @@ cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_
     }
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    {
-        // the selection as a programmatic dependent of the kernel that wrote the
-        // scores (it waits for that grid before reading them)
-        cudaLaunchConfig_t scfg = {};
-        scfg.gridDim = dim3(Hkv);
-        scfg.blockDim = dim3(SEL_THREADS);
-        scfg.dynamicSmemBytes = smem;
-        scfg.stream = st;
-        cudaLaunchAttribute sattr[1];
-        sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        sattr[0].val.programmaticStreamSerializationAllowed = 1;
-        scfg.attrs = sattr;
-        scfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&scfg, select_kernel, scores, N, n_chunks, k_sel, n_sink, n_recent, sel, part_len);
-        if (e != cudaSuccess) return e;
-    }
+    // the selection as a programmatic dependent of the kernel that wrote the
+    // scores (it waits for that grid before reading them)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(Hkv);
+    cfg.blockDim = dim3(SEL_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, select_kernel, scores, N, n_chunks, k_sel, n_sink, n_recent, sel, part_len);
+}
+
+cudaError_t launch_gather(const int32_t *sel, int Hkv, int64_t N, int n_chunks, int k_sel,
+                          const __nv_bfloat16 *k, const __nv_bfloat16 *v, int64_t ld_kv, int d,
+                          __nv_bfloat16 *k_part, __nv_bfloat16 *v_part, int64_t ld_part, cudaStream_t st) {
+    if (injected_launch_failure()) return cudaErrorInvalidValue;
+    if (k_sel <= 0 || n_chunks <= 0) return cudaSuccess;
     // the gather as a programmatic dependent of the selection
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(k_sel, Hkv);
@@ -419,12 +419,9 @@ cudaError_t launch_select_gather(const float *scores, int Hkv, int64_t N, int n_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (d == 128)
-        e = cudaLaunchKernelEx(&cfg, gather_kernel<128>, (const int32_t *)sel, N, n_chunks, k_sel, k, v, ld_kv, k_part,
-                               v_part, ld_part);
-    else
-        e = cudaLaunchKernelEx(&cfg, gather_kernel<64>, (const int32_t *)sel, N, n_chunks, k_sel, k, v, ld_kv, k_part,
-                               v_part, ld_part);
-    return e;
+        return cudaLaunchKernelEx(&cfg, gather_kernel<128>, sel, N, n_chunks, k_sel, k, v, ld_kv, k_part, v_part,
+                                  ld_part);
+    return cudaLaunchKernelEx(&cfg, gather_kernel<64>, sel, N, n_chunks, k_sel, k, v, ld_kv, k_part, v_part, ld_part);
 }
 
 }  // namespace ts

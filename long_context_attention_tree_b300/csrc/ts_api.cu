@@ -215,7 +215,8 @@ int ts_tree_attn_uses_tensor_cores(int T, int Hq, int Hkv, int d, int64_t N) {
 static ts_status tree_attn_impl(const void *q, const void *k, const void *v, int64_t ld_kv, int64_t N, int T,
                                 int Hq, int Hkv, int d, float scale, const uint64_t *mask,
                                 const int32_t *prefix_len, void *out, float *lse, float *chunk_scores,
-                                int score_row, void *workspace, size_t ws_bytes, ts_stream_t stream) {
+                                int score_row, void *workspace, size_t ws_bytes, ts_stream_t stream,
+                                const ts::SmallGather *gather = nullptr) {
     ts_status st = check_attn_shape(T, Hq, Hkv, d, N);
     if (st != TS_OK) return st;
     if (T == 0) return TS_OK;
@@ -231,6 +232,8 @@ static ts_status tree_attn_impl(const void *q, const void *k, const void *v, int
         return fail(TS_ERR_INVALID_ARG, "score_row=%d outside [0, T=%d)", score_row, T);
 
     const AttnPlan plan = plan_attention(T, Hq, Hkv, d, N);
+    if (gather != nullptr && !plan.small)
+        return fail(TS_ERR_UNSUPPORTED, "the gather-fused drafting pass takes d = 128 and T*Hq/Hkv <= 24");
     const size_t need = workspace_for(plan, T, Hq, d);
     if (need > 0 && (workspace == nullptr || ws_bytes < need))
         return fail(TS_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
@@ -275,7 +278,7 @@ static ts_status tree_attn_impl(const void *q, const void *k, const void *v, int
         e = ts::launch_tree_attn_tc(a, p, tq, tk, tv, s);
         if (e != cudaSuccess) return cuda_fail(e, "tree_attn_tc launch");
     } else if (plan.small) {
-        e = ts::launch_tree_attn_small(a, plan.splits, s);
+        e = ts::launch_tree_attn_small(a, gather, plan.splits, s);
         if (e != cudaSuccess) return cuda_fail(e, "tree_attn_small launch");
     } else {
         const ts::SimtPlan &p = plan.sp;
@@ -378,12 +381,12 @@ ts_status ts_rescore_tail(const float *scores_old, int64_t N_old, const void *q_
     return TS_OK;
 }
 
-ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
-                           int sink_chunks, int recent_chunks, const void *k, const void *v, int64_t ld_kv, int d,
-                           int32_t *sel, int32_t *part_len, void *k_part, void *v_part, int64_t ld_part,
-                           ts_stream_t stream) {
+// Shared checks of the selection calls; on success *k_sel is the number of
+// chunks kept per head (0: nothing to do).
+static ts_status check_select(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk, int sink_chunks,
+                              int recent_chunks, const int32_t *sel, const int32_t *part_len, int *k_sel) {
+    *k_sel = 0;
     if (chunk != 64) return fail(TS_ERR_UNSUPPORTED, "chunk=%d (supported: 64)", chunk);
-    if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
     if (Hkv <= 0) return fail(TS_ERR_INVALID_ARG, "Hkv=%d", Hkv);
     if (N < 0 || budget_tokens < 0) return fail(TS_ERR_INVALID_ARG, "negative N or budget");
     if (budget_tokens % chunk) return fail(TS_ERR_INVALID_ARG, "budget %d not a multiple of chunk", budget_tokens);
@@ -391,24 +394,85 @@ ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_t
         return fail(TS_ERR_INVALID_ARG, "need sink_chunks, recent_chunks >= 0 and their sum <= budget/chunk");
     const int64_t nc = (N + chunk - 1) / chunk;
     if (nc > 16384) return fail(TS_ERR_UNSUPPORTED, "%lld chunks > 16384", (long long)nc);
-    const int k_sel = (int)((int64_t)(budget_tokens / chunk) < nc ? budget_tokens / chunk : nc);
-    if (k_sel == 0) return TS_OK;
-    if (!scores || !k || !v || !sel || !k_part || !v_part) return fail(TS_ERR_INVALID_ARG, "null pointer");
-    if (!aligned16(k) || !aligned16(v) || !aligned16(k_part) || !aligned16(v_part) || !aligned4(scores) ||
-        !aligned4(sel) || (part_len && !aligned4(part_len)))
+    const int ks = (int)((int64_t)(budget_tokens / chunk) < nc ? budget_tokens / chunk : nc);
+    if (ks == 0) return TS_OK;
+    if (!scores || !sel) return fail(TS_ERR_INVALID_ARG, "null scores/sel");
+    if (!aligned4(scores) || !aligned4(sel) || (part_len && !aligned4(part_len)))
+        return fail(TS_ERR_INVALID_ARG, "misaligned scores/sel/part_len");
+    *k_sel = ks;
+    return TS_OK;
+}
+
+ts_status ts_select_gather(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk,
+                           int sink_chunks, int recent_chunks, const void *k, const void *v, int64_t ld_kv, int d,
+                           int32_t *sel, int32_t *part_len, void *k_part, void *v_part, int64_t ld_part,
+                           ts_stream_t stream) {
+    if (d != 64 && d != 128) return fail(TS_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    int k_sel = 0;
+    ts_status st = check_select(scores, Hkv, N, budget_tokens, chunk, sink_chunks, recent_chunks, sel, part_len,
+                                &k_sel);
+    if (st != TS_OK || k_sel == 0) return st;
+    if (!k || !v || !k_part || !v_part) return fail(TS_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_part) || !aligned16(v_part))
         return fail(TS_ERR_INVALID_ARG, "misaligned pointer");
     if (ld_kv < N) return fail(TS_ERR_INVALID_ARG, "ld_kv < N");
     if (ld_part < (int64_t)k_sel * chunk)
         return fail(TS_ERR_INVALID_ARG, "ld_part=%lld < k*chunk=%lld", (long long)ld_part, (long long)k_sel * chunk);
-    cudaError_t e = ts::launch_select_gather(scores, Hkv, N, (int)nc, k_sel, sink_chunks, recent_chunks,
-                                             static_cast<const __nv_bfloat16 *>(k),
-                                             static_cast<const __nv_bfloat16 *>(v), ld_kv, d, sel, part_len,
-                                             static_cast<__nv_bfloat16 *>(k_part),
-                                             static_cast<__nv_bfloat16 *>(v_part), ld_part, num_sms(),
-                                             reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "select_gather launch");
-    ts::note_launches(2);
+    const int nc = (int)((N + chunk - 1) / chunk);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = ts::launch_select(scores, Hkv, N, nc, k_sel, sink_chunks, recent_chunks, sel, part_len, s);
+    if (e != cudaSuccess) return cuda_fail(e, "select launch");
+    ts::note_launches(1);
+    e = ts::launch_gather(sel, Hkv, N, nc, k_sel, static_cast<const __nv_bfloat16 *>(k),
+                          static_cast<const __nv_bfloat16 *>(v), ld_kv, d, static_cast<__nv_bfloat16 *>(k_part),
+                          static_cast<__nv_bfloat16 *>(v_part), ld_part, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    ts::note_launches(1);
     return TS_OK;
+}
+
+ts_status ts_select_chunks(const float *scores, int Hkv, int64_t N, int budget_tokens, int chunk, int sink_chunks,
+                           int recent_chunks, int32_t *sel, int32_t *part_len, ts_stream_t stream) {
+    int k_sel = 0;
+    ts_status st = check_select(scores, Hkv, N, budget_tokens, chunk, sink_chunks, recent_chunks, sel, part_len,
+                                &k_sel);
+    if (st != TS_OK || k_sel == 0) return st;
+    cudaError_t e = ts::launch_select(scores, Hkv, N, (int)((N + chunk - 1) / chunk), k_sel, sink_chunks,
+                                      recent_chunks, sel, part_len, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "select launch");
+    ts::note_launches(1);
+    return TS_OK;
+}
+
+ts_status ts_gather_tree_attn(const void *q, const void *k, const void *v, int64_t ld_kv, int64_t N,
+                              const int32_t *sel, int k_sel, void *k_part, void *v_part, int64_t ld_part, int T,
+                              int Hq, int Hkv, int d, float scale, const uint64_t *mask, void *out, float *lse,
+                              void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    if (T == 0) return check_attn_shape(T, Hq, Hkv, d, N);
+    if (N < 1) return fail(TS_ERR_INVALID_ARG, "N=%lld: nothing to gather", (long long)N);
+    const int64_t nc = (N + 63) / 64;
+    if (k_sel < 1 || k_sel > nc) return fail(TS_ERR_INVALID_ARG, "k_sel=%d outside [1, ceil(N/64)=%lld]", k_sel,
+                                             (long long)nc);
+    if (!sel || !aligned4(sel)) return fail(TS_ERR_INVALID_ARG, "null or misaligned sel");
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return fail(TS_ERR_INVALID_ARG, "null or misaligned k/v");
+    if (!k_part || !v_part) return fail(TS_ERR_INVALID_ARG, "null k_part/v_part");
+    if (ld_kv < N) return fail(TS_ERR_INVALID_ARG, "ld_kv < N");
+    const int64_t B = (int64_t)k_sel * 64;
+    ts::SmallGather gs;
+    gs.sel = sel;
+    gs.k_sel = k_sel;
+    gs.n_chunks = (int)nc;
+    gs.k = static_cast<const __nv_bfloat16 *>(k);
+    gs.v = static_cast<const __nv_bfloat16 *>(v);
+    gs.ld = ld_kv;
+    gs.N = N;
+    gs.k_dst = static_cast<__nv_bfloat16 *>(k_part);
+    gs.v_dst = static_cast<__nv_bfloat16 *>(v_part);
+    // the attention over the compact cache (rows [0, B) as they are gathered,
+    // rows [B, B + T) the batch's own), every head's prefix complete but for
+    // rows a short last chunk lacks
+    return tree_attn_impl(q, k_part, v_part, ld_part, B, T, Hq, Hkv, d, scale, mask, nullptr, out, lse, nullptr, 0,
+                          workspace, ws_bytes, stream, &gs);
 }
 
 static ts_status vocab_stage(const float *logits, int T, int V, const int32_t *history, int W, float theta,

@@ -6,9 +6,11 @@ favours, dynamic over one-time):
   1. verify attention: the T-row batch (draft tree + n-gram chains) against
      the full KV cache, producing the chunk importance of the scoring row in
      the same pass;
-  2. top-k chunk selection up to the retrieval budget and gather into the
-     compact partial cache;
-  3. draft attention: the 4-row self-drafting batch over the partial cache.
+  2. top-k chunk selection up to the retrieval budget;
+  3. gather of the chosen chunks into the compact partial cache and the draft
+     attention of the 4-row self-drafting batch over it, in one pass over the
+     chosen K/V (fuse_gather; otherwise a separate gather call before the
+     drafting attention over the compact cache).
 Then, once per step, the vocabulary stage (penalty, min-p, greedy target,
 acceptance).
 
@@ -24,8 +26,8 @@ from typing import List, Optional
 import numpy as np
 import torch
 
-from . import (ts_penalty_minp_verify, ts_select_gather, ts_tree_attn, ts_tree_attn_partial,
-               ts_tree_attn_workspace_bytes, ts_tree_mask_from_parents)
+from . import (ts_gather_tree_attn, ts_penalty_minp_verify, ts_select_chunks, ts_select_gather, ts_tree_attn,
+               ts_tree_attn_partial, ts_tree_attn_workspace_bytes, ts_tree_mask_from_parents)
 from . import workloads as W
 
 
@@ -48,8 +50,10 @@ class LayerBuffers:
 
 class SpecStep:
     def __init__(self, cfg: W.Config, device="cuda", layers: Optional[int] = None, vocab: Optional[bool] = None,
-                 value_kind: str = "int", fill_draft_tail: bool = True, want_lse: bool = True):
+                 value_kind: str = "int", fill_draft_tail: bool = True, want_lse: bool = True,
+                 fuse_gather: bool = True):
         self.cfg = cfg
+        self.fuse_gather = fuse_gather
         # the log-sum-exp outputs (the method itself consumes only O; the
         # kernels skip the exact normaliser sum when it is not asked for)
         self.want_lse = want_lse
@@ -105,14 +109,21 @@ class SpecStep:
 
     def run_refresh(self, i: int, stream=None) -> None:
         cfg, L = self.cfg, self.layers[i]
-        ts_select_gather(L.scores, cfg.N, cfg.budget, L.k, L.v, L.sel, L.k_part, L.v_part, chunk=cfg.chunk,
-                         part_len=L.part_len, stream=stream)
+        if self.fuse_gather:
+            ts_select_chunks(L.scores, cfg.N, cfg.budget, L.sel, chunk=cfg.chunk, part_len=L.part_len, stream=stream)
+        else:
+            ts_select_gather(L.scores, cfg.N, cfg.budget, L.k, L.v, L.sel, L.k_part, L.v_part, chunk=cfg.chunk,
+                             part_len=L.part_len, stream=stream)
 
     def run_draft(self, i: int, stream=None) -> None:
         cfg, L = self.cfg, self.layers[i]
-        ts_tree_attn_partial(L.q_draft, L.k_part, L.v_part, self.B, self.mask_draft, L.part_len, L.out_draft,
-                             lse=L.lse_draft if self.want_lse else None, workspace=self.workspace, scale=cfg.scale,
-                             stream=stream)
+        lse = L.lse_draft if self.want_lse else None
+        if self.fuse_gather:
+            ts_gather_tree_attn(L.q_draft, L.k, L.v, cfg.N, L.sel, L.k_part, L.v_part, self.mask_draft, L.out_draft,
+                                lse=lse, workspace=self.workspace, scale=cfg.scale, stream=stream)
+        else:
+            ts_tree_attn_partial(L.q_draft, L.k_part, L.v_part, self.B, self.mask_draft, L.part_len, L.out_draft,
+                                 lse=lse, workspace=self.workspace, scale=cfg.scale, stream=stream)
 
     def run_layer(self, i: int, stream=None) -> None:
         self.run_verify(i, stream)

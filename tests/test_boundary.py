@@ -134,6 +134,38 @@ def test_select_gather_rejects():
                               None) == ts.TS_ERR_UNSUPPORTED
 
 
+def test_select_chunks_rejects():
+    L = ts.lib()
+    P = 0x10000
+    assert L.ts_select_chunks(P, 8, 4096, 100, 64, 0, 0, P, None, None) == ts.TS_ERR_INVALID_ARG   # budget % chunk
+    assert L.ts_select_chunks(P, 8, 8192, 4096, 32, 0, 0, P, None, None) == ts.TS_ERR_UNSUPPORTED  # chunk != 64
+    assert L.ts_select_chunks(P, 8, 4100, 4096, 64, 0, 0, P, P + 2, None) == ts.TS_ERR_INVALID_ARG  # part_len
+    assert L.ts_select_chunks(P, 8, 8192, 4096, 64, 40, 30, P, None, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_chunks(None, 8, 8192, 4096, 64, 0, 0, P, None, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_select_chunks(P, 8, 0, 4096, 64, 0, 0, P, None, None) == ts.TS_OK  # nothing to select
+
+
+def _gather_attn(N=20480, k_sel=64, ld_part=64 * 64 + 4, T=4, Hq=40, Hkv=8, d=128, sel=0x10000):
+    P = 0x10000
+    return ts.lib().ts_gather_tree_attn(P, P, P, N + 8, N, sel, k_sel, P, P, ld_part, T, Hq, Hkv, d, 0.088, P, P,
+                                        None, P, 1 << 30, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=5, ld_part=64 * 64 + 8), ts.TS_ERR_UNSUPPORTED),  # 5 rows x 5 heads > 24 pairs per KV head
+    (dict(T=64, Hq=8, Hkv=8, ld_part=64 * 64 + 64), ts.TS_ERR_UNSUPPORTED),  # a tensor-core sized batch
+    (dict(d=64), ts.TS_ERR_UNSUPPORTED),
+    (dict(k_sel=0), ts.TS_ERR_INVALID_ARG),
+    (dict(k_sel=321), ts.TS_ERR_INVALID_ARG),               # more chunks than the cache holds
+    (dict(ld_part=64 * 64 + 3), ts.TS_ERR_INVALID_ARG),     # no room for the batch's own rows
+    (dict(sel=None), ts.TS_ERR_INVALID_ARG),
+    (dict(N=0), ts.TS_ERR_INVALID_ARG),
+])
+def test_gather_tree_attn_rejects(kw, status):
+    assert _gather_attn(**kw) == status
+    assert ts.lib().ts_last_error()
+
+
 def test_rescore_tail_rejects():
     L = ts.lib()
     P = 0x10000

@@ -106,6 +106,17 @@ def test_llama8b_sweep_layers(N):
     _check_step(step, range(2))
 
 
+def test_qwen14b_layers_with_a_separate_gather():
+    """The step with the gather as its own call (selection + gather, then the
+    drafting attention over the compact cache) instead of fused with the
+    drafting pass."""
+    cfg = W.WORKLOADS["qwen14b-100k"]
+    step = SpecStep(cfg, layers=2, fuse_gather=False)
+    step.run()
+    torch.cuda.synchronize()
+    _check_step(step, range(2))
+
+
 def test_llama2_7b_mha_layer():
     cfg = W.WORKLOADS["llama2-7b-100k"]
     step = SpecStep(cfg)

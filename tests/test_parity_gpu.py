@@ -290,6 +290,73 @@ def test_partial_cache_drafting_with_a_short_last_chunk(N, Hq, Hkv, d):
     check_attn(out, lse, ro, rlse, "partial")
 
 
+@pytest.mark.parametrize("N,Hq,Hkv,Td,budget", [
+    (4100, 40, 8, 4, 1024),     # 20 (row, head) pairs per KV head, short last chunk
+    (20480, 40, 8, 4, 4096),
+    (20483, 32, 8, 4, 4096),    # 16 pairs
+    (102403, 40, 8, 4, 4096),
+    (1000, 32, 32, 4, 1024),    # 4 pairs; the budget covers every chunk, the short one last
+    (300, 8, 8, 24, 256),       # 24 pairs (the largest batch of the kernel)
+    (4096, 16, 4, 6, 4096),     # 24 pairs, no short chunk
+    (5000, 40, 8, 1, 2048),     # one row
+    (2000, 40, 8, 3, 1024),     # 15 pairs (a padding row)
+])
+def test_gather_tree_attn_matches_oracle_and_the_two_calls(N, Hq, Hkv, Td, budget):
+    """The gather fused with the drafting pass: the compact cache bit-exact
+    against the oracle's gather (rows a selected short last chunk lacks keep
+    their old contents), the output within the bars against the oracle over the
+    gathered cache, and bit-identical to ts_select_gather followed by
+    ts_tree_attn_partial."""
+    d = 128
+    q, k, v = W.make_qkv(Td, Hq, Hkv, d, N, seed=N + 7 * Td, device="cuda", value_kind="normal")
+    nc = (N + 63) // 64
+    rng = np.random.default_rng(N + Td)
+    s = rng.integers(-50, 50, size=(Hkv, nc)).astype(np.float32)
+    s[::2, nc - 1] = 1000.0    # every other head keeps the short last chunk,
+    s[1::2, nc - 1] = -1000.0  # the others drop it
+    scores = torch.from_numpy(s).cuda()
+    kk = min(budget // 64, nc)
+    B = kk * 64
+    fill_k = torch.full((Hkv, B + Td, d), 7.0, dtype=torch.bfloat16, device="cuda")  # stale rows stand out
+    fill_v = torch.full_like(fill_k, -7.0)
+    fill_k[:, B:] = k[:, N:N + Td]
+    fill_v[:, B:] = v[:, N:N + Td]
+    parent = list(range(-1, Td - 1))
+    mask = dev_mask(parent)
+    ws = torch.empty(max(16, ts.ts_tree_attn_workspace_bytes(Td, Hq, Hkv, d, B)), dtype=torch.uint8, device="cuda")
+    scale = 1 / math.sqrt(d)
+
+    sel = torch.empty((Hkv, kk), dtype=torch.int32, device="cuda")
+    plen = torch.empty((Hkv,), dtype=torch.int32, device="cuda")
+    kp, vp = fill_k.clone(), fill_v.clone()
+    out = torch.empty((Td, Hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((Td, Hq), dtype=torch.float32, device="cuda")
+    ts.ts_select_chunks(scores, N, budget, sel, part_len=plen)
+    ts.ts_gather_tree_attn(q, k, v, N, sel, kp, vp, mask, out, lse=lse, workspace=ws, scale=scale)
+
+    sel2 = torch.empty_like(sel)
+    plen2 = torch.empty_like(plen)
+    kp2, vp2 = fill_k.clone(), fill_v.clone()
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    ts.ts_select_gather(scores, N, budget, k, v, sel2, kp2, vp2, part_len=plen2)
+    ts.ts_tree_attn_partial(q, kp2, vp2, B, mask, plen2, out2, lse=lse2, workspace=ws, scale=scale)
+    torch.cuda.synchronize()
+    assert ts.ts_device_error(True) == ts.TS_OK
+
+    rsel = oracle.select(s, budget // 64)
+    np.testing.assert_array_equal(sel.cpu().numpy(), rsel)
+    rk, rl = oracle.gather(rsel, k.cpu(), N, 64, B + Td, fill=fill_k.cpu(), return_len=True)
+    assert torch.equal(kp.cpu(), rk)
+    assert torch.equal(vp.cpu(), oracle.gather(rsel, v.cpu(), N, 64, B + Td, fill=fill_v.cpu()))
+    np.testing.assert_array_equal(plen.cpu().numpy(), rl)
+    ro, rlse = oracle.tree_attn(q.cpu(), kp.cpu(), vp.cpu(), B, parent, scale, prefix_len=rl)
+    check_attn(out, lse, ro, rlse, "gather + draft")
+    # the two-call path: same selection, same caches, same output bits
+    assert torch.equal(sel, sel2) and torch.equal(plen, plen2)
+    assert torch.equal(kp, kp2) and torch.equal(vp, vp2)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
 @pytest.mark.parametrize("N_old,N_new", [(4094, 4098), (4096, 4100), (4100, 4100), (0, 37), (20480, 20483),
                                          (130, 135), (63, 64), (102400, 102404)])
 def test_rescore_tail_equals_full_scoring(N_old, N_new):
