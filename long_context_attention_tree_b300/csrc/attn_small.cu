@@ -6,38 +6,43 @@
 //
 // The work is fp32 FMAs (about 1 FMA per 1.5 bytes of K/V), so the kernel is
 // built to keep the FMA pipe busy with packed fp32x2 FMAs and few other
-// instructions per FMA.
+// instructions per FMA, with four warps per scheduler to hide latencies.
 //
-// CTA = (KV head g, 128-token KV range), four warps; warp w owns the range's
-// tokens 32w .. 32w+31 from the load to its partial result, so the warps
-// never wait for one another until the final combine.  Rows r = (t, j)
-// t-major, R = T*G, padded to 4 RG (RG = ceil(R/4)).
-//   load:  each warp copies its 32 K rows and 32 V rows into shared memory
-//          with 16-byte cp.async (K XOR-swizzled by 16-byte chunk so that a
-//          quarter-warp reading one chunk of eight rows hits eight banks);
-//          rows that are out of range or not gathered are zero-filled.
+// CTA = (KV head g, 128-token KV range) = four 32-token blocks, eight warps:
+// warp (b, h) = (w / 2, w % 2) owns dims 64h .. 64h+63 of block b from the
+// load to its partial result.  Rows r = (t, j) t-major, R = T*G, padded to
+// 4 RG (RG = ceil(R/4)).
+//   load:  each warp copies its half of the block's 32 K rows and 32 V rows
+//          into shared memory with 16-byte cp.async (K XOR-swizzled by
+//          16-byte chunk within each 128-byte half row, so that a quarter-warp
+//          reading one chunk of eight rows hits eight banks); rows out of range
+//          or not gathered are zero-filled.  Q comes first (its own copy group,
+//          waited for before the K/V copies go out) and is converted to fp32
+//          [dim/4][row slot][4].
 //   S:     lane (rg, tg) = (lane / 8, lane % 8) takes rows rg*RG .. +RG-1 and
-//          tokens tg + 8i (i < 4): per 8 dims it reads four K chunks and 2 RG
-//          Q quads (Q is fp32 in shared memory, [dim/4][row slot][4]), and
-//          issues 16 RG fp32x2 FMAs over dimension pairs.
-//   softmax: the warp's own row max and sum (shuffles over the eight token
-//          lanes); P goes to the warp's slab as (p, p) pairs.
+//          tokens tg + 8i (i < 4) of the block: per 8 dims of its half it reads
+//          four K chunks and 2 RG Q quads and issues 16 RG fp32x2 FMAs over
+//          dimension pairs.  The two warps of a block swap their half sums
+//          through shared memory (a 64-thread named barrier), so both hold S.
+//   softmax: both warps compute the block's row max, P and row sum (the same
+//          arithmetic, so the same values); each writes half of the rows' P to
+//          the block's slab as (p, p) pairs.
 //   O:     lane (rh, dg) = (lane / 16, lane % 16) takes rows rh*2RG .. +2RG-1
-//          and dims 8dg .. 8dg+7: per token one 16-byte V read, RG 16-byte P
-//          reads and 8 RG fp32x2 FMAs.
-//   combine: the four warp partials (m, l, O) are merged through shared
+//          and dims 64h + 4dg .. +3: per token one 8-byte V read, RG 16-byte P
+//          reads and 4 RG fp32x2 FMAs.
+//   combine: the four blocks' partials (m, l, O) are merged through shared
 //          memory (over the dead K/V buffers) into the range's partial, which
 //          goes to the split workspace for the log-sum-exp merge kernel (a
 //          single range writes the normalised output directly).
 // The chunk importance of the scoring row can be produced by the same pass
-// (a warp holds half a 64-token chunk).
+// (a block holds half a 64-token chunk).
 //
 // Gather variant: the prefix rows are not read from a compact cache but from
 // the chunks of the full cache that the top-k selection chose (position p of
 // the compact cache is row sel[g][p/64]*64 + p%64 of the full cache); each
-// warp also writes its gathered rows into the compact cache, so the refresh
-// of the partial cache (selection, gather) and the drafting pass over it read
-// the selected K/V bytes from HBM once.
+// warp also writes its gathered half rows into the compact cache, so the
+// refresh of the partial cache (selection, gather) and the drafting pass over
+// it read the selected K/V bytes from HBM once.
 #include "internal.h"
 #include "ts_common.cuh"
 
@@ -45,11 +50,13 @@ namespace ts {
 
 namespace {
 constexpr int D = 128;
-constexpr int WT = 32;              // tokens per warp
-constexpr int NWARP = 4;
+constexpr int WT = 32;              // tokens per block
+constexpr int NBLK = 4;             // blocks per CTA
+constexpr int NWARP = 2 * NBLK;     // two warps (dimension halves) per block
 constexpr int NTHR = NWARP * 32;
-constexpr int RANGE = NWARP * WT;   // tokens per CTA: two 64-token chunks
+constexpr int RANGE = NBLK * WT;    // tokens per CTA: two 64-token chunks
 constexpr int ROWB = D * 2;         // bytes of one K/V row
+constexpr int HALFB = ROWB / 2;     // bytes of one half row (64 dims)
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
@@ -62,6 +69,17 @@ __device__ __forceinline__ float2 bf16x2_f2(uint32_t w) {
     return make_float2(__uint_as_float(lo), __uint_as_float(hi));
 }
 
+// 2^x on the special-function unit (ex2.approx: relative error about 2^-22;
+// subnormal results flush to zero)
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The two warps of block b (named barrier 1 + b, 64 threads).
+__device__ __forceinline__ void pair_sync(int b) { asm volatile("bar.sync %0, 64;" ::"r"(1 + b) : "memory"); }
+
 template <int RG>
 struct SmallCfg {
     static constexpr int RP = 4 * RG;                  // rows incl. padding
@@ -73,67 +91,76 @@ struct SmallCfg {
     static constexpr size_t V_OFF = (size_t)RANGE * ROWB;
     static constexpr size_t Q_OFF = 2 * (size_t)RANGE * ROWB;
     static constexpr size_t P_OFF = Q_OFF + (size_t)(D / 4) * QSLOTS * 16;
-    static constexpr size_t SMEM = P_OFF + (size_t)NWARP * WT * PP * 8;
-    static_assert((size_t)NWARP * RP * D * 4 <= 2 * (size_t)RANGE * ROWB, "warp partials must fit the K/V buffers");
+    static constexpr size_t SMEM = P_OFF + (size_t)NBLK * WT * PP * 8;
+    static_assert((size_t)NBLK * RP * D * 4 <= 2 * (size_t)RANGE * ROWB, "block partials must fit the K/V buffers");
+    static_assert((size_t)RG * 32 * 16 <= (size_t)WT * HALFB, "half sums must fit a warp's K half");
+    static_assert((size_t)RP * ROWB <= (size_t)NBLK * WT * PP * 8, "Q staging must fit the P slabs");
 };
 }  // namespace
 
 template <int RG, bool GATHER>
-__global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a, const SmallGather gs, int n_splits) {
+__global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs a, const SmallGather gs, int n_splits) {
     using C = SmallCfg<RG>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     unsigned char *sK = smem_raw + C::K_OFF;
     unsigned char *sV = smem_raw + C::V_OFF;
     float *sQ = reinterpret_cast<float *>(smem_raw + C::Q_OFF);
     float *sP = reinterpret_cast<float *>(smem_raw + C::P_OFF);
-    __shared__ float red_m[NWARP][C::RP], red_l[NWARP][C::RP];  // per warp: row max and row sum
-    __shared__ float row_m[C::RP], row_l[C::RP];                // the range's
-    __shared__ float sc_part[NWARP][32];                        // scoring row: half-chunk sums per head
+    __shared__ float red_m[NBLK][C::RP], red_l[NBLK][C::RP];  // per block: row max and row sum
+    __shared__ float row_m[C::RP], row_l[C::RP];              // the range's
+    __shared__ float sc_part[NBLK][32];                       // scoring row: half-chunk sums per head
+    __shared__ uint64_t s_mask[24];                           // batch rows' mask words
 
     // a programmatic dependent: the previous kernel (the selection, the gather
     // of the partial cache) has completed and its writes are visible past here
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int b = w >> 1, hd = w & 1;                  // block, dimension half
     const int split = blockIdx.x, g = blockIdx.y;
     const int G = a.G, R = a.T * G;
     const int64_t Np = a.N, L = Np + a.T;            // prefix positions, all positions
     const int64_t t0 = (int64_t)split * RANGE;
-    const int64_t wb = t0 + (int64_t)w * WT;          // first position of this warp's block
-    const bool active = wb < L;
+    const int64_t wb = t0 + (int64_t)b * WT;          // first position of this warp's block
+    const bool active = wb < L;                       // the same for both warps of a block
     const int64_t plen = GATHER ? Np : prefix_of(a, g);
-    // gather: the full-cache chunk behind this warp's block (a block lies in
-    // one chunk: Np is a multiple of 64 there)
+    // gather: the full-cache chunk behind this block (a block lies in one
+    // chunk: Np is a multiple of 64 there)
     int64_t src_base = 0;
     if (GATHER && wb < Np) {
         const int c = min(max(gs.sel[(size_t)g * gs.k_sel + (int)(wb >> 6)], 0), gs.n_chunks - 1);
         src_base = (int64_t)c * 64 + (wb & 63);
     }
-    sc_part[w][lane] = 0.f;
+    if (threadIdx.x < NBLK * 32) sc_part[threadIdx.x >> 5][lane] = 0.f;
 
-    // ---- Q of the group: global loads first (they must not queue behind the
-    // K/V copies)
-    constexpr int QITER = (C::RP * 16 + NTHR - 1) / NTHR;
-    uint4 qw[QITER];
-#pragma unroll
-    for (int u = 0; u < QITER; ++u) {
-        const int e = threadIdx.x + u * NTHR, r = e >> 4, c8 = e & 15;
-        qw[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < R) {
-            const int t = r / G, j = r % G;
-            qw[u] = *reinterpret_cast<const uint4 *>(a.q + ((size_t)t * a.Hq + g * G + j) * D + c8 * 8);
-        }
+    // ---- the batch rows' mask words (T <= 24 rows and tail tokens: word 0)
+    // and Q of the group (copy group 0, staged as bf16 in the P slabs) ahead
+    // of the K/V copies
+    uint64_t mword = 0;
+    if (threadIdx.x < a.T) mword = a.mask[(size_t)threadIdx.x * a.mw];
+    unsigned char *sQb = reinterpret_cast<unsigned char *>(sP);  // [RP][256 B] until S starts
+    for (int e = threadIdx.x; e < C::RP * 16; e += NTHR) {
+        const int r = e >> 4, c8 = e & 15;
+        size_t off = 0;
+        if (r < R) off = ((size_t)(r / G) * a.Hq + g * G + r % G) * D + c8 * 8;
+        cp_async16_zfill(sQb + r * ROWB + c8 * 16, a.q + off, r < R);
     }
+    cp_async_commit();
+    // Q is waited for before the K/V copies go out: behind them it would land
+    // only when most of the grid's K/V has (the whole grid asks for its K/V at
+    // once), and no warp can start before Q is in place
+    if (threadIdx.x < a.T) s_mask[threadIdx.x] = mword;
+    cp_async_wait<0>();
+    __syncthreads();
 
-    // ---- this warp's 32 K rows (group 0) and V rows (group 1) -> shared memory
-    // lane: 16-byte chunk lane % 16 of rows lane / 16 + 2u
+    // ---- this warp's half of its block's K rows (group 1) and V rows (group 2)
+    // lane: 16-byte chunk lane % 8 of the half, rows lane / 8 + 4u
     {
-        const int c = lane & 15;
-        const __nv_bfloat16 *kbase = GATHER ? gs.k : a.k, *vbase = GATHER ? gs.v : a.v;
-        size_t off[16];
-        bool ok[16];
+        const int c = lane & 7;
+        size_t off[8];
+        bool ok[8];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int rl = (lane >> 4) + 2 * u;
+        for (int u = 0; u < 8; ++u) {
+            const int rl = (lane >> 3) + 4 * u;
             const int64_t p = wb + rl;
             ok[u] = false;
             off[u] = 0;
@@ -141,60 +168,57 @@ __global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a,
                 if (GATHER) {
                     const int64_t src = src_base + rl;
                     ok[u] = src < gs.N;
-                    off[u] = ((size_t)g * gs.ld + (size_t)src) * D + c * 8;
+                    off[u] = ((size_t)g * gs.ld + (size_t)src) * D + hd * 64 + c * 8;
                 } else {
                     ok[u] = p < plen;
-                    off[u] = ((size_t)g * a.ld_kv + (size_t)p) * D + c * 8;
+                    off[u] = ((size_t)g * a.ld_kv + (size_t)p) * D + hd * 64 + c * 8;
                 }
             } else if (p < L) {
                 ok[u] = true;
-                off[u] = ((size_t)g * a.ld_kv + (size_t)p) * D + c * 8;
+                off[u] = ((size_t)g * a.ld_kv + (size_t)p) * D + hd * 64 + c * 8;
             }
         }
+        const __nv_bfloat16 *ksrc = (GATHER && wb < Np) ? gs.k : a.k;
+        const __nv_bfloat16 *vsrc = (GATHER && wb < Np) ? gs.v : a.v;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int rho = w * WT + (lane >> 4) + 2 * u;
-            const __nv_bfloat16 *src = (GATHER && wb < Np) ? kbase : a.k;
-            cp_async16_zfill(sK + rho * ROWB + ((c ^ (rho & 7)) << 4), src + (ok[u] ? off[u] : 0), ok[u]);
+        for (int u = 0; u < 8; ++u) {
+            const int rho = b * WT + (lane >> 3) + 4 * u;
+            cp_async16_zfill(sK + rho * ROWB + hd * HALFB + ((c ^ (rho & 7)) << 4), ksrc + (ok[u] ? off[u] : 0),
+                             ok[u]);
         }
         cp_async_commit();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int rho = w * WT + (lane >> 4) + 2 * u;
-            const __nv_bfloat16 *src = (GATHER && wb < Np) ? vbase : a.v;
-            cp_async16_zfill(sV + rho * ROWB + (c << 4), src + (ok[u] ? off[u] : 0), ok[u]);
+        for (int u = 0; u < 8; ++u) {
+            const int rho = b * WT + (lane >> 3) + 4 * u;
+            cp_async16_zfill(sV + rho * ROWB + hd * HALFB + (c << 4), vsrc + (ok[u] ? off[u] : 0), ok[u]);
         }
         cp_async_commit();
     }
 
-    // ---- Q -> shared memory as fp32 [dim/4][slot][4]; row r in slot
-    // (r / RG) * QS + r % RG (padding rows zero)
-#pragma unroll
-    for (int u = 0; u < QITER; ++u) {
-        const int e = threadIdx.x + u * NTHR, r = e >> 4, c8 = e & 15;
-        if (r < C::RP) {
-            const uint4 x = qw[u];
-            const int slot = (r / RG) * C::QS + r % RG;
-            float4 *dst = reinterpret_cast<float4 *>(sQ);
-            dst[(2 * c8) * C::QSLOTS + slot] = make_float4(bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y));
-            dst[(2 * c8 + 1) * C::QSLOTS + slot] =
-                make_float4(bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w));
-        }
+    // ---- Q -> fp32 [dim/4][slot][4]; row r in slot (r / RG) * QS + r % RG
+    // (padding rows zero)
+    for (int e = threadIdx.x; e < C::RP * 16; e += NTHR) {
+        const int r = e >> 4, c8 = e & 15;
+        const uint4 x = *reinterpret_cast<const uint4 *>(sQb + r * ROWB + c8 * 16);
+        const int slot = (r / RG) * C::QS + r % RG;
+        float4 *dst = reinterpret_cast<float4 *>(sQ);
+        dst[(2 * c8) * C::QSLOTS + slot] = make_float4(bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y));
+        dst[(2 * c8 + 1) * C::QSLOTS + slot] = make_float4(bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w));
     }
-    __syncthreads();  // Q and the zeroed score slots are visible
+    __syncthreads();  // Q and the zeroed score slots are visible; the staging is dead
 
     cp_async_wait<1>();  // this lane's K copies have landed ...
     __syncwarp();        // ... and every lane's of the warp
 
-    // gather: the warp's K rows into the compact cache (rows that exist)
+    // gather: the warp's K half rows into the compact cache (rows that exist)
     if (GATHER && wb < Np) {
-        const int c = lane & 15;
-#pragma unroll 4
-        for (int u = 0; u < 16; ++u) {
-            const int rl = (lane >> 4) + 2 * u, rho = w * WT + rl;
+        const int c = lane & 7;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int rl = (lane >> 3) + 4 * u, rho = b * WT + rl;
             if (src_base + rl < gs.N) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(sK + rho * ROWB + ((c ^ (rho & 7)) << 4));
-                *reinterpret_cast<uint4 *>(gs.k_dst + ((size_t)g * a.ld_kv + (size_t)(wb + rl)) * D + c * 8) = x;
+                const uint4 x = *reinterpret_cast<const uint4 *>(sK + rho * ROWB + hd * HALFB + ((c ^ (rho & 7)) << 4));
+                *reinterpret_cast<uint4 *>(gs.k_dst + ((size_t)g * a.ld_kv + (size_t)(wb + rl)) * D + hd * 64 + c * 8) = x;
             }
         }
     }
@@ -206,19 +230,19 @@ __global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a,
         m[i] = -INFINITY;
         l[i] = 0.f;
     }
-    float *pw = sP + (size_t)w * WT * C::PP * 2;  // this warp's P slab [token][row][(p, p)]
+    float *pw = sP + (size_t)b * WT * C::PP * 2;  // the block's P slab [token][row][(p, p)]
     if (active) {
-        // ---- S for rows rg*RG + i, tokens tg + 8j of the block: acc[i][j] holds
-        // the even- and odd-dimension partial sums
+        // ---- S over this warp's 64 dims for rows rg*RG + i, tokens tg + 8j:
+        // acc[i][j] holds the even- and odd-dimension partial sums
         float2 acc[RG][4];
 #pragma unroll
         for (int i = 0; i < RG; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
-        const unsigned char *kb = sK + (w * WT + tg) * ROWB;  // token tg; + 8j rows (same swizzle: row & 7 = tg)
-        const float4 *qb = reinterpret_cast<const float4 *>(sQ) + rg * C::QS;
+        unsigned char *kb = sK + (b * WT + tg) * ROWB + hd * HALFB;  // token tg; + 8j rows (row & 7 = tg)
+        const float4 *qb = reinterpret_cast<const float4 *>(sQ) + (size_t)(16 * hd) * C::QSLOTS + rg * C::QS;
 #pragma unroll 2
-        for (int c = 0; c < D / 8; ++c) {
+        for (int c = 0; c < 8; ++c) {
             uint4 kw[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) kw[j] = *reinterpret_cast<const uint4 *>(kb + j * 8 * ROWB + ((c ^ tg) << 4));
@@ -227,26 +251,56 @@ __global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a,
                 float4 q4[RG];
 #pragma unroll
                 for (int i = 0; i < RG; ++i) q4[i] = qb[(2 * c + h) * C::QSLOTS + i];
+                float2 k0[4], k1[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float2 k0 = bf16x2_f2(h ? kw[j].z : kw[j].x);  // dims 8c + 4h, +1
-                    const float2 k1 = bf16x2_f2(h ? kw[j].w : kw[j].y);  // dims 8c + 4h + 2, +3
-#pragma unroll
-                    for (int i = 0; i < RG; ++i) {
-                        acc[i][j] = ffma2(k0, make_float2(q4[i].x, q4[i].y), acc[i][j]);
-                        acc[i][j] = ffma2(k1, make_float2(q4[i].z, q4[i].w), acc[i][j]);
-                    }
+                    k0[j] = bf16x2_f2(h ? kw[j].z : kw[j].x);  // dims 8c + 4h, +1 of the half
+                    k1[j] = bf16x2_f2(h ? kw[j].w : kw[j].y);  // dims 8c + 4h + 2, +3
                 }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int i = 0; i < RG; ++i) acc[i][j] = ffma2(k0[j], make_float2(q4[i].x, q4[i].y), acc[i][j]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int i = 0; i < RG; ++i) acc[i][j] = ffma2(k1[j], make_float2(q4[i].z, q4[i].w), acc[i][j]);
             }
         }
+        // ---- swap half sums with the block's other warp through this warp's
+        // (consumed) K half rows: slot-major [RG][lane][4 tokens]
         float s[RG][4];
+        float4 *xs_mine = reinterpret_cast<float4 *>(kb - tg * ROWB);  // the warp's K half, row 0 of the block
 #pragma unroll
-        for (int i = 0; i < RG; ++i)
+        for (int i = 0; i < RG; ++i) {
+            const float4 v4 = make_float4(acc[i][0].x + acc[i][0].y, acc[i][1].x + acc[i][1].y,
+                                          acc[i][2].x + acc[i][2].y, acc[i][3].x + acc[i][3].y);
+            s[i][0] = v4.x; s[i][1] = v4.y; s[i][2] = v4.z; s[i][3] = v4.w;
+        }
+        // the swap area of a warp: WT rows of HALFB bytes at stride ROWB, i.e. 8
+        // float4 per row; slot q lies in row q / 8, float4 q % 8
+        __syncwarp();  // every lane's K reads are done
 #pragma unroll
-            for (int j = 0; j < 4; ++j) s[i][j] = acc[i][j].x + acc[i][j].y;
+        for (int i = 0; i < RG; ++i) {
+            const int q = i * 32 + lane;
+            xs_mine[(q >> 3) * (ROWB / 16) + (q & 7)] = make_float4(s[i][0], s[i][1], s[i][2], s[i][3]);
+        }
+        pair_sync(b);
+        const float4 *xs_other = reinterpret_cast<const float4 *>(sK + (b * WT) * ROWB + (hd ^ 1) * HALFB);
+        // the sum in a fixed order (half 0 + half 1), so both warps hold the same S
+#pragma unroll
+        for (int i = 0; i < RG; ++i) {
+            const int q = i * 32 + lane;
+            const float4 o4 = xs_other[(q >> 3) * (ROWB / 16) + (q & 7)];
+            if (hd == 0) {
+                s[i][0] += o4.x; s[i][1] += o4.y; s[i][2] += o4.z; s[i][3] += o4.w;
+            } else {
+                s[i][0] = o4.x + s[i][0]; s[i][1] = o4.y + s[i][1]; s[i][2] = o4.z + s[i][2]; s[i][3] = o4.w + s[i][3];
+            }
+        }
 
         // ---- fused chunk importance of the scoring row (raw q.k over the
-        // prefix): this warp's half-chunk sum per head
+        // prefix): the block's half-chunk sum per head
         if (a.chunk_scores != nullptr) {
 #pragma unroll
             for (int i = 0; i < RG; ++i) {
@@ -257,27 +311,33 @@ __global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a,
                 x += __shfl_xor_sync(0xffffffffu, x, 2);
                 x += __shfl_xor_sync(0xffffffffu, x, 4);
                 const int r = rg * RG + i;
-                if (tg == 0 && r < R && r / G == a.score_row) sc_part[w][r % G] = x;
+                if (hd == 0 && tg == 0 && r < R && r / G == a.score_row) sc_part[b][r % G] = x;
             }
         }
 
-        // ---- visibility, scale, the warp's row max
+        // ---- visibility, scale, the block's row max.  A prefix token's
+        // visibility is the same for every row; a batch token's (tail block
+        // only) is the row's mask bit.
         const float cs = a.scale_log2;
+        const bool tail_block = wb + WT > Np;  // the block reaches the batch's own tokens
+        bool tok_ok[4];
+        int tail_u[4];                         // batch token index, or -1 past the batch
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t p = wb + tg + 8 * j;
+            tok_ok[j] = p < Np && (GATHER ? (src_base + tg + 8 * j < gs.N) : (p < plen));
+            tail_u[j] = (p >= Np && p < L) ? (int)(p - Np) : -1;
+        }
 #pragma unroll
         for (int i = 0; i < RG; ++i) {
             const int r = rg * RG + i;
-            const int t = r < R ? r / G : 0;
+            const bool row_ok = r < R;
+            const uint64_t mrow = (tail_block && row_ok) ? s_mask[r / G] : 0ull;
             float mx = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int64_t p = wb + tg + 8 * j;
-                bool vis = r < R && p < L;
-                if (vis) {
-                    if (p < Np)
-                        vis = GATHER ? (src_base + tg + 8 * j < gs.N) : (p < plen);
-                    else
-                        vis = mask_bit(a.mask, a.mw, t, (int)(p - Np));
-                }
+                bool vis = row_ok && tok_ok[j];
+                if (tail_block) vis = vis || (tail_u[j] >= 0 && ((mrow >> tail_u[j]) & 1ull));
                 s[i][j] = vis ? s[i][j] * cs : -INFINITY;
                 mx = fmaxf(mx, s[i][j]);
             }
@@ -286,16 +346,19 @@ __global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a,
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             m[i] = mx;
         }
-        // ---- P = 2^(s*c - m) into the slab as (p, p); the warp's row sums
+        // ---- P = 2^(s*c - m); this warp writes row groups 2hd, 2hd + 1 of the
+        // block's slab as (p, p); the block's row sums
+        const bool writer = (rg >> 1) == hd;
 #pragma unroll
         for (int i = 0; i < RG; ++i) {
             float ls = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float pv = (m[i] == -INFINITY) ? 0.f : exp2f(s[i][j] - m[i]);
+                const float pv = (m[i] == -INFINITY) ? 0.f : fast_exp2(s[i][j] - m[i]);
                 ls += pv;
-                *reinterpret_cast<float2 *>(pw + ((size_t)(tg + 8 * j) * C::PP + rg * RG + i) * 2) =
-                    make_float2(pv, pv);
+                if (writer)
+                    *reinterpret_cast<float2 *>(pw + ((size_t)(tg + 8 * j) * C::PP + rg * RG + i) * 2) =
+                        make_float2(pv, pv);
             }
             ls += __shfl_xor_sync(0xffffffffu, ls, 1);
             ls += __shfl_xor_sync(0xffffffffu, ls, 2);
@@ -303,59 +366,54 @@ __global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a,
             l[i] = ls;
         }
     }
-    if (tg == 0) {
+    if (hd == 0 && tg == 0) {
 #pragma unroll
         for (int i = 0; i < RG; ++i) {
-            red_m[w][rg * RG + i] = m[i];
-            red_l[w][rg * RG + i] = l[i];
+            red_m[b][rg * RG + i] = m[i];
+            red_l[b][rg * RG + i] = l[i];
         }
     }
 
     cp_async_wait<0>();  // V has landed (this lane's copies) ...
-    __syncwarp();        // ... and every lane's; this warp's P is visible too
+    __syncwarp();        // ... and every lane's
 
     if (GATHER && wb < Np) {
-        const int c = lane & 15;
-#pragma unroll 4
-        for (int u = 0; u < 16; ++u) {
-            const int rl = (lane >> 4) + 2 * u, rho = w * WT + rl;
+        const int c = lane & 7;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int rl = (lane >> 3) + 4 * u, rho = b * WT + rl;
             if (src_base + rl < gs.N) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(sV + rho * ROWB + (c << 4));
-                *reinterpret_cast<uint4 *>(gs.v_dst + ((size_t)g * a.ld_kv + (size_t)(wb + rl)) * D + c * 8) = x;
+                const uint4 x = *reinterpret_cast<const uint4 *>(sV + rho * ROWB + hd * HALFB + (c << 4));
+                *reinterpret_cast<uint4 *>(gs.v_dst + ((size_t)g * a.ld_kv + (size_t)(wb + rl)) * D + hd * 64 + c * 8) = x;
             }
         }
     }
 
-    // ---- O over the warp's 32 tokens: rows rh*2RG + i2, dims 8dg .. 8dg+7
+    // ---- O over the block's 32 tokens: rows rh*2RG + i2, dims 64hd + 4dg .. +3
     const int rh = lane >> 4, dg = lane & 15;
-    float2 o[2 * RG][4];
+    float2 o[2 * RG][2];
 #pragma unroll
-    for (int i = 0; i < 2 * RG; ++i)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o[i][k] = make_float2(0.f, 0.f);
+    for (int i = 0; i < 2 * RG; ++i) o[i][0] = o[i][1] = make_float2(0.f, 0.f);
     if (active) {
-        const unsigned char *vb = sV + (w * WT) * ROWB + dg * 16;
+        pair_sync(b);  // the block's P (both warps' rows) is visible
+        const unsigned char *vb = sV + (b * WT) * ROWB + hd * HALFB + dg * 8;
         const float *pb = pw + rh * 2 * RG * 2;
 #pragma unroll 4
         for (int tw = 0; tw < WT; ++tw) {
-            const uint4 vw = *reinterpret_cast<const uint4 *>(vb + tw * ROWB);
-            const float2 v0 = bf16x2_f2(vw.x), v1 = bf16x2_f2(vw.y), v2 = bf16x2_f2(vw.z), v3 = bf16x2_f2(vw.w);
+            const uint2 vw = *reinterpret_cast<const uint2 *>(vb + tw * ROWB);
+            const float2 v0 = bf16x2_f2(vw.x), v1 = bf16x2_f2(vw.y);
 #pragma unroll
             for (int i = 0; i < RG; ++i) {
                 const float4 pp = *reinterpret_cast<const float4 *>(pb + ((size_t)tw * C::PP + 2 * i) * 2);
                 const float2 pa = make_float2(pp.x, pp.y), pc = make_float2(pp.z, pp.w);
                 o[2 * i][0] = ffma2(pa, v0, o[2 * i][0]);
                 o[2 * i][1] = ffma2(pa, v1, o[2 * i][1]);
-                o[2 * i][2] = ffma2(pa, v2, o[2 * i][2]);
-                o[2 * i][3] = ffma2(pa, v3, o[2 * i][3]);
                 o[2 * i + 1][0] = ffma2(pc, v0, o[2 * i + 1][0]);
                 o[2 * i + 1][1] = ffma2(pc, v1, o[2 * i + 1][1]);
-                o[2 * i + 1][2] = ffma2(pc, v2, o[2 * i + 1][2]);
-                o[2 * i + 1][3] = ffma2(pc, v3, o[2 * i + 1][3]);
             }
         }
     }
-    __syncthreads();  // every warp's (m, l) and score sums are written; K and V are dead
+    __syncthreads();  // every block's (m, l) and score sums are written; K and V are dead
 
     if (a.chunk_scores != nullptr && threadIdx.x < 2) {
         const int64_t ch0 = t0 + 64 * threadIdx.x;
@@ -366,25 +424,24 @@ __global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a,
         }
     }
 
-    // ---- combine the four warp partials: each warp scales its O by
-    // 2^(m_w - M) and parks it over the K/V buffers as fp32 [warp][row][dim]
+    // ---- combine the four block partials: each warp scales its O by
+    // 2^(m_b - M) and parks it over the K/V buffers as fp32 [block][row][dim]
     float *sO = reinterpret_cast<float *>(smem_raw);
 #pragma unroll
     for (int i2 = 0; i2 < 2 * RG; ++i2) {
         const int r = rh * 2 * RG + i2;
         float M = red_m[0][r];
 #pragma unroll
-        for (int x = 1; x < NWARP; ++x) M = fmaxf(M, red_m[x][r]);
-        const float mw = red_m[w][r];
-        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        float4 *dst = reinterpret_cast<float4 *>(sO + ((size_t)w * C::RP + r) * D + dg * 8);
-        dst[0] = make_float4(o[i2][0].x * f, o[i2][0].y * f, o[i2][1].x * f, o[i2][1].y * f);
-        dst[1] = make_float4(o[i2][2].x * f, o[i2][2].y * f, o[i2][3].x * f, o[i2][3].y * f);
+        for (int x = 1; x < NBLK; ++x) M = fmaxf(M, red_m[x][r]);
+        const float mb = red_m[b][r];
+        const float f = (mb == -INFINITY) ? 0.f : fast_exp2(mb - M);
+        *reinterpret_cast<float4 *>(sO + ((size_t)b * C::RP + r) * D + hd * 64 + dg * 4) =
+            make_float4(o[i2][0].x * f, o[i2][0].y * f, o[i2][1].x * f, o[i2][1].y * f);
         if (w == 0 && dg == 0) {
             float Ls = 0.f;
 #pragma unroll
-            for (int x = 0; x < NWARP; ++x)
-                if (red_m[x][r] != -INFINITY) Ls += exp2f(red_m[x][r] - M) * red_l[x][r];
+            for (int x = 0; x < NBLK; ++x)
+                if (red_m[x][r] != -INFINITY) Ls += fast_exp2(red_m[x][r] - M) * red_l[x][r];
             row_m[r] = M;
             row_l[r] = Ls;
         }
@@ -398,7 +455,7 @@ __global__ void __launch_bounds__(NTHR) tree_attn_small_kernel(const AttnArgs a,
         const int r = e >> 5, q4 = e & 31;
         float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int x = 0; x < NWARP; ++x) {
+        for (int x = 0; x < NBLK; ++x) {
             const float4 y = *reinterpret_cast<const float4 *>(sO + ((size_t)x * C::RP + r) * D + 4 * q4);
             acc4.x += y.x; acc4.y += y.y; acc4.z += y.z; acc4.w += y.w;
         }

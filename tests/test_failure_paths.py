@@ -27,11 +27,12 @@ def _built():
 
 
 def test_injected_launch_failure_is_reported_on_the_host():
-    """No GPU needed: the injected failure is taken before any launch."""
+    """No GPU needed: the injected failure is taken before any launch (a batch
+    for the CUDA-core kernel that needs no tensor map)."""
     L = ts.lib()
     P = ctypes.c_void_p(0x10000)
     ts.ts_selftest_fail_launches(1)
-    st = L.ts_tree_attn(P, P, P, 4100, 4096, 4, 40, 8, 128, 0.088, P, P, None, None, 0, P, 1 << 30, None)
+    st = L.ts_tree_attn(P, P, P, 4100, 4000, 30, 40, 8, 128, 0.088, P, P, None, None, 0, P, 1 << 30, None)
     assert st == ts.TS_ERR_CUDA
     assert b"cudaErrorInvalidValue" in L.ts_last_error() and b"launch" in L.ts_last_error()
     ts.ts_selftest_fail_launches(0)
