@@ -16,9 +16,10 @@
 //          into shared memory with 16-byte cp.async (K XOR-swizzled by
 //          16-byte chunk within each 128-byte half row, so that a quarter-warp
 //          reading one chunk of eight rows hits eight banks); rows out of range
-//          or not gathered are zero-filled.  Q comes first (its own copy group,
-//          waited for before the K/V copies go out) and is converted to fp32
-//          [dim/4][row slot][4].
+//          or not gathered are zero-filled.  Q comes first (prefetched into L2
+//          before the kernel waits for its predecessor, then its own copy
+//          group, waited for before the K/V copies go out) and is converted to
+//          fp32 [dim/4][row slot][4].
 //   S:     lane (rg, tg) = (lane / 8, lane % 8) takes rows rg*RG .. +RG-1 and
 //          tokens tg + 8i (i < 4) of the block: per 8 dims of its half it reads
 //          four K chunks and 2 RG Q quads and issues 16 RG fp32x2 FMAs over
@@ -111,6 +112,13 @@ __global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs
     __shared__ float sc_part[NBLK][32];                       // scoring row: half-chunk sums per head
     __shared__ uint64_t s_mask[24];                           // batch rows' mask words
 
+    // Q into L2 while the previous kernel finishes (a prefetch is only a hint:
+    // a line that a later write replaces is replaced in L2 too)
+    for (int e = threadIdx.x; e < 2 * a.T * a.G; e += NTHR) {
+        const int r = e >> 1;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.q + ((size_t)(r / a.G) * a.Hq + blockIdx.y * a.G + r % a.G) * D +
+                                                      (e & 1) * 64));
+    }
     // a programmatic dependent: the previous kernel (the selection, the gather
     // of the partial cache) has completed and its writes are visible past here
     asm volatile("griddepcontrol.wait;" ::: "memory");
