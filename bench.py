@@ -366,7 +366,8 @@ def run_native(args, ws, rank, local):
     cfg = workload_config(args.workload)
     peaks = read_peaks()
     # the step computes what the method consumes: O (and the chunk scores), no log-sum-exp
-    step = SpecStep(cfg, layers=args.layers, want_lse=False, fuse_gather=not args.separate_gather)
+    step = SpecStep(cfg, layers=args.layers, want_lse=False, fuse_gather=not args.separate_gather,
+                    overlap_select=not args.one_stream)
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -661,6 +662,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip timing the verify call on the other workloads")
     ap.add_argument("--layers", type=int, default=None, help="run only this many layers (profiling)")
+    ap.add_argument("--one-stream", action="store_true",
+                    help="run each layer's calls in order on one stream (no selection beside the verify merge)")
     ap.add_argument("--separate-gather", action="store_true",
                     help="gather with the selection call, then the drafting attention over the compact cache")
     ap.add_argument("--cpu-row-fraction", type=float, default=1.0,

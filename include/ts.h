@@ -12,6 +12,7 @@
  *                            (verify pass over the full cache; draft pass over
  *                            the partial cache), split over the KV length with
  *                            a log-sum-exp merge, optional fused chunk scores;
+ *   ts_tree_attn_unmerged/_merge  the same in two halves (attention, merge);
  *   ts_tree_attn_partial     the drafting pass over the compact partial cache
  *                            (per-KV-head count of gathered tokens);
  *   ts_score_chunks          query-key importance of every 64-token KV chunk;
@@ -136,6 +137,29 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
                        const uint64_t *mask, void *out, float *lse,
                        float *chunk_scores, int score_row,
                        void *workspace, size_t ws_bytes, ts_stream_t stream);
+
+/*
+ * ts_tree_attn in two halves, for callers that run other work between the
+ * attention kernel and the merge of its split partials (the chunk selection
+ * needs only the chunk scores, so it can run beside the merge on another
+ * stream; the merge then needs its own workspace).
+ *   ts_tree_attn_unmerged: the same arguments and checks as ts_tree_attn; it
+ *     enqueues the attention kernel only.  When the plan has one split the
+ *     kernel writes out / lse itself; otherwise they are written by
+ *     ts_tree_attn_merge, which must follow on the same stream (or after it)
+ *     with the same T, Hq, Hkv, d, N, out, lse and workspace, before the
+ *     workspace is reused.  chunk_scores are complete when this half is.
+ *   ts_tree_attn_merge: the log-sum-exp merge of those partials (a no-op when
+ *     the plan has one split).
+ * Together they produce exactly what one ts_tree_attn call produces.
+ */
+ts_status ts_tree_attn_unmerged(const void *q, const void *k, const void *v, int64_t ld_kv,
+                                int64_t N, int T, int Hq, int Hkv, int d, float scale,
+                                const uint64_t *mask, void *out, float *lse,
+                                float *chunk_scores, int score_row,
+                                void *workspace, size_t ws_bytes, ts_stream_t stream);
+ts_status ts_tree_attn_merge(int64_t N, int T, int Hq, int Hkv, int d, void *out, float *lse,
+                             const void *workspace, size_t ws_bytes, ts_stream_t stream);
 
 /*
  * The self-drafting pass over the compact partial cache that ts_select_gather

@@ -28,7 +28,7 @@ _STATUS = {0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_UNSUPPORTED", 3: "TS_
 __all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree_attn_workspace_bytes",
            "ts_launch_count", "ts_tree_attn_uses_tensor_cores", "ts_device_error", "ts_selftest_bounded_wait",
            "ts_selftest_fail_launches", "ts_tree_attn",
-           "ts_tree_attn_partial", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_rescore_tail",
+           "ts_tree_attn_unmerged", "ts_tree_attn_merge", "ts_tree_attn_partial", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_rescore_tail",
            "ts_select_gather", "ts_select_chunks", "ts_gather_tree_attn", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path",
            "ts_ngram_table_bytes", "ts_ngram_reset", "ts_ngram_update", "ts_ngram_topk", "ts_vocab_verify"]
 
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         L.ts_selftest_fail_launches.restype = None
         L.ts_tree_attn.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P, sz, P]
         L.ts_tree_attn_partial.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, P, sz, P]
+        L.ts_tree_attn_unmerged.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P, sz, P]
+        L.ts_tree_attn_merge.argtypes = [i64, i32, i32, i32, i32, P, P, P, sz, P]
         L.ts_tree_attn_noalloc.argtypes = [P, P, P, i64, i64, i32, i32, i32, i32, f32, P, P, P, P, i32, P]
         L.ts_score_chunks.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P, P]
         L.ts_rescore_tail.argtypes = [P, i64, P, P, i64, i64, i32, i32, i32, i32, P, P]
@@ -89,7 +91,8 @@ def lib() -> ctypes.CDLL:
         u64 = ctypes.c_uint64
         L.ts_penalty_minp_sample_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, u64, u64, P, P,
                                                     ctypes.c_int32, P, P, P, P, P]
-        for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_partial", "ts_tree_attn_noalloc",
+        for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_unmerged", "ts_tree_attn_merge",
+                     "ts_tree_attn_partial", "ts_tree_attn_noalloc",
                      "ts_score_chunks", "ts_rescore_tail", "ts_select_gather", "ts_select_chunks",
                      "ts_gather_tree_attn", "ts_penalty_minp_verify",
                      "ts_commit_path", "ts_penalty_minp_sample_verify", "ts_ngram_reset", "ts_ngram_update",
@@ -176,6 +179,29 @@ def ts_tree_attn(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_
     _check(lib().ts_tree_attn(_ptr(q), _ptr(k), _ptr(v), ld, N, T, Hq, Hkv, d, scale, _ptr(mask), _ptr(out),
                               _ptr(lse), _ptr(chunk_scores), score_row, _ptr(workspace), ws_bytes,
                               _stream(stream)))
+
+
+def ts_tree_attn_unmerged(q, k, v, N: int, mask, out, lse=None, chunk_scores=None, score_row: int = 0,
+                          workspace=None, scale: Optional[float] = None, stream=None) -> None:
+    """The attention kernel of ts_tree_attn without the merge of its split
+    partials; ts_tree_attn_merge completes out / lse."""
+    T, Hq, d = q.shape
+    Hkv, ld, _ = k.shape
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ts_tree_attn_unmerged(_ptr(q), _ptr(k), _ptr(v), ld, N, T, Hq, Hkv, d, scale, _ptr(mask), _ptr(out),
+                                       _ptr(lse), _ptr(chunk_scores), score_row, _ptr(workspace), ws_bytes,
+                                       _stream(stream)))
+
+
+def ts_tree_attn_merge(out, Hkv: int, N: int, lse=None, workspace=None, stream=None) -> None:
+    """The log-sum-exp merge that completes ts_tree_attn_unmerged (same out,
+    lse, workspace and shapes)."""
+    T, Hq, d = out.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ts_tree_attn_merge(N, T, Hq, Hkv, d, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                    _stream(stream)))
 
 
 def ts_tree_attn_partial(q, k_part, v_part, B: int, mask, part_len, out, lse=None, workspace=None,

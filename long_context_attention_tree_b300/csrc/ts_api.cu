@@ -216,7 +216,7 @@ static ts_status tree_attn_impl(const void *q, const void *k, const void *v, int
                                 int Hq, int Hkv, int d, float scale, const uint64_t *mask,
                                 const int32_t *prefix_len, void *out, float *lse, float *chunk_scores,
                                 int score_row, void *workspace, size_t ws_bytes, ts_stream_t stream,
-                                const ts::SmallGather *gather = nullptr) {
+                                const ts::SmallGather *gather = nullptr, bool merge = true) {
     ts_status st = check_attn_shape(T, Hq, Hkv, d, N);
     if (st != TS_OK) return st;
     if (T == 0) return TS_OK;
@@ -289,7 +289,7 @@ static ts_status tree_attn_impl(const void *q, const void *k, const void *v, int
         if (e != cudaSuccess) return cuda_fail(e, "tree_attn_simt launch");
     }
     ts::note_launches(1);
-    if (plan.splits > 1) {
+    if (plan.splits > 1 && merge) {
         ts::MergeArgs m{a.ws_o, a.ws_ml, a.out, a.lse, T, Hq, plan.splits, T, plan.splits};
         if (plan.tc) {
             // rows of pair streams have s_pair partials, rows of the single stream s_single
@@ -313,6 +313,41 @@ ts_status ts_tree_attn(const void *q, const void *k, const void *v, int64_t ld_k
                        void *workspace, size_t ws_bytes, ts_stream_t stream) {
     return tree_attn_impl(q, k, v, ld_kv, N, T, Hq, Hkv, d, scale, mask, nullptr, out, lse, chunk_scores, score_row,
                           workspace, ws_bytes, stream);
+}
+
+ts_status ts_tree_attn_unmerged(const void *q, const void *k, const void *v, int64_t ld_kv,
+                                int64_t N, int T, int Hq, int Hkv, int d, float scale,
+                                const uint64_t *mask, void *out, float *lse,
+                                float *chunk_scores, int score_row,
+                                void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    return tree_attn_impl(q, k, v, ld_kv, N, T, Hq, Hkv, d, scale, mask, nullptr, out, lse, chunk_scores, score_row,
+                          workspace, ws_bytes, stream, nullptr, false);
+}
+
+ts_status ts_tree_attn_merge(int64_t N, int T, int Hq, int Hkv, int d, void *out, float *lse,
+                             const void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    ts_status st = check_attn_shape(T, Hq, Hkv, d, N);
+    if (st != TS_OK) return st;
+    if (T == 0) return TS_OK;
+    const AttnPlan plan = plan_attention(T, Hq, Hkv, d, N);
+    if (plan.splits <= 1) return TS_OK;  // the attention kernel wrote the output itself
+    if (!out || !aligned16(out) || (lse && !aligned4(lse)))
+        return fail(TS_ERR_INVALID_ARG, "null or misaligned out/lse");
+    const size_t need = workspace_for(plan, T, Hq, d);
+    if (workspace == nullptr || ws_bytes < need || !aligned16(workspace))
+        return fail(TS_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) needed, %zu given", need, ws_bytes);
+    const float *ws_o = static_cast<const float *>(workspace);
+    ts::MergeArgs m{ws_o, ws_o + (size_t)plan.splits * T * Hq * d, static_cast<__nv_bfloat16 *>(out), lse, T, Hq,
+                    plan.splits, T, plan.splits};
+    if (plan.tc) {
+        m.splits = plan.tcp.s_pair;
+        m.t_split = 2 * plan.tcp.n_pair * plan.tcp.tpb;
+        m.splits_hi = plan.tcp.s_single;
+    }
+    cudaError_t e = ts::launch_lse_merge(m, d, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
+    ts::note_launches(1);
+    return TS_OK;
 }
 
 ts_status ts_tree_attn_partial(const void *q, const void *k_part, const void *v_part, int64_t ld_part,

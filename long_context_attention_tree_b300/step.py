@@ -15,8 +15,10 @@ Then, once per step, the vocabulary stage (penalty, min-p, greedy target,
 acceptance).
 
 Every step is one C-ABI call into libts.so; this module only owns device
-memory (allocated once, through torch) and orders the calls on one stream.
-The step can be captured into a CUDA graph.
+memory (allocated once, through torch) and orders the calls on a stream
+(the selection and drafting pass of a layer on a side stream beside the merge
+of the verify partials, joined before the next layer).  The step can be
+captured into a CUDA graph.
 """
 from __future__ import annotations
 
@@ -27,7 +29,8 @@ import numpy as np
 import torch
 
 from . import (ts_gather_tree_attn, ts_penalty_minp_verify, ts_select_chunks, ts_select_gather, ts_tree_attn,
-               ts_tree_attn_partial, ts_tree_attn_workspace_bytes, ts_tree_mask_from_parents)
+               ts_tree_attn_merge, ts_tree_attn_partial, ts_tree_attn_unmerged, ts_tree_attn_workspace_bytes,
+               ts_tree_mask_from_parents)
 from . import workloads as W
 
 
@@ -51,9 +54,13 @@ class LayerBuffers:
 class SpecStep:
     def __init__(self, cfg: W.Config, device="cuda", layers: Optional[int] = None, vocab: Optional[bool] = None,
                  value_kind: str = "int", fill_draft_tail: bool = True, want_lse: bool = True,
-                 fuse_gather: bool = True):
+                 fuse_gather: bool = True, overlap_select: bool = True):
         self.cfg = cfg
         self.fuse_gather = fuse_gather
+        # with a stream given, the selection and the drafting pass of a layer
+        # run on a side stream beside the merge of the verify partials (the
+        # selection needs only the chunk scores of the verify kernel)
+        self.overlap_select = overlap_select
         # the log-sum-exp outputs (the method itself consumes only O; the
         # kernels skip the exact normaliser sum when it is not asked for)
         self.want_lse = want_lse
@@ -68,9 +75,10 @@ class SpecStep:
         self.draft_parents = [-1] + list(range(self.Td - 1))
         self.mask = torch.from_numpy(ts_tree_mask_from_parents(parents).view(np.int64)).to(self.device)
         self.mask_draft = torch.from_numpy(ts_tree_mask_from_parents(self.draft_parents).view(np.int64)).to(self.device)
-        ws = max(ts_tree_attn_workspace_bytes(self.T, cfg.Hq, cfg.Hkv, cfg.d, cfg.N),
-                 ts_tree_attn_workspace_bytes(self.Td, cfg.Hq, cfg.Hkv, cfg.d, self.B))
+        ws = ts_tree_attn_workspace_bytes(self.T, cfg.Hq, cfg.Hkv, cfg.d, cfg.N)
+        ws_d = ts_tree_attn_workspace_bytes(self.Td, cfg.Hq, cfg.Hkv, cfg.d, self.B)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.device)
+        self.workspace_draft = torch.empty(max(ws_d, 16), dtype=torch.uint8, device=self.device)
         self.layers: List[LayerBuffers] = []
         nc = cfg.n_chunks
         for layer in range(self.n_layers):
@@ -120,15 +128,34 @@ class SpecStep:
         lse = L.lse_draft if self.want_lse else None
         if self.fuse_gather:
             ts_gather_tree_attn(L.q_draft, L.k, L.v, cfg.N, L.sel, L.k_part, L.v_part, self.mask_draft, L.out_draft,
-                                lse=lse, workspace=self.workspace, scale=cfg.scale, stream=stream)
+                                lse=lse, workspace=self.workspace_draft, scale=cfg.scale, stream=stream)
         else:
             ts_tree_attn_partial(L.q_draft, L.k_part, L.v_part, self.B, self.mask_draft, L.part_len, L.out_draft,
-                                 lse=lse, workspace=self.workspace, scale=cfg.scale, stream=stream)
+                                 lse=lse, workspace=self.workspace_draft, scale=cfg.scale, stream=stream)
 
     def run_layer(self, i: int, stream=None) -> None:
-        self.run_verify(i, stream)
-        self.run_refresh(i, stream)
-        self.run_draft(i, stream)
+        if not (self.overlap_select and stream is not None):
+            self.run_verify(i, stream)
+            self.run_refresh(i, stream)
+            self.run_draft(i, stream)
+            return
+        cfg, L = self.cfg, self.layers[i]
+        if not hasattr(self, "_side"):
+            self._side = torch.cuda.Stream(device=self.device)
+            self._ev_scores = [torch.cuda.Event() for _ in range(self.n_layers)]
+            self._ev_draft = [torch.cuda.Event() for _ in range(self.n_layers)]
+        # verify kernel; its chunk scores feed the selection on the side
+        # stream while the split merge runs here
+        lse = L.lse if self.want_lse else None
+        ts_tree_attn_unmerged(L.q, L.k, L.v, cfg.N, self.mask, L.out, lse=lse, chunk_scores=L.scores, score_row=0,
+                              workspace=self.workspace, scale=cfg.scale, stream=stream)
+        self._ev_scores[i].record(stream)
+        self._side.wait_event(self._ev_scores[i])
+        self.run_refresh(i, self._side)
+        self.run_draft(i, self._side)
+        self._ev_draft[i].record(self._side)
+        ts_tree_attn_merge(L.out, cfg.Hkv, cfg.N, lse=lse, workspace=self.workspace, stream=stream)
+        stream.wait_event(self._ev_draft[i])
 
     def run_vocab(self, stream=None) -> None:
         cfg, vi = self.cfg, self.vocab_inputs

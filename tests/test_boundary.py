@@ -166,6 +166,18 @@ def test_gather_tree_attn_rejects(kw, status):
     assert ts.lib().ts_last_error()
 
 
+def test_tree_attn_merge_host_checks():
+    L = ts.lib()
+    P = 0x10000
+    # a multi-split plan needs the workspace the unmerged half filled
+    assert L.ts_tree_attn_merge(20480, 120, 40, 8, 128, P, None, P, 16, None) == ts.TS_ERR_INVALID_ARG
+    assert L.ts_tree_attn_merge(20480, 120, 40, 8, 128, None, None, P, 1 << 30, None) == ts.TS_ERR_INVALID_ARG
+    # one split (the kernel wrote the output) and an empty batch: nothing to do
+    assert L.ts_tree_attn_merge(60, 4, 8, 8, 128, P, None, None, 0, None) == ts.TS_OK
+    assert L.ts_tree_attn_merge(4096, 0, 40, 8, 128, None, None, None, 0, None) == ts.TS_OK
+    assert L.ts_tree_attn_merge(4096, 4, 40, 7, 128, P, None, P, 1 << 30, None) == ts.TS_ERR_INVALID_ARG
+
+
 def test_rescore_tail_rejects():
     L = ts.lib()
     P = 0x10000

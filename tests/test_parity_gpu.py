@@ -357,6 +357,31 @@ def test_gather_tree_attn_matches_oracle_and_the_two_calls(N, Hq, Hkv, Td, budge
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
 
 
+@pytest.mark.parametrize("T,Hq,Hkv,N", [(120, 40, 8, 20480), (4, 40, 8, 4100), (30, 32, 8, 5000), (4, 8, 8, 60)])
+def test_unmerged_then_merge_equals_one_call(T, Hq, Hkv, N):
+    """ts_tree_attn_unmerged, then ts_tree_attn_merge on another stream after
+    an event: bit for bit what one ts_tree_attn call produces (tensor-core,
+    small-batch and CUDA-core plans, and a one-split plan)."""
+    d = 128
+    q, k, v = W.make_qkv(T, Hq, Hkv, d, N, seed=T + N, device="cuda", value_kind="normal")
+    parent = verify_parent(T)
+    o1, l1, s1 = run_attn(q, k, v, N, parent, 1 / math.sqrt(d), scores=True)
+    out = torch.empty_like(o1)
+    lse = torch.empty_like(l1)
+    sc = torch.full_like(s1, float("nan"))
+    ws = torch.empty(max(16, ts.ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N)), dtype=torch.uint8, device="cuda")
+    s_main, s_side = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    ts.ts_tree_attn_unmerged(q, k, v, N, dev_mask(parent), out, lse=lse, chunk_scores=sc, workspace=ws,
+                             scale=1 / math.sqrt(d), stream=s_main)
+    ev.record(s_main)
+    s_side.wait_event(ev)
+    ts.ts_tree_attn_merge(out, Hkv, N, lse=lse, workspace=ws, stream=s_side)
+    torch.cuda.synchronize()
+    assert ts.ts_device_error(True) == ts.TS_OK
+    assert torch.equal(out, o1) and torch.equal(lse, l1) and torch.equal(sc, s1)
+
+
 @pytest.mark.parametrize("N_old,N_new", [(4094, 4098), (4096, 4100), (4100, 4100), (0, 37), (20480, 20483),
                                          (130, 135), (63, 64), (102400, 102404)])
 def test_rescore_tail_equals_full_scoring(N_old, N_new):
