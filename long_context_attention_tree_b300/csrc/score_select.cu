@@ -106,17 +106,21 @@ cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *score
 
 // ---------------------------------------------------------------------------
 // Top-k selection, then the gather.
-// select_kernel: one CTA per KV head computes sel[g][.] and part_len[g] from
-// composite keys (order key << 32 | ~chunk index), which are unique and order
-// equal scores by lower index.  For k <= 256 every warp keeps a sorted list of
-// its best L = 32R keys in registers (R per lane), merging in one batch of L
-// keys at a time, and the 32 lists are merged pairwise through shared memory;
-// larger k sort all keys in shared memory.
+// select_kernel: one CTA per KV head computes sel[g][.] and part_len[g].
+// Every chunk has a 32-bit order key (the score's bits mapped so that unsigned
+// order is numeric order, -0 = +0; always-kept chunks take the largest key);
+// the chosen set is the k largest keys, equal keys going to the lower chunk
+// index.  A radix select finds the k-th largest key tau in four passes of
+// 8-bit digits (a 256-bin shared-memory histogram of the keys that match the
+// digits found so far, then a suffix scan by one warp); then every key above
+// tau is chosen, and of the keys equal to tau the lowest-indexed ones that
+// complete k.  The chosen indices are written in ascending order by a block
+// scan over contiguous index ranges (one range per thread).
 // gather_kernel: CTA = (selected chunk, KV head) copies the chunk's K and V
 // rows.  The gather is launched as a programmatic dependent of the selection
 // so its CTAs are resident and waiting when the selection finishes.
 // ---------------------------------------------------------------------------
-constexpr int SEL_THREADS = 1024;
+constexpr int SEL_THREADS = 512;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int GA_THREADS = 256;
 
@@ -126,205 +130,136 @@ __device__ __forceinline__ uint32_t order_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// The composite key of chunk c: always-kept chunks (the first n_sink, the
-// last n_recent) take the largest order key, above every finite score's;
-// padding (c >= n_chunks) is 0, below every key.
-__device__ __forceinline__ uint64_t chunk_key(const float *sc, int c, int n_chunks, int n_sink, int n_recent) {
-    if (c >= n_chunks) return 0ull;
-    const uint32_t key = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
-    return ((uint64_t)key << 32) | (uint32_t)~(uint32_t)c;
-}
-
-// One compare-exchange step of a bitonic network at distance j over a list of
-// 32R keys held by one warp, element e = s*32 + lane in v[s].  Runs of length
-// k end in descending order where (e & k) == 0 for DESC (ascending otherwise).
-template <int R, typename K, bool DESC>
-__device__ __forceinline__ void warp_cx(K (&v)[R], int k, int j, int lane) {
-    if (j >= 32) {
-        const int js = j >> 5;
+// Exclusive prefix sum of v over the CTA in thread order; *total gets the sum.
+// Uses warp_tot[SEL_WARPS] in shared memory; two CTA barriers.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
 #pragma unroll
-        for (int s = 0; s < R; ++s) {
-            if ((s & js) == 0) {
-                const int e = s * 32 + lane;
-                const bool desc = ((e & k) == 0) == DESC;
-                const K a = v[s], b = v[s + js];
-                const bool sw = desc ? (a < b) : (a > b);
-                v[s] = sw ? b : a;
-                v[s + js] = sw ? a : b;
-            }
-        }
-    } else {
-        const bool lower = (lane & j) == 0;
-#pragma unroll
-        for (int s = 0; s < R; ++s) {
-            const int e = s * 32 + lane;
-            const bool desc = ((e & k) == 0) == DESC;
-            const K o = __shfl_xor_sync(0xffffffffu, v[s], j);
-            v[s] = (lower == desc) ? (v[s] > o ? v[s] : o) : (v[s] < o ? v[s] : o);
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-}
-template <int R, typename K, bool DESC>
-__device__ __forceinline__ void warp_sort(K (&v)[R], int lane) {
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    int base = 0, sum = 0;
 #pragma unroll
-    for (int k = 2; k <= 32 * R; k <<= 1)
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) warp_cx<R, K, DESC>(v, k, j, lane);
-}
-// v (descending) and b (ascending): v <- the 32R largest of both, descending.
-// The element-wise maximum of a descending and an ascending list holds the
-// largest half of their union as a bitonic sequence, which the half-cleaner
-// stages then sort.
-template <int R>
-__device__ __forceinline__ void warp_merge_top(uint64_t (&v)[R], const uint64_t (&b)[R], int lane) {
-#pragma unroll
-    for (int s = 0; s < R; ++s) v[s] = v[s] > b[s] ? v[s] : b[s];
-#pragma unroll
-    for (int j = 16 * R; j > 0; j >>= 1) warp_cx<R, uint64_t, true>(v, 64 * R, j, lane);
-}
-
-template <int R>
-__device__ void select_topk_warps(const float *sc, int n_chunks, int k_sel, int n_sink, int n_recent,
-                                  uint64_t *lists, int32_t *sel_g, int *last_selected) {
-    constexpr int L = 32 * R;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_batches = (n_chunks + L - 1) / L;
-    uint64_t v[R];
-#pragma unroll
-    for (int s = 0; s < R; ++s) v[s] = 0ull;
-    if (warp < n_batches) {
-        // the warp's first batch, sorted descending, is its list
-#pragma unroll
-        for (int s = 0; s < R; ++s) v[s] = chunk_key(sc, warp * L + s * 32 + lane, n_chunks, n_sink, n_recent);
-        warp_sort<R, uint64_t, true>(v, lane);
+    for (int w = 0; w < SEL_WARPS; ++w) {
+        const int t = warp_tot[w];
+        base += (w < warp) ? t : 0;
+        sum += t;
     }
-    for (int bt = warp + SEL_WARPS; bt < n_batches; bt += SEL_WARPS) {
-        uint64_t b[R];
-#pragma unroll
-        for (int s = 0; s < R; ++s) b[s] = chunk_key(sc, bt * L + s * 32 + lane, n_chunks, n_sink, n_recent);
-        warp_sort<R, uint64_t, false>(b, lane);
-        warp_merge_top<R>(v, b, lane);
-    }
-    // pairwise merge of the warps' lists: list w takes list w + act, reversed
-    int act = 1;
-    while (act < n_batches && act < SEL_WARPS) act <<= 1;
-    for (act >>= 1; act >= 1; act >>= 1) {
-        if (warp >= act && warp < 2 * act) {
-#pragma unroll
-            for (int s = 0; s < R; ++s) lists[(warp - act) * L + s * 32 + lane] = v[s];
-        }
-        __syncthreads();
-        if (warp < act) {
-            uint64_t b[R];
-#pragma unroll
-            for (int s = 0; s < R; ++s) b[s] = lists[warp * L + (L - 1 - (s * 32 + lane))];
-            warp_merge_top<R>(v, b, lane);
-        }
-        __syncthreads();
-    }
-    if (warp == 0) {
-        // the chosen chunk indices (padding: all ones)
-        uint32_t c[R];
-#pragma unroll
-        for (int s = 0; s < R; ++s) c[s] = (s * 32 + lane < k_sel) ? ~(uint32_t)v[s] : 0xffffffffu;
-        bool last = false;
-#pragma unroll
-        for (int s = 0; s < R; ++s) last |= (int)c[s] == n_chunks - 1;
-        // ascending order by rank: the indices are distinct, and the padding
-        // (all ones) is above every index, so a chosen index's rank is the
-        // number of chosen indices below it
-        int rank[R];
-#pragma unroll
-        for (int s = 0; s < R; ++s) rank[s] = 0;
-#pragma unroll
-        for (int t = 0; t < R; ++t)
-#pragma unroll 8
-            for (int src = 0; src < 32; ++src) {
-                const uint32_t o = __shfl_sync(0xffffffffu, c[t], src);
-#pragma unroll
-                for (int s = 0; s < R; ++s) rank[s] += o < c[s] ? 1 : 0;
-            }
-#pragma unroll
-        for (int s = 0; s < R; ++s)
-            if (s * 32 + lane < k_sel) sel_g[rank[s]] = (int32_t)c[s];
-        const bool any_last = __any_sync(0xffffffffu, last);
-        if (lane == 0) *last_selected = any_last ? 1 : 0;
-    }
-}
-
-// Bitonic sort of v[0, P) (P a power of two, at least 64) into descending
-// (DESC) or ascending order by every thread of the CTA.  Stages whose stride
-// is below 64 pair elements inside one warp's 64-element window, so only the
-// wider stages need a block barrier.
-template <typename K, bool DESC>
-__device__ void bitonic_sort_block(K *v, int P) {
-    const int nthr = blockDim.x;
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const int ls = __ffs(stride) - 1;
-            for (int i = threadIdx.x; i < (P >> 1); i += nthr) {
-                const int lo = ((i >> ls) << (ls + 1)) + (i & (stride - 1)), hi = lo + stride;
-                const bool first = (lo & size) == 0;  // this run ends in the requested order
-                const K a = v[lo], b = v[hi];
-                if ((first == DESC) ? (a < b) : (a > b)) {
-                    v[lo] = b;
-                    v[hi] = a;
-                }
-            }
-            if (stride > 32 || (P >> 1) > nthr) __syncthreads(); else __syncwarp();
-        }
-        __syncthreads();
-    }
+    __syncthreads();  // warp_tot may be reused
+    *total = sum;
+    return base + x - v;
 }
 
 __global__ void __launch_bounds__(SEL_THREADS)
 select_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
               int32_t *__restrict__ sel, int32_t *__restrict__ part_len) {
-    extern __shared__ __align__(16) uint64_t keys[];
-    __shared__ int s_last;
+    extern __shared__ __align__(16) uint32_t keys[];  // [n_chunks]
+    __shared__ uint32_t hist[256];
+    __shared__ int warp_tot[SEL_WARPS];
+    __shared__ uint32_t s_digit;
+    __shared__ int s_above;
     // the gather grid may launch now; it waits for this grid's results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // this grid is itself a programmatic dependent: the scores are the previous
     // kernel's output
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int g = blockIdx.x, tid = threadIdx.x;
+    const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *sc = scores + (size_t)g * n_chunks;
     int32_t *sel_g = sel + (size_t)g * k_sel;
-    if (k_sel <= 64) {
-        select_topk_warps<2>(sc, n_chunks, k_sel, n_sink, n_recent, keys, sel_g, &s_last);
-    } else if (k_sel <= 128) {
-        select_topk_warps<4>(sc, n_chunks, k_sel, n_sink, n_recent, keys, sel_g, &s_last);
-    } else if (k_sel <= 256) {
-        select_topk_warps<8>(sc, n_chunks, k_sel, n_sink, n_recent, keys, sel_g, &s_last);
-    } else {
-        // all keys sorted descending, then the first k_sel indices ascending
-        int P = 64;
-        while (P < n_chunks) P <<= 1;
-        int PK = 64;
-        while (PK < k_sel) PK <<= 1;
-        uint32_t *idx = reinterpret_cast<uint32_t *>(keys + P);
-        for (int c = tid; c < P; c += SEL_THREADS) keys[c] = chunk_key(sc, c, n_chunks, n_sink, n_recent);
-        if (tid == 0) s_last = 0;
+    for (int c = tid; c < n_chunks; c += SEL_THREADS)
+        keys[c] = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
+    __syncthreads();
+
+    // ---- the k-th largest key tau, 8 bits at a time from the top: after a pass,
+    // `prefix` holds tau's digits so far and `rem` how many of the keys that
+    // match them are still to be taken
+    uint32_t prefix = 0, pmask = 0;
+    int rem = k_sel;
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        if (tid < 256) hist[tid] = 0;
         __syncthreads();
-        bitonic_sort_block<uint64_t, true>(keys, P);
-        for (int i = tid; i < PK; i += SEL_THREADS) {
-            uint32_t c = 0xffffffffu;  // padding sorts last
-            if (i < k_sel) {
-                c = ~(uint32_t)keys[i];
-                if ((int)c == n_chunks - 1) s_last = 1;
-            }
-            idx[i] = c;
+        for (int c = tid; c < n_chunks; c += SEL_THREADS) {
+            const uint32_t u = keys[c];
+            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
         }
         __syncthreads();
-        bitonic_sort_block<uint32_t, false>(idx, PK);
-        for (int i = tid; i < k_sel; i += SEL_THREADS) sel_g[i] = (int32_t)idx[i];
+        if (warp == 0) {
+            // lane l holds digits 255 - 8l .. 248 - 8l (descending); the digit
+            // where the count from the top first reaches rem
+            uint32_t h[8];
+            int run = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                h[i] = hist[255 - 8 * lane - i];
+                run += (int)h[i];
+            }
+            int incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int excl = incl - run;  // count of the digits above this lane's
+            if (excl < rem && incl >= rem) {
+                int above = excl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (above + (int)h[i] >= rem) {
+                        s_digit = 255u - 8u * lane - (uint32_t)i;
+                        s_above = above;
+                        break;
+                    }
+                    above += (int)h[i];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= s_digit << shift;
+        pmask |= 255u << shift;
+        rem -= s_above;
+        __syncthreads();  // s_digit / s_above are rewritten by the next pass
     }
-    __syncthreads();
+    const uint32_t tau = prefix;
+    const int need = rem;  // keys equal to tau to take, the lowest-indexed ones
+
+    // ---- the chosen indices in ascending order: thread t owns the contiguous
+    // index range [t * per, t * per + per)
+    const int per = (n_chunks + SEL_THREADS - 1) / SEL_THREADS;
+    const int c0 = tid * per, c1 = min(c0 + per, n_chunks);
+    int n_eq = 0;
+    for (int c = c0; c < c1; ++c) n_eq += keys[c] == tau ? 1 : 0;
+    int tot;
+    const int eq_before = block_exclusive_scan(n_eq, warp_tot, &tot);
+    int n_take = 0;
+    {
+        int e = eq_before;
+        for (int c = c0; c < c1; ++c) {
+            const uint32_t u = keys[c];
+            if (u > tau) ++n_take;
+            else if (u == tau) n_take += (e++ < need) ? 1 : 0;
+        }
+    }
+    const int out0 = block_exclusive_scan(n_take, warp_tot, &tot);
+    bool last_taken = false;  // chunk n_chunks - 1 chosen (only its owner can tell)
+    {
+        int e = eq_before, o = out0;
+        for (int c = c0; c < c1; ++c) {
+            const uint32_t u = keys[c];
+            const bool take = u > tau || (u == tau && e++ < need);
+            if (take) sel_g[o++] = c;
+            if (c == n_chunks - 1) last_taken = take;
+        }
+    }
     // tokens gathered for this head: only the last chunk of the prefix can be
-    // short, and being the largest index it is the last one selected
-    if (tid == 0 && part_len != nullptr) {
+    // short, and being the largest index it is the last one chosen
+    if (part_len != nullptr && c0 < c1 && c1 == n_chunks) {
         const int64_t tail = N - (int64_t)(n_chunks - 1) * CHUNK;  // tokens of the last chunk, 1..64
-        part_len[g] = k_sel * CHUNK - (s_last ? (int)(CHUNK - tail) : 0);
+        part_len[g] = k_sel * CHUNK - (last_taken ? (int)(CHUNK - tail) : 0);
     }
 }
 
@@ -374,17 +309,7 @@ cudaError_t launch_select(const float *scores, int Hkv, int64_t N, int n_chunks,
                           int32_t *sel, int32_t *part_len, cudaStream_t st) {
     if (injected_launch_failure()) return cudaErrorInvalidValue;
     if (k_sel <= 0 || n_chunks <= 0) return cudaSuccess;
-    size_t smem;
-    if (k_sel <= 256) {
-        int R = 2;
-        while (32 * R < k_sel) R <<= 1;
-        smem = sizeof(uint64_t) * (size_t)(SEL_WARPS / 2) * 32 * R;  // the lists merged in the first round
-    } else {
-        int P = 64, PK = 64;
-        while (P < n_chunks) P <<= 1;
-        while (PK < k_sel) PK <<= 1;
-        smem = sizeof(uint64_t) * (size_t)P + sizeof(uint32_t) * (size_t)PK;
-    }
+    const size_t smem = sizeof(uint32_t) * (size_t)n_chunks;
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // the selection as a programmatic dependent of the kernel that wrote the
