@@ -428,6 +428,36 @@ def test_select_gather_keeps_sink_and_recent_chunks(N, sink, recent):
         assert (sel[:, kk - recent:].cpu() == torch.arange(nc - recent, nc, dtype=torch.int32)).all()
 
 
+@pytest.mark.parametrize("nc", [1, 63, 5000, 16384])
+@pytest.mark.parametrize("kind", ["normal", "ties", "constant"])
+def test_select_chunks_sizes_and_ties(nc, kind):
+    """The selection alone up to the largest chunk count, budgets from one
+    chunk to all of them, with many equal scores: bit-exact indices and
+    gathered lengths (lowest indices win ties)."""
+    Hkv = 2
+    rng = np.random.default_rng(nc)
+    if kind == "normal":
+        s = rng.standard_normal((Hkv, nc)).astype(np.float32)
+    elif kind == "ties":
+        s = rng.integers(-2, 3, size=(Hkv, nc)).astype(np.float32)
+        s[:, ::3] = -0.0
+    else:
+        s = np.full((Hkv, nc), 1.5, dtype=np.float32)
+    scores = torch.from_numpy(s).cuda()
+    N = nc * 64 - 17 if nc > 1 else 5
+    for k in sorted({1, 64, 300, 1024, nc}):
+        kk = min(k, nc)
+        sel = torch.empty((Hkv, kk), dtype=torch.int32, device="cuda")
+        plen = torch.empty((Hkv,), dtype=torch.int32, device="cuda")
+        ts.ts_select_chunks(scores, N, k * 64, sel, part_len=plen)
+        torch.cuda.synchronize()
+        rsel = oracle.select(s, k)
+        np.testing.assert_array_equal(sel.cpu().numpy(), rsel, err_msg=f"k={k}")
+        last = (rsel == nc - 1).any(axis=1)
+        tail = N - (nc - 1) * 64
+        np.testing.assert_array_equal(plen.cpu().numpy(), kk * 64 - np.where(last, 64 - tail, 0))
+
+
 def test_select_ties_and_signed_zero():
     Hkv, nc = 3, 300
     rng = np.random.default_rng(1)
