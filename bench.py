@@ -11,6 +11,7 @@ over a 1024-token window, min-p 0.1, greedy target, acceptance).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--workload qwen14b-100k|qwen14b-<N>|llama8b-<N>|llama2-7b-100k] [--no-cpu-baseline]
+                    [--one-stream] [--separate-gather]
 
 Prints one JSON line (rank 0).  Metric: verify-attention KV throughput
 (prefix K+V bytes read by the verify pass, per second of the whole step).
