@@ -330,6 +330,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = tl->tmem_base;
+    // a programmatic dependent: the set-up above overlaps the previous kernel's
+    // tail; every global access of this kernel comes after the wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp < 3) {
       if (warp == 0) {
@@ -784,12 +787,20 @@ cudaError_t launch_tree_attn_tc(const AttnArgs &a, const TcPlan &p, const CUtens
     L.n_tiles = p.n_tiles;
     L.ctas_per_head = p.ctas_per_head;
     L.direct = p.splits == 1 ? 1 : 0;
-    dim3 grid(p.ctas_per_head * a.Hkv);
-    if (exact)
-        tree_attn_tc_kernel<true><<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(tq, tk, tv, a, L);
-    else
-        tree_attn_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(tq, tk, tv, a, L);
-    return cudaGetLastError();
+    // launched as a programmatic dependent of whatever precedes it on the
+    // stream (the kernel waits for that grid before touching global memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.ctas_per_head * a.Hkv);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = TC_SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return exact ? cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<true>, tq, tk, tv, a, L)
+                 : cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<false>, tq, tk, tv, a, L);
 }
 
 // Self-test of the bounded-wait failure path: one warp waits on an mbarrier

@@ -16,8 +16,8 @@ acceptance).
 
 Every step is one C-ABI call into libts.so; this module only owns device
 memory (allocated once, through torch) and orders the calls on a stream
-(the selection and drafting pass of a layer on a side stream beside the merge
-of the verify partials, joined before the next layer).  The step can be
+(the merge of a layer's verify partials on a side stream beside the
+selection and drafting pass, joined before the next layer).  The step can be
 captured into a CUDA graph.
 """
 from __future__ import annotations
@@ -57,8 +57,8 @@ class SpecStep:
                  fuse_gather: bool = True, overlap_select: bool = True):
         self.cfg = cfg
         self.fuse_gather = fuse_gather
-        # with a stream given, the selection and the drafting pass of a layer
-        # run on a side stream beside the merge of the verify partials (the
+        # with a stream given, the merge of a layer's verify partials runs on a
+        # side stream beside the selection and the drafting pass (the
         # selection needs only the chunk scores of the verify kernel)
         self.overlap_select = overlap_select
         # the log-sum-exp outputs (the method itself consumes only O; the
@@ -144,18 +144,20 @@ class SpecStep:
             self._side = torch.cuda.Stream(device=self.device)
             self._ev_scores = [torch.cuda.Event() for _ in range(self.n_layers)]
             self._ev_draft = [torch.cuda.Event() for _ in range(self.n_layers)]
-        # verify kernel; its chunk scores feed the selection on the side
-        # stream while the split merge runs here
+        # verify kernel; its chunk scores feed the selection and drafting pass
+        # right behind it on this stream (each a programmatic dependent of the
+        # kernel before it), while the merge of its split partials runs on the
+        # side stream
         lse = L.lse if self.want_lse else None
         ts_tree_attn_unmerged(L.q, L.k, L.v, cfg.N, self.mask, L.out, lse=lse, chunk_scores=L.scores, score_row=0,
                               workspace=self.workspace, scale=cfg.scale, stream=stream)
         self._ev_scores[i].record(stream)
         self._side.wait_event(self._ev_scores[i])
-        self.run_refresh(i, self._side)
-        self.run_draft(i, self._side)
+        ts_tree_attn_merge(L.out, cfg.Hkv, cfg.N, lse=lse, workspace=self.workspace, stream=self._side)
         self._ev_draft[i].record(self._side)
-        ts_tree_attn_merge(L.out, cfg.Hkv, cfg.N, lse=lse, workspace=self.workspace, stream=stream)
-        stream.wait_event(self._ev_draft[i])
+        self.run_refresh(i, stream)
+        self.run_draft(i, stream)
+        stream.wait_event(self._ev_draft[i])  # the merge is done before the workspace is used again
 
     def run_vocab(self, stream=None) -> None:
         cfg, vi = self.cfg, self.vocab_inputs
