@@ -46,8 +46,8 @@ UNIT = "GB/s"
 # prefix K/V), expressed per prefix K/V byte.  It holds only for the kernel
 # code it was taken on: the fingerprint below is of that code with comments and
 # whitespace removed; for any other code the traffic is unknown (null).
-VERIFY_TRAFFIC_PER_KV_BYTE = (751.821824 + 3.734272) / 419.430400
-VERIFY_TRAFFIC_CODE_SHA1 = "3ddb4335b947345b6c9040a9fb9fbb9d8c1332aa"
+VERIFY_TRAFFIC_PER_KV_BYTE = (751.376128 + 3.720704) / 419.430400
+VERIFY_TRAFFIC_CODE_SHA1 = "f38d9cdabd162bcf6b6fcd83f711e5d624ea67f7"
 
 
 def _code_fingerprint(paths) -> str:
