@@ -209,7 +209,10 @@ def test_fused_scores_any_row(score_row):
 
 
 @pytest.mark.parametrize("T,Hq,Hkv,N,score_row", [(4, 40, 8, 4100, 3), (4, 32, 8, 1000, 0), (1, 8, 8, 63, 0),
-                                                   (6, 16, 4, 130, 5), (4, 32, 32, 257, 2)])
+                                                   (6, 16, 4, 130, 5), (4, 32, 32, 257, 2),
+                                                   (2, 40, 8, 4090, 1),    # 10 pairs; batch rows straddle a block
+                                                   (3, 24, 8, 31, 2),      # 9 pairs; one block holds all of it
+                                                   (12, 16, 8, 6000, 11)])  # 24 pairs; 12-row tail
 def test_small_batch_fused_scores_and_attention(T, Hq, Hkv, N, score_row):
     """Batches of at most 24 (row, head) pairs per KV head run on the CUDA-core
     small-batch kernel: its fused chunk scores are bit-exact, its output within
@@ -300,6 +303,8 @@ def test_partial_cache_drafting_with_a_short_last_chunk(N, Hq, Hkv, d):
     (4096, 16, 4, 6, 4096),     # 24 pairs, no short chunk
     (5000, 40, 8, 1, 2048),     # one row
     (2000, 40, 8, 3, 1024),     # 15 pairs (a padding row)
+    (3000, 40, 8, 2, 2048),     # 10 pairs
+    (64, 40, 8, 4, 4096),       # one chunk: the gathered cache is a single block pair
 ])
 def test_gather_tree_attn_matches_oracle_and_the_two_calls(N, Hq, Hkv, Td, budget):
     """The gather fused with the drafting pass: the compact cache bit-exact
