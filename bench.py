@@ -11,7 +11,7 @@ over a 1024-token window, min-p 0.1, greedy target, acceptance).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                     [--workload qwen14b-100k|qwen14b-<N>|llama8b-<N>|llama2-7b-100k] [--no-cpu-baseline]
-                    [--one-stream] [--separate-gather]
+                    [--one-stream] [--separate-select] [--separate-gather]
 
 Prints one JSON line (rank 0).  Metric: verify-attention KV throughput
 (prefix K+V bytes read by the verify pass, per second of the whole step).
@@ -368,7 +368,7 @@ def run_native(args, ws, rank, local):
     peaks = read_peaks()
     # the step computes what the method consumes: O (and the chunk scores), no log-sum-exp
     step = SpecStep(cfg, layers=args.layers, want_lse=False, fuse_gather=not args.separate_gather,
-                    overlap_select=not args.one_stream)
+                    overlap_select=not args.one_stream, fuse_select=not args.separate_select)
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -492,7 +492,14 @@ def run_native(args, ws, rank, local):
         "verify": {"us": verify_avg_s * 1e6, "kv_gbs": kv_layer / verify_avg_s / 1e9,
                    "tflops": flops / verify_avg_s / 1e12},
     }
-    if step.fuse_gather:
+    if step.fuse_select:
+        # selection, gather and drafting pass in one kernel (the selected K/V
+        # read once, written once into the compact cache)
+        fused_bytes = gather_bytes + 2 * cfg.Hkv * Td * d * 2
+        t = refresh_s + draft_s
+        kernels["select_gather_draft_attention"] = {"us": t * 1e6, "gbs": fused_bytes / t / 1e9,
+                                                    "bytes": fused_bytes, "tflops": draft_flops / t / 1e12}
+    elif step.fuse_gather:
         # selection alone, then the gather fused with the drafting pass (the
         # selected K/V read once, written once into the compact cache)
         fused_bytes = gather_bytes + 2 * cfg.Hkv * Td * d * 2
@@ -724,6 +731,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="run only this many layers (profiling)")
     ap.add_argument("--one-stream", action="store_true",
                     help="run each layer's calls in order on one stream (no selection beside the verify merge)")
+    ap.add_argument("--separate-select", action="store_true",
+                    help="the selection as its own call before the gather-and-draft call")
     ap.add_argument("--separate-gather", action="store_true",
                     help="gather with the selection call, then the drafting attention over the compact cache")
     ap.add_argument("--cpu-row-fraction", type=float, default=1.0,

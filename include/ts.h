@@ -22,6 +22,8 @@
  *   ts_select_chunks         the selection alone;
  *   ts_gather_tree_attn      the gather fused with the drafting pass over the
  *                            gathered cache (the chosen K/V read once);
+ *   ts_select_gather_tree_attn  the selection, the gather and the drafting
+ *                            pass in one kernel;
  *   ts_penalty_minp_verify   windowed contextual penalty, temperature, min-p,
  *                            greedy target and exact-match acceptance.
  *   ts_penalty_minp_sample_verify  the same with min-p sampled targets;
@@ -345,6 +347,24 @@ ts_status ts_gather_tree_attn(const void *q, const void *k, const void *v, int64
                               const int32_t *sel, int k_sel, void *k_part, void *v_part, int64_t ld_part,
                               int T, int Hq, int Hkv, int d, float scale, const uint64_t *mask,
                               void *out, float *lse, void *workspace, size_t ws_bytes, ts_stream_t stream);
+
+/*
+ * ts_select_chunks and ts_gather_tree_attn in one pass: every CTA of the
+ * drafting kernel selects its KV head's chunks from `scores` itself (the same
+ * radix selection as ts_select_chunks), then gathers the two chunks it attends
+ * over.  sel and part_len are written as ts_select_chunks writes them; the
+ * compact cache, out and lse are those of ts_gather_tree_attn with that sel.
+ * Arguments, sizes and errors: those of ts_select_chunks (scores, N,
+ * budget_tokens, chunk, sink_chunks, recent_chunks, sel, part_len) and of
+ * ts_gather_tree_attn (the rest; k_sel = min(budget_tokens/chunk,
+ * ceil(N/chunk)), at least 1).
+ */
+ts_status ts_select_gather_tree_attn(const float *scores, int64_t N, int budget_tokens, int chunk,
+                                     int sink_chunks, int recent_chunks, int32_t *sel, int32_t *part_len,
+                                     const void *q, const void *k, const void *v, int64_t ld_kv,
+                                     void *k_part, void *v_part, int64_t ld_part, int T, int Hq, int Hkv, int d,
+                                     float scale, const uint64_t *mask, void *out, float *lse,
+                                     void *workspace, size_t ws_bytes, ts_stream_t stream);
 
 /*
  * Vocabulary side of one verification step (model card flags --penalty,

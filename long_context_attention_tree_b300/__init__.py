@@ -29,7 +29,8 @@ __all__ = ["TSError", "lib", "ts_version", "ts_tree_mask_from_parents", "ts_tree
            "ts_launch_count", "ts_tree_attn_uses_tensor_cores", "ts_device_error", "ts_selftest_bounded_wait",
            "ts_selftest_fail_launches", "ts_tree_attn",
            "ts_tree_attn_unmerged", "ts_tree_attn_merge", "ts_tree_attn_partial", "ts_tree_attn_noalloc", "ts_score_chunks", "ts_rescore_tail",
-           "ts_select_gather", "ts_select_chunks", "ts_gather_tree_attn", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path",
+           "ts_select_gather", "ts_select_chunks", "ts_gather_tree_attn",
+           "ts_select_gather_tree_attn", "ts_penalty_minp_verify", "ts_penalty_minp_sample_verify", "ts_commit_path",
            "ts_ngram_table_bytes", "ts_ngram_reset", "ts_ngram_update", "ts_ngram_topk", "ts_vocab_verify"]
 
 
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.ts_select_chunks.argtypes = [P, i32, i64, i32, i32, i32, i32, P, P, P]
         L.ts_gather_tree_attn.argtypes = [P, P, P, i64, i64, P, i32, P, P, i64, i32, i32, i32, i32, f32, P, P, P,
                                           P, sz, P]
+        L.ts_select_gather_tree_attn.argtypes = [P, i64, i32, i32, i32, i32, P, P, P, P, P, i64, P, P, i64, i32, i32,
+                                                 i32, i32, f32, P, P, P, P, sz, P]
         L.ts_vocab_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, ctypes.c_uint, ctypes.c_uint64,
                                       ctypes.c_uint64, P, P, ctypes.c_int32, P, P, P, P, P]
         L.ts_penalty_minp_verify.argtypes = [P, i32, i32, P, i32, f32, f32, f32, P, P, ctypes.c_int32,
@@ -94,7 +97,7 @@ def lib() -> ctypes.CDLL:
         for name in ("ts_tree_mask_from_parents", "ts_tree_attn", "ts_tree_attn_unmerged", "ts_tree_attn_merge",
                      "ts_tree_attn_partial", "ts_tree_attn_noalloc",
                      "ts_score_chunks", "ts_rescore_tail", "ts_select_gather", "ts_select_chunks",
-                     "ts_gather_tree_attn", "ts_penalty_minp_verify",
+                     "ts_gather_tree_attn", "ts_select_gather_tree_attn", "ts_penalty_minp_verify",
                      "ts_commit_path", "ts_penalty_minp_sample_verify", "ts_ngram_reset", "ts_ngram_update",
                      "ts_ngram_topk", "ts_vocab_verify"):
             getattr(L, name).restype = i32
@@ -279,6 +282,23 @@ def ts_gather_tree_attn(q, k, v, N: int, sel, k_part, v_part, mask, out, lse=Non
     _check(lib().ts_gather_tree_attn(_ptr(q), _ptr(k), _ptr(v), ld, N, _ptr(sel), k_sel, _ptr(k_part), _ptr(v_part),
                                      ld_part, T, Hq, Hkv, d, scale, _ptr(mask), _ptr(out), _ptr(lse),
                                      _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def ts_select_gather_tree_attn(scores, q, k, v, N: int, budget_tokens: int, sel, k_part, v_part, mask, out,
+                               part_len=None, lse=None, workspace=None, chunk: int = 64, sink_chunks: int = 0,
+                               recent_chunks: int = 0, scale: Optional[float] = None, stream=None) -> None:
+    """ts_select_chunks and ts_gather_tree_attn in one pass (every CTA selects
+    its head's chunks itself): sel, part_len, the compact cache, out, lse."""
+    T, Hq, d = q.shape
+    Hkv, ld, _ = k.shape
+    ld_part = k_part.shape[1]
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().ts_select_gather_tree_attn(_ptr(scores), N, budget_tokens, chunk, int(sink_chunks),
+                                            int(recent_chunks), _ptr(sel), _ptr(part_len), _ptr(q), _ptr(k), _ptr(v),
+                                            ld, _ptr(k_part), _ptr(v_part), ld_part, T, Hq, Hkv, d, scale, _ptr(mask),
+                                            _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def ts_penalty_minp_verify(logits, history, theta: float, min_p: float, temperature: float, draft, parent,

@@ -45,6 +45,7 @@
 // refresh of the partial cache (selection, gather) and the drafting pass over
 // it read the selected K/V bytes from HBM once.
 #include "internal.h"
+#include "topk_radix.cuh"
 #include "ts_common.cuh"
 
 namespace ts {
@@ -99,7 +100,7 @@ struct SmallCfg {
 };
 }  // namespace
 
-template <int RG, bool GATHER>
+template <int RG, bool GATHER, bool SELECT>
 __global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs a, const SmallGather gs, int n_splits) {
     using C = SmallCfg<RG>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs
     // gather: the full-cache chunk behind this block (a block lies in one
     // chunk: Np is a multiple of 64 there)
     int64_t src_base = 0;
-    if (GATHER && wb < Np) {
+    if (GATHER && !SELECT && wb < Np) {
         const int c = min(max(gs.sel[(size_t)g * gs.k_sel + (int)(wb >> 6)], 0), gs.n_chunks - 1);
         src_base = (int64_t)c * 64 + (wb & 63);
     }
@@ -153,6 +154,27 @@ __global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs
         cp_async16_zfill(sQb + r * ROWB + c8 * 16, a.q + off, r < R);
     }
     cp_async_commit();
+    if (SELECT) {
+        // this head's top-k chunks (the keys over the K/V buffers, which no
+        // copy has touched yet): the range's two chunks, and the full list
+        // and gathered length from the CTAs of the first range
+        __shared__ TopkSmem tsm;
+        __shared__ int s_chunk[2];
+        const int pos0 = 2 * split;
+        const bool last_taken = radix_topk_ascending<NTHR>(
+            gs.scores + (size_t)g * gs.n_chunks, gs.n_chunks, gs.k_sel, gs.n_sink, gs.n_recent,
+            reinterpret_cast<uint32_t *>(sK), tsm, [&](int pos, int c) {
+                if (split == 0) gs.sel_out[(size_t)g * gs.k_sel + pos] = c;
+                if (pos == pos0 || pos == pos0 + 1) s_chunk[pos - pos0] = c;
+            });
+        const int per = (gs.n_chunks + NTHR - 1) / NTHR;
+        if (split == 0 && gs.part_len_out != nullptr && (int)threadIdx.x == (gs.n_chunks - 1) / per) {
+            const int64_t tail = gs.N - (int64_t)(gs.n_chunks - 1) * 64;  // tokens of the last chunk, 1..64
+            gs.part_len_out[g] = gs.k_sel * 64 - (last_taken ? (int)(64 - tail) : 0);
+        }
+        __syncthreads();  // the range's chunks are known; the keys are dead
+        if (wb < Np) src_base = (int64_t)s_chunk[b >> 1] * 64 + (wb & 63);
+    }
     // Q is waited for before the K/V copies go out: behind them it would land
     // only when most of the grid's K/V has (the whole grid asks for its K/V at
     // once), and no warp can start before Q is in place
@@ -490,10 +512,10 @@ bool small_ok(int T, int Hq, int Hkv, int d) { return d == 128 && T >= 1 && T * 
 
 int small_splits(int T, int64_t N) { return (int)((N + T + RANGE - 1) / RANGE); }
 
-template <int RG, bool GATHER>
+template <int RG, bool GATHER, bool SELECT>
 static cudaError_t launch_small_t(const AttnArgs &a, const SmallGather &gs, int splits, cudaStream_t st) {
     const size_t smem = SmallCfg<RG>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_small_kernel<RG, GATHER>,
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_small_kernel<RG, GATHER, SELECT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -506,26 +528,27 @@ static cudaError_t launch_small_t(const AttnArgs &a, const SmallGather &gs, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tree_attn_small_kernel<RG, GATHER>, a, gs, splits);
+    return cudaLaunchKernelEx(&cfg, tree_attn_small_kernel<RG, GATHER, SELECT>, a, gs, splits);
 }
 
-template <bool GATHER>
+template <bool GATHER, bool SELECT>
 static cudaError_t launch_small_g(const AttnArgs &a, const SmallGather &gs, int splits, cudaStream_t st) {
     switch ((a.T * a.G + 3) / 4) {
-        case 1: return launch_small_t<1, GATHER>(a, gs, splits, st);
-        case 2: return launch_small_t<2, GATHER>(a, gs, splits, st);
-        case 3: return launch_small_t<3, GATHER>(a, gs, splits, st);
-        case 4: return launch_small_t<4, GATHER>(a, gs, splits, st);
-        case 5: return launch_small_t<5, GATHER>(a, gs, splits, st);
-        case 6: return launch_small_t<6, GATHER>(a, gs, splits, st);
+        case 1: return launch_small_t<1, GATHER, SELECT>(a, gs, splits, st);
+        case 2: return launch_small_t<2, GATHER, SELECT>(a, gs, splits, st);
+        case 3: return launch_small_t<3, GATHER, SELECT>(a, gs, splits, st);
+        case 4: return launch_small_t<4, GATHER, SELECT>(a, gs, splits, st);
+        case 5: return launch_small_t<5, GATHER, SELECT>(a, gs, splits, st);
+        case 6: return launch_small_t<6, GATHER, SELECT>(a, gs, splits, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_tree_attn_small(const AttnArgs &a, const SmallGather *gs, int splits, cudaStream_t st) {
     if (injected_launch_failure()) return cudaErrorInvalidValue;
-    if (gs != nullptr) return launch_small_g<true>(a, *gs, splits, st);
-    return launch_small_g<false>(a, SmallGather{}, splits, st);
+    if (gs != nullptr && gs->scores != nullptr) return launch_small_g<true, true>(a, *gs, splits, st);
+    if (gs != nullptr) return launch_small_g<true, false>(a, *gs, splits, st);
+    return launch_small_g<false, false>(a, SmallGather{}, splits, st);
 }
 
 }  // namespace ts

@@ -81,6 +81,12 @@ struct SmallGather {
     const __nv_bfloat16 *k = nullptr, *v = nullptr;  // full cache [Hkv][ld][d]
     int64_t ld = 0, N = 0;
     __nv_bfloat16 *k_dst = nullptr, *v_dst = nullptr;
+    // selection in the same pass (scores != nullptr): every CTA selects the
+    // k_sel chunks of its KV head from scores [Hkv][n_chunks] itself; the
+    // CTAs of the first range write sel_out [Hkv][k_sel] and part_len_out
+    const float *scores = nullptr;
+    int n_sink = 0, n_recent = 0;
+    int32_t *sel_out = nullptr, *part_len_out = nullptr;
 };
 cudaError_t launch_tree_attn_small(const AttnArgs &a, const SmallGather *gs, int splits, cudaStream_t st);
 

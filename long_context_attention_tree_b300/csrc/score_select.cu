@@ -4,6 +4,7 @@
 // KV cache that is refreshed every step from the chunks whose keys score
 // highest against the current query; model card: retrieval budget 4096).
 #include "internal.h"
+#include "topk_radix.cuh"
 #include "ts_common.cuh"
 
 namespace ts {
@@ -106,158 +107,35 @@ cudaError_t launch_copy_scores(const float *scores_old, int nc_old, float *score
 
 // ---------------------------------------------------------------------------
 // Top-k selection, then the gather.
-// select_kernel: one CTA per KV head computes sel[g][.] and part_len[g].
-// Every chunk has a 32-bit order key (the score's bits mapped so that unsigned
-// order is numeric order, -0 = +0; always-kept chunks take the largest key);
-// the chosen set is the k largest keys, equal keys going to the lower chunk
-// index.  A radix select finds the k-th largest key tau in four passes of
-// 8-bit digits (a 256-bin shared-memory histogram of the keys that match the
-// digits found so far, then a suffix scan by one warp); then every key above
-// tau is chosen, and of the keys equal to tau the lowest-indexed ones that
-// complete k.  The chosen indices are written in ascending order by a block
-// scan over contiguous index ranges (one range per thread).
+// select_kernel: one CTA per KV head computes sel[g][.] and part_len[g] with
+// the radix select of topk_radix.cuh.
 // gather_kernel: CTA = (selected chunk, KV head) copies the chunk's K and V
 // rows.  The gather is launched as a programmatic dependent of the selection
 // so its CTAs are resident and waiting when the selection finishes.
 // ---------------------------------------------------------------------------
 constexpr int SEL_THREADS = 512;
-constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int GA_THREADS = 256;
-
-__device__ __forceinline__ uint32_t order_key(float x) {
-    x = x + 0.0f;  // -0 -> +0 (round-to-nearest), so equal values get equal keys
-    const uint32_t u = __float_as_uint(x);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Exclusive prefix sum of v over the CTA in thread order; *total gets the sum.
-// Uses warp_tot[SEL_WARPS] in shared memory; two CTA barriers.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_tot[warp] = x;
-    __syncthreads();
-    int base = 0, sum = 0;
-#pragma unroll
-    for (int w = 0; w < SEL_WARPS; ++w) {
-        const int t = warp_tot[w];
-        base += (w < warp) ? t : 0;
-        sum += t;
-    }
-    __syncthreads();  // warp_tot may be reused
-    *total = sum;
-    return base + x - v;
-}
 
 __global__ void __launch_bounds__(SEL_THREADS)
 select_kernel(const float *__restrict__ scores, int64_t N, int n_chunks, int k_sel, int n_sink, int n_recent,
               int32_t *__restrict__ sel, int32_t *__restrict__ part_len) {
     extern __shared__ __align__(16) uint32_t keys[];  // [n_chunks]
-    __shared__ uint32_t hist[256];
-    __shared__ int warp_tot[SEL_WARPS];
-    __shared__ uint32_t s_digit;
-    __shared__ int s_above;
+    __shared__ TopkSmem sm;
     // the gather grid may launch now; it waits for this grid's results
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // this grid is itself a programmatic dependent: the scores are the previous
     // kernel's output
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float *sc = scores + (size_t)g * n_chunks;
+    const int g = blockIdx.x;
     int32_t *sel_g = sel + (size_t)g * k_sel;
-    for (int c = tid; c < n_chunks; c += SEL_THREADS)
-        keys[c] = (c < n_sink || c >= n_chunks - n_recent) ? 0xffffffffu : order_key(sc[c]);
-    __syncthreads();
-
-    // ---- the k-th largest key tau, 8 bits at a time from the top: after a pass,
-    // `prefix` holds tau's digits so far and `rem` how many of the keys that
-    // match them are still to be taken
-    uint32_t prefix = 0, pmask = 0;
-    int rem = k_sel;
-#pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        if (tid < 256) hist[tid] = 0;
-        __syncthreads();
-        for (int c = tid; c < n_chunks; c += SEL_THREADS) {
-            const uint32_t u = keys[c];
-            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // lane l holds digits 255 - 8l .. 248 - 8l (descending); the digit
-            // where the count from the top first reaches rem
-            uint32_t h[8];
-            int run = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                h[i] = hist[255 - 8 * lane - i];
-                run += (int)h[i];
-            }
-            int incl = run;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const int excl = incl - run;  // count of the digits above this lane's
-            if (excl < rem && incl >= rem) {
-                int above = excl;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (above + (int)h[i] >= rem) {
-                        s_digit = 255u - 8u * lane - (uint32_t)i;
-                        s_above = above;
-                        break;
-                    }
-                    above += (int)h[i];
-                }
-            }
-        }
-        __syncthreads();
-        prefix |= s_digit << shift;
-        pmask |= 255u << shift;
-        rem -= s_above;
-        __syncthreads();  // s_digit / s_above are rewritten by the next pass
-    }
-    const uint32_t tau = prefix;
-    const int need = rem;  // keys equal to tau to take, the lowest-indexed ones
-
-    // ---- the chosen indices in ascending order: thread t owns the contiguous
-    // index range [t * per, t * per + per)
-    const int per = (n_chunks + SEL_THREADS - 1) / SEL_THREADS;
-    const int c0 = tid * per, c1 = min(c0 + per, n_chunks);
-    int n_eq = 0;
-    for (int c = c0; c < c1; ++c) n_eq += keys[c] == tau ? 1 : 0;
-    int tot;
-    const int eq_before = block_exclusive_scan(n_eq, warp_tot, &tot);
-    int n_take = 0;
-    {
-        int e = eq_before;
-        for (int c = c0; c < c1; ++c) {
-            const uint32_t u = keys[c];
-            if (u > tau) ++n_take;
-            else if (u == tau) n_take += (e++ < need) ? 1 : 0;
-        }
-    }
-    const int out0 = block_exclusive_scan(n_take, warp_tot, &tot);
-    bool last_taken = false;  // chunk n_chunks - 1 chosen (only its owner can tell)
-    {
-        int e = eq_before, o = out0;
-        for (int c = c0; c < c1; ++c) {
-            const uint32_t u = keys[c];
-            const bool take = u > tau || (u == tau && e++ < need);
-            if (take) sel_g[o++] = c;
-            if (c == n_chunks - 1) last_taken = take;
-        }
-    }
+    const bool last_taken = radix_topk_ascending<SEL_THREADS>(
+        scores + (size_t)g * n_chunks, n_chunks, k_sel, n_sink, n_recent, keys, sm,
+        [&](int pos, int c) { sel_g[pos] = c; });
     // tokens gathered for this head: only the last chunk of the prefix can be
-    // short, and being the largest index it is the last one chosen
-    if (part_len != nullptr && c0 < c1 && c1 == n_chunks) {
+    // short, and being the largest index it is the last one chosen (the
+    // thread whose range holds that chunk knows whether it was chosen)
+    const int per = (n_chunks + SEL_THREADS - 1) / SEL_THREADS;
+    if (part_len != nullptr && (int)threadIdx.x == (n_chunks - 1) / per) {
         const int64_t tail = N - (int64_t)(n_chunks - 1) * CHUNK;  // tokens of the last chunk, 1..64
         part_len[g] = k_sel * CHUNK - (last_taken ? (int)(CHUNK - tail) : 0);
     }

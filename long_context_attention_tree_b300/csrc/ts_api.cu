@@ -510,6 +510,39 @@ ts_status ts_gather_tree_attn(const void *q, const void *k, const void *v, int64
                           workspace, ws_bytes, stream, &gs);
 }
 
+ts_status ts_select_gather_tree_attn(const float *scores, int64_t N, int budget_tokens, int chunk, int sink_chunks,
+                                     int recent_chunks, int32_t *sel, int32_t *part_len, const void *q, const void *k,
+                                     const void *v, int64_t ld_kv, void *k_part, void *v_part, int64_t ld_part, int T,
+                                     int Hq, int Hkv, int d, float scale, const uint64_t *mask, void *out, float *lse,
+                                     void *workspace, size_t ws_bytes, ts_stream_t stream) {
+    int k_sel = 0;
+    ts_status st = check_select(scores, Hkv, N, budget_tokens, chunk, sink_chunks, recent_chunks, sel, part_len,
+                                &k_sel);
+    if (st != TS_OK) return st;
+    if (k_sel == 0) return fail(TS_ERR_INVALID_ARG, "N=%lld: nothing to select", (long long)N);
+    if (T == 0) return check_attn_shape(T, Hq, Hkv, d, N);
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return fail(TS_ERR_INVALID_ARG, "null or misaligned k/v");
+    if (!k_part || !v_part) return fail(TS_ERR_INVALID_ARG, "null k_part/v_part");
+    if (ld_kv < N) return fail(TS_ERR_INVALID_ARG, "ld_kv < N");
+    const int64_t nc = (N + 63) / 64;
+    ts::SmallGather gs;
+    gs.k_sel = k_sel;
+    gs.n_chunks = (int)nc;
+    gs.k = static_cast<const __nv_bfloat16 *>(k);
+    gs.v = static_cast<const __nv_bfloat16 *>(v);
+    gs.ld = ld_kv;
+    gs.N = N;
+    gs.k_dst = static_cast<__nv_bfloat16 *>(k_part);
+    gs.v_dst = static_cast<__nv_bfloat16 *>(v_part);
+    gs.scores = scores;
+    gs.n_sink = sink_chunks;
+    gs.n_recent = recent_chunks;
+    gs.sel_out = sel;
+    gs.part_len_out = part_len;
+    return tree_attn_impl(q, k_part, v_part, ld_part, (int64_t)k_sel * 64, T, Hq, Hkv, d, scale, mask, nullptr, out,
+                          lse, nullptr, 0, workspace, ws_bytes, stream, &gs);
+}
+
 static ts_status vocab_stage(const float *logits, int T, int V, const int32_t *history, int W, float theta,
                              float min_p, float temperature, unsigned flags, uint64_t seed, uint64_t offset,
                              const int32_t *draft, const int32_t *parent, int32_t anchor, int32_t *target,

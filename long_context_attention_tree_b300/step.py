@@ -10,7 +10,9 @@ favours, dynamic over one-time):
   3. gather of the chosen chunks into the compact partial cache and the draft
      attention of the 4-row self-drafting batch over it, in one pass over the
      chosen K/V (fuse_gather; otherwise a separate gather call before the
-     drafting attention over the compact cache).
+     drafting attention over the compact cache).  By default (fuse_select)
+     steps 2 and 3 are one kernel: every CTA of the drafting kernel selects its
+     KV head's chunks itself.
 Then, once per step, the vocabulary stage (penalty, min-p, greedy target,
 acceptance).
 
@@ -28,9 +30,9 @@ from typing import List, Optional
 import numpy as np
 import torch
 
-from . import (ts_gather_tree_attn, ts_penalty_minp_verify, ts_select_chunks, ts_select_gather, ts_tree_attn,
-               ts_tree_attn_merge, ts_tree_attn_partial, ts_tree_attn_unmerged, ts_tree_attn_workspace_bytes,
-               ts_tree_mask_from_parents)
+from . import (ts_gather_tree_attn, ts_penalty_minp_verify, ts_select_chunks, ts_select_gather,
+               ts_select_gather_tree_attn, ts_tree_attn, ts_tree_attn_merge, ts_tree_attn_partial,
+               ts_tree_attn_unmerged, ts_tree_attn_workspace_bytes, ts_tree_mask_from_parents)
 from . import workloads as W
 
 
@@ -54,9 +56,12 @@ class LayerBuffers:
 class SpecStep:
     def __init__(self, cfg: W.Config, device="cuda", layers: Optional[int] = None, vocab: Optional[bool] = None,
                  value_kind: str = "int", fill_draft_tail: bool = True, want_lse: bool = True,
-                 fuse_gather: bool = True, overlap_select: bool = True):
+                 fuse_gather: bool = True, overlap_select: bool = True, fuse_select: bool = True):
         self.cfg = cfg
         self.fuse_gather = fuse_gather
+        # the selection inside the drafting kernel (every CTA selects its head's
+        # chunks), so the refresh call has nothing left to do
+        self.fuse_select = fuse_gather and fuse_select
         # with a stream given, the merge of a layer's verify partials runs on a
         # side stream beside the selection and the drafting pass (the
         # selection needs only the chunk scores of the verify kernel)
@@ -117,6 +122,8 @@ class SpecStep:
 
     def run_refresh(self, i: int, stream=None) -> None:
         cfg, L = self.cfg, self.layers[i]
+        if self.fuse_select:
+            return  # done by the drafting kernel
         if self.fuse_gather:
             ts_select_chunks(L.scores, cfg.N, cfg.budget, L.sel, chunk=cfg.chunk, part_len=L.part_len, stream=stream)
         else:
@@ -126,7 +133,12 @@ class SpecStep:
     def run_draft(self, i: int, stream=None) -> None:
         cfg, L = self.cfg, self.layers[i]
         lse = L.lse_draft if self.want_lse else None
-        if self.fuse_gather:
+        if self.fuse_select:
+            ts_select_gather_tree_attn(L.scores, L.q_draft, L.k, L.v, cfg.N, cfg.budget, L.sel, L.k_part, L.v_part,
+                                       self.mask_draft, L.out_draft, part_len=L.part_len, lse=lse,
+                                       workspace=self.workspace_draft, chunk=cfg.chunk, scale=cfg.scale,
+                                       stream=stream)
+        elif self.fuse_gather:
             ts_gather_tree_attn(L.q_draft, L.k, L.v, cfg.N, L.sel, L.k_part, L.v_part, self.mask_draft, L.out_draft,
                                 lse=lse, workspace=self.workspace_draft, scale=cfg.scale, stream=stream)
         else:

@@ -117,6 +117,16 @@ def test_qwen14b_layers_with_a_separate_gather():
     _check_step(step, range(2))
 
 
+def test_qwen14b_layers_with_the_selection_as_its_own_call():
+    """The step with the selection as its own call before the gather-and-draft
+    call (instead of inside the drafting kernel)."""
+    cfg = W.WORKLOADS["qwen14b-100k"]
+    step = SpecStep(cfg, layers=2, fuse_select=False)
+    step.run()
+    torch.cuda.synchronize()
+    _check_step(step, range(2))
+
+
 def test_llama2_7b_mha_layer():
     cfg = W.WORKLOADS["llama2-7b-100k"]
     step = SpecStep(cfg)

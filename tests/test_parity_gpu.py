@@ -311,7 +311,7 @@ def test_gather_tree_attn_matches_oracle_and_the_two_calls(N, Hq, Hkv, Td, budge
     against the oracle's gather (rows a selected short last chunk lacks keep
     their old contents), the output within the bars against the oracle over the
     gathered cache, and bit-identical to ts_select_gather followed by
-    ts_tree_attn_partial."""
+    ts_tree_attn_partial, and to the one-pass call that also selects."""
     d = 128
     q, k, v = W.make_qkv(Td, Hq, Hkv, d, N, seed=N + 7 * Td, device="cuda", value_kind="normal")
     nc = (N + 63) // 64
@@ -360,6 +360,18 @@ def test_gather_tree_attn_matches_oracle_and_the_two_calls(N, Hq, Hkv, Td, budge
     assert torch.equal(sel, sel2) and torch.equal(plen, plen2)
     assert torch.equal(kp, kp2) and torch.equal(vp, vp2)
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    # and the one-pass call that also selects: the same bits again
+    sel3 = torch.full_like(sel, -1)
+    plen3 = torch.full_like(plen, -1)
+    kp3, vp3 = fill_k.clone(), fill_v.clone()
+    out3, lse3 = torch.empty_like(out), torch.empty_like(lse)
+    ts.ts_select_gather_tree_attn(scores, q, k, v, N, budget, sel3, kp3, vp3, mask, out3, part_len=plen3, lse=lse3,
+                                  workspace=ws, scale=scale)
+    torch.cuda.synchronize()
+    assert ts.ts_device_error(True) == ts.TS_OK
+    assert torch.equal(sel3, sel) and torch.equal(plen3, plen)
+    assert torch.equal(kp3, kp) and torch.equal(vp3, vp)
+    assert torch.equal(out3, out) and torch.equal(lse3, lse)
 
 
 @pytest.mark.parametrize("T,Hq,Hkv,N", [(120, 40, 8, 20480), (4, 40, 8, 4100), (30, 32, 8, 5000), (4, 8, 8, 60)])
