@@ -178,6 +178,29 @@ def test_tree_attn_merge_host_checks():
     assert L.ts_tree_attn_merge(4096, 4, 40, 7, 128, P, None, P, 1 << 30, None) == ts.TS_ERR_INVALID_ARG
 
 
+def _select_gather_attn(scores=0x10000, N=20480, budget=4096, chunk=64, sink=0, recent=0, sel=0x10000,
+                        ld_part=64 * 64 + 4, T=4, Hq=40, Hkv=8, d=128):
+    P = 0x10000
+    return ts.lib().ts_select_gather_tree_attn(scores, N, budget, chunk, sink, recent, sel, None, P, P, P, N + 8, P, P,
+                                               ld_part, T, Hq, Hkv, d, 0.088, P, P, None, P, 1 << 30, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(budget=100), ts.TS_ERR_INVALID_ARG),               # budget not a multiple of the chunk
+    (dict(chunk=32), ts.TS_ERR_UNSUPPORTED),
+    (dict(scores=None), ts.TS_ERR_INVALID_ARG),
+    (dict(sel=None), ts.TS_ERR_INVALID_ARG),
+    (dict(N=0), ts.TS_ERR_INVALID_ARG),                       # nothing to select
+    (dict(sink=40, recent=30), ts.TS_ERR_INVALID_ARG),        # always-kept chunks beyond the budget
+    (dict(T=5, ld_part=64 * 64 + 8), ts.TS_ERR_UNSUPPORTED),  # 25 (row, head) pairs per KV head
+    (dict(d=64), ts.TS_ERR_UNSUPPORTED),
+    (dict(ld_part=64 * 64 + 3), ts.TS_ERR_INVALID_ARG),       # no room for the batch's own rows
+])
+def test_select_gather_tree_attn_rejects(kw, status):
+    assert _select_gather_attn(**kw) == status
+    assert ts.lib().ts_last_error()
+
+
 def test_rescore_tail_rejects():
     L = ts.lib()
     P = 0x10000
