@@ -374,6 +374,77 @@ def test_gather_tree_attn_matches_oracle_and_the_two_calls(N, Hq, Hkv, Td, budge
     assert torch.equal(out3, out) and torch.equal(lse3, lse)
 
 
+@pytest.mark.parametrize("N,Hq,Hkv,Td,budget,sink,recent,kind", [
+    (102400, 40, 8, 4, 4096, 1, 4, "normal"),        # the drafting shape with always-kept chunks
+    (16384 * 64 - 5, 4, 1, 4, 4096, 0, 0, "normal"),  # the most chunks a call takes (keys over both K/V buffers)
+    (16384 * 64, 8, 1, 2, 64 * 300, 2, 3, "ties"),
+    (5000, 40, 8, 4, 2048, 3, 2, "constant"),          # every score equal: the lowest indices complete k
+    (3000, 16, 4, 3, 64 * 47, 0, 0, "normal"),         # the budget covers every chunk
+])
+def test_one_pass_select_sink_recent_and_most_chunks(N, Hq, Hkv, Td, budget, sink, recent, kind):
+    """The one-pass call (each CTA selects its head's chunks) with always-kept
+    first/last chunks, continuous, tied and constant scores, up to 16384
+    chunks: indices and gathered lengths bit-exact against the oracle's
+    selection, and every output bit-identical to ts_select_gather followed by
+    ts_tree_attn_partial (whose gather and attention other tests pin to the
+    oracle); at the smaller sizes the attention against the oracle too."""
+    d = 128
+    q, k, v = W.make_qkv(Td, Hq, Hkv, d, N, seed=N + Td + sink, device="cuda", value_kind="normal")
+    nc = (N + 63) // 64
+    rng = np.random.default_rng(N + 3 * Td)
+    if kind == "normal":
+        s = rng.standard_normal((Hkv, nc)).astype(np.float32)
+    elif kind == "ties":
+        s = rng.integers(-3, 4, size=(Hkv, nc)).astype(np.float32)
+    else:
+        s = np.full((Hkv, nc), 1.5, dtype=np.float32)
+    scores = torch.from_numpy(s).cuda()
+    kk = min(budget // 64, nc)
+    B = kk * 64
+    fill_k = torch.full((Hkv, B + Td, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    fill_v = torch.full_like(fill_k, -7.0)
+    fill_k[:, B:] = k[:, N:N + Td]
+    fill_v[:, B:] = v[:, N:N + Td]
+    parent = list(range(-1, Td - 1))
+    mask = dev_mask(parent)
+    ws = torch.empty(max(16, ts.ts_tree_attn_workspace_bytes(Td, Hq, Hkv, d, B)), dtype=torch.uint8, device="cuda")
+    scale = 1 / math.sqrt(d)
+
+    sel = torch.full((Hkv, kk), -1, dtype=torch.int32, device="cuda")
+    plen = torch.full((Hkv,), -1, dtype=torch.int32, device="cuda")
+    kp, vp = fill_k.clone(), fill_v.clone()
+    out = torch.empty((Td, Hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((Td, Hq), dtype=torch.float32, device="cuda")
+    ts.ts_select_gather_tree_attn(scores, q, k, v, N, budget, sel, kp, vp, mask, out, part_len=plen, lse=lse,
+                                  workspace=ws, sink_chunks=sink, recent_chunks=recent, scale=scale)
+    sel2 = torch.empty_like(sel)
+    plen2 = torch.empty_like(plen)
+    kp2, vp2 = fill_k.clone(), fill_v.clone()
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    ts.ts_select_gather(scores, N, budget, k, v, sel2, kp2, vp2, part_len=plen2, sink_chunks=sink,
+                        recent_chunks=recent)
+    ts.ts_tree_attn_partial(q, kp2, vp2, B, mask, plen2, out2, lse=lse2, workspace=ws, scale=scale)
+    torch.cuda.synchronize()
+    assert ts.ts_device_error(True) == ts.TS_OK
+
+    rsel = oracle.select(s, budget // 64, sink=sink, recent=recent)
+    np.testing.assert_array_equal(sel.cpu().numpy(), rsel)
+    last = (rsel == nc - 1).any(axis=1)
+    tail = N - (nc - 1) * 64
+    np.testing.assert_array_equal(plen.cpu().numpy(), kk * 64 - np.where(last, 64 - tail, 0))
+    if nc > kk:
+        assert (sel[:, :sink].cpu() == torch.arange(sink, dtype=torch.int32)).all()
+        assert (sel[:, kk - recent:].cpu() == torch.arange(nc - recent, nc, dtype=torch.int32)).all()
+    assert torch.equal(sel, sel2) and torch.equal(plen, plen2)
+    assert torch.equal(kp, kp2) and torch.equal(vp, vp2)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    if N <= 102400:
+        rk, rl = oracle.gather(rsel, k.cpu(), N, 64, B + Td, fill=fill_k.cpu(), return_len=True)
+        assert torch.equal(kp.cpu(), rk)
+        ro, rlse = oracle.tree_attn(q.cpu(), kp.cpu(), vp.cpu(), B, parent, scale, prefix_len=rl)
+        check_attn(out, lse, ro, rlse, "one-pass select + gather + draft")
+
+
 @pytest.mark.parametrize("T,Hq,Hkv,N", [(120, 40, 8, 20480), (4, 40, 8, 4100), (30, 32, 8, 5000), (4, 8, 8, 60)])
 def test_unmerged_then_merge_equals_one_call(T, Hq, Hkv, N):
     """ts_tree_attn_unmerged, then ts_tree_attn_merge on another stream after
