@@ -351,7 +351,7 @@ ts_status ts_gather_tree_attn(const void *q, const void *k, const void *v, int64
 /*
  * ts_select_chunks and ts_gather_tree_attn in one pass: every CTA of the
  * drafting kernel selects its KV head's chunks from `scores` itself (the same
- * radix selection as ts_select_chunks), then gathers the two chunks it attends
+ * radix selection as ts_select_chunks), then gathers the chunks it attends
  * over.  sel and part_len are written as ts_select_chunks writes them; the
  * compact cache, out and lse are those of ts_gather_tree_attn with that sel.
  * Arguments, sizes and errors: those of ts_select_chunks (scores, N,

@@ -8,7 +8,10 @@
 // built to keep the FMA pipe busy with packed fp32x2 FMAs and few other
 // instructions per FMA, with four warps per scheduler to hide latencies.
 //
-// CTA = (KV head g, 128-token KV range) = four 32-token blocks, eight warps:
+// CTA = (KV head g, 256-token KV range) = eight 32-token blocks, sixteen
+// warps, one CTA per SM (a range's K/V fill 128 KB of shared memory; half as
+// many ranges as with 128-token CTAs, two per SM, which leaves the split
+// merge half the partials at the same kernel time):
 // warp (b, h) = (w / 2, w % 2) owns dims 64h .. 64h+63 of block b from the
 // load to its partial result.  Rows r = (t, j) t-major, R = T*G, padded to
 // 4 RG (RG = ceil(R/4)).
@@ -31,7 +34,7 @@
 //   O:     lane (rh, dg) = (lane / 16, lane % 16) takes rows rh*2RG .. +2RG-1
 //          and dims 64h + 4dg .. +3: per token one 8-byte V read, RG 16-byte P
 //          reads and 4 RG fp32x2 FMAs.
-//   combine: the four blocks' partials (m, l, O) are merged through shared
+//   combine: the eight blocks' partials (m, l, O) are merged through shared
 //          memory (over the dead K/V buffers) into the range's partial, which
 //          goes to the split workspace for the log-sum-exp merge kernel (a
 //          single range writes the normalised output directly).
@@ -53,10 +56,11 @@ namespace ts {
 namespace {
 constexpr int D = 128;
 constexpr int WT = 32;              // tokens per block
-constexpr int NBLK = 4;             // blocks per CTA
+constexpr int NBLK = 8;             // blocks per CTA
 constexpr int NWARP = 2 * NBLK;     // two warps (dimension halves) per block
 constexpr int NTHR = NWARP * 32;
-constexpr int RANGE = NBLK * WT;    // tokens per CTA: two 64-token chunks
+constexpr int RANGE = NBLK * WT;    // tokens per CTA: four 64-token chunks
+constexpr int CPR = NBLK / 2;       // chunks per range
 constexpr int ROWB = D * 2;         // bytes of one K/V row
 constexpr int HALFB = ROWB / 2;     // bytes of one half row (64 dims)
 
@@ -101,7 +105,7 @@ struct SmallCfg {
 }  // namespace
 
 template <int RG, bool GATHER, bool SELECT>
-__global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs a, const SmallGather gs, int n_splits) {
+__global__ void __launch_bounds__(NTHR, 1) tree_attn_small_kernel(const AttnArgs a, const SmallGather gs, int n_splits) {
     using C = SmallCfg<RG>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     unsigned char *sK = smem_raw + C::K_OFF;
@@ -156,16 +160,16 @@ __global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs
     cp_async_commit();
     if (SELECT) {
         // this head's top-k chunks (the keys over the K/V buffers, which no
-        // copy has touched yet): the range's two chunks, and the full list
+        // copy has touched yet): the range's four chunks, and the full list
         // and gathered length from the CTAs of the first range
         __shared__ TopkSmem tsm;
-        __shared__ int s_chunk[2];
-        const int pos0 = 2 * split;
+        __shared__ int s_chunk[CPR];
+        const int pos0 = CPR * split;
         const bool last_taken = radix_topk_ascending<NTHR>(
             gs.scores + (size_t)g * gs.n_chunks, gs.n_chunks, gs.k_sel, gs.n_sink, gs.n_recent,
             reinterpret_cast<uint32_t *>(sK), tsm, [&](int pos, int c) {
                 if (split == 0) gs.sel_out[(size_t)g * gs.k_sel + pos] = c;
-                if (pos == pos0 || pos == pos0 + 1) s_chunk[pos - pos0] = c;
+                if (pos >= pos0 && pos < pos0 + CPR) s_chunk[pos - pos0] = c;
             });
         const int per = (gs.n_chunks + NTHR - 1) / NTHR;
         if (split == 0 && gs.part_len_out != nullptr && (int)threadIdx.x == (gs.n_chunks - 1) / per) {
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs
     }
     __syncthreads();  // every block's (m, l) and score sums are written; K and V are dead
 
-    if (a.chunk_scores != nullptr && threadIdx.x < 2) {
+    if (a.chunk_scores != nullptr && threadIdx.x < CPR) {
         const int64_t ch0 = t0 + 64 * threadIdx.x;
         if (ch0 < Np) {
             float best = -INFINITY;
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(NTHR, 2) tree_attn_small_kernel(const AttnArgs
         }
     }
 
-    // ---- combine the four block partials: each warp scales its O by
+    // ---- combine the eight block partials: each warp scales its O by
     // 2^(m_b - M) and parks it over the K/V buffers as fp32 [block][row][dim]
     float *sO = reinterpret_cast<float *>(smem_raw);
 #pragma unroll

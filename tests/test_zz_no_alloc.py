@@ -87,11 +87,11 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 def test_noalloc_rejects_sizes_above_its_scratch():
     """Sizes whose split partials need more than the fixed array are refused
     before any pointer is read or any kernel is launched, and the message names
-    the maximum.  A 4-row drafting batch over 200000 tokens splits into 1563
-    ranges of 128 tokens: 1563 x 4 x 40 x 130 x 4 bytes, above 64 MiB."""
+    the maximum.  A 4-row drafting batch over 400000 tokens splits into 1563
+    ranges of 256 tokens: 1563 x 4 x 40 x 130 x 4 bytes, above 64 MiB."""
     from long_context_attention_tree_b300 import build
     build.build()
-    T, Hq, Hkv, d, N = 4, 40, 8, 128, 200000
+    T, Hq, Hkv, d, N = 4, 40, 8, 128, 400000
     need = ts.ts_tree_attn_workspace_bytes(T, Hq, Hkv, d, N)
     assert need > ts.TS_NOALLOC_SCRATCH_BYTES
     L = ts.lib()
