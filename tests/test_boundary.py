@@ -195,6 +195,7 @@ def _select_gather_attn(scores=0x10000, N=20480, budget=4096, chunk=64, sink=0, 
     (dict(T=5, ld_part=64 * 64 + 8), ts.TS_ERR_UNSUPPORTED),  # 25 (row, head) pairs per KV head
     (dict(d=64), ts.TS_ERR_UNSUPPORTED),
     (dict(ld_part=64 * 64 + 3), ts.TS_ERR_INVALID_ARG),       # no room for the batch's own rows
+    (dict(N=16384 * 64 + 1), ts.TS_ERR_UNSUPPORTED),          # 16385 chunks: the keys would overflow the K/V buffers
 ])
 def test_select_gather_tree_attn_rejects(kw, status):
     assert _select_gather_attn(**kw) == status
